@@ -1,0 +1,186 @@
+"""fp64 CPU oracle for the speculative-decoding verification step.
+
+TEST INFRASTRUCTURE. Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline
+leg of ``bench.py`` may import this package. The CUDA library never imports, links or
+calls it, and it shares no code with the CUDA library.
+
+The arithmetic lives in ``oracle.c`` (plain C, fp64, OpenMP over (batch, KV-head)
+units); this module compiles it with gcc on first use and marshals numpy arrays.
+
+Functions and the passages they follow (page title, then section):
+
+* ``verify_attn`` -- GQA verify attention with a window-causal mask and a materialised
+  softmax. "GPU and LLM, chapter 5": "GQA", "FlashAttention" (attention =
+  softmax(Q K^T) V) and "Speculative decoding (2)" (one forward over the 1+D positions).
+* ``verify_attn_online`` -- the same result through the online-softmax update of
+  "GPU and LLM, chapter 5", "Online softmax: carry the max and the sum".
+* ``argmax_rows`` -- naive first-index argmax (target's greedy choice per window row).
+* ``accept`` -- first-mismatch acceptance: "Co-Designing AI Models Using Speculative
+  Decoding" summary, "basic structure" (AL in [1, 1+D]); "GPU and LLM, chapter 5",
+  "Speculative decoding (2)" (the target's own token replaces the first rejected draft).
+* ``bf16_to_f64`` / ``e4m3_to_f64`` -- decoders written from the binary32 and OCP E4M3
+  format definitions.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``oracle.c`` into ``liboracle.so`` next to it (gcc, OpenMP, no FMA
+    contraction so results do not depend on the host's vector unit)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + ".tmp%d" % os.getpid()
+        cmd = ["gcc", "-O2", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
+               "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            p = ctypes.c_void_p
+            i32, i64, dbl = ctypes.c_int, ctypes.c_int64, ctypes.c_double
+            lib.orc_bf16_to_f64.argtypes = [ctypes.c_uint16]
+            lib.orc_bf16_to_f64.restype = dbl
+            lib.orc_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+            lib.orc_e4m3_to_f64.restype = dbl
+            lib.orc_num_threads.restype = i32
+            attn = [i32, i32, i32, i32, p, p, i32, p, p, p, p, dbl, p, p, i32]
+            lib.orc_verify_attn.argtypes = attn
+            lib.orc_verify_attn.restype = i32
+            lib.orc_verify_attn_online.argtypes = attn + [i32]
+            lib.orc_verify_attn_online.restype = i32
+            lib.orc_argmax_rows.argtypes = [i64, i64, i32, p, p, i32]
+            lib.orc_argmax_rows.restype = i32
+            lib.orc_accept.argtypes = [i32, p, p, p, p, p]
+            lib.orc_accept.restype = i32
+            _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def num_threads() -> int:
+    return _load().orc_num_threads()
+
+
+def bf16_to_f64(bits: int) -> float:
+    return _load().orc_bf16_to_f64(int(bits))
+
+
+def e4m3_to_f64(bits: int) -> float:
+    return _load().orc_e4m3_to_f64(int(bits))
+
+
+def _attn_args(q, k, v, seq_lens, draft_len, kv_scale, Hq, Hkv, d, scale, units):
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    fp8 = k.dtype == np.uint8
+    k = np.ascontiguousarray(k)
+    v = np.ascontiguousarray(v)
+    if k.dtype != v.dtype or k.dtype not in (np.uint8, np.uint16):
+        raise TypeError("k and v must both be uint16 (bf16 bits) or uint8 (e4m3 codes)")
+    seq_lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    draft_len = np.ascontiguousarray(draft_len, dtype=np.int32)
+    B = seq_lens.shape[0]
+    if kv_scale is not None:
+        kv_scale = np.ascontiguousarray(kv_scale, dtype=np.float32).reshape(2, Hkv)
+    elif fp8:
+        raise ValueError("fp8 k/v need kv_scale")
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    mask = None
+    if units is not None:
+        mask = np.zeros(B * Hkv, dtype=np.uint8)
+        for (b, g) in units:
+            mask[b * Hkv + g] = 1
+    rows = int(np.sum(draft_len.astype(np.int64) + 1))
+    kv_rows = int(np.sum(seq_lens.astype(np.int64) + draft_len + 1))
+    if q.size != rows * Hq * d or k.size < kv_rows * Hkv * d or v.size < kv_rows * Hkv * d:
+        raise ValueError("array sizes do not match seq_lens / draft_len")
+    return q, k, v, seq_lens, draft_len, kv_scale, float(scale), mask, fp8, B, rows
+
+
+def verify_attn(q, k, v, seq_lens, draft_len, *, Hq, Hkv, d, kv_scale=None, scale=None,
+                units=None, nthreads=0, online_tile=0, out=None):
+    """fp64 verify attention. q: bf16 bits [sum W, Hq, d]; k, v: bf16 bits or e4m3 codes
+    [sum (T+W), Hkv, d]. Returns fp64 [sum W, Hq, d]; rows of units not listed in
+    ``units`` (an iterable of (b, kv_head)) are NaN."""
+    (q, k, v, seq_lens, draft_len, kv_scale, scale, mask, fp8, B,
+     rows) = _attn_args(q, k, v, seq_lens, draft_len, kv_scale, Hq, Hkv, d, scale, units)
+    if out is None:
+        out = np.full((rows, Hq, d), np.nan, dtype=np.float64)
+    lib = _load()
+    args = [B, Hq, Hkv, d, _ptr(seq_lens), _ptr(draft_len), int(fp8), _ptr(q), _ptr(k),
+            _ptr(v), _ptr(kv_scale), scale, _ptr(mask), _ptr(out), int(nthreads)]
+    if online_tile:
+        rc = lib.orc_verify_attn_online(*args, int(online_tile))
+    else:
+        rc = lib.orc_verify_attn(*args)
+    if rc:
+        raise ValueError("oracle rejected the arguments")
+    return out
+
+
+def verify_attn_online(q, k, v, seq_lens, draft_len, *, tile, **kw):
+    """The online-softmax (tile-by-tile) variant of ``verify_attn``."""
+    return verify_attn(q, k, v, seq_lens, draft_len, online_tile=tile, **kw)
+
+
+def argmax_rows(logits, nthreads=0):
+    """logits: [rows, V] fp32, or uint16 bf16 bits. Returns int32 [rows]."""
+    logits = np.ascontiguousarray(logits)
+    if logits.dtype == np.uint16:
+        dt = 0
+    elif logits.dtype == np.float32:
+        dt = 2
+    else:
+        raise TypeError("logits must be float32 or uint16 (bf16 bits)")
+    rows, vocab = logits.shape
+    amax = np.empty(rows, dtype=np.int32)
+    if _load().orc_argmax_rows(rows, vocab, dt, _ptr(logits), _ptr(amax), int(nthreads)):
+        raise ValueError("oracle rejected the arguments")
+    return amax
+
+
+def accept(amax, draft_tokens, draft_len):
+    """First-mismatch acceptance from per-row argmax. Returns (accept_len, next_token)."""
+    amax = np.ascontiguousarray(amax, dtype=np.int32)
+    draft_tokens = np.ascontiguousarray(draft_tokens, dtype=np.int32)
+    draft_len = np.ascontiguousarray(draft_len, dtype=np.int32)
+    B = draft_len.shape[0]
+    if amax.shape[0] != int(np.sum(draft_len.astype(np.int64) + 1)):
+        raise ValueError("amax must have sum(1 + D_b) rows")
+    if draft_tokens.shape[0] != int(np.sum(draft_len.astype(np.int64))):
+        raise ValueError("draft_tokens must have sum(D_b) entries")
+    al = np.empty(B, dtype=np.int32)
+    nt = np.empty(B, dtype=np.int32)
+    if _load().orc_accept(B, _ptr(draft_len), _ptr(draft_tokens), _ptr(amax), _ptr(al),
+                          _ptr(nt)):
+        raise ValueError("oracle rejected the arguments")
+    return al, nt
+
+
+def spec_accept(logits, draft_tokens, draft_len, nthreads=0):
+    """Argmax of every window row, then first-mismatch acceptance."""
+    amax = argmax_rows(logits, nthreads)
+    al, nt = accept(amax, draft_tokens, draft_len)
+    return al, nt, amax

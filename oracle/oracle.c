@@ -1,0 +1,286 @@
+/*
+ * oracle.c -- plain fp64 CPU oracle for the speculative-decoding verification step.
+ *
+ * TEST INFRASTRUCTURE. Only the tests, the smoke check and the benchmark's CPU-baseline
+ * leg may load this library. It shares no code, header, table or constant with the
+ * CUDA library; it is written straight from the definitions it cites and is slow on
+ * purpose: every score table is materialised, every argmax is a naive loop.
+ *
+ * Sources (page title, then section):
+ *   [P2] "Co-Designing AI Models Using Speculative Decoding ..." (summary page),
+ *        section "basic structure of speculative decoding": draft length D, acceptance
+ *        length AL in [1, 1+D], accept draft tokens up to the first mismatch.
+ *   [P3] "GPU and LLM, chapter 5", sections "Online softmax: carry the max and the sum"
+ *        (the m / l / O update, exact rather than approximate), "GQA: several Q heads share
+ *        one K/V head", "Speculative decoding (2): verify together" (3 accepted, the 4th
+ *        rejected, the target's own token inserted; one forward over k+1 positions).
+ *
+ * Readings where the pages are silent:
+ *   - The 1+D window rows' K/V are already in the cache at positions T..T+D; window row i
+ *     sees keys 0..T+i inclusive (T+i+1 keys).
+ *   - Query head h uses KV head h / G (consecutive groups of G query heads).
+ *   - FP8 values are OCP E4M3 codes times a per-KV-head fp32 scale (kv_scale[0][g] for K,
+ *     kv_scale[1][g] for V).
+ *   - Argmax ties go to the lowest index; -0.0 equals +0.0.
+ *
+ * Layouts (packed ragged batch): q and out [sum_b W_b, Hq, d]; k and v
+ * [sum_b (T_b + W_b), Hkv, d]; W_b = 1 + D_b; sequences in batch order.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* bfloat16 is the upper half of an IEEE-754 binary32 word. */
+double orc_bf16_to_f64(uint16_t bits) {
+  uint32_t u = ((uint32_t)bits) << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+/* OCP 8-bit floating point, E4M3 variant: 1 sign bit, 4 exponent bits (bias 7),
+ * 3 mantissa bits, no infinities; S.1111.111 is NaN. */
+double orc_e4m3_to_f64(uint8_t bits) {
+  int s = (bits >> 7) & 1;
+  int e = (bits >> 3) & 15;
+  int m = bits & 7;
+  double mag;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0)
+    mag = ldexp((double)m / 8.0, 1 - 7);
+  else
+    mag = ldexp(1.0 + (double)m / 8.0, e - 7);
+  return s ? -mag : mag;
+}
+
+double orc_f32_to_f64(float f) { return (double)f; }
+
+int orc_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+typedef struct {
+  int B, Hq, Hkv, d, G;
+  int kv_fp8;
+  const uint16_t* q;
+  const void* k;
+  const void* v;
+  const float* kv_scale;
+  double scale;
+  int64_t* q_off;   /* [B+1] prefix sums of W_b */
+  int64_t* kv_off;  /* [B+1] prefix sums of T_b + W_b */
+  const int32_t* seq_lens;
+  const int32_t* draft_len;
+  double lut[256]; /* e4m3 code -> value, from orc_e4m3_to_f64 */
+} orc_ctx;
+
+static double kv_elem(const orc_ctx* c, const void* base, int which, int64_t row, int g,
+                      int col) {
+  int64_t idx = (row * c->Hkv + g) * (int64_t)c->d + col;
+  if (c->kv_fp8)
+    return c->lut[((const uint8_t*)base)[idx]] * (double)c->kv_scale[which * c->Hkv + g];
+  return orc_bf16_to_f64(((const uint16_t*)base)[idx]);
+}
+
+static int setup(orc_ctx* c, int B, int Hq, int Hkv, int d, const int32_t* seq_lens,
+                 const int32_t* draft_len, int kv_fp8, const uint16_t* q, const void* k,
+                 const void* v, const float* kv_scale, double scale) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv != 0) return 1;
+  if (kv_fp8 && !kv_scale) return 1;
+  c->B = B; c->Hq = Hq; c->Hkv = Hkv; c->d = d; c->G = Hq / Hkv;
+  c->kv_fp8 = kv_fp8; c->q = q; c->k = k; c->v = v; c->kv_scale = kv_scale;
+  c->scale = scale; c->seq_lens = seq_lens; c->draft_len = draft_len;
+  c->q_off = (int64_t*)malloc(sizeof(int64_t) * (B + 1));
+  c->kv_off = (int64_t*)malloc(sizeof(int64_t) * (B + 1));
+  c->q_off[0] = 0; c->kv_off[0] = 0;
+  for (int b = 0; b < B; ++b) {
+    if (seq_lens[b] < 0 || draft_len[b] < 0) return 1;
+    c->q_off[b + 1] = c->q_off[b] + 1 + draft_len[b];
+    c->kv_off[b + 1] = c->kv_off[b] + seq_lens[b] + 1 + draft_len[b];
+  }
+  for (int i = 0; i < 256; ++i) c->lut[i] = orc_e4m3_to_f64((uint8_t)i);
+  return 0;
+}
+
+static void teardown(orc_ctx* c) { free(c->q_off); free(c->kv_off); }
+
+/* One output row, materialised softmax ([P3] attention = softmax(q K^T) V over the
+ * visible keys; the window-causal mask keeps keys 0..T+i). */
+static void row_materialised(const orc_ctx* c, int b, int h, int i, double* s,
+                             double* out_row) {
+  const int g = h / c->G, d = c->d;
+  const int64_t nkeys = (int64_t)c->seq_lens[b] + i + 1;
+  const int64_t qrow = c->q_off[b] + i;
+  const uint16_t* qv = c->q + (qrow * c->Hq + h) * (int64_t)d;
+  double mx = -INFINITY;
+  for (int64_t j = 0; j < nkeys; ++j) {
+    double acc = 0.0;
+    for (int col = 0; col < d; ++col)
+      acc += orc_bf16_to_f64(qv[col]) * kv_elem(c, c->k, 0, c->kv_off[b] + j, g, col);
+    s[j] = acc * c->scale;
+    if (s[j] > mx) mx = s[j];
+  }
+  double denom = 0.0;
+  for (int64_t j = 0; j < nkeys; ++j) {
+    s[j] = exp(s[j] - mx);
+    denom += s[j];
+  }
+  for (int col = 0; col < d; ++col) out_row[col] = 0.0;
+  for (int64_t j = 0; j < nkeys; ++j) {
+    double p = s[j] / denom;
+    for (int col = 0; col < d; ++col)
+      out_row[col] += p * kv_elem(c, c->v, 1, c->kv_off[b] + j, g, col);
+  }
+}
+
+/* One output row with the online-softmax update of [P3] "Online softmax", applied tile by
+ * tile: m_new = max(m, max s); l_new = l*exp(m - m_new) + sum exp(s - m_new);
+ * O_new = O*exp(m - m_new) + sum exp(s - m_new) v; finally O / l. */
+static void row_online(const orc_ctx* c, int b, int h, int i, int tile, double* s,
+                       double* out_row) {
+  const int g = h / c->G, d = c->d;
+  const int64_t nkeys = (int64_t)c->seq_lens[b] + i + 1;
+  const int64_t qrow = c->q_off[b] + i;
+  const uint16_t* qv = c->q + (qrow * c->Hq + h) * (int64_t)d;
+  double m = -INFINITY, l = 0.0;
+  for (int col = 0; col < d; ++col) out_row[col] = 0.0;
+  for (int64_t j0 = 0; j0 < nkeys; j0 += tile) {
+    int64_t j1 = j0 + tile < nkeys ? j0 + tile : nkeys;
+    double tmax = -INFINITY;
+    for (int64_t j = j0; j < j1; ++j) {
+      double acc = 0.0;
+      for (int col = 0; col < d; ++col)
+        acc += orc_bf16_to_f64(qv[col]) * kv_elem(c, c->k, 0, c->kv_off[b] + j, g, col);
+      s[j - j0] = acc * c->scale;
+      if (s[j - j0] > tmax) tmax = s[j - j0];
+    }
+    double m_new = m > tmax ? m : tmax;
+    double alpha = exp(m - m_new); /* exp(-inf) = 0 on the first tile */
+    l *= alpha;
+    for (int col = 0; col < d; ++col) out_row[col] *= alpha;
+    for (int64_t j = j0; j < j1; ++j) {
+      double p = exp(s[j - j0] - m_new);
+      l += p;
+      for (int col = 0; col < d; ++col)
+        out_row[col] += p * kv_elem(c, c->v, 1, c->kv_off[b] + j, g, col);
+    }
+    m = m_new;
+  }
+  for (int col = 0; col < d; ++col) out_row[col] /= l;
+}
+
+static int run_attn(int B, int Hq, int Hkv, int d, const int32_t* seq_lens,
+                    const int32_t* draft_len, int kv_fp8, const uint16_t* q, const void* k,
+                    const void* v, const float* kv_scale, double scale,
+                    const uint8_t* unit_mask, double* out, int nthreads, int tile) {
+  orc_ctx c;
+  if (setup(&c, B, Hq, Hkv, d, seq_lens, draft_len, kv_fp8, q, k, v, kv_scale, scale)) {
+    return 1;
+  }
+  int64_t max_keys = 1;
+  for (int b = 0; b < B; ++b) {
+    int64_t n = (int64_t)seq_lens[b] + 1 + draft_len[b];
+    if (n > max_keys) max_keys = n;
+  }
+  const int64_t units = (int64_t)B * Hkv;
+#ifdef _OPENMP
+  if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel num_threads(nthreads)
+#endif
+  {
+    double* s = (double*)malloc(sizeof(double) * (size_t)(tile > 0 ? tile : max_keys));
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+    for (int64_t u = 0; u < units; ++u) {
+      if (unit_mask && !unit_mask[u]) continue;
+      int b = (int)(u / Hkv), g = (int)(u % Hkv);
+      for (int hl = 0; hl < c.G; ++hl) {
+        int h = g * c.G + hl;
+        for (int i = 0; i <= draft_len[b]; ++i) {
+          double* o = out + ((c.q_off[b] + i) * Hq + h) * (int64_t)d;
+          if (tile > 0)
+            row_online(&c, b, h, i, tile, s, o);
+          else
+            row_materialised(&c, b, h, i, s, o);
+        }
+      }
+    }
+    free(s);
+  }
+  teardown(&c);
+  return 0;
+}
+
+/* Verify attention, materialised softmax. unit_mask [B*Hkv] selects (b, kv-head) units to
+ * compute (NULL: all); rows of unselected units are left untouched. kv_fp8 = 0: k/v are
+ * bf16 bit patterns; 1: E4M3 codes with kv_scale [2, Hkv]. Returns 0 on success. */
+int orc_verify_attn(int B, int Hq, int Hkv, int d, const int32_t* seq_lens,
+                    const int32_t* draft_len, int kv_fp8, const uint16_t* q, const void* k,
+                    const void* v, const float* kv_scale, double scale,
+                    const uint8_t* unit_mask, double* out, int nthreads) {
+  return run_attn(B, Hq, Hkv, d, seq_lens, draft_len, kv_fp8, q, k, v, kv_scale, scale,
+                  unit_mask, out, nthreads, 0);
+}
+
+/* The same attention through the tile-by-tile online-softmax update (tile >= 1 keys). */
+int orc_verify_attn_online(int B, int Hq, int Hkv, int d, const int32_t* seq_lens,
+                           const int32_t* draft_len, int kv_fp8, const uint16_t* q,
+                           const void* k, const void* v, const float* kv_scale,
+                           double scale, const uint8_t* unit_mask, double* out,
+                           int nthreads, int tile) {
+  if (tile < 1) return 1;
+  return run_attn(B, Hq, Hkv, d, seq_lens, draft_len, kv_fp8, q, k, v, kv_scale, scale,
+                  unit_mask, out, nthreads, tile);
+}
+
+/* Row-wise argmax, naive loop, first index wins ties (strict '>' keeps the earliest).
+ * dtype 0: bf16 bit patterns (uint16); 2: fp32. Values are compared exactly in fp64. */
+int orc_argmax_rows(int64_t rows, int64_t vocab, int dtype, const void* logits,
+                    int32_t* amax, int nthreads) {
+  if (rows < 0 || vocab <= 0 || (dtype != 0 && dtype != 2)) return 1;
+#ifdef _OPENMP
+  if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel for num_threads(nthreads) schedule(static)
+#endif
+  for (int64_t r = 0; r < rows; ++r) {
+    double best = 0.0;
+    int64_t arg = 0;
+    for (int64_t j = 0; j < vocab; ++j) {
+      double x = dtype == 0 ? orc_bf16_to_f64(((const uint16_t*)logits)[r * vocab + j])
+                            : (double)((const float*)logits)[r * vocab + j];
+      if (j == 0 || x > best) { best = x; arg = j; }
+    }
+    amax[r] = (int32_t)arg;
+  }
+  return 0;
+}
+
+/* Greedy acceptance ([P2] "accept tokens until the first mismatch"; [P3] the target's own
+ * token replaces the first rejected draft, and with all k drafts accepted the step yields
+ * k+1 tokens). amax holds the target's argmax for every window row [sum_b W_b];
+ * draft_tokens is packed [sum_b D_b]. For sequence b: n = number of leading positions j
+ * with draft[j] == amax[j]; AL = n + 1; next_token = amax[n]. */
+int orc_accept(int B, const int32_t* draft_len, const int32_t* draft_tokens,
+               const int32_t* amax, int32_t* accept_len, int32_t* next_token) {
+  int64_t q_off = 0, d_off = 0;
+  for (int b = 0; b < B; ++b) {
+    int D = draft_len[b];
+    if (D < 0) return 1;
+    int n = 0;
+    while (n < D && draft_tokens[d_off + n] == amax[q_off + n]) ++n;
+    accept_len[b] = n + 1;
+    next_token[b] = amax[q_off + n];
+    q_off += 1 + D;
+    d_off += D;
+  }
+  return 0;
+}
