@@ -1,0 +1,166 @@
+/*
+ * specverify.h -- C ABI of libspecverify.so: the target-model verification step of
+ * speculative decoding on one NVIDIA GB300 (sm_103a).
+ *
+ * Sources (page title, then section):
+ *   "Co-Designing AI Models Using Speculative Decoding for Faster LLM Inference"
+ *   (summary page), "basic structure": a drafter proposes D tokens, the target verifies
+ *   them in parallel and keeps them up to the first mismatch; the acceptance length AL
+ *   lies in [1, 1+D]. Same page, guideline 2: with GQA group size G = Hq / Hkv the
+ *   verify attention has G * (1 + D) query rows per KV head.
+ *   "GPU and LLM, chapter 5": "FlashAttention" and "Online softmax" (the score table is
+ *   processed tile by tile in on-chip memory with a running max m and sum l, never
+ *   written to HBM); "GQA" (groups of query heads share one K/V head); "Speculative
+ *   decoding (2)" (one forward over the k+1 positions; the target's own token replaces
+ *   the first rejected draft).
+ *
+ * Conventions shared by every entry point:
+ *   - Every data pointer is a DEVICE pointer owned by the caller, unless stated otherwise.
+ *     The library keeps no pointer after a call returns and allocates no device memory:
+ *     scratch space is the caller's `workspace`.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy default
+ *     stream). Host-side checks cover sizes, pointers and alignment only: device arrays
+ *     (lengths, tokens) are never read on the host, so no call synchronises.
+ *   - Device-side checks (a length beyond its stated maximum, packed sizes beyond the
+ *     buffers) make the kernels skip all work and leave outputs untouched; they set a
+ *     sticky flag in the workspace that sv_workspace_status() reports.
+ *   - A workspace must be zero-filled once before its first use (the flags live in its
+ *     first 256 bytes) and may be reused by later calls on the same stream. Two calls
+ *     that run concurrently must not share a workspace.
+ *   - Return value: SV_OK or an error code; nothing is printed and nothing is thrown.
+ *
+ * Packed ragged layout (uniform batches are the special case with equal lengths):
+ *   for sequence b with cached prefix T_b = seq_lens[b] and draft length D_b = draft_len[b],
+ *   W_b = 1 + D_b window rows. Window row 0 is the last accepted token, rows 1..D_b the
+ *   drafts. Sequences are stored back to back in batch order:
+ *     q, out        [sum_b W_b,         Hq,  d]  rows q_off[b] .. q_off[b] + D_b
+ *     k/v cache     [sum_b (T_b + W_b), Hkv, d]  rows kv_off[b] .. kv_off[b] + T_b + D_b
+ *   The caller has already written the window's K/V rows at cache positions T_b..T_b+D_b
+ *   (the verify forward appends them before attention, as a prefill does).
+ *   Window row i attends to cache positions 0..T_b+i inclusive (window-causal mask).
+ *   Query head h uses KV head h / G.
+ */
+#ifndef SPECVERIFY_H
+#define SPECVERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SV_API __attribute__((visibility("default")))
+#else
+#define SV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SV_OK = 0,
+  SV_ERR_NULL = 1,        /* a required pointer is NULL */
+  SV_ERR_SHAPE = 2,       /* a size is out of range or inconsistent */
+  SV_ERR_DTYPE = 3,       /* unsupported dtype */
+  SV_ERR_ALIGN = 4,       /* a pointer is not 16-byte aligned */
+  SV_ERR_WORKSPACE = 5,   /* workspace too small */
+  SV_ERR_CUDA = 6,        /* a CUDA runtime call or kernel launch failed */
+  SV_ERR_TIMEOUT = 7,     /* a device-side wait gave up (reported by sv_workspace_status) */
+  SV_ERR_DEVICE_SHAPE = 8 /* device-side length check failed (sv_workspace_status) */
+} sv_status;
+
+typedef enum { SV_BF16 = 0, SV_FP8_E4M3 = 1, SV_FP32 = 2 } sv_dtype;
+
+/* Shape of one spec_verify_attn call. */
+typedef struct {
+  int32_t batch;          /* B >= 0 (0: nothing to do) */
+  int32_t num_q_heads;    /* Hq, a multiple of num_kv_heads */
+  int32_t num_kv_heads;   /* Hkv >= 1 */
+  int32_t head_dim;       /* d: 64 or 128 */
+  int32_t max_draft_len;  /* upper bound on every D_b, 0 <= D_b <= max_draft_len <= 255 */
+  int32_t max_seq_len;    /* upper bound on every T_b */
+  int64_t q_rows;         /* rows allocated in q and out, >= sum_b (1 + D_b) */
+  int64_t kv_rows;        /* rows allocated in k_cache and v_cache, >= sum_b (T_b+1+D_b) */
+  int32_t kv_dtype;       /* SV_BF16, or SV_FP8_E4M3 (OCP E4M3 codes) */
+  float softmax_scale;    /* scale on q.k; 0 selects 1/sqrt(head_dim) */
+} sv_attn_desc;
+
+/* Bytes of workspace spec_verify_attn needs for `desc` on the CURRENT CUDA device
+ * (the split-KV partial results depend on its SM count). Returns 0 if desc is invalid. */
+SV_API size_t spec_verify_attn_workspace_size(const sv_attn_desc* desc);
+
+/*
+ * spec_verify_attn -- GQA verify attention over the cached prefix plus the draft window.
+ *
+ * For every sequence b, KV head g, query head h in [g*G, (g+1)*G) and window row
+ * i in [0, D_b]:
+ *   s_j = scale * q[q_off[b]+i, h, :] . K[kv_off[b]+j, g, :],   j = 0 .. T_b + i
+ *   out[q_off[b]+i, h, :] = sum_j softmax(s)_j * V[kv_off[b]+j, g, :]
+ * computed tile by tile with the online-softmax update, so no score table reaches HBM.
+ *
+ *   q        bf16 [q_rows, Hq, d]
+ *   k_cache  bf16 or E4M3 codes [kv_rows, Hkv, d]; v_cache likewise
+ *   seq_lens int32 [B] = T_b (prefix length, excluding the window)
+ *   draft_len int32 [B] = D_b
+ *   kv_scale fp32 [2, Hkv] for SV_FP8_E4M3 (row 0 scales K, row 1 scales V: the real
+ *            value of a code c is e4m3(c) * scale); must be NULL for SV_BF16
+ *   out      bf16 [q_rows, Hq, d]; only the sum_b W_b packed rows are written
+ *   workspace >= spec_verify_attn_workspace_size(desc) bytes, 256-byte aligned
+ * q, k_cache, v_cache and out must be 16-byte aligned.
+ */
+SV_API sv_status spec_verify_attn(const sv_attn_desc* desc, const void* q, const void* k_cache,
+                           const void* v_cache, const int32_t* seq_lens,
+                           const int32_t* draft_len, const float* kv_scale, void* out,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace spec_accept needs on the current CUDA device. 0 if invalid. */
+SV_API size_t spec_accept_workspace_size(int32_t batch, int32_t max_draft_len, int32_t vocab);
+
+/*
+ * spec_accept -- greedy acceptance of the drafts.
+ *
+ * For every window row r the target's greedy token is amax[r] = the smallest index
+ * attaining max(logits[r, :]) (exact comparison; -0.0 ties +0.0; NaN never wins).
+ * For sequence b: n_b = the number of leading positions j < D_b with
+ * draft_tokens[d_off[b] + j] == amax[q_off[b] + j]; accept_len[b] = n_b + 1 (in
+ * [1, 1 + D_b]); next_token[b] = amax[q_off[b] + n_b] (the target's token at the first
+ * mismatch, or the bonus token after D_b accepted drafts).
+ *
+ *   logits       bf16 or fp32 [sum_b (1 + D_b), vocab], row q_off[b] + j is the target's
+ *                prediction after window token j of sequence b
+ *   draft_tokens int32 [sum_b D_b] packed, d_off[b] = sum_{b'<b} D_b'
+ *   draft_len    int32 [B]
+ *   accept_len, next_token int32 [B] (outputs)
+ *   target_tokens int32 [sum_b (1 + D_b)] (optional output, may be NULL): amax per row
+ *   workspace >= spec_accept_workspace_size(batch, max_draft_len, vocab) bytes
+ */
+SV_API sv_status spec_accept(int32_t batch, int32_t max_draft_len, int32_t vocab,
+                      int32_t logits_dtype, const void* logits, const int32_t* draft_tokens,
+                      const int32_t* draft_len, int32_t* accept_len, int32_t* next_token,
+                      int32_t* target_tokens, void* workspace, size_t workspace_bytes,
+                      void* stream);
+
+/* Synchronises `stream`, then reads the sticky device-side flags of a workspace used by
+ * either call: SV_OK, SV_ERR_DEVICE_SHAPE or SV_ERR_TIMEOUT. clear != 0 resets them. */
+SV_API sv_status sv_workspace_status(void* workspace, int clear, void* stream);
+
+/* Human-readable name of a status code (static string). */
+SV_API const char* sv_status_string(sv_status status);
+
+/* Attention kernel selection, for measurement and tests: 0 = automatic (default),
+ * 1 = warp-level mma.sync kernel, 2 = tcgen05 kernel. Returns the previous value, or -1
+ * if the value is unknown or the kernel is not built. Process-wide. */
+SV_API int sv_set_attn_kernel(int which);
+
+/* Profiling hook: when both are non-NULL, every later spec_verify_attn records `start`
+ * just before and `stop` just after its main attention kernel, on the call's stream
+ * (cudaEvent_t handles owned by the caller). Pass NULLs to turn it off. Process-wide. */
+SV_API void sv_set_profile_events(void* start_event, void* stop_event);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+SV_API int sv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECVERIFY_H */

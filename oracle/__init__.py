@@ -4,8 +4,8 @@ TEST INFRASTRUCTURE. Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-ba
 leg of ``bench.py`` may import this package. The CUDA library never imports, links or
 calls it, and it shares no code with the CUDA library.
 
-The arithmetic lives in ``oracle.c`` (plain C, fp64, OpenMP over (batch, KV-head)
-units); this module compiles it with gcc on first use and marshals numpy arrays.
+The arithmetic lives in ``oracle.c`` (plain C, fp64, OpenMP over independent output
+rows); this module compiles it with gcc on first use and marshals numpy arrays.
 
 Functions and the passages they follow (page title, then section):
 
@@ -62,7 +62,7 @@ def _load():
             lib.orc_e4m3_to_f64.argtypes = [ctypes.c_uint8]
             lib.orc_e4m3_to_f64.restype = dbl
             lib.orc_num_threads.restype = i32
-            attn = [i32, i32, i32, i32, p, p, i32, p, p, p, p, dbl, p, p, i32]
+            attn = [i32, i32, i32, i32, p, p, i32, p, p, p, p, dbl, p, p, p, i32]
             lib.orc_verify_attn.argtypes = attn
             lib.orc_verify_attn.restype = i32
             lib.orc_verify_attn_online.argtypes = attn + [i32]
@@ -91,7 +91,7 @@ def e4m3_to_f64(bits: int) -> float:
     return _load().orc_e4m3_to_f64(int(bits))
 
 
-def _attn_args(q, k, v, seq_lens, draft_len, kv_scale, Hq, Hkv, d, scale, units):
+def _attn_args(q, k, v, seq_lens, draft_len, kv_scale, Hq, Hkv, d, scale, units, rows_sel):
     q = np.ascontiguousarray(q, dtype=np.uint16)
     fp8 = k.dtype == np.uint8
     k = np.ascontiguousarray(k)
@@ -113,24 +113,31 @@ def _attn_args(q, k, v, seq_lens, draft_len, kv_scale, Hq, Hkv, d, scale, units)
         for (b, g) in units:
             mask[b * Hkv + g] = 1
     rows = int(np.sum(draft_len.astype(np.int64) + 1))
+    rmask = None
+    if rows_sel is not None:
+        rmask = np.ascontiguousarray(rows_sel, dtype=np.uint8).reshape(-1)
+        if rmask.size != rows * Hq:
+            raise ValueError("row selection must have sum(1 + D_b) * Hq entries")
     kv_rows = int(np.sum(seq_lens.astype(np.int64) + draft_len + 1))
     if q.size != rows * Hq * d or k.size < kv_rows * Hkv * d or v.size < kv_rows * Hkv * d:
         raise ValueError("array sizes do not match seq_lens / draft_len")
-    return q, k, v, seq_lens, draft_len, kv_scale, float(scale), mask, fp8, B, rows
+    return q, k, v, seq_lens, draft_len, kv_scale, float(scale), mask, rmask, fp8, B, rows
 
 
 def verify_attn(q, k, v, seq_lens, draft_len, *, Hq, Hkv, d, kv_scale=None, scale=None,
-                units=None, nthreads=0, online_tile=0, out=None):
+                units=None, rows=None, nthreads=0, online_tile=0, out=None):
     """fp64 verify attention. q: bf16 bits [sum W, Hq, d]; k, v: bf16 bits or e4m3 codes
-    [sum (T+W), Hkv, d]. Returns fp64 [sum W, Hq, d]; rows of units not listed in
-    ``units`` (an iterable of (b, kv_head)) are NaN."""
-    (q, k, v, seq_lens, draft_len, kv_scale, scale, mask, fp8, B,
-     rows) = _attn_args(q, k, v, seq_lens, draft_len, kv_scale, Hq, Hkv, d, scale, units)
+    [sum (T+W), Hkv, d]. Returns fp64 [sum W, Hq, d]. ``units`` (an iterable of
+    (b, kv_head)) and ``rows`` (a bool array [sum W, Hq]) restrict the outputs computed;
+    the others are NaN."""
+    (q, k, v, seq_lens, draft_len, kv_scale, scale, mask, rmask, fp8, B,
+     rows) = _attn_args(q, k, v, seq_lens, draft_len, kv_scale, Hq, Hkv, d, scale, units,
+                        rows)
     if out is None:
         out = np.full((rows, Hq, d), np.nan, dtype=np.float64)
     lib = _load()
     args = [B, Hq, Hkv, d, _ptr(seq_lens), _ptr(draft_len), int(fp8), _ptr(q), _ptr(k),
-            _ptr(v), _ptr(kv_scale), scale, _ptr(mask), _ptr(out), int(nthreads)]
+            _ptr(v), _ptr(kv_scale), scale, _ptr(mask), _ptr(rmask), _ptr(out), int(nthreads)]
     if online_tile:
         rc = lib.orc_verify_attn_online(*args, int(online_tile))
     else:

@@ -180,7 +180,8 @@ static void row_online(const orc_ctx* c, int b, int h, int i, int tile, double* 
 static int run_attn(int B, int Hq, int Hkv, int d, const int32_t* seq_lens,
                     const int32_t* draft_len, int kv_fp8, const uint16_t* q, const void* k,
                     const void* v, const float* kv_scale, double scale,
-                    const uint8_t* unit_mask, double* out, int nthreads, int tile) {
+                    const uint8_t* unit_mask, const uint8_t* row_mask, double* out,
+                    int nthreads, int tile) {
   orc_ctx c;
   if (setup(&c, B, Hq, Hkv, d, seq_lens, draft_len, kv_fp8, q, k, v, kv_scale, scale)) {
     return 1;
@@ -190,7 +191,12 @@ static int run_attn(int B, int Hq, int Hkv, int d, const int32_t* seq_lens,
     int64_t n = (int64_t)seq_lens[b] + 1 + draft_len[b];
     if (n > max_keys) max_keys = n;
   }
-  const int64_t units = (int64_t)B * Hkv;
+  /* packed query row -> sequence */
+  const int64_t qrows = c.q_off[B];
+  int32_t* row_b = (int32_t*)malloc(sizeof(int32_t) * (size_t)(qrows > 0 ? qrows : 1));
+  for (int b = 0; b < B; ++b)
+    for (int64_t r = c.q_off[b]; r < c.q_off[b + 1]; ++r) row_b[r] = b;
+  const int64_t total = qrows * Hq; /* one task per (query row, head) */
 #ifdef _OPENMP
   if (nthreads <= 0) nthreads = omp_get_max_threads();
 #pragma omp parallel num_threads(nthreads)
@@ -198,48 +204,50 @@ static int run_attn(int B, int Hq, int Hkv, int d, const int32_t* seq_lens,
   {
     double* s = (double*)malloc(sizeof(double) * (size_t)(tile > 0 ? tile : max_keys));
 #ifdef _OPENMP
-#pragma omp for schedule(dynamic, 1)
+#pragma omp for schedule(dynamic, 4)
 #endif
-    for (int64_t u = 0; u < units; ++u) {
-      if (unit_mask && !unit_mask[u]) continue;
-      int b = (int)(u / Hkv), g = (int)(u % Hkv);
-      for (int hl = 0; hl < c.G; ++hl) {
-        int h = g * c.G + hl;
-        for (int i = 0; i <= draft_len[b]; ++i) {
-          double* o = out + ((c.q_off[b] + i) * Hq + h) * (int64_t)d;
-          if (tile > 0)
-            row_online(&c, b, h, i, tile, s, o);
-          else
-            row_materialised(&c, b, h, i, s, o);
-        }
-      }
+    for (int64_t task = 0; task < total; ++task) {
+      if (row_mask && !row_mask[task]) continue;
+      const int64_t qrow = task / Hq;
+      const int h = (int)(task % Hq);
+      const int b = row_b[qrow];
+      if (unit_mask && !unit_mask[(int64_t)b * Hkv + h / c.G]) continue;
+      const int i = (int)(qrow - c.q_off[b]);
+      double* o = out + task * (int64_t)d;
+      if (tile > 0)
+        row_online(&c, b, h, i, tile, s, o);
+      else
+        row_materialised(&c, b, h, i, s, o);
     }
     free(s);
   }
+  free(row_b);
   teardown(&c);
   return 0;
 }
 
-/* Verify attention, materialised softmax. unit_mask [B*Hkv] selects (b, kv-head) units to
- * compute (NULL: all); rows of unselected units are left untouched. kv_fp8 = 0: k/v are
- * bf16 bit patterns; 1: E4M3 codes with kv_scale [2, Hkv]. Returns 0 on success. */
+/* Verify attention, materialised softmax. unit_mask [B*Hkv] selects (b, kv-head) units and
+ * row_mask [sum W * Hq] selects (query row, head) outputs to compute (NULL: all); outputs
+ * not selected are left untouched. kv_fp8 = 0: k/v are bf16 bit patterns; 1: E4M3 codes
+ * with kv_scale [2, Hkv]. Returns 0 on success. */
 int orc_verify_attn(int B, int Hq, int Hkv, int d, const int32_t* seq_lens,
                     const int32_t* draft_len, int kv_fp8, const uint16_t* q, const void* k,
                     const void* v, const float* kv_scale, double scale,
-                    const uint8_t* unit_mask, double* out, int nthreads) {
+                    const uint8_t* unit_mask, const uint8_t* row_mask, double* out,
+                    int nthreads) {
   return run_attn(B, Hq, Hkv, d, seq_lens, draft_len, kv_fp8, q, k, v, kv_scale, scale,
-                  unit_mask, out, nthreads, 0);
+                  unit_mask, row_mask, out, nthreads, 0);
 }
 
 /* The same attention through the tile-by-tile online-softmax update (tile >= 1 keys). */
 int orc_verify_attn_online(int B, int Hq, int Hkv, int d, const int32_t* seq_lens,
                            const int32_t* draft_len, int kv_fp8, const uint16_t* q,
                            const void* k, const void* v, const float* kv_scale,
-                           double scale, const uint8_t* unit_mask, double* out,
-                           int nthreads, int tile) {
+                           double scale, const uint8_t* unit_mask, const uint8_t* row_mask,
+                           double* out, int nthreads, int tile) {
   if (tile < 1) return 1;
   return run_attn(B, Hq, Hkv, d, seq_lens, draft_len, kv_fp8, q, k, v, kv_scale, scale,
-                  unit_mask, out, nthreads, tile);
+                  unit_mask, row_mask, out, nthreads, tile);
 }
 
 /* Row-wise argmax, naive loop, first index wins ties (strict '>' keeps the earliest).

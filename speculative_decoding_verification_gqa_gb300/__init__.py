@@ -1,2 +1,13 @@
 """GB300-native speculative-decoding verification: GQA verify attention and greedy
-acceptance as hand-written sm_103a CUDA kernels behind a C ABI (libspecverify.so)."""
+acceptance as hand-written sm_103a CUDA kernels behind a C ABI (libspecverify.so).
+
+Python entry points (argument marshalling over the C ABI; see ``api``):
+``spec_verify_attn``, ``spec_accept``, ``workspace_status``.
+"""
+from .api import (SpecVerifyError, accept_workspace_bytes, load_library, new_workspace,
+                  set_attn_kernel, set_profile_events, spec_accept, spec_verify_attn,
+                  verify_workspace_bytes, workspace_status)
+
+__all__ = ["SpecVerifyError", "accept_workspace_bytes", "load_library", "new_workspace",
+           "set_attn_kernel", "set_profile_events", "spec_accept", "spec_verify_attn",
+           "verify_workspace_bytes", "workspace_status"]

@@ -1,0 +1,222 @@
+"""Thin Python binding of libspecverify.so (ctypes). Argument marshalling only: every
+step of the verification path runs in the library's CUDA kernels; there is no CPU or
+PyTorch fallback, and every call raises if the library is missing or returns an error.
+
+PyTorch supplies device memory and the current stream. Entry points mirror the C ABI in
+include/specverify.h:
+
+* ``spec_verify_attn`` -- GQA verify attention over cached prefix + draft window.
+* ``spec_accept`` -- greedy acceptance (argmax per window row, first mismatch).
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libspecverify.so")
+
+SV_BF16, SV_FP8_E4M3, SV_FP32 = 0, 1, 2
+STATUS = {0: "SV_OK", 1: "SV_ERR_NULL", 2: "SV_ERR_SHAPE", 3: "SV_ERR_DTYPE",
+          4: "SV_ERR_ALIGN", 5: "SV_ERR_WORKSPACE", 6: "SV_ERR_CUDA", 7: "SV_ERR_TIMEOUT",
+          8: "SV_ERR_DEVICE_SHAPE"}
+EXPORTS = ("spec_verify_attn_workspace_size", "spec_verify_attn", "spec_accept_workspace_size",
+           "spec_accept", "sv_workspace_status", "sv_status_string", "sv_set_attn_kernel",
+           "sv_set_profile_events", "sv_version")
+
+
+class SpecVerifyError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__("%s failed: %s (%d)" % (where, STATUS.get(status, "?"), status))
+
+
+class AttnDesc(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("max_draft_len", ctypes.c_int32), ("max_seq_len", ctypes.c_int32),
+                ("q_rows", ctypes.c_int64), ("kv_rows", ctypes.c_int64),
+                ("kv_dtype", ctypes.c_int32), ("softmax_scale", ctypes.c_float)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libspecverify.so (built by ``build.build()``); raises if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError("libspecverify.so is not built (%s); run "
+                               "speculative_decoding_verification_gqa_gb300.build.build()" % path)
+        lib = ctypes.CDLL(path)
+        vp, sz, i32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32
+        lib.spec_verify_attn_workspace_size.argtypes = [ctypes.POINTER(AttnDesc)]
+        lib.spec_verify_attn_workspace_size.restype = sz
+        lib.spec_verify_attn.argtypes = [ctypes.POINTER(AttnDesc), vp, vp, vp, vp, vp, vp, vp,
+                                         vp, sz, vp]
+        lib.spec_verify_attn.restype = ctypes.c_int
+        lib.spec_accept_workspace_size.argtypes = [i32, i32, i32]
+        lib.spec_accept_workspace_size.restype = sz
+        lib.spec_accept.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        lib.spec_accept.restype = ctypes.c_int
+        lib.sv_workspace_status.argtypes = [vp, ctypes.c_int, vp]
+        lib.sv_workspace_status.restype = ctypes.c_int
+        lib.sv_status_string.argtypes = [ctypes.c_int]
+        lib.sv_status_string.restype = ctypes.c_char_p
+        lib.sv_set_attn_kernel.argtypes = [ctypes.c_int]
+        lib.sv_set_attn_kernel.restype = ctypes.c_int
+        lib.sv_set_profile_events.argtypes = [vp, vp]
+        lib.sv_set_profile_events.restype = None
+        lib.sv_version.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check(st: int, where: str):
+    if st != 0:
+        raise SpecVerifyError(st, where)
+
+
+def _need(t: torch.Tensor, name: str, dtypes):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError("%s must be a CUDA tensor" % name)
+    if t.dtype not in dtypes:
+        raise TypeError("%s has dtype %s, expected one of %s" % (name, t.dtype, dtypes))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+
+
+def attn_desc(q: torch.Tensor, k_cache: torch.Tensor, batch: int, max_draft_len: int,
+              max_seq_len: int, softmax_scale: float = 0.0) -> AttnDesc:
+    fp8 = k_cache.dtype in (torch.uint8, torch.float8_e4m3fn)
+    return AttnDesc(batch=batch, num_q_heads=q.shape[1], num_kv_heads=k_cache.shape[1],
+                    head_dim=q.shape[2], max_draft_len=max_draft_len, max_seq_len=max_seq_len,
+                    q_rows=q.shape[0], kv_rows=k_cache.shape[0],
+                    kv_dtype=SV_FP8_E4M3 if fp8 else SV_BF16,
+                    softmax_scale=float(softmax_scale))
+
+
+def verify_workspace_bytes(desc: AttnDesc) -> int:
+    n = load_library().spec_verify_attn_workspace_size(ctypes.byref(desc))
+    if n == 0:
+        raise SpecVerifyError(2, "spec_verify_attn_workspace_size")
+    return n
+
+
+def accept_workspace_bytes(batch: int, max_draft_len: int, vocab: int) -> int:
+    n = load_library().spec_accept_workspace_size(batch, max_draft_len, vocab)
+    if n == 0:
+        raise SpecVerifyError(2, "spec_accept_workspace_size")
+    return n
+
+
+def new_workspace(nbytes: int, device=None) -> torch.Tensor:
+    """A zero-filled device workspace (the library's flag word must start at zero)."""
+    return torch.zeros(nbytes, dtype=torch.uint8, device=device or "cuda")
+
+
+def spec_verify_attn(q, k_cache, v_cache, seq_lens, draft_len, *, max_draft_len: int,
+                     max_seq_len: int, kv_scale=None, out=None, workspace=None,
+                     softmax_scale: float = 0.0, stream=None) -> torch.Tensor:
+    """q [rows, Hq, d] bf16; k_cache/v_cache [kv_rows, Hkv, d] bf16, or uint8 /
+    float8_e4m3fn E4M3 codes with kv_scale fp32 [2, Hkv]; seq_lens, draft_len int32 [B].
+    Returns out [rows, Hq, d] bf16 (only the packed rows sum_b (1 + D_b) are written)."""
+    _need(q, "q", (torch.bfloat16,))
+    _need(k_cache, "k_cache", (torch.bfloat16, torch.uint8, torch.float8_e4m3fn))
+    _need(v_cache, "v_cache", (k_cache.dtype,))
+    _need(seq_lens, "seq_lens", (torch.int32,))
+    _need(draft_len, "draft_len", (torch.int32,))
+    if kv_scale is not None:
+        _need(kv_scale, "kv_scale", (torch.float32,))
+    if q.dim() != 3 or k_cache.dim() != 3 or v_cache.shape != k_cache.shape:
+        raise ValueError("q must be [rows, Hq, d], k/v caches [kv_rows, Hkv, d]")
+    desc = attn_desc(q, k_cache, seq_lens.shape[0], max_draft_len, max_seq_len, softmax_scale)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", (torch.bfloat16,))
+    if out.shape != q.shape:
+        raise ValueError("out must have q's shape")
+    if workspace is None:
+        workspace = new_workspace(verify_workspace_bytes(desc), q.device)
+    st = load_library().spec_verify_attn(
+        ctypes.byref(desc), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens),
+        _ptr(draft_len), _ptr(kv_scale), _ptr(out), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "spec_verify_attn")
+    return out
+
+
+def spec_accept(logits, draft_tokens, draft_len, *, max_draft_len: int, accept_len=None,
+                next_token=None, target_tokens=None, workspace=None, stream=None):
+    """logits [sum (1 + D_b), V] bf16 or fp32; draft_tokens int32 [sum D_b]; draft_len int32
+    [B]. Returns (accept_len, next_token), int32 [B] each; fills ``target_tokens`` (int32
+    [sum (1 + D_b)]) with the target's greedy token per row when it is given."""
+    _need(logits, "logits", (torch.bfloat16, torch.float32))
+    _need(draft_tokens, "draft_tokens", (torch.int32,))
+    _need(draft_len, "draft_len", (torch.int32,))
+    B = draft_len.shape[0]
+    V = logits.shape[-1]
+    if accept_len is None:
+        accept_len = torch.empty(B, dtype=torch.int32, device=logits.device)
+    if next_token is None:
+        next_token = torch.empty(B, dtype=torch.int32, device=logits.device)
+    for t, n in ((accept_len, "accept_len"), (next_token, "next_token")):
+        _need(t, n, (torch.int32,))
+    if target_tokens is not None:
+        _need(target_tokens, "target_tokens", (torch.int32,))
+    if workspace is None:
+        workspace = new_workspace(accept_workspace_bytes(B, max_draft_len, V), logits.device)
+    dt = SV_BF16 if logits.dtype == torch.bfloat16 else SV_FP32
+    dtok = draft_tokens if draft_tokens.numel() > 0 else None
+    st = load_library().spec_accept(
+        B, max_draft_len, V, dt, _ptr(logits), _ptr(dtok), _ptr(draft_len), _ptr(accept_len),
+        _ptr(next_token), _ptr(target_tokens), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "spec_accept")
+    return accept_len, next_token
+
+
+def workspace_status(workspace: torch.Tensor, clear: bool = False, stream=None) -> int:
+    """Synchronises and returns the workspace's sticky device-side status (0 = ok)."""
+    return load_library().sv_workspace_status(_ptr(workspace), int(clear), _stream(stream))
+
+
+def set_attn_kernel(which: int) -> int:
+    """0 automatic, 1 mma.sync kernel, 2 tcgen05 kernel. Returns the previous choice."""
+    prev = load_library().sv_set_attn_kernel(int(which))
+    if prev < 0:
+        raise ValueError("attention kernel %d is not available" % which)
+    return prev
+
+
+def set_profile_events(start=None, stop=None):
+    """Record CUDA events around the main attention kernel of later calls (None: off)."""
+    lib = load_library()
+    if start is None or stop is None:
+        lib.sv_set_profile_events(None, None)
+    else:
+        lib.sv_set_profile_events(ctypes.c_void_p(start.cuda_event),
+                                  ctypes.c_void_p(stop.cuda_event))
+
+
+def default_scale(head_dim: int) -> float:
+    return 1.0 / math.sqrt(head_dim)

@@ -1,0 +1,211 @@
+// api.cu -- the C ABI of libspecverify: argument checks, workspace layout, launches.
+// Every entry point is declared and documented in include/specverify.h.
+#include <math.h>
+#include <stdint.h>
+
+#include "internal.cuh"
+
+using namespace sv;
+
+namespace {
+
+int g_attn_kernel = 0;  // 0 automatic, 1 mma.sync, 2 tcgen05
+cudaEvent_t g_ev_start = nullptr;
+cudaEvent_t g_ev_stop = nullptr;
+
+int current_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
+
+sv_status check_desc(const sv_attn_desc* d) {
+  if (!d) return SV_ERR_NULL;
+  if (d->batch < 0 || d->num_kv_heads < 1 || d->num_q_heads < 1 ||
+      d->num_q_heads % d->num_kv_heads != 0 || d->num_q_heads > 4096 ||
+      d->max_draft_len < 0 || d->max_draft_len > 255 || d->max_seq_len < 0 ||
+      d->q_rows < 0 || d->kv_rows < 0)
+    return SV_ERR_SHAPE;
+  if (d->head_dim != 64 && d->head_dim != 128) return SV_ERR_SHAPE;
+  if (!(d->softmax_scale >= 0.f) || isinf(d->softmax_scale)) return SV_ERR_SHAPE;
+  if (d->kv_dtype != SV_BF16 && d->kv_dtype != SV_FP8_E4M3) return SV_ERR_DTYPE;
+  return SV_OK;
+}
+
+AttnWs layout_for(const sv_attn_desc* d, int sms) {
+  return attn_ws_layout(d->batch, d->num_kv_heads, d->num_q_heads / d->num_kv_heads,
+                        d->head_dim, d->max_draft_len, sms);
+}
+
+// 1 = mma.sync, 2 = tcgen05
+int pick_kernel(const sv_attn_desc* d) {
+  if (g_attn_kernel == 1) return 1;
+  if (g_attn_kernel == 2) return attn_tc_available() ? 2 : 1;
+  (void)d;
+  return attn_tc_available() ? 2 : 1;
+}
+
+}  // namespace
+
+extern "C" {
+
+SV_API int sv_version(void) { return 100; }
+
+SV_API const char* sv_status_string(sv_status s) {
+  switch (s) {
+    case SV_OK: return "ok";
+    case SV_ERR_NULL: return "null pointer";
+    case SV_ERR_SHAPE: return "invalid shape";
+    case SV_ERR_DTYPE: return "unsupported dtype";
+    case SV_ERR_ALIGN: return "misaligned pointer";
+    case SV_ERR_WORKSPACE: return "workspace too small";
+    case SV_ERR_CUDA: return "CUDA error";
+    case SV_ERR_TIMEOUT: return "device-side wait timed out";
+    case SV_ERR_DEVICE_SHAPE: return "device-side length check failed";
+  }
+  return "unknown status";
+}
+
+SV_API int sv_set_attn_kernel(int which) {
+  if (which < 0 || which > 2) return -1;
+  if (which == 2 && !attn_tc_available()) return -1;
+  const int prev = g_attn_kernel;
+  g_attn_kernel = which;
+  return prev;
+}
+
+SV_API void sv_set_profile_events(void* start_event, void* stop_event) {
+  if (start_event && stop_event) {
+    g_ev_start = (cudaEvent_t)start_event;
+    g_ev_stop = (cudaEvent_t)stop_event;
+  } else {
+    g_ev_start = g_ev_stop = nullptr;
+  }
+}
+
+SV_API size_t spec_verify_attn_workspace_size(const sv_attn_desc* desc) {
+  if (check_desc(desc) != SV_OK) return 0;
+  const int sms = current_sms();
+  if (sms <= 0) return 0;
+  return layout_for(desc, sms).total;
+}
+
+SV_API sv_status spec_verify_attn(const sv_attn_desc* desc, const void* q, const void* k_cache,
+                                  const void* v_cache, const int32_t* seq_lens,
+                                  const int32_t* draft_len, const float* kv_scale, void* out,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
+  sv_status st = check_desc(desc);
+  if (st != SV_OK) return st;
+  if (desc->batch == 0) return SV_OK;
+  if (!q || !k_cache || !v_cache || !seq_lens || !draft_len || !out || !workspace)
+    return SV_ERR_NULL;
+  const bool fp8 = desc->kv_dtype == SV_FP8_E4M3;
+  if (fp8 && !kv_scale) return SV_ERR_NULL;
+  if (!fp8 && kv_scale) return SV_ERR_SHAPE;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+      !aligned(workspace, 256) || !aligned(seq_lens, 4) || !aligned(draft_len, 4) ||
+      (kv_scale && !aligned(kv_scale, 4)))
+    return SV_ERR_ALIGN;
+  const int sms = current_sms();
+  if (sms <= 0) return SV_ERR_CUDA;
+  const AttnWs lay = layout_for(desc, sms);
+  if (workspace_bytes < lay.total) return SV_ERR_WORKSPACE;
+
+  const int which = pick_kernel(desc);
+  const int kt = which == 2 ? attn_tc_kt() : attn_mma_kt();
+  const int G = desc->num_q_heads / desc->num_kv_heads;
+  const int64_t rows_per_kv = (int64_t)G * (1 + desc->max_draft_len);
+  const int64_t max_tiles = (int64_t)desc->batch * desc->num_kv_heads * ((rows_per_kv + MT - 1) / MT) *
+                            ((desc->max_seq_len + 1 + desc->max_draft_len + kt - 1) / kt);
+
+  uint8_t* ws = (uint8_t*)workspace;
+  AttnParams p;
+  p.q = q;
+  p.k = k_cache;
+  p.v = v_cache;
+  p.out = out;
+  p.kv_scale = kv_scale;
+  p.seq_lens = seq_lens;
+  p.draft_len = draft_len;
+  p.flags = (uint32_t*)(ws + lay.ctrl);
+  p.hdr = (PlanHdr*)(ws + lay.hdr);
+  p.q_off = (int64_t*)(ws + lay.q_off);
+  p.kv_off = (int64_t*)(ws + lay.kv_off);
+  p.units = (int4*)(ws + lay.units);
+  p.ubeg = (int32_t*)(ws + lay.ubeg);
+  p.part_o = (float*)(ws + lay.part_o);
+  p.part_ml = (float2*)(ws + lay.part_ml);
+  p.B = desc->batch;
+  p.Hq = desc->num_q_heads;
+  p.Hkv = desc->num_kv_heads;
+  p.G = G;
+  p.d = desc->head_dim;
+  p.max_draft = desc->max_draft_len;
+  p.max_seq = desc->max_seq_len;
+  p.q_rows = desc->q_rows;
+  p.kv_rows = desc->kv_rows;
+  p.max_units = max_units_for(p.B, p.Hkv, G, p.max_draft);
+  p.n_ctas = (int)(max_tiles < sms ? (max_tiles > 0 ? max_tiles : 1) : sms);
+  const float scale = desc->softmax_scale > 0.f ? desc->softmax_scale
+                                                : 1.f / sqrtf((float)desc->head_dim);
+  p.scale_log2 = scale * 1.4426950408889634f;
+
+  cudaStream_t s = (cudaStream_t)stream;
+  if (launch_plan(p, kt, s) != cudaSuccess) return SV_ERR_CUDA;
+  if (g_ev_start && cudaEventRecord(g_ev_start, s) != cudaSuccess) return SV_ERR_CUDA;
+  const cudaError_t e = which == 2 ? launch_attn_tc(p, fp8, s) : launch_attn_mma(p, fp8, s);
+  if (e != cudaSuccess) return SV_ERR_CUDA;
+  if (g_ev_stop && cudaEventRecord(g_ev_stop, s) != cudaSuccess) return SV_ERR_CUDA;
+  if (launch_combine(p, s) != cudaSuccess) return SV_ERR_CUDA;
+  return SV_OK;
+}
+
+SV_API size_t spec_accept_workspace_size(int32_t batch, int32_t max_draft_len, int32_t vocab) {
+  if (batch < 0 || max_draft_len < 0 || max_draft_len > 255 || vocab <= 0) return 0;
+  const int sms = current_sms();
+  if (sms <= 0) return 0;
+  return accept_ws_layout(batch, max_draft_len, vocab, sms).total;
+}
+
+SV_API sv_status spec_accept(int32_t batch, int32_t max_draft_len, int32_t vocab,
+                             int32_t logits_dtype, const void* logits,
+                             const int32_t* draft_tokens, const int32_t* draft_len,
+                             int32_t* accept_len, int32_t* next_token, int32_t* target_tokens,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+  if (batch < 0 || max_draft_len < 0 || max_draft_len > 255 || vocab <= 0) return SV_ERR_SHAPE;
+  if (logits_dtype != SV_BF16 && logits_dtype != SV_FP32) return SV_ERR_DTYPE;
+  if (batch == 0) return SV_OK;
+  if (!logits || !draft_len || !accept_len || !next_token || !workspace) return SV_ERR_NULL;
+  if (max_draft_len > 0 && !draft_tokens) return SV_ERR_NULL;
+  const uintptr_t es = logits_dtype == SV_BF16 ? 2 : 4;
+  if (!aligned(logits, es) || !aligned(draft_len, 4) || !aligned(accept_len, 4) ||
+      !aligned(next_token, 4) || (draft_tokens && !aligned(draft_tokens, 4)) ||
+      (target_tokens && !aligned(target_tokens, 4)) || !aligned(workspace, 256))
+    return SV_ERR_ALIGN;
+  const int sms = current_sms();
+  if (sms <= 0) return SV_ERR_CUDA;
+  const AcceptWs lay = accept_ws_layout(batch, max_draft_len, vocab, sms);
+  if (workspace_bytes < lay.total) return SV_ERR_WORKSPACE;
+  const cudaError_t e = launch_accept(batch, max_draft_len, vocab, logits_dtype, logits,
+                                      draft_tokens, draft_len, accept_len, next_token,
+                                      target_tokens, workspace, lay, (cudaStream_t)stream);
+  return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+SV_API sv_status sv_workspace_status(void* workspace, int clear, void* stream) {
+  if (!workspace) return SV_ERR_NULL;
+  cudaStream_t s = (cudaStream_t)stream;
+  uint32_t flags = 0;
+  if (cudaMemcpyAsync(&flags, workspace, sizeof flags, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return SV_ERR_CUDA;
+  if (clear && cudaMemsetAsync(workspace, 0, sizeof flags, s) != cudaSuccess) return SV_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return SV_ERR_CUDA;
+  if (flags & FLAG_TIMEOUT) return SV_ERR_TIMEOUT;
+  if (flags & (FLAG_ATTN_SHAPE | FLAG_ACCEPT_SHAPE)) return SV_ERR_DEVICE_SHAPE;
+  return SV_OK;
+}
+
+}  // extern "C"

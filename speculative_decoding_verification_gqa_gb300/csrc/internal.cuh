@@ -1,0 +1,117 @@
+// internal.cuh -- shared declarations of libspecverify's kernels and host code.
+//
+// Work decomposition of verify attention (plan, attention, combine):
+//   unit  = (sequence b, KV head g, row tile mt): up to 128 of the G*(1+D_b) query rows
+//           that share KV head g ("GQA", "GPU and LLM, chapter 5"; guideline 2 of the
+//           co-design summary: G*(1+D) rows per KV head, M = 128 fills a tile).
+//   tile  = KT consecutive cache positions of one unit's key range 0 .. T_b + D_b.
+//   Units are laid end to end on one global tile line; persistent CTA c processes the
+//   contiguous range [c*TT/C, (c+1)*TT/C) of it, so every CTA gets the same number of
+//   tiles (to within one) whatever the mix of lengths. A CTA that covers a whole unit
+//   writes the normalised output itself; otherwise each CTA covering part of the unit
+//   writes a partial (O unnormalised, running max m, running sum l) to slot c + u and the
+//   combine kernel merges them with the same rescaling rule as the online softmax.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/specverify.h"
+
+namespace sv {
+
+constexpr uint32_t FLAG_ATTN_SHAPE = 1u;
+constexpr uint32_t FLAG_TIMEOUT = 2u;
+constexpr uint32_t FLAG_ACCEPT_SHAPE = 4u;
+
+constexpr int MT = 128;  // query rows per unit (one tensor-core M tile)
+
+// Plan header written by the plan kernel.
+struct PlanHdr {
+  int32_t num_units;
+  int32_t total_tiles;
+  int32_t kt;
+  int32_t pad0;
+  int64_t sum_w;
+  int64_t sum_kv;
+};
+
+// Byte offsets inside a spec_verify_attn workspace.
+struct AttnWs {
+  size_t ctrl, hdr, q_off, kv_off, units, ubeg, part_o, part_ml, total;
+};
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline int max_units_for(int B, int Hkv, int G, int max_draft) {
+  const int rows = G * (1 + max_draft);
+  return B * Hkv * ((rows + MT - 1) / MT);
+}
+
+inline AttnWs attn_ws_layout(int B, int Hkv, int G, int d, int max_draft, int n_ctas) {
+  AttnWs w;
+  const size_t U = (size_t)max_units_for(B, Hkv, G, max_draft);
+  const size_t slots = (size_t)n_ctas + U;
+  size_t o = 0;
+  w.ctrl = o;    o += 256;
+  w.hdr = o;     o += 256;
+  w.q_off = o;   o = align_up(o + sizeof(int64_t) * (B + 1), 256);
+  w.kv_off = o;  o = align_up(o + sizeof(int64_t) * (B + 1), 256);
+  w.units = o;   o = align_up(o + sizeof(int4) * U, 256);
+  w.ubeg = o;    o = align_up(o + sizeof(int32_t) * (U + 1), 256);
+  w.part_o = o;  o = align_up(o + sizeof(float) * slots * MT * d, 256);
+  w.part_ml = o; o = align_up(o + sizeof(float2) * slots * MT, 256);
+  w.total = o;
+  return w;
+}
+
+struct AttnParams {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* out;
+  const float* kv_scale;      // [2, Hkv] or nullptr
+  const int32_t* seq_lens;    // [B]
+  const int32_t* draft_len;   // [B]
+  uint32_t* flags;            // workspace control word
+  PlanHdr* hdr;
+  int64_t* q_off;             // [B+1]
+  int64_t* kv_off;            // [B+1]
+  int4* units;                // [U] (b, kv head, row tile, tiles in the unit)
+  int32_t* ubeg;              // [U+1] first global tile of each unit
+  float* part_o;              // [slots, MT, d]
+  float2* part_ml;            // [slots, MT] (m in log2 units, l)
+  int B, Hq, Hkv, G, d;
+  int max_draft, max_seq;
+  int64_t q_rows, kv_rows;
+  int max_units;
+  int n_ctas;
+  float scale_log2;           // softmax_scale * log2(e)
+};
+
+// First CTA whose tile range contains global tile t (ranges [c*TT/C, (c+1)*TT/C)).
+__host__ __device__ inline int cta_of_tile(int64_t t, int64_t TT, int C) {
+  return (int)(((t + 1) * (int64_t)C - 1) / TT);
+}
+
+// Launchers (each returns the cudaGetLastError() of its launch).
+cudaError_t launch_plan(const AttnParams& p, int kt, cudaStream_t s);
+cudaError_t launch_combine(const AttnParams& p, cudaStream_t s);
+cudaError_t launch_attn_mma(const AttnParams& p, bool fp8, cudaStream_t s);
+int attn_mma_kt();
+bool attn_tc_available();
+int attn_tc_kt();
+cudaError_t launch_attn_tc(const AttnParams& p, bool fp8, cudaStream_t s);
+
+// Acceptance.
+struct AcceptWs {
+  size_t ctrl, part, total;
+  int splits;
+};
+AcceptWs accept_ws_layout(int B, int max_draft, int vocab, int num_sms);
+cudaError_t launch_accept(int B, int max_draft, int vocab, int dtype, const void* logits,
+                          const int32_t* draft_tokens, const int32_t* draft_len,
+                          int32_t* accept_len, int32_t* next_token, int32_t* target_tokens,
+                          void* ws, const AcceptWs& lay, cudaStream_t s);
+
+}  // namespace sv

@@ -1,0 +1,178 @@
+// plan_combine.cu -- the two small kernels around verify attention.
+//
+// plan:    per-sequence offsets of the packed layout, the unit list and each unit's first
+//          tile on the global tile line; device-side length checks.
+// combine: merges the split-KV partials of one unit. For partials s with running max m_s,
+//          sum l_s and unnormalised output O_s: m* = max m_s, l* = sum l_s 2^(m_s - m*),
+//          O* = sum O_s 2^(m_s - m*) / l*. This is the online-softmax update of
+//          "GPU and LLM, chapter 5", "Online softmax", applied across key ranges instead
+//          of across tiles (log2 units: the scores were pre-multiplied by log2(e)).
+#include <cuda_bf16.h>
+
+#include "internal.cuh"
+
+namespace sv {
+
+// Exclusive scan of one int64 per thread over a 1024-thread block.
+__device__ int64_t block_excl_scan(int64_t v, int64_t* s_warp, int64_t* total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int nw = blockDim.x >> 5;
+  int64_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_warp[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    int64_t w = lane < nw ? s_warp[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int64_t y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    s_warp[lane] = w;
+  }
+  __syncthreads();
+  const int64_t excl = x - v + (wid > 0 ? s_warp[wid - 1] : 0);
+  *total = s_warp[nw - 1];
+  __syncthreads();
+  return excl;
+}
+
+__global__ void __launch_bounds__(1024) plan_kernel(AttnParams p, int kt) {
+  __shared__ int64_t s_warp[32];
+  __shared__ int64_t carry[4];
+  __shared__ int bad;
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    carry[0] = carry[1] = carry[2] = carry[3] = 0;
+    bad = 0;
+  }
+  __syncthreads();
+  for (int base = 0; base < p.B; base += blockDim.x) {
+    const int b = base + tid;
+    int64_t w = 0, kvn = 0, nunits = 0, ntiles = 0;
+    int nmt = 0, nt = 0;
+    if (b < p.B) {
+      const int T = p.seq_lens[b], D = p.draft_len[b];
+      if (T < 0 || T > p.max_seq || D < 0 || D > p.max_draft) {
+        bad = 1;
+      } else {
+        w = 1 + D;
+        kvn = T + w;
+        nmt = (int)((p.G * w + MT - 1) / MT);
+        nt = (int)((kvn + kt - 1) / kt);
+        nunits = (int64_t)p.Hkv * nmt;
+        ntiles = nunits * nt;
+      }
+    }
+    int64_t tq, tkv, tu, tt;
+    const int64_t eq = block_excl_scan(w, s_warp, &tq);
+    const int64_t ekv = block_excl_scan(kvn, s_warp, &tkv);
+    const int64_t eu = block_excl_scan(nunits, s_warp, &tu);
+    const int64_t et = block_excl_scan(ntiles, s_warp, &tt);
+    if (b < p.B) {
+      p.q_off[b] = carry[0] + eq;
+      p.kv_off[b] = carry[1] + ekv;
+      const int64_t ub = carry[2] + eu, tb = carry[3] + et;
+      for (int g = 0; g < p.Hkv; ++g)
+        for (int mt = 0; mt < nmt; ++mt) {
+          const int64_t u = ub + (int64_t)g * nmt + mt;
+          if (u < p.max_units) {
+            p.units[u] = make_int4(b, g, mt, nt);
+            p.ubeg[u] = (int32_t)(tb + ((int64_t)g * nmt + mt) * nt);
+          }
+        }
+    }
+    __syncthreads();
+    if (tid == 0) {
+      carry[0] += tq;
+      carry[1] += tkv;
+      carry[2] += tu;
+      carry[3] += tt;
+    }
+    __syncthreads();
+  }
+  if (tid == 0) {
+    const bool err = bad || carry[0] > p.q_rows || carry[1] > p.kv_rows ||
+                     carry[2] > p.max_units || carry[3] >= (int64_t)0x7fffffff;
+    p.q_off[p.B] = carry[0];
+    p.kv_off[p.B] = carry[1];
+    p.hdr->sum_w = carry[0];
+    p.hdr->sum_kv = carry[1];
+    p.hdr->kt = kt;
+    if (err) {
+      atomicOr(p.flags, FLAG_ATTN_SHAPE);
+      p.hdr->num_units = 0;
+      p.hdr->total_tiles = 0;
+    } else {
+      p.hdr->num_units = (int32_t)carry[2];
+      p.hdr->total_tiles = (int32_t)carry[3];
+      p.ubeg[carry[2]] = (int32_t)carry[3];
+    }
+  }
+}
+
+cudaError_t launch_plan(const AttnParams& p, int kt, cudaStream_t s) {
+  plan_kernel<<<1, 1024, 0, s>>>(p, kt);
+  return cudaGetLastError();
+}
+
+// One CTA per unit; one warp per query row; lane handles d/32 consecutive columns.
+template <int HD>
+__global__ void __launch_bounds__(256) combine_kernel(AttnParams p) {
+  constexpr int PER = HD / 32;
+  const int u = blockIdx.x;
+  const int nu = p.hdr->num_units;
+  if (u >= nu) return;
+  const int64_t TT = p.hdr->total_tiles;
+  const int64_t ub = p.ubeg[u], ue = p.ubeg[u + 1];
+  const int c_lo = cta_of_tile(ub, TT, p.n_ctas), c_hi = cta_of_tile(ue - 1, TT, p.n_ctas);
+  if (c_lo == c_hi) return;  // one CTA covered the unit and wrote the output itself
+  const int4 info = p.units[u];
+  const int b = info.x, g = info.y, mt = info.z;
+  const int W = 1 + p.draft_len[b];
+  const int rows_total = p.G * W;
+  const int rows = min(MT, rows_total - mt * MT);
+  const int64_t qo = p.q_off[b];
+  const float vs = p.kv_scale ? p.kv_scale[p.Hkv + g] : 1.f;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  for (int r = wid; r < rows; r += blockDim.x >> 5) {
+    float mx = -INFINITY;
+    for (int c = c_lo; c <= c_hi; ++c) mx = fmaxf(mx, p.part_ml[(size_t)(c + u) * MT + r].x);
+    const float muse = mx == -INFINITY ? 0.f : mx;
+    float L = 0.f, acc[PER];
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+    for (int c = c_lo; c <= c_hi; ++c) {
+      const size_t slot = (size_t)(c + u);
+      const float2 ml = p.part_ml[slot * MT + r];
+      const float wgt = exp2f(ml.x - muse);
+      L += ml.y * wgt;
+      const float* src = p.part_o + (slot * MT + r) * HD + lane * PER;
+#pragma unroll
+      for (int e = 0; e < PER; ++e) acc[e] += wgt * src[e];
+    }
+    const float inv = vs / L;
+    const int rg = mt * MT + r;
+    const int i = rg / p.G, hl = rg % p.G;
+    __nv_bfloat16* dst = (__nv_bfloat16*)p.out +
+                         ((qo + i) * p.Hq + (int64_t)g * p.G + hl) * HD + lane * PER;
+#pragma unroll
+    for (int e = 0; e < PER; e += 2)
+      *(__nv_bfloat162*)(dst + e) = __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
+  }
+}
+
+cudaError_t launch_combine(const AttnParams& p, cudaStream_t s) {
+  if (p.max_units <= 0) return cudaSuccess;
+  if (p.d == 128)
+    combine_kernel<128><<<p.max_units, 256, 0, s>>>(p);
+  else
+    combine_kernel<64><<<p.max_units, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace sv

@@ -221,7 +221,7 @@ def accept_inputs(w: Workload, seed: int, draft_len=None, p=None):
     for b, D in enumerate(draft_len.tolist()):
         for j in range(D):
             tgt = int(greedy[q_off + j])
-            if g.random() < p[b]:
+            if g.random() < p[b] or w.V == 1:
                 drafts.append(tgt)
             else:
                 o = int(g.integers(0, w.V - 1))

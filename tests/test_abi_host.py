@@ -1,0 +1,108 @@
+"""The C-ABI library builds, loads without a GPU, exports every symbol the header declares,
+and rejects bad arguments on the host before touching the device. CPU only."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from speculative_decoding_verification_gqa_gb300 import api, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "specverify.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return api.load_library()
+
+
+def declared_symbols():
+    txt = open(HEADER).read()
+    return sorted(set(re.findall(r"^SV_API\s+[\w\s\*]*?\b(\w+)\s*\(", txt, re.M)))
+
+
+def test_header_declares_the_boundary():
+    syms = declared_symbols()
+    for s in ("spec_verify_attn", "spec_accept", "spec_verify_attn_workspace_size",
+              "spec_accept_workspace_size", "sv_workspace_status", "sv_status_string"):
+        assert s in syms
+
+
+def test_exports_every_declared_symbol(lib):
+    for s in declared_symbols():
+        assert hasattr(lib, s), s
+    assert set(api.EXPORTS) <= set(declared_symbols())
+
+
+def test_status_strings(lib):
+    for code in range(9):
+        assert lib.sv_status_string(code)
+    assert lib.sv_status_string(0) == b"ok"
+    assert lib.sv_version() >= 100
+
+
+def _desc(**kw):
+    d = dict(batch=2, num_q_heads=8, num_kv_heads=2, head_dim=128, max_draft_len=3,
+             max_seq_len=100, q_rows=8, kv_rows=208, kv_dtype=0, softmax_scale=0.0)
+    d.update(kw)
+    return api.AttnDesc(**d)
+
+
+FAKE = ctypes.c_void_p(0x10000)  # never dereferenced: checks fail before any launch
+
+
+def _attn(lib, desc, **ptrs):
+    p = dict(q=FAKE, k=FAKE, v=FAKE, T=FAKE, D=FAKE, sc=None, out=FAKE, ws=FAKE)
+    p.update(ptrs)
+    return lib.spec_verify_attn(None if desc is None else ctypes.byref(desc), p["q"], p["k"],
+                                p["v"], p["T"], p["D"], p["sc"], p["out"], p["ws"], 1 << 30,
+                                None)
+
+
+@pytest.mark.parametrize("bad,status", [
+    (dict(num_q_heads=6, num_kv_heads=4), 2),   # Hq % Hkv != 0
+    (dict(head_dim=96), 2),
+    (dict(max_draft_len=-1), 2),
+    (dict(max_draft_len=256), 2),
+    (dict(batch=-1), 2),
+    (dict(kv_dtype=7), 3),
+    (dict(softmax_scale=float("nan")), 2),
+    (dict(softmax_scale=-1.0), 2),
+])
+def test_attn_rejects_bad_descriptors(lib, bad, status):
+    assert _attn(lib, _desc(**bad)) == status
+    assert lib.spec_verify_attn_workspace_size(ctypes.byref(_desc(**bad))) == 0
+
+
+def test_attn_null_and_alignment(lib):
+    assert _attn(lib, None) == 1
+    assert _attn(lib, _desc(), q=None) == 1
+    assert _attn(lib, _desc(), ws=None) == 1
+    assert _attn(lib, _desc(kv_dtype=1)) == 1                 # FP8 needs kv_scale
+    assert _attn(lib, _desc(), sc=FAKE) == 2                  # bf16 must not get scales
+    assert _attn(lib, _desc(), q=ctypes.c_void_p(0x10008)) == 4
+    assert _attn(lib, _desc(), ws=ctypes.c_void_p(0x10010)) == 4
+    assert _attn(lib, _desc(batch=0), q=None) == 0            # empty batch: nothing to do
+
+
+def test_accept_rejects_bad_arguments(lib):
+    f = FAKE
+    assert lib.spec_accept(2, 3, 100, 5, f, f, f, f, f, None, f, 1 << 20, None) == 3
+    assert lib.spec_accept(2, -1, 100, 0, f, f, f, f, f, None, f, 1 << 20, None) == 2
+    assert lib.spec_accept(2, 3, 0, 0, f, f, f, f, f, None, f, 1 << 20, None) == 2
+    assert lib.spec_accept(2, 3, 100, 0, None, f, f, f, f, None, f, 1 << 20, None) == 1
+    assert lib.spec_accept(2, 3, 100, 0, f, None, f, f, f, None, f, 1 << 20, None) == 1
+    assert lib.spec_accept(2, 3, 100, 2, ctypes.c_void_p(0x10002), f, f, f, f, None, f,
+                           1 << 20, None) == 4
+    assert lib.spec_accept(0, 3, 100, 0, None, None, None, None, None, None, None, 0,
+                           None) == 0
+
+
+def test_no_device_means_no_workspace_size(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert lib.spec_verify_attn_workspace_size(ctypes.byref(_desc())) == 0
+    assert lib.spec_accept_workspace_size(2, 3, 100) == 0

@@ -1,0 +1,96 @@
+"""GPU parity of spec_accept against the oracle: bit-exact target tokens, acceptance
+lengths and next tokens, on every workload at full size and on edge cases."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from speculative_decoding_verification_gqa_gb300 import synth
+
+from gpu_util import dev_accept, ensure_built, gpu_accept
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    ensure_built()
+
+
+def _check(a, max_draft=None):
+    al, nt, tgt = gpu_accept(a, max_draft)
+    ral, rnt, ramax = oracle.spec_accept(a["logits"], a["draft_tokens"], a["draft_len"])
+    assert np.array_equal(tgt, ramax)
+    assert np.array_equal(al, ral)
+    assert np.array_equal(nt, rnt)
+    assert np.all(al >= 1) and np.all(al <= a["draft_len"] + 1)
+    return al
+
+
+@pytest.mark.parametrize("cfg", ["c1", "c2", "c3", "c4", "c5"])
+def test_full_size_workloads(cfg):
+    w = synth.CONFIGS[cfg]
+    a = synth.accept_inputs(w, 1)
+    al = _check(a)
+    if cfg != "c1":
+        assert al.max() > 1  # drafts do get accepted
+
+
+@pytest.mark.parametrize("D", synth.C4_SWEEP_D)
+def test_tile_sweep_draft_lengths(D):
+    w = synth.CONFIGS["c4"].with_(B=8)
+    T, Dv, p = synth.lengths(w, 2, D=D)
+    _check(synth.accept_inputs(w, 2, draft_len=Dv, p=p))
+
+
+@pytest.mark.parametrize("V,dtype", [(1, "bf16"), (7, "fp32"), (13, "bf16"), (1001, "bf16"),
+                                     (1001, "fp32"), (32003, "bf16"), (65537, "fp32")])
+def test_ragged_vocab_and_alignment(V, dtype):
+    """V not a multiple of the vector width: rows start at unaligned addresses."""
+    w = synth.Workload("v", B=5, Hq=1, Hkv=1, d=8, D=3, T=1, V=V, p=0.8, logits_dtype=dtype)
+    Dv = np.array([3, 0, 1, 3, 2], dtype=np.int32)
+    _check(synth.accept_inputs(w, 3, draft_len=Dv, p=np.full(5, 0.8)), max_draft=4)
+
+
+def test_ties_and_signed_zero():
+    V = 4099
+    rows = 4
+    logits = np.full((rows, V), -1.0, dtype=np.float32)
+    logits[0, [5, 4000, 4098]] = 3.0
+    logits[1, :] = 0.0
+    logits[1, 2:7] = -0.0
+    logits[2, [17, 4097]] = 2.0
+    logits[3, 4098] = 9.0
+    for dt in ("fp32", "bf16"):
+        lg = logits if dt == "fp32" else synth.bf16_bits(logits)
+        a = dict(logits=lg, draft_tokens=np.array([5, 0, 17], dtype=np.int32),
+                 draft_len=np.array([3], dtype=np.int32))
+        al, nt, tgt = gpu_accept(a)
+        assert list(tgt) == [5, 0, 17, 4098]
+        assert al[0] == 4 and nt[0] == 4098
+
+
+def test_reuse_workspace_and_repeat():
+    import speculative_decoding_verification_gqa_gb300 as sv
+    w = synth.CONFIGS["c2"].with_(B=4)
+    a = synth.accept_inputs(w, 4)
+    lg, dt, dl = dev_accept(a)
+    ws = sv.new_workspace(sv.accept_workspace_bytes(4, 31, w.V))
+    r1 = [t.cpu().clone() for t in sv.spec_accept(lg, dt, dl, max_draft_len=31, workspace=ws)]
+    r2 = [t.cpu().clone() for t in sv.spec_accept(lg, dt, dl, max_draft_len=31, workspace=ws)]
+    assert all(torch.equal(x, y) for x, y in zip(r1, r2))
+    assert sv.workspace_status(ws) == 0
+
+
+def test_device_side_length_check_sets_flag():
+    import speculative_decoding_verification_gqa_gb300 as sv
+    w = synth.Workload("e", B=3, Hq=1, Hkv=1, d=8, D=2, T=1, V=64, p=0.5, logits_dtype="fp32")
+    a = synth.accept_inputs(w, 5)
+    lg, dt, dl = dev_accept(a)
+    ws = sv.new_workspace(sv.accept_workspace_bytes(3, 1, 64))
+    al = torch.full((3,), -7, dtype=torch.int32, device="cuda")
+    nt = torch.full((3,), -7, dtype=torch.int32, device="cuda")
+    sv.spec_accept(lg, dt, dl, max_draft_len=1, accept_len=al, next_token=nt, workspace=ws)
+    assert sv.workspace_status(ws, clear=True) == 8
+    assert (al.cpu() == -7).all() and (nt.cpu() == -7).all()
+    assert sv.workspace_status(ws) == 0
