@@ -42,10 +42,10 @@ AttnWs layout_for(const sv_attn_desc* d, int sms) {
 
 // 1 = mma.sync, 2 = tcgen05
 int pick_kernel(const sv_attn_desc* d) {
+  const bool tc_ok = attn_tc_available() && d->kv_dtype == SV_BF16;
   if (g_attn_kernel == 1) return 1;
-  if (g_attn_kernel == 2) return attn_tc_available() ? 2 : 1;
-  (void)d;
-  return attn_tc_available() ? 2 : 1;
+  if (g_attn_kernel == 2) return tc_ok ? 2 : 1;
+  return tc_ok ? 2 : 1;
 }
 
 }  // namespace

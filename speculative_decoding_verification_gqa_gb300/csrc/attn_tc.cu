@@ -1,13 +1,633 @@
-// attn_tc.cu -- verify attention on the fifth-generation tensor cores (tcgen05).
-// Not built yet: the selector falls back to the mma.sync kernel.
+// attn_tc.cu -- verify attention on the fifth-generation tensor cores (tcgen05, TMEM, TMA).
+//
+// Same work decomposition as the mma.sync kernel (persistent CTAs walking contiguous ranges
+// of the global tile line; see internal.cuh), with 128-key tiles and warp-specialised roles:
+//
+//   warp 0      TMA producer: K and V tiles of one KV head (128 keys x d, bf16, 128-byte
+//               swizzle) into a 3-stage shared-memory ring.
+//   warp 1      MMA issuer (one thread): S = Q K^T into a double-buffered TMEM score tile,
+//               then O += P V into the TMEM accumulator. Q and P are tcgen05 A operands
+//               read straight from TMEM; K (K-major) and V (MN-major) come from shared
+//               memory through UMMA descriptors.
+//   warps 4..7  softmax: thread r owns query row r (TMEM lane r). It writes its Q row into
+//               TMEM once per unit, then per tile reads its 128 scores, applies the scale
+//               and the window-causal mask, updates the running max m and sum l ("GPU and
+//               LLM, chapter 5", "Online softmax"), writes P = 2^(s - m) as bf16 into TMEM,
+//               and at the end normalises O (or stores an unnormalised split partial).
+//
+// The online-softmax rescale O *= 2^(m_old - m_new) is applied lazily: the reference max
+// only moves when the tile max exceeds it by more than 2^8, so P stays below 256 and the
+// exact result is unchanged (numerator and denominator use the same reference).
+//
+// Every mbarrier wait is bounded: on timeout the kernel sets a flag in the workspace,
+// every role leaves its loop, the producer waits (bounded) for its copies in flight, and
+// TMEM is freed before the kernel returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
 #include "internal.cuh"
 
 namespace sv {
+namespace {
 
-bool attn_tc_available() { return false; }
-int attn_tc_kt() { return 128; }
-cudaError_t launch_attn_tc(const AttnParams&, bool, cudaStream_t) {
-  return cudaErrorNotSupported;
+constexpr int KT = 128;          // keys per tile
+constexpr int NS = 3;            // shared-memory ring depth
+constexpr int NTHREADS = 256;
+constexpr int SOFTMAX_WARP0 = 4;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t COL_O = 0, COL_S0 = 128, COL_P = 384, COL_Q = 448;
+constexpr long long TIMEOUT_CYCLES = 4000000000LL;  // ~2 s at 2 GHz
+constexpr float RESCALE_THRESHOLD = 8.f;            // log2 units
+
+struct __align__(8) Bars {
+  uint64_t k_full[NS], v_full[NS], kv_empty[NS];
+  uint64_t s_full[2], s_free[2];
+  uint64_t p_full, o_done, q_full, mma_final;
+  uint32_t tmem_base;
+  int abort;
+  int u0;
+};
+
+__device__ __forceinline__ uint32_t saddr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(b)), "r"(count));
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr(b)) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(saddr(b)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(saddr(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for the phase with the given parity. Returns false (and raises the CTA's
+// abort flag and the workspace timeout flag) if it gives up or another role already did.
+__device__ __noinline__ bool mbar_wait(uint64_t* b, uint32_t parity, volatile int* abort,
+                                       uint32_t* flags) {
+  if (mbar_try(b, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try(b, parity)) return true;
+    if (*abort) return false;
+    if (clock64() - t0 > TIMEOUT_CYCLES) {
+      *abort = 1;
+      atomicOr(flags, FLAG_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint64_t* bar,
+                                            int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"((uint64_t)map), "r"(c0), "r"(c1), "r"(c2), "r"(saddr(bar))
+      : "memory");
+}
+
+// tcgen05 shared-memory matrix descriptor: start address, leading / stride byte offsets,
+// descriptor version 1, 128-byte swizzle.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((addr & 0x3FFFF) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, A K-major,
+// B K-major (b_mn = 0) or MN-major (b_mn = 1), M = 128, N = n.
+__host__ __device__ constexpr uint32_t idesc_bf16(int n, int b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn << 16) |
+         ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate));
+}
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          saddr(bar))
+      : "memory");
+}
+__device__ __forceinline__ void fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+#define SV_R8(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), \
+                 "=r"(r[i + 4]), "=r"(r[i + 5]), "=r"(r[i + 6]), "=r"(r[i + 7])
+#define SV_W8(i) "r"(r[i]), "r"(r[i + 1]), "r"(r[i + 2]), "r"(r[i + 3]), \
+                 "r"(r[i + 4]), "r"(r[i + 5]), "r"(r[i + 6]), "r"(r[i + 7])
+
+// 32 consecutive TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : SV_R8(0), SV_R8(8), SV_R8(16), SV_R8(24)
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(
+          taddr),
+      SV_W8(0), SV_W8(8), SV_W8(16), SV_W8(24)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+// Ties registers written by tcgen05.ld to a point after tcgen05.wait::ld, so the compiler
+// cannot move their first use above the wait.
+__device__ __forceinline__ void reg_fence32(uint32_t* r) {
+  asm volatile("" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+               "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+               "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
+               "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+               "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
+               "+r"(r[30]), "+r"(r[31]));
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+struct Seg {
+  int u, b, g, mt, nt, j0, j1;
+};
+
+// Next (unit, tile range) of this CTA's contiguous range of the global tile line.
+__device__ __forceinline__ bool seg_next(const AttnParams& p, int num_units, int64_t& t,
+                                         int64_t t_end, int& u, Seg& s) {
+  if (t >= t_end || u >= num_units) return false;
+  const int4 info = p.units[u];
+  const int64_t ub = p.ubeg[u];
+  s.u = u;
+  s.b = info.x;
+  s.g = info.y;
+  s.mt = info.z;
+  s.nt = info.w;
+  s.j0 = (int)(t - ub);
+  s.j1 = (int)(min(t_end, ub + info.w) - ub);
+  if (s.j1 <= s.j0) return false;
+  t = ub + s.j1;
+  ++u;
+  return true;
+}
+
+template <int HD>
+struct TcLayout {
+  static constexpr int BLK = KT * 128;            // one 64-column block of a 128-key tile
+  static constexpr int NBLK = HD / 64;            // column blocks per tile
+  static constexpr int TILE = KT * HD * 2;        // one K or V tile (bf16)
+  static constexpr int STAGE = 2 * TILE;          // K then V
+  static constexpr int BARS = NS * STAGE;         // offset of the barrier block
+  static constexpr size_t SMEM = (size_t)BARS + sizeof(Bars) + 1024;  // + alignment slack
+};
+
+template <int HD>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    attn_tc_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmk,
+                   const __grid_constant__ CUtensorMap tmv) {
+  using L = TcLayout<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  Bars* bars = (Bars*)(smem + L::BARS);
+  volatile int* abort = &bars->abort;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  const int TT = p.hdr->total_tiles;
+  const int num_units = p.hdr->num_units;
+  const int C = p.n_ctas;
+  const int64_t t_begin = (int64_t)blockIdx.x * TT / C;
+  const int64_t t_end = (int64_t)(blockIdx.x + 1) * TT / C;
+  if (TT == 0 || t_begin >= t_end) return;  // uniform across the CTA
+
+  if (tid == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->kv_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->s_full[s], 1);
+      mbar_init(&bars->s_free[s], 128);
+    }
+    mbar_init(&bars->p_full, 128);
+    mbar_init(&bars->o_done, 1);
+    mbar_init(&bars->q_full, 128);
+    mbar_init(&bars->mma_final, 1);
+    bars->abort = 0;
+    int lo = 0, hi = num_units - 1;  // last unit whose first tile is <= t_begin
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.ubeg[mid] <= t_begin) lo = mid; else hi = mid - 1;
+    }
+    bars->u0 = lo;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     saddr(&bars->tmem_base)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  const int u_first = bars->u0;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmk) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmv) : "memory");
+      int64_t t = t_begin;
+      int u = u_first;
+      Seg s;
+      uint32_t it = 0;
+      bool ok = true;
+      while (ok && seg_next(p, num_units, t, t_end, u, s)) {
+        const int row0 = (int)p.kv_off[s.b];
+        for (int j = s.j0; j < s.j1; ++j, ++it) {
+          const uint32_t st = it % NS;
+          if (it >= NS && !mbar_wait(&bars->kv_empty[st], ((it / NS) - 1) & 1, abort, p.flags)) {
+            ok = false;
+            break;
+          }
+          const uint32_t kdst = saddr(smem + st * L::STAGE);
+          const uint32_t vdst = kdst + L::TILE;
+          mbar_expect_tx(&bars->k_full[st], L::TILE);
+#pragma unroll
+          for (int c = 0; c < L::NBLK; ++c)
+            tma_load_3d(kdst + c * L::BLK, &tmk, &bars->k_full[st], c * 64, s.g, row0 + j * KT);
+          mbar_expect_tx(&bars->v_full[st], L::TILE);
+#pragma unroll
+          for (int c = 0; c < L::NBLK; ++c)
+            tma_load_3d(vdst + c * L::BLK, &tmv, &bars->v_full[st], c * 64, s.g, row0 + j * KT);
+        }
+      }
+      if (!ok || *abort) {
+        // leave no copy in flight: wait (bounded) for the last fill of every stage
+        for (uint32_t st = 0; st < NS && st < it; ++st) {
+          const uint32_t fills = (it - 1 - st) / NS + 1;
+          const uint32_t par = (fills - 1) & 1;
+          const long long t0 = clock64();
+          while (!(mbar_try(&bars->k_full[st], par) && mbar_try(&bars->v_full[st], par)) &&
+                 clock64() - t0 < TIMEOUT_CYCLES) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t ID_S = idesc_bf16(KT, 0);
+      constexpr uint32_t ID_PV = idesc_bf16(HD, 1);
+      int64_t t = t_begin;
+      int u = u_first;
+      Seg s;
+      uint32_t it = 0, seg_i = 0;
+      bool ok = true;
+      auto issue_pv = [&](uint32_t itp, bool first) -> bool {
+        const uint32_t st = itp % NS;
+        if (!mbar_wait(&bars->p_full, itp & 1, abort, p.flags)) return false;
+        if (!mbar_wait(&bars->v_full[st], (itp / NS) & 1, abort, p.flags)) return false;
+        fence_after();
+        const uint32_t vbase = saddr(smem + st * L::STAGE + L::TILE);
+#pragma unroll
+        for (int kk = 0; kk < KT / 16; ++kk) {
+          // V: MN-major, 64-column blocks L::BLK apart (LBO), 8-key groups 1024 B apart (SBO)
+          const uint64_t bd = smem_desc(vbase + kk * 16 * 128, L::BLK, 1024);
+          mma_ts(tmem + COL_O, tmem + COL_P + kk * 8, bd, ID_PV, (first && kk == 0) ? 0u : 1u);
+        }
+        mma_commit(&bars->o_done);
+        mma_commit(&bars->kv_empty[st]);
+        return true;
+      };
+      while (ok && seg_next(p, num_units, t, t_end, u, s)) {
+        if (!mbar_wait(&bars->q_full, seg_i & 1, abort, p.flags)) break;
+        fence_after();
+        for (int j = s.j0; j < s.j1; ++j, ++it) {
+          const uint32_t st = it % NS, sb = it & 1;
+          if (!mbar_wait(&bars->k_full[st], (it / NS) & 1, abort, p.flags) ||
+              (it >= 2 && !mbar_wait(&bars->s_free[sb], ((it >> 1) - 1) & 1, abort, p.flags))) {
+            ok = false;
+            break;
+          }
+          fence_after();
+          const uint32_t kbase = saddr(smem + st * L::STAGE);
+#pragma unroll
+          for (int kk = 0; kk < HD / 16; ++kk) {
+            // K: K-major, 128-byte rows, 8-row groups 1024 B apart; 32 B per 16-element step
+            const uint64_t bd = smem_desc(kbase + (kk >> 2) * L::BLK + (kk & 3) * 32, 16, 1024);
+            mma_ts(tmem + COL_S0 + sb * 128, tmem + COL_Q + kk * 8, bd, ID_S, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&bars->s_full[sb]);
+          if (j > s.j0 && !issue_pv(it - 1, j - 1 == s.j0)) {
+            ok = false;
+            break;
+          }
+        }
+        if (!ok || !issue_pv(it - 1, s.j1 - 1 == s.j0)) break;
+        ++seg_i;
+      }
+      mma_commit(&bars->mma_final);
+      const long long t0 = clock64();
+      while (!mbar_try(&bars->mma_final, 0) && clock64() - t0 < TIMEOUT_CYCLES) {
+      }
+    }
+  } else if (warp >= SOFTMAX_WARP0) {
+    // ------------------------------------------------------------ softmax / epilogue
+    const int r = tid - SOFTMAX_WARP0 * 32;  // query row = TMEM lane
+    const uint32_t lane_base = (uint32_t)((warp - SOFTMAX_WARP0) * 32) << 16;
+    const uint32_t tq = tmem + lane_base;
+    // waits agree across the warp, so warp-collective tcgen05.ld/st stay converged
+    auto wwait = [&](uint64_t* bar, uint32_t par) -> bool {
+      return __all_sync(0xffffffffu, mbar_wait(bar, par, abort, p.flags));
+    };
+    int64_t t = t_begin;
+    int u = u_first;
+    Seg s;
+    uint32_t it = 0;
+    bool ok = true;
+    while (ok && seg_next(p, num_units, t, t_end, u, s)) {
+      const int T = p.seq_lens[s.b];
+      const int D = p.draft_len[s.b];
+      const int rows_total = p.G * (D + 1);
+      const int rows = min(MT, rows_total - s.mt * MT);
+      const int nkeys = T + D + 1;
+      const int rg = s.mt * MT + r;
+      const bool live = r < rows;
+      const int i_row = live ? rg / p.G : D;
+      const int hl = live ? rg % p.G : 0;
+      const int64_t qrow = p.q_off[s.b] + i_row;
+      const float sc = p.scale_log2;
+
+      // Q row -> TMEM columns [COL_Q, COL_Q + HD/2) as packed bf16 pairs
+      {
+        const uint4* src = reinterpret_cast<const uint4*>(
+            (const __nv_bfloat16*)p.q + (qrow * p.Hq + (int64_t)s.g * p.G + hl) * HD);
+#pragma unroll
+        for (int c = 0; c < HD / 64; ++c) {
+          uint32_t rq[32];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const uint4 v = live ? __ldg(src + c * 8 + e) : make_uint4(0, 0, 0, 0);
+            rq[4 * e] = v.x;
+            rq[4 * e + 1] = v.y;
+            rq[4 * e + 2] = v.z;
+            rq[4 * e + 3] = v.w;
+          }
+          tmem_st32(tq + COL_Q + c * 32, rq);
+        }
+        tmem_wait_st();
+        fence_before();
+        mbar_arrive(&bars->q_full);
+      }
+
+      float m_ref = -INFINITY, l = 0.f;
+      for (int j = s.j0; j < s.j1; ++j, ++it) {
+        const uint32_t sb = it & 1;
+        if (!wwait(&bars->s_full[sb], (it >> 1) & 1)) {
+          ok = false;
+          break;
+        }
+        fence_after();
+        float sv[KT];
+        {
+          uint32_t* raw = reinterpret_cast<uint32_t*>(sv);
+#pragma unroll
+          for (int c = 0; c < KT / 32; ++c) tmem_ld32(tq + COL_S0 + sb * 128 + c * 32, raw + c * 32);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < KT / 32; ++c) reg_fence32(raw + c * 32);
+        }
+        fence_before();
+        mbar_arrive(&bars->s_free[sb]);
+
+        const int key0 = j * KT;
+        const bool edge = key0 + KT - 1 > T;
+        float mt = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < KT; ++c) {
+          float x = sv[c] * sc;
+          if (edge && key0 + c > T + i_row) x = -INFINITY;
+          sv[c] = x;
+          mt = fmaxf(mt, x);
+        }
+        if (j > s.j0) {
+          if (!wwait(&bars->o_done, (it - 1) & 1)) {
+            ok = false;
+            break;
+          }
+          fence_after();
+        }
+        if (m_ref == -INFINITY) {
+          m_ref = mt;  // O holds nothing yet for this row (zeros or about to be overwritten)
+        } else if (mt > m_ref + RESCALE_THRESHOLD) {
+          const float alpha = ex2(m_ref - mt);
+          l *= alpha;
+          m_ref = mt;
+#pragma unroll 1
+          for (int c = 0; c < HD / 32; ++c) {
+            uint32_t ro[32];
+            tmem_ld32(tq + COL_O + c * 32, ro);
+            tmem_wait_ld();
+            reg_fence32(ro);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) ro[e] = __float_as_uint(__uint_as_float(ro[e]) * alpha);
+            tmem_st32(tq + COL_O + c * 32, ro);
+          }
+          tmem_wait_st();
+        }
+        const float mu = m_ref == -INFINITY ? 0.f : m_ref;
+        float rs = 0.f;
+#pragma unroll
+        for (int c = 0; c < KT; ++c) {
+          sv[c] = ex2(sv[c] - mu);
+          rs += sv[c];
+        }
+        l += rs;
+#pragma unroll
+        for (int c = 0; c < KT / 64; ++c) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) pk[e] = pack_bf16(sv[c * 64 + 2 * e], sv[c * 64 + 2 * e + 1]);
+          tmem_st32(tq + COL_P + c * 32, pk);
+        }
+        tmem_wait_st();
+        if (key0 + KT > nkeys) {
+          // last tile of the sequence: clear the V rows past its end so that P = 0 never
+          // meets non-finite data (they may hold the next sequence or unwritten memory)
+          const uint32_t st = it % NS;
+          if (!wwait(&bars->v_full[st], (it / NS) & 1)) {
+            ok = false;
+            break;
+          }
+          const int first = nkeys - key0;
+          uint8_t* vt = smem + st * L::STAGE + L::TILE;
+          const int chunks = (KT - first) * 8;  // 16-byte chunks per 64-column block
+          for (int q = r; q < chunks * L::NBLK; q += 128) {
+            const int blk = q / chunks, rem = q % chunks;
+            *reinterpret_cast<uint4*>(vt + blk * L::BLK + (first + rem / 8) * 128 + (rem % 8) * 16) =
+                make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async();
+        }
+        fence_before();
+        mbar_arrive(&bars->p_full);
+      }
+      if (!ok) break;
+      if (!wwait(&bars->o_done, (it - 1) & 1)) break;
+      fence_after();
+
+      // ---- epilogue
+      const bool whole = s.j0 == 0 && s.j1 == s.nt;
+      if (whole) {
+        const float inv = 1.f / l;
+        __nv_bfloat16* dst = (__nv_bfloat16*)p.out +
+                             ((p.q_off[s.b] + i_row) * p.Hq + (int64_t)s.g * p.G + hl) * HD;
+#pragma unroll 1
+        for (int c = 0; c < HD / 32; ++c) {
+          uint32_t ro[32];
+          tmem_ld32(tq + COL_O + c * 32, ro);
+          tmem_wait_ld();
+          reg_fence32(ro);
+          if (live) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              pk[e] = pack_bf16(__uint_as_float(ro[2 * e]) * inv, __uint_as_float(ro[2 * e + 1]) * inv);
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              d4[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+          }
+        }
+      } else {
+        const size_t slot = (size_t)blockIdx.x + s.u;
+        float* dst = p.part_o + (slot * MT + r) * HD;
+#pragma unroll 1
+        for (int c = 0; c < HD / 32; ++c) {
+          uint32_t ro[32];
+          tmem_ld32(tq + COL_O + c * 32, ro);
+          tmem_wait_ld();
+          reg_fence32(ro);
+          if (live) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              d4[e] = make_uint4(ro[4 * e], ro[4 * e + 1], ro[4 * e + 2], ro[4 * e + 3]);
+          }
+        }
+        if (live) p.part_ml[slot * MT + r] = make_float2(m_ref, l);
+      }
+      fence_before();  // TMEM reads above complete before the next unit's MMAs
+    }
+  }
+
+  fence_before();
+  __syncthreads();
+  fence_after();
+  if (warp == 1) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+// ---------------------------------------------------------------- host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (EncodeTiledFn)f;
+  }
+  return fn;
+}
+
+// [kv_rows, Hkv, HD] bf16 -> boxes of 64 columns x 1 head x KT rows, 128-byte swizzle.
+bool make_kv_map(CUtensorMap* map, const void* base, int64_t kv_rows, int hkv, int hd) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)hd, (cuuint64_t)hkv, (cuuint64_t)kv_rows};
+  const cuuint64_t strides[2] = {(cuuint64_t)hd * 2, (cuuint64_t)hkv * hd * 2};
+  const cuuint32_t box[3] = {64, 1, KT};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int HD>
+cudaError_t launch_hd(const AttnParams& p, cudaStream_t s) {
+  CUtensorMap mk, mv;
+  if (!make_kv_map(&mk, p.k, p.kv_rows, p.Hkv, HD) || !make_kv_map(&mv, p.v, p.kv_rows, p.Hkv, HD))
+    return cudaErrorInvalidValue;
+  const size_t smem = TcLayout<HD>::SMEM;
+  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<HD>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  attn_tc_kernel<HD><<<p.n_ctas, NTHREADS, smem, s>>>(p, mk, mv);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool attn_tc_available() { return encode_fn() != nullptr; }
+int attn_tc_kt() { return KT; }
+
+cudaError_t launch_attn_tc(const AttnParams& p, bool fp8, cudaStream_t s) {
+  if (fp8 || p.kv_rows <= 0 || p.kv_rows > 0x7fffffffLL) return cudaErrorNotSupported;
+  return p.d == 128 ? launch_hd<128>(p, s) : launch_hd<64>(p, s);
 }
 
 }  // namespace sv

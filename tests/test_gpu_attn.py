@@ -152,3 +152,69 @@ def test_full_size_sampled_units(kernel, cfg, D):
     ma, mr = assert_close(got, ref)
     # every packed row was written with finite values
     assert np.isfinite(bf16_to_f64(got)).all()
+
+
+# ------------------------------------------------------------------ closed forms on the GPU
+
+def _bits(x):
+    return synth.bf16_bits(np.asarray(x, dtype=np.float32))
+
+
+def _run_raw(q, k, v, T, D):
+    x = dict(q=q, k=k, v=v, kv_scale=None, seq_lens=np.asarray(T, dtype=np.int32),
+             draft_len=np.asarray(D, dtype=np.int32))
+    return bf16_to_f64(gpu_attn(x))
+
+
+@pytest.mark.parametrize("T,D", [(300, 9), (250, 15), (127, 1), (0, 31)])
+def test_window_mask_with_dominant_window_keys(kernel, T, D):
+    """Window keys score far above the prefix, so row i averages the V rows of the window
+    keys it may see, positions T..T+i. V column 0 holds the window index j, so row i must
+    return i/2 exactly; a mask off by one key moves it by 0.5."""
+    Hq, Hkv, d = 8, 2, 128
+    W = D + 1
+    q = np.zeros((W, Hq, d), dtype=np.float32)
+    q[:, :, 0] = 4.0
+    k = np.zeros((T + W, Hkv, d), dtype=np.float32)
+    k[T:, :, 0] = 64.0                           # score 4*64/sqrt(128) = 22.6 vs 0
+    vals = np.zeros((T + W, Hkv, d), dtype=np.float32)
+    vals[T:, :, 0] = np.arange(W)[:, None]
+    vals[T:, :, 1] = 1.0
+    out = _run_raw(_bits(q), _bits(k), _bits(vals), [T], [D])
+    for i in range(W):
+        assert np.abs(out[i, :, 0] - i / 2.0).max() <= 0.05, (i, out[i, :, 0])
+        assert np.abs(out[i, :, 1] - 1.0).max() <= 1e-2
+
+
+def test_constant_values_select_the_kv_group(kernel):
+    """V constant per KV head -> query head h returns the constant of KV head h // G."""
+    B, Hq, Hkv, d, T, D = 3, 32, 4, 128, 500, 7
+    rng = np.random.default_rng(1)
+    n_kv = B * (T + D + 1)
+    q = _bits(rng.standard_normal((B * (D + 1), Hq, d)))
+    k = _bits(rng.standard_normal((n_kv, Hkv, d)))
+    c = np.array([1.0, -2.0, 3.5, 0.25], dtype=np.float32)
+    v = _bits(np.broadcast_to(c[None, :, None], (n_kv, Hkv, d)))
+    out = _run_raw(q, k, v, [T] * B, [D] * B)
+    expect = np.repeat(c, Hq // Hkv)[None, :, None]
+    assert np.abs(out - expect).max() <= 1e-2
+
+
+def test_dominant_key_wins(kernel):
+    """One key scoring far above the others returns its V row, for a key in the prefix and
+    for the last window key (which only the last window row may see)."""
+    Hq, Hkv, d, T, D = 4, 1, 64, 700, 3
+    W = D + 1
+    q = np.zeros((W, Hq, d), dtype=np.float32)
+    q[:, :, 0] = 8.0
+    k = np.zeros((T + W, Hkv, d), dtype=np.float32)
+    k[333, 0, 0] = 16.0
+    v = np.random.default_rng(2).standard_normal((T + W, Hkv, d)).astype(np.float32)
+    vb = _bits(v)
+    out = _run_raw(_bits(q), _bits(k), vb, [T], [D])
+    assert np.abs(out - bf16_to_f64(vb)[333, 0][None, None, :]).max() <= 1e-2
+    k2 = np.zeros_like(k)
+    k2[T + D, 0, 0] = 16.0                      # visible to window row D only
+    out2 = _run_raw(_bits(q), _bits(k2), vb, [T], [D])
+    assert np.abs(out2[D] - bf16_to_f64(vb)[T + D, 0][None, :]).max() <= 1e-2
+    assert np.abs(out2[0] - bf16_to_f64(vb)[T + D, 0][None, :]).max() > 0.1
