@@ -139,6 +139,36 @@ SV_API sv_status spec_accept(int32_t batch, int32_t max_draft_len, int32_t vocab
                       int32_t* target_tokens, void* workspace, size_t workspace_bytes,
                       void* stream);
 
+/*
+ * spec_accept_noalloc -- spec_accept without a workspace argument. It has no counterpart
+ * on the pages: it exists for callers that cannot allocate device memory per call, such
+ * as inference engines that reserve all device memory once at start-up and pass each
+ * operator only its inputs and outputs, leaving nowhere to put per-call scratch.
+ *
+ * Arguments, results and device-side checks are those of spec_accept. The scratch lives
+ * in a device array of SV_ACCEPT_NOALLOC_MAX_WORKSPACE bytes compiled into the library:
+ *   - every GPU that loads the library holds that memory until the process exits;
+ *   - a shape whose spec_accept_workspace_size() exceeds it is rejected with
+ *     SV_ERR_WORKSPACE and nothing is launched (512 KiB covers, for example, 65,000
+ *     window rows on a 152-SM GPU);
+ *   - the first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call before any
+ *     stream capture;
+ *   - all calls share the array and it keeps the last call's contents: two calls that can
+ *     run at the same time on the GPU (different streams or host threads) race and may
+ *     return wrong tokens;
+ *   - device-side length errors leave the outputs untouched and cannot be read back
+ *     (there is no workspace to pass to sv_workspace_status): pre-fill accept_len with 0
+ *     to detect them.
+ * Calls no cudaMalloc, cudaFree or allocating routine.
+ */
+#define SV_ACCEPT_NOALLOC_MAX_WORKSPACE (512u * 1024u)
+SV_API sv_status spec_accept_noalloc(int32_t batch, int32_t max_draft_len, int32_t vocab,
+                                     int32_t logits_dtype, const void* logits,
+                                     const int32_t* draft_tokens, const int32_t* draft_len,
+                                     int32_t* accept_len, int32_t* next_token,
+                                     int32_t* target_tokens, void* stream);
+
 /* Synchronises `stream`, then reads the sticky device-side flags of a workspace used by
  * either call: SV_OK, SV_ERR_DEVICE_SHAPE or SV_ERR_TIMEOUT. clear != 0 resets them. */
 SV_API sv_status sv_workspace_status(void* workspace, int clear, void* stream);
