@@ -4,16 +4,18 @@
 // of the global tile line; see internal.cuh), with 128-key tiles and warp-specialised roles:
 //
 //   warp 0      TMA producer: K and V tiles of one KV head (128 keys x d, bf16, 128-byte
-//               swizzle) into a 3-stage shared-memory ring.
+//               swizzle) into a 3-stage shared-memory ring; a stage is released once the
+//               O += P V that reads its V tile has completed.
 //   warp 1      MMA issuer (one thread): S = Q K^T into a double-buffered TMEM score tile,
 //               then O += P V into the TMEM accumulator. Q and P are tcgen05 A operands
 //               read straight from TMEM; K (K-major) and V (MN-major) come from shared
 //               memory through UMMA descriptors.
-//   warps 4..7  softmax: thread r owns query row r (TMEM lane r). It writes its Q row into
-//               TMEM once per unit, then per tile reads its 128 scores, applies the scale
-//               and the window-causal mask, updates the running max m and sum l ("GPU and
-//               LLM, chapter 5", "Online softmax"), writes P = 2^(s - m) as bf16 into TMEM,
-//               and at the end normalises O (or stores an unnormalised split partial).
+//   warps 4..11 softmax, two warpgroups: in each, thread r owns query row r (TMEM lane r)
+//               and one half of the columns. Per unit they write the Q row into TMEM; per
+//               tile they read their 64 scores, apply the scale and the window-causal
+//               mask, exchange half-tile maxima, update the running max m and sum l ("GPU
+//               and LLM, chapter 5", "Online softmax"), and write P = 2^(s - m) as bf16
+//               into TMEM; at the end they normalise O (or store a split partial).
 //
 // The online-softmax rescale O *= 2^(m_old - m_new) is applied lazily: the reference max
 // only moves when the tile max exceeds it by more than 2^8, so P stays below 256 and the
@@ -32,8 +34,9 @@ namespace {
 
 constexpr int KT = 128;          // keys per tile
 constexpr int NS = 3;            // shared-memory ring depth
-constexpr int NTHREADS = 256;
-constexpr int SOFTMAX_WARP0 = 4;
+constexpr int NTHREADS = 384;
+constexpr int SOFTMAX_WARP0 = 4;  // warps 4..7: columns 0..63 of a tile, 8..11: 64..127
+constexpr int NSOFT = 256;        // softmax threads (two warpgroups)
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_O = 0, COL_S0 = 128, COL_P = 384, COL_Q = 448;
 constexpr long long TIMEOUT_CYCLES = 4000000000LL;  // ~2 s at 2 GHz
@@ -46,6 +49,8 @@ struct __align__(8) Bars {
   uint32_t tmem_base;
   int abort;
   int u0;
+  float xmax[2][2][128];  // [tile parity][warpgroup][row]: half-tile row maxima
+  float xl[2][128];       // [warpgroup][row]: half sums at the end of a unit
 };
 
 __device__ __forceinline__ uint32_t saddr(const void* p) {
@@ -175,6 +180,20 @@ __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// Named barrier 1 over the 256 softmax threads with an AND of `v`: the two warpgroups meet
+// here once per tile (and once per unit epilogue), and a failed wait in either one makes
+// both leave together, so neither can be left waiting at the barrier.
+__device__ __forceinline__ bool softmax_pair_and(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, 1, 256, p;\n"
+      " selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)v)
+      : "memory");
+  return r != 0;
+}
+
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -244,11 +263,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->s_full[s], 1);
-      mbar_init(&bars->s_free[s], 128);
+      mbar_init(&bars->s_free[s], NSOFT);
     }
-    mbar_init(&bars->p_full, 128);
+    mbar_init(&bars->p_full, NSOFT);
     mbar_init(&bars->o_done, 1);
-    mbar_init(&bars->q_full, 128);
+    mbar_init(&bars->q_full, NSOFT);
     mbar_init(&bars->mma_final, 1);
     bars->abort = 0;
     int lo = 0, hi = num_units - 1;  // last unit whose first tile is <= t_begin
@@ -374,10 +393,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
   } else if (warp >= SOFTMAX_WARP0) {
     // ------------------------------------------------------------ softmax / epilogue
-    const int r = tid - SOFTMAX_WARP0 * 32;  // query row = TMEM lane
-    const uint32_t lane_base = (uint32_t)((warp - SOFTMAX_WARP0) * 32) << 16;
-    const uint32_t tq = tmem + lane_base;
-    // waits agree across the warp, so warp-collective tcgen05.ld/st stay converged
+    // Two warpgroups share every query row: warpgroup h handles columns [64h, 64h + 64) of
+    // each score tile and the same half of the output columns. They exchange half-tile
+    // row maxima through shared memory at one named barrier per tile, so both apply the
+    // same reference max; the half sums are added once per unit.
+    const int wg = (warp - SOFTMAX_WARP0) >> 2;
+    const int r = (warp & 3) * 32 + lane;  // query row = TMEM lane
+    const int st_id = wg * 128 + r;        // 0..255 within the softmax threads
+    const uint32_t tq = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    constexpr int HC = KT / 2;             // score columns per warpgroup
+    constexpr int OC = HD / 2;             // output columns per warpgroup
     auto wwait = [&](uint64_t* bar, uint32_t par) -> bool {
       return __all_sync(0xffffffffu, mbar_wait(bar, par, abort, p.flags));
     };
@@ -399,134 +424,147 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int64_t qrow = p.q_off[s.b] + i_row;
       const float sc = p.scale_log2;
 
-      // Q row -> TMEM columns [COL_Q, COL_Q + HD/2) as packed bf16 pairs
-      {
+      // Q row -> TMEM columns [COL_Q, COL_Q + HD/2) as packed bf16 pairs, 32 columns per
+      // store (both warpgroups for d = 128, the first one for d = 64)
+      if (wg < HD / 64) {
         const uint4* src = reinterpret_cast<const uint4*>(
             (const __nv_bfloat16*)p.q + (qrow * p.Hq + (int64_t)s.g * p.G + hl) * HD);
+        uint32_t rq[32];
 #pragma unroll
-        for (int c = 0; c < HD / 64; ++c) {
-          uint32_t rq[32];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const uint4 v = live ? __ldg(src + c * 8 + e) : make_uint4(0, 0, 0, 0);
-            rq[4 * e] = v.x;
-            rq[4 * e + 1] = v.y;
-            rq[4 * e + 2] = v.z;
-            rq[4 * e + 3] = v.w;
-          }
-          tmem_st32(tq + COL_Q + c * 32, rq);
+        for (int e = 0; e < 8; ++e) {
+          const uint4 v = live ? __ldg(src + wg * 8 + e) : make_uint4(0, 0, 0, 0);
+          rq[4 * e] = v.x;
+          rq[4 * e + 1] = v.y;
+          rq[4 * e + 2] = v.z;
+          rq[4 * e + 3] = v.w;
         }
+        tmem_st32(tq + COL_Q + wg * 32, rq);
         tmem_wait_st();
-        fence_before();
-        mbar_arrive(&bars->q_full);
       }
+      fence_before();
+      mbar_arrive(&bars->q_full);
 
-      float m_ref = -INFINITY, l = 0.f;
+      float m_ref = -INFINITY, lh = 0.f;
+      bool good = true;
       for (int j = s.j0; j < s.j1; ++j, ++it) {
         const uint32_t sb = it & 1;
-        if (!wwait(&bars->s_full[sb], (it >> 1) & 1)) {
+        float sv[HC];
+        float mx = -INFINITY;
+        const int key0 = j * KT + wg * HC;
+        if (good && (good = wwait(&bars->s_full[sb], (it >> 1) & 1))) {
+          fence_after();
+          uint32_t* raw = reinterpret_cast<uint32_t*>(sv);
+#pragma unroll
+          for (int c = 0; c < HC / 32; ++c)
+            tmem_ld32(tq + COL_S0 + sb * 128 + wg * HC + c * 32, raw + c * 32);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < HC / 32; ++c) reg_fence32(raw + c * 32);
+          fence_before();
+          mbar_arrive(&bars->s_free[sb]);
+          if (key0 + HC - 1 > T) {  // the window-causal mask reaches into this half tile
+            const int lim = T + i_row - key0;
+#pragma unroll
+            for (int c = 0; c < HC; ++c)
+              if (c > lim) sv[c] = -INFINITY;
+          }
+          float m8[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) m8[e] = sv[e];
+#pragma unroll
+          for (int c = 8; c < HC; ++c) m8[c & 7] = fmaxf(m8[c & 7], sv[c]);
+          mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                     fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+          bars->xmax[sb][wg][r] = mx;
+        }
+        if (!softmax_pair_and(good)) {
           ok = false;
           break;
         }
-        fence_after();
-        float sv[KT];
-        {
-          uint32_t* raw = reinterpret_cast<uint32_t*>(sv);
-#pragma unroll
-          for (int c = 0; c < KT / 32; ++c) tmem_ld32(tq + COL_S0 + sb * 128 + c * 32, raw + c * 32);
-          tmem_wait_ld();
-#pragma unroll
-          for (int c = 0; c < KT / 32; ++c) reg_fence32(raw + c * 32);
-        }
-        fence_before();
-        mbar_arrive(&bars->s_free[sb]);
-
-        const int key0 = j * KT;
-        const bool edge = key0 + KT - 1 > T;
-        float mt = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < KT; ++c) {
-          float x = sv[c] * sc;
-          if (edge && key0 + c > T + i_row) x = -INFINITY;
-          sv[c] = x;
-          mt = fmaxf(mt, x);
-        }
+        mx = fmaxf(mx, bars->xmax[sb][wg ^ 1][r]);
+        const float mt = mx * sc;  // tile max in log2 units (sc > 0)
         if (j > s.j0) {
-          if (!wwait(&bars->o_done, (it - 1) & 1)) {
-            ok = false;
-            break;
-          }
+          good = wwait(&bars->o_done, (it - 1) & 1);
+          if (!good) continue;  // leave together at the next barrier
           fence_after();
         }
         if (m_ref == -INFINITY) {
           m_ref = mt;  // O holds nothing yet for this row (zeros or about to be overwritten)
         } else if (mt > m_ref + RESCALE_THRESHOLD) {
           const float alpha = ex2(m_ref - mt);
-          l *= alpha;
+          lh *= alpha;
           m_ref = mt;
 #pragma unroll 1
-          for (int c = 0; c < HD / 32; ++c) {
+          for (int c = 0; c < OC / 32; ++c) {
             uint32_t ro[32];
-            tmem_ld32(tq + COL_O + c * 32, ro);
+            tmem_ld32(tq + COL_O + wg * OC + c * 32, ro);
             tmem_wait_ld();
             reg_fence32(ro);
 #pragma unroll
             for (int e = 0; e < 32; ++e) ro[e] = __float_as_uint(__uint_as_float(ro[e]) * alpha);
-            tmem_st32(tq + COL_O + c * 32, ro);
+            tmem_st32(tq + COL_O + wg * OC + c * 32, ro);
           }
           tmem_wait_st();
         }
-        const float mu = m_ref == -INFINITY ? 0.f : m_ref;
-        float rs = 0.f;
+        const float nmu = m_ref == -INFINITY ? 0.f : -m_ref;
+        float s8[8];
 #pragma unroll
-        for (int c = 0; c < KT; ++c) {
-          sv[c] = ex2(sv[c] - mu);
-          rs += sv[c];
+        for (int e = 0; e < 8; ++e) s8[e] = 0.f;
+#pragma unroll
+        for (int c = 0; c < HC; ++c) {
+          sv[c] = ex2(fmaf(sv[c], sc, nmu));
+          s8[c & 7] += sv[c];
         }
-        l += rs;
-#pragma unroll
-        for (int c = 0; c < KT / 64; ++c) {
+        lh += ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
+        {
           uint32_t pk[32];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) pk[e] = pack_bf16(sv[c * 64 + 2 * e], sv[c * 64 + 2 * e + 1]);
-          tmem_st32(tq + COL_P + c * 32, pk);
+          for (int e = 0; e < 32; ++e) pk[e] = pack_bf16(sv[2 * e], sv[2 * e + 1]);
+          tmem_st32(tq + COL_P + wg * 32, pk);
+          tmem_wait_st();
         }
-        tmem_wait_st();
-        if (key0 + KT > nkeys) {
+        const int tkey0 = j * KT;
+        bool zeroed = false;
+        if (tkey0 + KT > nkeys) {
           // last tile of the sequence: clear the V rows past its end so that P = 0 never
           // meets non-finite data (they may hold the next sequence or unwritten memory)
           const uint32_t st = it % NS;
-          if (!wwait(&bars->v_full[st], (it / NS) & 1)) {
-            ok = false;
-            break;
-          }
-          const int first = nkeys - key0;
+          good = wwait(&bars->v_full[st], (it / NS) & 1);
+          if (!good) continue;
+          const int first = nkeys - tkey0;
           uint8_t* vt = smem + st * L::STAGE + L::TILE;
           const int chunks = (KT - first) * 8;  // 16-byte chunks per 64-column block
-          for (int q = r; q < chunks * L::NBLK; q += 128) {
+          for (int q = st_id; q < chunks * L::NBLK; q += NSOFT) {
             const int blk = q / chunks, rem = q % chunks;
             *reinterpret_cast<uint4*>(vt + blk * L::BLK + (first + rem / 8) * 128 + (rem % 8) * 16) =
                 make_uint4(0, 0, 0, 0);
           }
-          fence_proxy_async();
+          zeroed = true;
         }
+        if (zeroed) fence_proxy_async();
         fence_before();
         mbar_arrive(&bars->p_full);
       }
       if (!ok) break;
-      if (!wwait(&bars->o_done, (it - 1) & 1)) break;
-      fence_after();
+      if (good) {
+        good = wwait(&bars->o_done, (it - 1) & 1);
+        if (good) fence_after();
+      }
+      bars->xl[wg][r] = lh;
+      if (!softmax_pair_and(good)) break;
+      const float l = lh + bars->xl[wg ^ 1][r];
 
-      // ---- epilogue
+      // ---- epilogue: this warpgroup's half of the output columns
       const bool whole = s.j0 == 0 && s.j1 == s.nt;
       if (whole) {
         const float inv = 1.f / l;
         __nv_bfloat16* dst = (__nv_bfloat16*)p.out +
-                             ((p.q_off[s.b] + i_row) * p.Hq + (int64_t)s.g * p.G + hl) * HD;
+                             ((p.q_off[s.b] + i_row) * p.Hq + (int64_t)s.g * p.G + hl) * HD +
+                             wg * OC;
 #pragma unroll 1
-        for (int c = 0; c < HD / 32; ++c) {
+        for (int c = 0; c < OC / 32; ++c) {
           uint32_t ro[32];
-          tmem_ld32(tq + COL_O + c * 32, ro);
+          tmem_ld32(tq + COL_O + wg * OC + c * 32, ro);
           tmem_wait_ld();
           reg_fence32(ro);
           if (live) {
@@ -542,11 +580,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
       } else {
         const size_t slot = (size_t)blockIdx.x + s.u;
-        float* dst = p.part_o + (slot * MT + r) * HD;
+        float* dst = p.part_o + (slot * MT + r) * HD + wg * OC;
 #pragma unroll 1
-        for (int c = 0; c < HD / 32; ++c) {
+        for (int c = 0; c < OC / 32; ++c) {
           uint32_t ro[32];
-          tmem_ld32(tq + COL_O + c * 32, ro);
+          tmem_ld32(tq + COL_O + wg * OC + c * 32, ro);
           tmem_wait_ld();
           reg_fence32(ro);
           if (live) {
@@ -556,7 +594,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               d4[e] = make_uint4(ro[4 * e], ro[4 * e + 1], ro[4 * e + 2], ro[4 * e + 3]);
           }
         }
-        if (live) p.part_ml[slot * MT + r] = make_float2(m_ref, l);
+        if (live && wg == 0) p.part_ml[slot * MT + r] = make_float2(m_ref, l);
       }
       fence_before();  // TMEM reads above complete before the next unit's MMAs
     }

@@ -89,9 +89,14 @@ struct AttnParams {
   float scale_log2;           // softmax_scale * log2(e)
 };
 
-// First CTA whose tile range contains global tile t (ranges [c*TT/C, (c+1)*TT/C)).
+// The CTA whose tile range [c*TT/C, (c+1)*TT/C) contains global tile t.
 __host__ __device__ inline int cta_of_tile(int64_t t, int64_t TT, int C) {
   return (int)(((t + 1) * (int64_t)C - 1) / TT);
+}
+// Whether CTA c has any tile (with fewer tiles than CTAs some ranges are empty; such a CTA
+// writes no partial for the units its neighbours split).
+__host__ __device__ inline bool cta_has_tiles(int c, int64_t TT, int C) {
+  return (int64_t)(c + 1) * TT / C > (int64_t)c * TT / C;
 }
 
 // Launchers (each returns the cudaGetLastError() of its launch).

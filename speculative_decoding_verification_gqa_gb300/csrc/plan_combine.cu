@@ -120,58 +120,76 @@ cudaError_t launch_plan(const AttnParams& p, int kt, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-// One CTA per unit; one warp per query row; lane handles d/32 consecutive columns.
+// Eight query rows per CTA, 32 lanes per row, each lane d/32 consecutive columns; the CTAs
+// of units that a single attention CTA covered exit at once.
+constexpr int COMBINE_ROWS = 8;
+
 template <int HD>
 __global__ void __launch_bounds__(256) combine_kernel(AttnParams p) {
   constexpr int PER = HD / 32;
-  const int u = blockIdx.x;
-  const int nu = p.hdr->num_units;
-  if (u >= nu) return;
+  const int u = blockIdx.x / (MT / COMBINE_ROWS);
+  const int r = (blockIdx.x % (MT / COMBINE_ROWS)) * COMBINE_ROWS + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (u >= p.hdr->num_units) return;
   const int64_t TT = p.hdr->total_tiles;
   const int64_t ub = p.ubeg[u], ue = p.ubeg[u + 1];
   const int c_lo = cta_of_tile(ub, TT, p.n_ctas), c_hi = cta_of_tile(ue - 1, TT, p.n_ctas);
   if (c_lo == c_hi) return;  // one CTA covered the unit and wrote the output itself
   const int4 info = p.units[u];
   const int b = info.x, g = info.y, mt = info.z;
-  const int W = 1 + p.draft_len[b];
-  const int rows_total = p.G * W;
-  const int rows = min(MT, rows_total - mt * MT);
-  const int64_t qo = p.q_off[b];
-  const float vs = p.kv_scale ? p.kv_scale[p.Hkv + g] : 1.f;
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  for (int r = wid; r < rows; r += blockDim.x >> 5) {
-    float mx = -INFINITY;
-    for (int c = c_lo; c <= c_hi; ++c) mx = fmaxf(mx, p.part_ml[(size_t)(c + u) * MT + r].x);
-    const float muse = mx == -INFINITY ? 0.f : mx;
-    float L = 0.f, acc[PER];
+  const int rows_total = p.G * (1 + p.draft_len[b]);
+  if (r >= min(MT, rows_total - mt * MT)) return;
+  float mx = -INFINITY;
+  for (int c = c_lo; c <= c_hi; ++c)
+    if (cta_has_tiles(c, TT, p.n_ctas)) mx = fmaxf(mx, p.part_ml[(size_t)(c + u) * MT + r].x);
+  const float muse = mx == -INFINITY ? 0.f : mx;
+  float L = 0.f, acc[PER];
 #pragma unroll
-    for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-    for (int c = c_lo; c <= c_hi; ++c) {
-      const size_t slot = (size_t)(c + u);
-      const float2 ml = p.part_ml[slot * MT + r];
-      const float wgt = exp2f(ml.x - muse);
-      L += ml.y * wgt;
-      const float* src = p.part_o + (slot * MT + r) * HD + lane * PER;
-#pragma unroll
-      for (int e = 0; e < PER; ++e) acc[e] += wgt * src[e];
+  for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+  for (int c = c_lo; c <= c_hi; ++c) {
+    if (!cta_has_tiles(c, TT, p.n_ctas)) continue;
+    const size_t slot = (size_t)(c + u);
+    const float2 ml = p.part_ml[slot * MT + r];
+    const float wgt = exp2f(ml.x - muse);
+    L += ml.y * wgt;
+    const float* src = p.part_o + (slot * MT + r) * HD + lane * PER;
+    if constexpr (PER == 4) {
+      const float4 v = __ldcs(reinterpret_cast<const float4*>(src));
+      acc[0] += wgt * v.x;
+      acc[1] += wgt * v.y;
+      acc[2] += wgt * v.z;
+      acc[3] += wgt * v.w;
+    } else {
+      const float2 v = __ldcs(reinterpret_cast<const float2*>(src));
+      acc[0] += wgt * v.x;
+      acc[1] += wgt * v.y;
     }
-    const float inv = vs / L;
-    const int rg = mt * MT + r;
-    const int i = rg / p.G, hl = rg % p.G;
-    __nv_bfloat16* dst = (__nv_bfloat16*)p.out +
-                         ((qo + i) * p.Hq + (int64_t)g * p.G + hl) * HD + lane * PER;
-#pragma unroll
-    for (int e = 0; e < PER; e += 2)
-      *(__nv_bfloat162*)(dst + e) = __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
+  }
+  const float vs = p.kv_scale ? p.kv_scale[p.Hkv + g] : 1.f;
+  const float inv = vs / L;
+  const int rg = mt * MT + r;
+  const int i = rg / p.G, hl = rg % p.G;
+  __nv_bfloat16* dst = (__nv_bfloat16*)p.out +
+                       ((p.q_off[b] + i) * p.Hq + (int64_t)g * p.G + hl) * HD + lane * PER;
+  if constexpr (PER == 4) {
+    __nv_bfloat162 a = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
+    __nv_bfloat162 c = __floats2bfloat162_rn(acc[2] * inv, acc[3] * inv);
+    uint2 w;
+    w.x = *reinterpret_cast<uint32_t*>(&a);
+    w.y = *reinterpret_cast<uint32_t*>(&c);
+    *reinterpret_cast<uint2*>(dst) = w;
+  } else {
+    *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
   }
 }
 
 cudaError_t launch_combine(const AttnParams& p, cudaStream_t s) {
   if (p.max_units <= 0) return cudaSuccess;
+  const unsigned grid = (unsigned)p.max_units * (MT / COMBINE_ROWS);
   if (p.d == 128)
-    combine_kernel<128><<<p.max_units, 256, 0, s>>>(p);
+    combine_kernel<128><<<grid, 256, 0, s>>>(p);
   else
-    combine_kernel<64><<<p.max_units, 256, 0, s>>>(p);
+    combine_kernel<64><<<grid, 256, 0, s>>>(p);
   return cudaGetLastError();
 }
 

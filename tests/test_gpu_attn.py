@@ -90,6 +90,24 @@ def test_repeatable_and_workspace_reuse(kernel):
     assert sv.workspace_status(ws) == 0
 
 
+@pytest.mark.parametrize("name", ["ragged", "d64_ragged", "empty_prefix", "c1"])
+def test_stale_workspace_is_never_read(kernel, name):
+    """Partials are only read where this call wrote them: a workspace full of NaN bytes
+    (flag word zeroed) must give the same result as a fresh one, including ragged batches
+    with fewer tiles than CTAs (some CTAs then own no tile)."""
+    w, x = _small(seed=5, **SMALL[name])
+    q, k, v, sc, T, D = dev_attn(x)
+    md, ms = int(x["draft_len"].max()), int(x["seq_lens"].max())
+    nbytes = sv.verify_workspace_bytes(sv.api.attn_desc(q, k, len(x["seq_lens"]), md, ms))
+    ws = torch.full((nbytes,), 0xFF, dtype=torch.uint8, device="cuda")
+    ws[:256] = 0
+    out = sv.spec_verify_attn(q, k, v, T, D, max_draft_len=md, max_seq_len=ms, workspace=ws)
+    torch.cuda.synchronize()
+    assert sv.workspace_status(ws) == 0
+    got = out.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert_close(got, oracle_attn(w, x))
+
+
 def test_device_side_length_check(kernel):
     w, x = _small(B=2, Hq=8, Hkv=2, d=128, T=(100, 50), D=(3, 2))
     q, k, v, sc, T, D = dev_attn(x)
