@@ -6,10 +6,10 @@
 //   warp 0      TMA producer: K and V tiles of one KV head (128 keys x d, bf16, 128-byte
 //               swizzle) into a 3-stage shared-memory ring; a stage is released once the
 //               O += P V that reads its V tile has completed.
-//   warp 1      MMA issuer (one thread): S = Q K^T into a double-buffered TMEM score tile,
-//               then O += P V into the TMEM accumulator. Q and P are tcgen05 A operands
-//               read straight from TMEM; K (K-major) and V (MN-major) come from shared
-//               memory through UMMA descriptors.
+//   warp 1      S issuer (one thread): S = Q K^T into a double-buffered TMEM score tile.
+//   warp 3      P V issuer (one thread): O += P V into the TMEM accumulator.
+//               Q and P are tcgen05 A operands read straight from TMEM; K (K-major) and V
+//               (MN-major) come from shared memory through UMMA descriptors.
 //   warps 4..11 softmax, two warpgroups: in each, thread r owns query row r (TMEM lane r)
 //               and one half of the columns. Per unit they write the Q row into TMEM; per
 //               tile they read their 64 scores, apply the scale and the window-causal
@@ -45,7 +45,7 @@ constexpr float RESCALE_THRESHOLD = 8.f;            // log2 units
 struct __align__(8) Bars {
   uint64_t k_full[NS], v_full[NS], kv_empty[NS];
   uint64_t s_full[2], s_free[2];
-  uint64_t p_full, o_done, q_full, mma_final;
+  uint64_t p_full, o_done, q_full, s_final, pv_final;
   uint32_t tmem_base;
   int abort;
   int u0;
@@ -80,9 +80,8 @@ __device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
 }
 // Bounded wait for the phase with the given parity. Returns false (and raises the CTA's
 // abort flag and the workspace timeout flag) if it gives up or another role already did.
-__device__ __noinline__ bool mbar_wait(uint64_t* b, uint32_t parity, volatile int* abort,
-                                       uint32_t* flags) {
-  if (mbar_try(b, parity)) return true;
+__device__ __noinline__ bool mbar_wait_slow(uint64_t* b, uint32_t parity, volatile int* abort,
+                                            uint32_t* flags) {
   const long long t0 = clock64();
   while (true) {
     if (mbar_try(b, parity)) return true;
@@ -93,6 +92,12 @@ __device__ __noinline__ bool mbar_wait(uint64_t* b, uint32_t parity, volatile in
       return false;
     }
   }
+}
+
+// The common case (phase already complete) costs one try_wait and no call.
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, volatile int* abort,
+                                          uint32_t* flags) {
+  return mbar_try(b, parity) || mbar_wait_slow(b, parity, abort, flags);
 }
 
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint64_t* bar,
@@ -268,7 +273,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     mbar_init(&bars->p_full, NSOFT);
     mbar_init(&bars->o_done, 1);
     mbar_init(&bars->q_full, NSOFT);
-    mbar_init(&bars->mma_final, 1);
+    mbar_init(&bars->s_final, 1);
+    mbar_init(&bars->pv_final, 1);
     bars->abort = 0;
     int lo = 0, hi = num_units - 1;  // last unit whose first tile is <= t_begin
     while (lo < hi) {
@@ -334,31 +340,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ S = Q K^T issuer
     if (lane == 0) {
       constexpr uint32_t ID_S = idesc_bf16(KT, 0);
-      constexpr uint32_t ID_PV = idesc_bf16(HD, 1);
+      // K: K-major, 128-byte rows, 8-row groups 1024 B apart; 32 B per 16-element step
+      const uint64_t kdesc0 = smem_desc(saddr(smem), 16, 1024);
       int64_t t = t_begin;
       int u = u_first;
       Seg s;
       uint32_t it = 0, seg_i = 0;
       bool ok = true;
-      auto issue_pv = [&](uint32_t itp, bool first) -> bool {
-        const uint32_t st = itp % NS;
-        if (!mbar_wait(&bars->p_full, itp & 1, abort, p.flags)) return false;
-        if (!mbar_wait(&bars->v_full[st], (itp / NS) & 1, abort, p.flags)) return false;
-        fence_after();
-        const uint32_t vbase = saddr(smem + st * L::STAGE + L::TILE);
-#pragma unroll
-        for (int kk = 0; kk < KT / 16; ++kk) {
-          // V: MN-major, 64-column blocks L::BLK apart (LBO), 8-key groups 1024 B apart (SBO)
-          const uint64_t bd = smem_desc(vbase + kk * 16 * 128, L::BLK, 1024);
-          mma_ts(tmem + COL_O, tmem + COL_P + kk * 8, bd, ID_PV, (first && kk == 0) ? 0u : 1u);
-        }
-        mma_commit(&bars->o_done);
-        mma_commit(&bars->kv_empty[st]);
-        return true;
-      };
       while (ok && seg_next(p, num_units, t, t_end, u, s)) {
         if (!mbar_wait(&bars->q_full, seg_i & 1, abort, p.flags)) break;
         fence_after();
@@ -370,25 +361,56 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             break;
           }
           fence_after();
-          const uint32_t kbase = saddr(smem + st * L::STAGE);
+          const uint64_t kd = kdesc0 + ((st * L::STAGE) >> 4);
+          const uint32_t dcol = tmem + COL_S0 + sb * 128;
 #pragma unroll
-          for (int kk = 0; kk < HD / 16; ++kk) {
-            // K: K-major, 128-byte rows, 8-row groups 1024 B apart; 32 B per 16-element step
-            const uint64_t bd = smem_desc(kbase + (kk >> 2) * L::BLK + (kk & 3) * 32, 16, 1024);
-            mma_ts(tmem + COL_S0 + sb * 128, tmem + COL_Q + kk * 8, bd, ID_S, kk > 0 ? 1u : 0u);
-          }
+          for (int kk = 0; kk < HD / 16; ++kk)
+            mma_ts(dcol, tmem + COL_Q + kk * 8, kd + ((((kk >> 2) * L::BLK) + (kk & 3) * 32) >> 4),
+                   ID_S, kk > 0 ? 1u : 0u);
           mma_commit(&bars->s_full[sb]);
-          if (j > s.j0 && !issue_pv(it - 1, j - 1 == s.j0)) {
+        }
+        ++seg_i;
+      }
+      mma_commit(&bars->s_final);
+      const long long t0 = clock64();
+      while (!mbar_try(&bars->s_final, 0) && clock64() - t0 < TIMEOUT_CYCLES) {
+      }
+    }
+  } else if (warp == 3) {
+    // ------------------------------------------------------------ O += P V issuer
+    // A thread of its own, so that P V starts as soon as P is ready instead of after
+    // the next S has been issued. A stage is released after its P V, which follows its
+    // S (the softmax read the scores before publishing P).
+    if (lane == 0) {
+      constexpr uint32_t ID_PV = idesc_bf16(HD, 1);
+      // V: MN-major, 64-column blocks L::BLK apart (LBO), 8-key groups 1024 B apart (SBO)
+      const uint64_t vdesc0 = smem_desc(saddr(smem + L::TILE), L::BLK, 1024);
+      int64_t t = t_begin;
+      int u = u_first;
+      Seg s;
+      uint32_t it = 0;
+      bool ok = true;
+      while (ok && seg_next(p, num_units, t, t_end, u, s)) {
+        for (int j = s.j0; j < s.j1; ++j, ++it) {
+          const uint32_t st = it % NS;
+          if (!mbar_wait(&bars->p_full, it & 1, abort, p.flags) ||
+              !mbar_wait(&bars->v_full[st], (it / NS) & 1, abort, p.flags)) {
             ok = false;
             break;
           }
+          fence_after();
+          const uint64_t vd = vdesc0 + ((st * L::STAGE) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < KT / 16; ++kk)
+            mma_ts(tmem + COL_O, tmem + COL_P + kk * 8, vd + ((kk * 16 * 128) >> 4), ID_PV,
+                   (j == s.j0 && kk == 0) ? 0u : 1u);
+          mma_commit(&bars->o_done);
+          mma_commit(&bars->kv_empty[st]);
         }
-        if (!ok || !issue_pv(it - 1, s.j1 - 1 == s.j0)) break;
-        ++seg_i;
       }
-      mma_commit(&bars->mma_final);
+      mma_commit(&bars->pv_final);
       const long long t0 = clock64();
-      while (!mbar_try(&bars->mma_final, 0) && clock64() - t0 < TIMEOUT_CYCLES) {
+      while (!mbar_try(&bars->pv_final, 0) && clock64() - t0 < TIMEOUT_CYCLES) {
       }
     }
   } else if (warp >= SOFTMAX_WARP0) {
