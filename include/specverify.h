@@ -149,7 +149,7 @@ SV_API sv_status spec_accept(int32_t batch, int32_t max_draft_len, int32_t vocab
  * in a device array of SV_ACCEPT_NOALLOC_MAX_WORKSPACE bytes compiled into the library:
  *   - every GPU that loads the library holds that memory until the process exits;
  *   - a shape whose spec_accept_workspace_size() exceeds it is rejected with
- *     SV_ERR_WORKSPACE and nothing is launched (512 KiB covers, for example, 65,000
+ *     SV_ERR_WORKSPACE and nothing is launched (512 KiB covers, for example, 64,000
  *     window rows on a 152-SM GPU);
  *   - the first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call before any

@@ -136,6 +136,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_mma_kernel(const AttnParams 
   uint8_t* sConv = sKV + NSTAGE * STAGE_BYTES;  // fp8 only: converted K | V (f16)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  pdl_trigger();
+  pdl_wait();  // the plan of this call is complete
   const int64_t TT = p.hdr->total_tiles;
   if (TT == 0) return;
   const int C = p.n_ctas;
@@ -422,8 +424,7 @@ cudaError_t launch_one(const AttnParams& p, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(attn_mma_kernel<HD, FP8>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  attn_mma_kernel<HD, FP8><<<p.n_ctas, NTHREADS, smem, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(attn_mma_kernel<HD, FP8>, dim3(p.n_ctas), dim3(NTHREADS), smem, s, p);
 }
 
 }  // namespace

@@ -252,6 +252,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   Bars* bars = (Bars*)(smem + L::BARS);
   volatile int* abort = &bars->abort;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  pdl_trigger();
+  pdl_wait();  // the plan of this call is complete
 
   const int TT = p.hdr->total_tiles;
   const int num_units = p.hdr->num_units;
@@ -676,8 +678,7 @@ cudaError_t launch_hd(const AttnParams& p, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<HD>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  attn_tc_kernel<HD><<<p.n_ctas, NTHREADS, smem, s>>>(p, mk, mv);
-  return cudaGetLastError();
+  return launch_pdl(attn_tc_kernel<HD>, dim3(p.n_ctas), dim3(NTHREADS), smem, s, p, mk, mv);
 }
 
 }  // namespace

@@ -16,6 +16,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/specverify.h"
 
 namespace sv {
@@ -99,6 +101,30 @@ __host__ __device__ inline bool cta_has_tiles(int c, int64_t TT, int C) {
   return (int64_t)(c + 1) * TT / C > (int64_t)c * TT / C;
 }
 
+// Programmatic dependent launch: every kernel of the library is launched so that it may
+// start while the previous kernel on the stream drains; it lets its own dependents launch
+// at once (pdl_trigger) and waits for the previous grid's results (pdl_wait) before it
+// reads any input, so results are those of ordinary stream order.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // Launchers (each returns the cudaGetLastError() of its launch).
 cudaError_t launch_plan(const AttnParams& p, int kt, cudaStream_t s);
 cudaError_t launch_combine(const AttnParams& p, cudaStream_t s);
@@ -111,7 +137,7 @@ cudaError_t launch_attn_tc(const AttnParams& p, bool fp8, cudaStream_t s);
 // Acceptance.
 struct AcceptWs {
   size_t ctrl, part, total;
-  int splits;
+  int nctas;  // persistent argmax CTAs
 };
 AcceptWs accept_ws_layout(int B, int max_draft, int vocab, int num_sms);
 cudaError_t launch_accept(int B, int max_draft, int vocab, int dtype, const void* logits,

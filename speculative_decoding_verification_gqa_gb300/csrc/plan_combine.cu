@@ -46,6 +46,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(AttnParams p, int kt) {
   __shared__ int64_t carry[4];
   __shared__ int bad;
   const int tid = threadIdx.x;
+  pdl_trigger();
+  pdl_wait();
   if (tid == 0) {
     carry[0] = carry[1] = carry[2] = carry[3] = 0;
     bad = 0;
@@ -116,8 +118,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(AttnParams p, int kt) {
 }
 
 cudaError_t launch_plan(const AttnParams& p, int kt, cudaStream_t s) {
-  plan_kernel<<<1, 1024, 0, s>>>(p, kt);
-  return cudaGetLastError();
+  return launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, s, p, kt);
 }
 
 // Eight query rows per CTA, 32 lanes per row, each lane d/32 consecutive columns; the CTAs
@@ -127,6 +128,9 @@ constexpr int COMBINE_ROWS = 8;
 template <int HD>
 __global__ void __launch_bounds__(256) combine_kernel(AttnParams p) {
   constexpr int PER = HD / 32;
+  constexpr int MAXP = 4;  // partials loaded in one batch
+  pdl_trigger();
+  pdl_wait();
   const int u = blockIdx.x / (MT / COMBINE_ROWS);
   const int r = (blockIdx.x % (MT / COMBINE_ROWS)) * COMBINE_ROWS + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -139,31 +143,48 @@ __global__ void __launch_bounds__(256) combine_kernel(AttnParams p) {
   const int b = info.x, g = info.y, mt = info.z;
   const int rows_total = p.G * (1 + p.draft_len[b]);
   if (r >= min(MT, rows_total - mt * MT)) return;
-  float mx = -INFINITY;
-  for (int c = c_lo; c <= c_hi; ++c)
-    if (cta_has_tiles(c, TT, p.n_ctas)) mx = fmaxf(mx, p.part_ml[(size_t)(c + u) * MT + r].x);
-  const float muse = mx == -INFINITY ? 0.f : mx;
-  float L = 0.f, acc[PER];
+  float mx = -INFINITY, L = 0.f, acc[PER];
 #pragma unroll
   for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-  for (int c = c_lo; c <= c_hi; ++c) {
-    if (!cta_has_tiles(c, TT, p.n_ctas)) continue;
-    const size_t slot = (size_t)(c + u);
-    const float2 ml = p.part_ml[slot * MT + r];
-    const float wgt = exp2f(ml.x - muse);
-    L += ml.y * wgt;
-    const float* src = p.part_o + (slot * MT + r) * HD + lane * PER;
-    if constexpr (PER == 4) {
-      const float4 v = __ldcs(reinterpret_cast<const float4*>(src));
-      acc[0] += wgt * v.x;
-      acc[1] += wgt * v.y;
-      acc[2] += wgt * v.z;
-      acc[3] += wgt * v.w;
-    } else {
-      const float2 v = __ldcs(reinterpret_cast<const float2*>(src));
-      acc[0] += wgt * v.x;
-      acc[1] += wgt * v.y;
+  for (int c0 = c_lo; c0 <= c_hi; c0 += MAXP) {
+    // issue every load of the batch before using any (one L2 round trip per batch)
+    float2 ml[MAXP];
+    float ov[MAXP][PER];
+#pragma unroll
+    for (int k = 0; k < MAXP; ++k) {
+      const int c = c0 + k;
+      const bool use = c <= c_hi && cta_has_tiles(c, TT, p.n_ctas);
+      const size_t slot = (size_t)(c + u);
+      ml[k] = use ? p.part_ml[slot * MT + r] : make_float2(-INFINITY, 0.f);
+      const float* src = p.part_o + (slot * MT + r) * HD + lane * PER;
+      if constexpr (PER == 4) {
+        const float4 v = use ? __ldcs(reinterpret_cast<const float4*>(src)) : make_float4(0, 0, 0, 0);
+        ov[k][0] = v.x;
+        ov[k][1] = v.y;
+        ov[k][2] = v.z;
+        ov[k][3] = v.w;
+      } else {
+        const float2 v = use ? __ldcs(reinterpret_cast<const float2*>(src)) : make_float2(0, 0);
+        ov[k][0] = v.x;
+        ov[k][1] = v.y;
+      }
     }
+    float bm = mx;
+#pragma unroll
+    for (int k = 0; k < MAXP; ++k) bm = fmaxf(bm, ml[k].x);
+    const float muse = bm == -INFINITY ? 0.f : bm;
+    const float rs = exp2f(mx - muse);  // rescale what earlier batches accumulated
+    L *= rs;
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc[e] *= rs;
+#pragma unroll
+    for (int k = 0; k < MAXP; ++k) {
+      const float wgt = exp2f(ml[k].x - muse);  // 0 for unused slots (m = -inf)
+      L += ml[k].y * wgt;
+#pragma unroll
+      for (int e = 0; e < PER; ++e) acc[e] += wgt * ov[k][e];
+    }
+    mx = bm;
   }
   const float vs = p.kv_scale ? p.kv_scale[p.Hkv + g] : 1.f;
   const float inv = vs / L;
@@ -186,11 +207,8 @@ __global__ void __launch_bounds__(256) combine_kernel(AttnParams p) {
 cudaError_t launch_combine(const AttnParams& p, cudaStream_t s) {
   if (p.max_units <= 0) return cudaSuccess;
   const unsigned grid = (unsigned)p.max_units * (MT / COMBINE_ROWS);
-  if (p.d == 128)
-    combine_kernel<128><<<grid, 256, 0, s>>>(p);
-  else
-    combine_kernel<64><<<grid, 256, 0, s>>>(p);
-  return cudaGetLastError();
+  return p.d == 128 ? launch_pdl(combine_kernel<128>, dim3(grid), dim3(256), 0, s, p)
+                    : launch_pdl(combine_kernel<64>, dim3(grid), dim3(256), 0, s, p);
 }
 
 }  // namespace sv
