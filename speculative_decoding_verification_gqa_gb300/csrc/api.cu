@@ -42,7 +42,8 @@ AttnWs layout_for(const sv_attn_desc* d, int sms) {
 
 // 1 = mma.sync, 2 = tcgen05
 int pick_kernel(const sv_attn_desc* d) {
-  const bool tc_ok = attn_tc_available() && d->kv_dtype == SV_BF16;
+  const bool tc_ok =
+      attn_tc_available() && attn_tc_supports(d->head_dim, d->kv_dtype == SV_FP8_E4M3);
   if (g_attn_kernel == 1) return 1;
   if (g_attn_kernel == 2) return tc_ok ? 2 : 1;
   return tc_ok ? 2 : 1;

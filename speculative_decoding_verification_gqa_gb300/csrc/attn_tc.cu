@@ -7,6 +7,9 @@
 //               swizzle) into a 3-stage shared-memory ring; a stage is released once the
 //               O += P V that reads its V tile has completed.
 //   warp 1      S issuer (one thread): S = Q K^T into a double-buffered TMEM score tile.
+//   warps 12-15 (FP8 K/V only) decode E4M3 tiles to f16 operand tiles; the MMAs then run
+//               in f16 (Q and P too), the K scale folds into the score scale and the V
+//               scale into the normalisation.
 //   warp 3      P V issuer (one thread): O += P V into the TMEM accumulator.
 //               Q and P are tcgen05 A operands read straight from TMEM; K (K-major) and V
 //               (MN-major) come from shared memory through UMMA descriptors.
@@ -26,6 +29,8 @@
 // TMEM is freed before the kernel returns.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include "internal.cuh"
 
@@ -37,6 +42,8 @@ constexpr int NS = 3;            // shared-memory ring depth
 constexpr int NTHREADS = 384;
 constexpr int SOFTMAX_WARP0 = 4;  // warps 4..7: columns 0..63 of a tile, 8..11: 64..127
 constexpr int NSOFT = 256;        // softmax threads (two warpgroups)
+constexpr int CONV_WARP0 = 12;    // FP8 only: warps 12-13 decode K tiles, 14-15 V tiles
+constexpr int NCONV = 64;         // decoding threads per tensor
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_O = 0, COL_S0 = 128, COL_P = 384, COL_Q = 448;
 constexpr long long TIMEOUT_CYCLES = 4000000000LL;  // ~2 s at 2 GHz
@@ -44,6 +51,7 @@ constexpr float RESCALE_THRESHOLD = 8.f;            // log2 units
 
 struct __align__(8) Bars {
   uint64_t k_full[NS], v_full[NS], kv_empty[NS];
+  uint64_t kc_full[2], kc_empty[2], vc_full[2], vc_empty[2];  // FP8: decoded f16 tiles
   uint64_t s_full[2], s_free[2];
   uint64_t p_full, o_done, q_full, s_final, pv_final;
   uint32_t tmem_base;
@@ -122,6 +130,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int n, int b_mn) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn << 16) |
          ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
 }
+// The same with f16 A and B (FP8 K/V decoded to f16).
+__host__ __device__ constexpr uint32_t idesc_f16(int n, int b_mn) {
+  return (1u << 4) | ((uint32_t)b_mn << 16) | ((uint32_t)(n >> 3) << 17) |
+         ((uint32_t)(128 >> 4) << 24);
+}
 
 // D[tmem] (+)= A[tmem] * B[smem]
 __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
@@ -189,9 +202,10 @@ __device__ __forceinline__ void tmem_wait_st() {
 // here once per tile (and once per unit epilogue), and a failed wait in either one makes
 // both leave together, so neither can be left waiting at the barrier.
 __device__ __forceinline__ bool softmax_pair_and(bool v) {
+  __syncwarp();  // the reduction counts whole warps: arrive converged
   uint32_t r;
   asm volatile(
-      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, 1, 256, p;\n"
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n barrier.red.and.pred q, 1, 256, p;\n"
       " selp.u32 %0, 1, 0, q;\n}\n"
       : "=r"(r)
       : "r"((uint32_t)v)
@@ -207,6 +221,24 @@ __device__ __forceinline__ float ex2(float x) {
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+template <bool F16>
+__device__ __forceinline__ uint32_t pack_p(float lo, float hi) {
+  return F16 ? pack_f16(lo, hi) : pack_bf16(lo, hi);
+}
+// bf16 pair -> f16 pair (exact for |x| in f16's normal range)
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+  const float2 f = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&w));
+  return pack_f16(f.x, f.y);
+}
+// two E4M3 codes (low byte first) -> f16 pair; exact, every E4M3 value is an f16 value
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t x) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(x & 0xffff), __NV_E4M3);
+  return (uint32_t)h.x | ((uint32_t)h.y << 16);
 }
 
 struct Seg {
@@ -232,21 +264,31 @@ __device__ __forceinline__ bool seg_next(const AttnParams& p, int num_units, int
   return true;
 }
 
-template <int HD>
+// Shared memory. bf16 K/V: NS stages of (K tile, V tile), filled by TMA and read by the
+// MMAs. FP8 K/V: an NS-stage ring of raw E4M3 (K, V) tile pairs filled by TMA, decoded to
+// f16 by the converter warps into a 2-stage K ring and a 1-stage V ring read by the MMAs.
+template <int HD, bool F8>
 struct TcLayout {
   static constexpr int BLK = KT * 128;            // one 64-column block of a 128-key tile
   static constexpr int NBLK = HD / 64;            // column blocks per tile
-  static constexpr int TILE = KT * HD * 2;        // one K or V tile (bf16)
-  static constexpr int STAGE = 2 * TILE;          // K then V
-  static constexpr int BARS = NS * STAGE;         // offset of the barrier block
+  static constexpr int TILE = KT * HD * 2;        // one 16-bit K or V tile
+  static constexpr int STAGE = 2 * TILE;          // bf16: K then V
+  static constexpr int RAW = KT * HD;             // one E4M3 tile
+  static constexpr int NCK = 2, NCV = 1;          // FP8: decoded K / V stages
+  static constexpr int CK = 0;                    // FP8 offsets
+  static constexpr int CV = CK + NCK * TILE;
+  static constexpr int RK = CV + NCV * TILE;
+  static constexpr int RV = RK + NS * RAW;
+  static constexpr int BARS = F8 ? RV + NS * RAW : NS * STAGE;  // offset of the barrier block
   static constexpr size_t SMEM = (size_t)BARS + sizeof(Bars) + 1024;  // + alignment slack
+  static constexpr int THREADS = F8 ? NTHREADS + 4 * 32 : NTHREADS;
 };
 
-template <int HD>
-__global__ void __launch_bounds__(NTHREADS, 1)
+template <int HD, bool F8>
+__global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
     attn_tc_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv) {
-  using L = TcLayout<HD>;
+  using L = TcLayout<HD, F8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   Bars* bars = (Bars*)(smem + L::BARS);
@@ -266,7 +308,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     for (int s = 0; s < NS; ++s) {
       mbar_init(&bars->k_full[s], 1);
       mbar_init(&bars->v_full[s], 1);
-      mbar_init(&bars->kv_empty[s], 1);
+      mbar_init(&bars->kv_empty[s], F8 ? 2 * NCONV : 1);  // FP8: freed by the converters
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->kc_full[s], NCONV);
+      mbar_init(&bars->vc_full[s], NCONV);
+      mbar_init(&bars->kc_empty[s], 1);
+      mbar_init(&bars->vc_empty[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->s_full[s], 1);
@@ -317,16 +365,26 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             ok = false;
             break;
           }
-          const uint32_t kdst = saddr(smem + st * L::STAGE);
-          const uint32_t vdst = kdst + L::TILE;
-          mbar_expect_tx(&bars->k_full[st], L::TILE);
+          if constexpr (F8) {
+            // one box per tensor: 128 keys x 128 one-byte codes
+            mbar_expect_tx(&bars->k_full[st], L::RAW);
+            tma_load_3d(saddr(smem + L::RK + st * L::RAW), &tmk, &bars->k_full[st], 0, s.g,
+                        row0 + j * KT);
+            mbar_expect_tx(&bars->v_full[st], L::RAW);
+            tma_load_3d(saddr(smem + L::RV + st * L::RAW), &tmv, &bars->v_full[st], 0, s.g,
+                        row0 + j * KT);
+          } else {
+            const uint32_t kdst = saddr(smem + st * L::STAGE);
+            const uint32_t vdst = kdst + L::TILE;
+            mbar_expect_tx(&bars->k_full[st], L::TILE);
 #pragma unroll
-          for (int c = 0; c < L::NBLK; ++c)
-            tma_load_3d(kdst + c * L::BLK, &tmk, &bars->k_full[st], c * 64, s.g, row0 + j * KT);
-          mbar_expect_tx(&bars->v_full[st], L::TILE);
+            for (int c = 0; c < L::NBLK; ++c)
+              tma_load_3d(kdst + c * L::BLK, &tmk, &bars->k_full[st], c * 64, s.g, row0 + j * KT);
+            mbar_expect_tx(&bars->v_full[st], L::TILE);
 #pragma unroll
-          for (int c = 0; c < L::NBLK; ++c)
-            tma_load_3d(vdst + c * L::BLK, &tmv, &bars->v_full[st], c * 64, s.g, row0 + j * KT);
+            for (int c = 0; c < L::NBLK; ++c)
+              tma_load_3d(vdst + c * L::BLK, &tmv, &bars->v_full[st], c * 64, s.g, row0 + j * KT);
+          }
         }
       }
       if (!ok || *abort) {
@@ -344,9 +402,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ S = Q K^T issuer
     if (lane == 0) {
-      constexpr uint32_t ID_S = idesc_bf16(KT, 0);
+      constexpr uint32_t ID_S = F8 ? idesc_f16(KT, 0) : idesc_bf16(KT, 0);
       // K: K-major, 128-byte rows, 8-row groups 1024 B apart; 32 B per 16-element step
-      const uint64_t kdesc0 = smem_desc(saddr(smem), 16, 1024);
+      const uint64_t kdesc0 = smem_desc(saddr(smem + (F8 ? L::CK : 0)), 16, 1024);
       int64_t t = t_begin;
       int u = u_first;
       Seg s;
@@ -356,20 +414,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (!mbar_wait(&bars->q_full, seg_i & 1, abort, p.flags)) break;
         fence_after();
         for (int j = s.j0; j < s.j1; ++j, ++it) {
-          const uint32_t st = it % NS, sb = it & 1;
-          if (!mbar_wait(&bars->k_full[st], (it / NS) & 1, abort, p.flags) ||
+          const uint32_t st = F8 ? it % L::NCK : it % NS, sb = it & 1;
+          uint64_t* kready = F8 ? &bars->kc_full[st] : &bars->k_full[st];
+          const uint32_t kpar = F8 ? (it / L::NCK) & 1 : (it / NS) & 1;
+          if (!mbar_wait(kready, kpar, abort, p.flags) ||
               (it >= 2 && !mbar_wait(&bars->s_free[sb], ((it >> 1) - 1) & 1, abort, p.flags))) {
             ok = false;
             break;
           }
           fence_after();
-          const uint64_t kd = kdesc0 + ((st * L::STAGE) >> 4);
+          const uint64_t kd = kdesc0 + ((st * (F8 ? L::TILE : L::STAGE)) >> 4);
           const uint32_t dcol = tmem + COL_S0 + sb * 128;
 #pragma unroll
           for (int kk = 0; kk < HD / 16; ++kk)
             mma_ts(dcol, tmem + COL_Q + kk * 8, kd + ((((kk >> 2) * L::BLK) + (kk & 3) * 32) >> 4),
                    ID_S, kk > 0 ? 1u : 0u);
           mma_commit(&bars->s_full[sb]);
+          if constexpr (F8) mma_commit(&bars->kc_empty[st]);
         }
         ++seg_i;
       }
@@ -384,9 +445,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // the next S has been issued. A stage is released after its P V, which follows its
     // S (the softmax read the scores before publishing P).
     if (lane == 0) {
-      constexpr uint32_t ID_PV = idesc_bf16(HD, 1);
+      constexpr uint32_t ID_PV = F8 ? idesc_f16(HD, 1) : idesc_bf16(HD, 1);
       // V: MN-major, 64-column blocks L::BLK apart (LBO), 8-key groups 1024 B apart (SBO)
-      const uint64_t vdesc0 = smem_desc(saddr(smem + L::TILE), L::BLK, 1024);
+      const uint64_t vdesc0 = smem_desc(saddr(smem + (F8 ? L::CV : L::TILE)), L::BLK, 1024);
       int64_t t = t_begin;
       int u = u_first;
       Seg s;
@@ -394,20 +455,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       bool ok = true;
       while (ok && seg_next(p, num_units, t, t_end, u, s)) {
         for (int j = s.j0; j < s.j1; ++j, ++it) {
-          const uint32_t st = it % NS;
+          const uint32_t st = F8 ? it % L::NCV : it % NS;
+          uint64_t* vready = F8 ? &bars->vc_full[st] : &bars->v_full[st];
+          const uint32_t vpar = F8 ? (it / L::NCV) & 1 : (it / NS) & 1;
           if (!mbar_wait(&bars->p_full, it & 1, abort, p.flags) ||
-              !mbar_wait(&bars->v_full[st], (it / NS) & 1, abort, p.flags)) {
+              !mbar_wait(vready, vpar, abort, p.flags)) {
             ok = false;
             break;
           }
           fence_after();
-          const uint64_t vd = vdesc0 + ((st * L::STAGE) >> 4);
+          const uint64_t vd = vdesc0 + ((st * (F8 ? L::TILE : L::STAGE)) >> 4);
 #pragma unroll
           for (int kk = 0; kk < KT / 16; ++kk)
             mma_ts(tmem + COL_O, tmem + COL_P + kk * 8, vd + ((kk * 16 * 128) >> 4), ID_PV,
                    (j == s.j0 && kk == 0) ? 0u : 1u);
           mma_commit(&bars->o_done);
-          mma_commit(&bars->kv_empty[st]);
+          mma_commit(F8 ? &bars->vc_empty[st] : &bars->kv_empty[st]);
         }
       }
       mma_commit(&bars->pv_final);
@@ -415,7 +478,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       while (!mbar_try(&bars->pv_final, 0) && clock64() - t0 < TIMEOUT_CYCLES) {
       }
     }
-  } else if (warp >= SOFTMAX_WARP0) {
+  } else if (warp >= SOFTMAX_WARP0 && warp < SOFTMAX_WARP0 + NSOFT / 32) {
     // ------------------------------------------------------------ softmax / epilogue
     // Two warpgroups share every query row: warpgroup h handles columns [64h, 64h + 64) of
     // each score tile and the same half of the output columns. They exchange half-tile
@@ -446,7 +509,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int i_row = live ? rg / p.G : D;
       const int hl = live ? rg % p.G : 0;
       const int64_t qrow = p.q_off[s.b] + i_row;
-      const float sc = p.scale_log2;
+      const float sc = F8 ? p.scale_log2 * p.kv_scale[s.g] : p.scale_log2;
+      const float vs = F8 ? p.kv_scale[p.Hkv + s.g] : 1.f;
 
       // Q row -> TMEM columns [COL_Q, COL_Q + HD/2) as packed bf16 pairs, 32 columns per
       // store (both warpgroups for d = 128, the first one for d = 64)
@@ -461,6 +525,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           rq[4 * e + 1] = v.y;
           rq[4 * e + 2] = v.z;
           rq[4 * e + 3] = v.w;
+        }
+        if constexpr (F8) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) rq[e] = bf16x2_to_f16x2(rq[e]);
         }
         tmem_st32(tq + COL_Q + wg * 32, rq);
         tmem_wait_st();
@@ -512,12 +580,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           if (!good) continue;  // leave together at the next barrier
           fence_after();
         }
+        // The decision is per row, but TMEM loads and stores are warp-collective: the whole
+        // warp rescales when any of its rows needs it, with alpha = 1 for the others.
+        float alpha = 1.f;
+        const bool grow = m_ref != -INFINITY && mt > m_ref + RESCALE_THRESHOLD;
         if (m_ref == -INFINITY) {
           m_ref = mt;  // O holds nothing yet for this row (zeros or about to be overwritten)
-        } else if (mt > m_ref + RESCALE_THRESHOLD) {
-          const float alpha = ex2(m_ref - mt);
+        } else if (grow) {
+          alpha = ex2(m_ref - mt);
           lh *= alpha;
           m_ref = mt;
+        }
+        if (__any_sync(0xffffffffu, grow)) {
 #pragma unroll 1
           for (int c = 0; c < OC / 32; ++c) {
             uint32_t ro[32];
@@ -543,13 +617,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         {
           uint32_t pk[32];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) pk[e] = pack_bf16(sv[2 * e], sv[2 * e + 1]);
+          for (int e = 0; e < 32; ++e) pk[e] = pack_p<F8>(sv[2 * e], sv[2 * e + 1]);
           tmem_st32(tq + COL_P + wg * 32, pk);
           tmem_wait_st();
         }
         const int tkey0 = j * KT;
         bool zeroed = false;
-        if (tkey0 + KT > nkeys) {
+        if (!F8 && tkey0 + KT > nkeys) {
           // last tile of the sequence: clear the V rows past its end so that P = 0 never
           // meets non-finite data (they may hold the next sequence or unwritten memory)
           const uint32_t st = it % NS;
@@ -581,7 +655,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // ---- epilogue: this warpgroup's half of the output columns
       const bool whole = s.j0 == 0 && s.j1 == s.nt;
       if (whole) {
-        const float inv = 1.f / l;
+        const float inv = vs / l;
         __nv_bfloat16* dst = (__nv_bfloat16*)p.out +
                              ((p.q_off[s.b] + i_row) * p.Hq + (int64_t)s.g * p.G + hl) * HD +
                              wg * OC;
@@ -624,6 +698,62 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
   }
 
+  if constexpr (F8) {
+    if (warp >= CONV_WARP0) {
+      // ---------------------------------------------------------- E4M3 -> f16 decoding
+      // warps 12-13 decode K tiles, 14-15 V tiles: raw 128-byte swizzled rows in, the
+      // 16-bit operand layout of the bf16 path (two 64-column swizzled blocks) out. Every
+      // code decodes to a finite value, so keys past a sequence's end need no clearing.
+      const bool is_k = warp < CONV_WARP0 + 2;
+      const int ct = (warp - CONV_WARP0 - (is_k ? 0 : 2)) * 32 + lane;
+      uint64_t* raw_full = is_k ? bars->k_full : bars->v_full;
+      uint64_t* cv_full = is_k ? bars->kc_full : bars->vc_full;
+      uint64_t* cv_empty = is_k ? bars->kc_empty : bars->vc_empty;
+      const uint32_t ncv = is_k ? L::NCK : L::NCV;
+      const uint8_t* raw0 = smem + (is_k ? L::RK : L::RV);
+      uint8_t* cv0 = smem + (is_k ? L::CK : L::CV);
+      int64_t t = t_begin;
+      int u = u_first;
+      Seg s;
+      uint32_t it = 0;
+      bool ok = true;
+      while (ok && seg_next(p, num_units, t, t_end, u, s)) {
+        for (int j = s.j0; j < s.j1; ++j, ++it) {
+          const uint32_t rs = it % NS, cs = it % ncv;
+          if (!mbar_wait(&raw_full[rs], (it / NS) & 1, abort, p.flags) ||
+              (it >= ncv && !mbar_wait(&cv_empty[cs], ((it / ncv) - 1) & 1, abort, p.flags))) {
+            ok = false;
+            break;
+          }
+          fence_after();
+          const uint8_t* raw = raw0 + rs * L::RAW;
+          uint8_t* cv = cv0 + cs * L::TILE;
+          // 128 rows x 8 sixteen-byte chunks; each chunk -> two 16-byte f16 chunks
+#pragma unroll 4
+          for (int q = ct; q < KT * 8; q += NCONV) {
+            const int r = q >> 3, c = q & 7;
+            const uint4 w = *reinterpret_cast<const uint4*>(raw + r * 128 + ((c ^ (r & 7)) << 4));
+            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+            uint32_t h[8];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              h[2 * e] = e4m3x2_to_f16x2(ww[e]);
+              h[2 * e + 1] = e4m3x2_to_f16x2(ww[e] >> 16);
+            }
+            uint8_t* row = cv + (c >> 2) * L::BLK + r * 128;
+            const int c0 = 2 * (c & 3);
+            *reinterpret_cast<uint4*>(row + ((c0 ^ (r & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+            *reinterpret_cast<uint4*>(row + (((c0 + 1) ^ (r & 7)) << 4)) =
+                make_uint4(h[4], h[5], h[6], h[7]);
+          }
+          fence_proxy_async();
+          mbar_arrive(&cv_full[cs]);
+          mbar_arrive(&bars->kv_empty[rs]);
+        }
+      }
+    }
+  }
+
   fence_before();
   __syncthreads();
   fence_after();
@@ -656,29 +786,34 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// [kv_rows, Hkv, HD] bf16 -> boxes of 64 columns x 1 head x KT rows, 128-byte swizzle.
-bool make_kv_map(CUtensorMap* map, const void* base, int64_t kv_rows, int hkv, int hd) {
+// [kv_rows, Hkv, HD] -> boxes of 128 bytes x 1 head x KT rows, 128-byte swizzle: 64 bf16
+// columns, or 128 one-byte E4M3 codes.
+bool make_kv_map(CUtensorMap* map, const void* base, int64_t kv_rows, int hkv, int hd, bool fp8) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
+  const cuuint64_t es = fp8 ? 1 : 2;
   const cuuint64_t dims[3] = {(cuuint64_t)hd, (cuuint64_t)hkv, (cuuint64_t)kv_rows};
-  const cuuint64_t strides[2] = {(cuuint64_t)hd * 2, (cuuint64_t)hkv * hd * 2};
-  const cuuint32_t box[3] = {64, 1, KT};
+  const cuuint64_t strides[2] = {(cuuint64_t)hd * es, (cuuint64_t)hkv * hd * es};
+  const cuuint32_t box[3] = {(cuuint32_t)(128 / es), 1, KT};
   const cuuint32_t estr[3] = {1, 1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
-            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return fn(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+            const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int HD>
+template <int HD, bool F8>
 cudaError_t launch_hd(const AttnParams& p, cudaStream_t s) {
+  using L = TcLayout<HD, F8>;
   CUtensorMap mk, mv;
-  if (!make_kv_map(&mk, p.k, p.kv_rows, p.Hkv, HD) || !make_kv_map(&mv, p.v, p.kv_rows, p.Hkv, HD))
+  if (!make_kv_map(&mk, p.k, p.kv_rows, p.Hkv, HD, F8) ||
+      !make_kv_map(&mv, p.v, p.kv_rows, p.Hkv, HD, F8))
     return cudaErrorInvalidValue;
-  const size_t smem = TcLayout<HD>::SMEM;
-  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<HD>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<HD, F8>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::SMEM);
   if (e != cudaSuccess) return e;
-  return launch_pdl(attn_tc_kernel<HD>, dim3(p.n_ctas), dim3(NTHREADS), smem, s, p, mk, mv);
+  return launch_pdl(attn_tc_kernel<HD, F8>, dim3(p.n_ctas), dim3(L::THREADS), L::SMEM, s, p, mk,
+                    mv);
 }
 
 }  // namespace
@@ -686,9 +821,13 @@ cudaError_t launch_hd(const AttnParams& p, cudaStream_t s) {
 bool attn_tc_available() { return encode_fn() != nullptr; }
 int attn_tc_kt() { return KT; }
 
+bool attn_tc_supports(int head_dim, bool fp8) { return head_dim == 128 || !fp8; }
+
 cudaError_t launch_attn_tc(const AttnParams& p, bool fp8, cudaStream_t s) {
-  if (fp8 || p.kv_rows <= 0 || p.kv_rows > 0x7fffffffLL) return cudaErrorNotSupported;
-  return p.d == 128 ? launch_hd<128>(p, s) : launch_hd<64>(p, s);
+  if (!attn_tc_supports(p.d, fp8) || p.kv_rows <= 0 || p.kv_rows > 0x7fffffffLL)
+    return cudaErrorNotSupported;
+  if (fp8) return launch_hd<128, true>(p, s);
+  return p.d == 128 ? launch_hd<128, false>(p, s) : launch_hd<64, false>(p, s);
 }
 
 }  // namespace sv

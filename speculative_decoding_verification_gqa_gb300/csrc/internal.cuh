@@ -131,6 +131,7 @@ cudaError_t launch_combine(const AttnParams& p, cudaStream_t s);
 cudaError_t launch_attn_mma(const AttnParams& p, bool fp8, cudaStream_t s);
 int attn_mma_kt();
 bool attn_tc_available();
+bool attn_tc_supports(int head_dim, bool fp8);
 int attn_tc_kt();
 cudaError_t launch_attn_tc(const AttnParams& p, bool fp8, cudaStream_t s);
 

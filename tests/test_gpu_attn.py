@@ -204,6 +204,33 @@ def test_window_mask_with_dominant_window_keys(kernel, T, D):
         assert np.abs(out[i, :, 1] - 1.0).max() <= 1e-2
 
 
+@pytest.mark.parametrize("kv", ["bf16", "fp8_e4m3"])
+def test_running_max_grows_on_some_rows_only(kernel, kv):
+    """Scores of half the query heads jump by ~12 (log2 units) from one 128-key tile to
+    the next while the other half stay flat, so the online-softmax rescale of O happens on
+    some rows of a warp and not on others, tile after tile."""
+    Hq, Hkv, d, T, D = 8, 2, 128, 700, 7
+    W = D + 1
+    rng = np.random.default_rng(3)
+    q = rng.standard_normal((W, Hq, d)).astype(np.float32) * 0.25
+    q[:, 0::2, 0] = 8.0                                # even heads see the ramp
+    q[:, 1::2, 0] = 0.0
+    k = rng.standard_normal((T + W, Hkv, d)).astype(np.float32) * 0.25
+    k[:, :, 0] = (np.arange(T + W) // 128)[:, None] * 12.0
+    v = rng.standard_normal((T + W, Hkv, d)).astype(np.float32)
+    w = synth.Workload("r", B=1, Hq=Hq, Hkv=Hkv, d=d, D=0, T=0, V=8, p=0.5, kv_dtype=kv)
+    if kv == "bf16":
+        x = dict(q=_bits(q), k=_bits(k), v=_bits(v), kv_scale=None)
+    else:
+        sk = np.abs(k).max(axis=(0, 2)) / 448.0
+        sv_ = np.abs(v).max(axis=(0, 2)) / 448.0
+        x = dict(q=_bits(q), k=synth.e4m3_codes(k / sk[None, :, None]),
+                 v=synth.e4m3_codes(v / sv_[None, :, None]),
+                 kv_scale=np.stack([sk, sv_]).astype(np.float32))
+    x.update(seq_lens=np.array([T], dtype=np.int32), draft_len=np.array([D], dtype=np.int32))
+    assert_close(gpu_attn(x), oracle_attn(w, x))
+
+
 def test_constant_values_select_the_kv_group(kernel):
     """V constant per KV head -> query head h returns the constant of KV head h // G."""
     B, Hq, Hkv, d, T, D = 3, 32, 4, 128, 500, 7
