@@ -57,8 +57,9 @@ struct __align__(8) Bars {
   uint32_t tmem_base;
   int abort;
   int u0;
-  float xmax[2][2][128];  // [tile parity][warpgroup][row]: half-tile row maxima
-  float xl[2][128];       // [warpgroup][row]: half sums at the end of a unit
+  // [tile parity][warpgroup][row]: half-tile row maxima; at the end of a unit the half
+  // sums go through the parity not used by the unit's last tile
+  float xmax[2][2][128];
 };
 
 __device__ __forceinline__ uint32_t saddr(const void* p) {
@@ -266,7 +267,7 @@ __device__ __forceinline__ bool seg_next(const AttnParams& p, int num_units, int
 
 // Shared memory. bf16 K/V: NS stages of (K tile, V tile), filled by TMA and read by the
 // MMAs. FP8 K/V: an NS-stage ring of raw E4M3 (K, V) tile pairs filled by TMA, decoded to
-// f16 by the converter warps into a 2-stage K ring and a 1-stage V ring read by the MMAs.
+// f16 by the converter warps into 2-stage K and V rings read by the MMAs.
 template <int HD, bool F8>
 struct TcLayout {
   static constexpr int BLK = KT * 128;            // one 64-column block of a 128-key tile
@@ -274,13 +275,13 @@ struct TcLayout {
   static constexpr int TILE = KT * HD * 2;        // one 16-bit K or V tile
   static constexpr int STAGE = 2 * TILE;          // bf16: K then V
   static constexpr int RAW = KT * HD;             // one E4M3 tile
-  static constexpr int NCK = 2, NCV = 1;          // FP8: decoded K / V stages
+  static constexpr int NCK = 2, NCV = 2;          // FP8: decoded K / V stages
   static constexpr int CK = 0;                    // FP8 offsets
   static constexpr int CV = CK + NCK * TILE;
   static constexpr int RK = CV + NCV * TILE;
   static constexpr int RV = RK + NS * RAW;
   static constexpr int BARS = F8 ? RV + NS * RAW : NS * STAGE;  // offset of the barrier block
-  static constexpr size_t SMEM = (size_t)BARS + sizeof(Bars) + 1024;  // + alignment slack
+  static constexpr size_t SMEM = (size_t)BARS + sizeof(Bars);
   static constexpr int THREADS = F8 ? NTHREADS + 4 * 32 : NTHREADS;
 };
 
@@ -289,8 +290,7 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
     attn_tc_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv) {
   using L = TcLayout<HD, F8>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  extern __shared__ __align__(1024) uint8_t smem[];  // 128-byte swizzled tiles: 1 KiB aligned
   Bars* bars = (Bars*)(smem + L::BARS);
   volatile int* abort = &bars->abort;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -303,6 +303,10 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
   const int64_t t_begin = (int64_t)blockIdx.x * TT / C;
   const int64_t t_end = (int64_t)(blockIdx.x + 1) * TT / C;
   if (TT == 0 || t_begin >= t_end) return;  // uniform across the CTA
+  if (saddr(smem) & 1023) {  // the swizzle phases below assume a 1 KiB-aligned base
+    if (tid == 0) atomicOr(p.flags, FLAG_ATTN_SHAPE);
+    return;
+  }
 
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
@@ -648,9 +652,10 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
         good = wwait(&bars->o_done, (it - 1) & 1);
         if (good) fence_after();
       }
-      bars->xl[wg][r] = lh;
+      float* xl = bars->xmax[it & 1][0];  // the last tile used parity (it - 1) & 1
+      xl[wg * 128 + r] = lh;
       if (!softmax_pair_and(good)) break;
-      const float l = lh + bars->xl[wg ^ 1][r];
+      const float l = lh + xl[(wg ^ 1) * 128 + r];
 
       // ---- epilogue: this warpgroup's half of the output columns
       const bool whole = s.j0 == 0 && s.j1 == s.nt;
@@ -728,23 +733,36 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
           fence_after();
           const uint8_t* raw = raw0 + rs * L::RAW;
           uint8_t* cv = cv0 + cs * L::TILE;
-          // 128 rows x 8 sixteen-byte chunks; each chunk -> two 16-byte f16 chunks
-#pragma unroll 4
-          for (int q = ct; q < KT * 8; q += NCONV) {
-            const int r = q >> 3, c = q & 7;
-            const uint4 w = *reinterpret_cast<const uint4*>(raw + r * 128 + ((c ^ (r & 7)) << 4));
-            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-            uint32_t h[8];
+          // 128 rows x 8 sixteen-byte chunks; each chunk -> two 16-byte f16 chunks. A thread
+          // owns 16 chunks, read 8 at a time so the shared-memory loads overlap.
+          constexpr int PER = KT * 8 / NCONV;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              h[2 * e] = e4m3x2_to_f16x2(ww[e]);
-              h[2 * e + 1] = e4m3x2_to_f16x2(ww[e] >> 16);
+          for (int h8 = 0; h8 < PER; h8 += 8) {
+            uint4 w[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const int q = ct + (h8 + k) * NCONV;
+              const int r = q >> 3, c = q & 7;
+              w[k] = *reinterpret_cast<const uint4*>(raw + r * 128 + ((c ^ (r & 7)) << 4));
             }
-            uint8_t* row = cv + (c >> 2) * L::BLK + r * 128;
-            const int c0 = 2 * (c & 3);
-            *reinterpret_cast<uint4*>(row + ((c0 ^ (r & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
-            *reinterpret_cast<uint4*>(row + (((c0 + 1) ^ (r & 7)) << 4)) =
-                make_uint4(h[4], h[5], h[6], h[7]);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const int q = ct + (h8 + k) * NCONV;
+              const int r = q >> 3, c = q & 7;
+              const uint32_t ww[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
+              uint32_t h[8];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                h[2 * e] = e4m3x2_to_f16x2(ww[e]);
+                h[2 * e + 1] = e4m3x2_to_f16x2(ww[e] >> 16);
+              }
+              uint8_t* row = cv + (c >> 2) * L::BLK + r * 128;
+              const int c0 = 2 * (c & 3);
+              *reinterpret_cast<uint4*>(row + ((c0 ^ (r & 7)) << 4)) =
+                  make_uint4(h[0], h[1], h[2], h[3]);
+              *reinterpret_cast<uint4*>(row + (((c0 + 1) ^ (r & 7)) << 4)) =
+                  make_uint4(h[4], h[5], h[6], h[7]);
+            }
           }
           fence_proxy_async();
           mbar_arrive(&cv_full[cs]);
