@@ -816,7 +816,10 @@ bool make_kv_map(CUtensorMap* map, const void* base, int64_t kv_rows, int hkv, i
   const cuuint32_t estr[3] = {1, 1, 1};
   return fn(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
             const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_SWIZZLE_128B,
+            // promote L2 fills to the bytes of one (row, head): 256 B of bf16, 128 B of E4M3;
+            // wider fills would pull in the neighbouring head and double the DRAM traffic
+            fp8 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B : CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
