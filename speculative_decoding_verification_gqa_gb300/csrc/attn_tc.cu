@@ -30,7 +30,6 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
-#include <cuda_fp8.h>
 
 #include "internal.cuh"
 
@@ -236,10 +235,13 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
   const float2 f = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&w));
   return pack_f16(f.x, f.y);
 }
-// two E4M3 codes (low byte first) -> f16 pair; exact, every E4M3 value is an f16 value
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t x) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(x & 0xffff), __NV_E4M3);
-  return (uint32_t)h.x | ((uint32_t)h.y << 16);
+// Four E4M3 codes (low byte first) -> two f16 pairs of the same values; exact, every E4M3
+// value is an f16 value. The 32-bit word splits into its two 16-bit halves for free.
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n .reg .b16 a, b;\n mov.b32 {a, b}, %2;\n cvt.rn.f16x2.e4m3x2 %0, a;\n"
+      " cvt.rn.f16x2.e4m3x2 %1, b;\n}\n"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
 }
 
 struct Seg {
@@ -733,35 +735,30 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
           fence_after();
           const uint8_t* raw = raw0 + rs * L::RAW;
           uint8_t* cv = cv0 + cs * L::TILE;
-          // 128 rows x 8 sixteen-byte chunks; each chunk -> two 16-byte f16 chunks. A thread
-          // owns 16 chunks, read 8 at a time so the shared-memory loads overlap.
+          // 128 rows x 8 sixteen-byte chunks; each chunk -> two 16-byte f16 chunks. Thread ct
+          // owns chunk column ct & 7 of rows ct / 8 + 8k, k = 0..15: its swizzle phase is the
+          // same for all of them, so the addresses advance by 1 KiB per row step.
+          const uint8_t* rsrc = raw + (ct >> 3) * 128 + (((ct & 7) ^ ((ct >> 3) & 7)) << 4);
+          const int rr = (ct >> 3) & 7, c0 = 2 * (ct & 3);
+          uint8_t* cdst = cv + ((ct & 7) >> 2) * L::BLK + (ct >> 3) * 128;
+          const int w0 = (c0 ^ rr) << 4, w1 = ((c0 + 1) ^ rr) << 4;
           constexpr int PER = KT * 8 / NCONV;
 #pragma unroll
           for (int h8 = 0; h8 < PER; h8 += 8) {
             uint4 w[8];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              const int q = ct + (h8 + k) * NCONV;
-              const int r = q >> 3, c = q & 7;
-              w[k] = *reinterpret_cast<const uint4*>(raw + r * 128 + ((c ^ (r & 7)) << 4));
-            }
+            for (int k = 0; k < 8; ++k)
+              w[k] = *reinterpret_cast<const uint4*>(rsrc + (h8 + k) * 1024);
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
-              const int q = ct + (h8 + k) * NCONV;
-              const int r = q >> 3, c = q & 7;
-              const uint32_t ww[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
               uint32_t h[8];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                h[2 * e] = e4m3x2_to_f16x2(ww[e]);
-                h[2 * e + 1] = e4m3x2_to_f16x2(ww[e] >> 16);
-              }
-              uint8_t* row = cv + (c >> 2) * L::BLK + r * 128;
-              const int c0 = 2 * (c & 3);
-              *reinterpret_cast<uint4*>(row + ((c0 ^ (r & 7)) << 4)) =
-                  make_uint4(h[0], h[1], h[2], h[3]);
-              *reinterpret_cast<uint4*>(row + (((c0 + 1) ^ (r & 7)) << 4)) =
-                  make_uint4(h[4], h[5], h[6], h[7]);
+              e4m3x4_to_f16x4(w[k].x, h[0], h[1]);
+              e4m3x4_to_f16x4(w[k].y, h[2], h[3]);
+              e4m3x4_to_f16x4(w[k].z, h[4], h[5]);
+              e4m3x4_to_f16x4(w[k].w, h[6], h[7]);
+              uint8_t* row = cdst + (h8 + k) * 1024;
+              *reinterpret_cast<uint4*>(row + w0) = make_uint4(h[0], h[1], h[2], h[3]);
+              *reinterpret_cast<uint4*>(row + w1) = make_uint4(h[4], h[5], h[6], h[7]);
             }
           }
           fence_proxy_async();
