@@ -3,16 +3,18 @@
 // Same work decomposition as the mma.sync kernel (persistent CTAs walking contiguous ranges
 // of the global tile line; see internal.cuh), with 128-key tiles and warp-specialised roles:
 //
-//   warp 0      TMA producer: K and V tiles of one KV head (128 keys x d, bf16, 128-byte
-//               swizzle) into a 3-stage shared-memory ring; a stage is released once the
-//               O += P V that reads its V tile has completed.
+//   warp 0      TMA producer: K and V tiles of one KV head (128 keys x d, 128-byte swizzle)
+//               into a shared-memory ring (3 stages of bf16, 4 of E4M3); a stage is
+//               released once every reader of it has finished.
 //   warp 1      S issuer (one thread): S = Q K^T into a double-buffered TMEM score tile.
-//   warps 12-15 (FP8 K/V only) decode E4M3 tiles to f16 operand tiles; the MMAs then run
-//               in f16 (Q and P too), the K scale folds into the score scale and the V
-//               scale into the normalisation.
 //   warp 3      P V issuer (one thread): O += P V into the TMEM accumulator.
 //               Q and P are tcgen05 A operands read straight from TMEM; K (K-major) and V
 //               (MN-major) come from shared memory through UMMA descriptors.
+//   warps 12-15 (FP8 K/V only) decode E4M3 V tiles to f16 operand tiles for P V (f16
+//               MMAs, P in f16). K is not decoded: S runs on the 8-bit tensor path with the
+//               raw E4M3 K tile as B and Q as A, Q held exactly as the sum of two E4M3
+//               terms (see split_q_e4m3), so S takes two 8-bit MMAs per 32-element step.
+//               The K scale folds into the score scale, the V scale into the normalisation.
 //   warps 4..11 softmax, two warpgroups: in each, thread r owns query row r (TMEM lane r)
 //               and one half of the columns. Per unit they write the Q row into TMEM; per
 //               tile they read their 64 scores, apply the scale and the window-causal
@@ -37,22 +39,27 @@ namespace sv {
 namespace {
 
 constexpr int KT = 128;          // keys per tile
-constexpr int NS = 3;            // shared-memory ring depth
+constexpr int NS = 3;            // shared-memory ring depth, bf16 K/V
+constexpr int NS8 = 4;           // shared-memory ring depth, E4M3 K/V
+constexpr int NSMAX = 4;
 constexpr int NTHREADS = 384;
 constexpr int SOFTMAX_WARP0 = 4;  // warps 4..7: columns 0..63 of a tile, 8..11: 64..127
 constexpr int NSOFT = 256;        // softmax threads (two warpgroups)
-constexpr int CONV_WARP0 = 12;    // FP8 only: warps 12-13 decode K tiles, 14-15 V tiles
-constexpr int NCONV = 64;         // decoding threads per tensor
+constexpr int CONV_WARP0 = 12;    // FP8 only: warps 12-15 decode V tiles
+constexpr int NCONV = 128;        // decoding threads
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t COL_O = 0, COL_S0 = 128, COL_P = 384, COL_Q = 448;
+// TMEM columns: O accumulator, two score tiles (each tile's P overwrites the first 32
+// columns of each warpgroup's half of it), Q as the A operand of S
+constexpr uint32_t COL_O = 0, COL_S0 = 128, COL_Q = 384;
 constexpr long long TIMEOUT_CYCLES = 4000000000LL;  // ~2 s at 2 GHz
 constexpr float RESCALE_THRESHOLD = 8.f;            // log2 units
 
 struct __align__(8) Bars {
-  uint64_t k_full[NS], v_full[NS], kv_empty[NS];
-  uint64_t kc_full[2], kc_empty[2], vc_full[2], vc_empty[2];  // FP8: decoded f16 tiles
-  uint64_t s_full[2], s_free[2];
-  uint64_t p_full, o_done, q_full, s_final, pv_final;
+  uint64_t k_full[NSMAX], v_full[NSMAX], kv_empty[NSMAX];
+  uint64_t vc_full[2], vc_empty[2];  // FP8: decoded f16 V tiles
+  uint64_t s_full[2], s_free[2];  // per score buffer; freed by the P V that reads its P
+  uint64_t p_full[2], o_done[2];  // per score buffer: P published / its P V complete
+  uint64_t q_full, s_final, pv_final;
   uint32_t tmem_base;
   int abort;
   int u0;
@@ -136,12 +143,26 @@ __host__ __device__ constexpr uint32_t idesc_f16(int n, int b_mn) {
          ((uint32_t)(128 >> 4) << 24);
 }
 
+// Instruction descriptor, kind::f8f6f4: fp32 accumulator, E4M3 A and B (format code 0),
+// both K-major, M = 128, N = n.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int n) {
+  return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+}
+
 // D[tmem] (+)= A[tmem] * B[smem]
 __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                        uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate));
+}
+// The same on the 8-bit path: A (TMEM) and B (shared memory) both E4M3, 32 K-elements.
+__device__ __forceinline__ void mma_ts_e4m3(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
@@ -179,6 +200,13 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
       "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(
           taddr),
       SV_W8(0), SV_W8(8), SV_W8(16), SV_W8(24)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16};" ::"r"(taddr),
+      SV_W8(0), SV_W8(8)
       : "memory");
 }
 __device__ __forceinline__ void tmem_wait_ld() {
@@ -230,11 +258,6 @@ template <bool F16>
 __device__ __forceinline__ uint32_t pack_p(float lo, float hi) {
   return F16 ? pack_f16(lo, hi) : pack_bf16(lo, hi);
 }
-// bf16 pair -> f16 pair (exact for |x| in f16's normal range)
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
-  const float2 f = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&w));
-  return pack_f16(f.x, f.y);
-}
 // Four E4M3 codes (low byte first) -> two f16 pairs of the same values; exact, every E4M3
 // value is an f16 value. The 32-bit word splits into its two 16-bit halves for free.
 __device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
@@ -242,6 +265,34 @@ __device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32
       " cvt.rn.f16x2.e4m3x2 %1, b;\n}\n"
       : "=r"(lo), "=r"(hi)
       : "r"(w));
+}
+
+// Two floats -> two E4M3 codes (the first in the low byte), nearest even, saturating.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// Two E4M3 codes (low byte first, in the low 16 bits) -> their values.
+__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t c) {
+  uint32_t h;
+  asm("{\n .reg .b16 a, b;\n mov.b32 {a, b}, %1;\n cvt.rn.f16x2.e4m3x2 %0, a;\n}\n"
+      : "=r"(h)
+      : "r"(c));
+  return __half22float2(*reinterpret_cast<__half2*>(&h));
+}
+// Four scaled Q elements x (|x| < 256, at most 8 significant bits each) as hi + lo, both
+// E4M3 (the first element in the low byte): hi = x rounded to E4M3, lo = x - hi rounded
+// to E4M3. hi keeps the top 4 significant bits and the remainder x - hi is k * ulp(x) with
+// |k| <= 8, so lo is exact whenever ulp(x) >= 2^-9 (E4M3's finest step), i.e. |x| >= 1/4;
+// below that, |x - hi - lo| <= 2^-10.
+__device__ __forceinline__ void split_q_e4m3(const float* x, uint32_t& whi, uint32_t& wlo) {
+  const uint32_t h01 = f32x2_to_e4m3x2(x[0], x[1]), h23 = f32x2_to_e4m3x2(x[2], x[3]);
+  const float2 d01 = e4m3x2_to_f32x2(h01), d23 = e4m3x2_to_f32x2(h23);
+  const uint32_t l01 = f32x2_to_e4m3x2(x[0] - d01.x, x[1] - d01.y);
+  const uint32_t l23 = f32x2_to_e4m3x2(x[2] - d23.x, x[3] - d23.y);
+  whi = h01 | (h23 << 16);
+  wlo = l01 | (l23 << 16);
 }
 
 struct Seg {
@@ -268,21 +319,22 @@ __device__ __forceinline__ bool seg_next(const AttnParams& p, int num_units, int
 }
 
 // Shared memory. bf16 K/V: NS stages of (K tile, V tile), filled by TMA and read by the
-// MMAs. FP8 K/V: an NS-stage ring of raw E4M3 (K, V) tile pairs filled by TMA, decoded to
-// f16 by the converter warps into 2-stage K and V rings read by the MMAs.
+// MMAs. FP8 K/V: an NS8-stage ring of raw E4M3 K and V tiles filled by TMA (K read by the
+// S MMAs as it is), and a 2-stage ring of V tiles decoded to f16 for the P V MMAs.
 template <int HD, bool F8>
 struct TcLayout {
+  static_assert(!F8 || HD == 128, "E4M3 rows of one head are one 128-byte swizzle row");
+  static constexpr int NR = F8 ? NS8 : NS;        // TMA ring stages
   static constexpr int BLK = KT * 128;            // one 64-column block of a 128-key tile
   static constexpr int NBLK = HD / 64;            // column blocks per tile
   static constexpr int TILE = KT * HD * 2;        // one 16-bit K or V tile
   static constexpr int STAGE = 2 * TILE;          // bf16: K then V
   static constexpr int RAW = KT * HD;             // one E4M3 tile
-  static constexpr int NCK = 2, NCV = 2;          // FP8: decoded K / V stages
-  static constexpr int CK = 0;                    // FP8 offsets
-  static constexpr int CV = CK + NCK * TILE;
+  static constexpr int NCV = 2;                   // FP8: decoded V stages
+  static constexpr int CV = 0;                    // FP8 offsets
   static constexpr int RK = CV + NCV * TILE;
-  static constexpr int RV = RK + NS * RAW;
-  static constexpr int BARS = F8 ? RV + NS * RAW : NS * STAGE;  // offset of the barrier block
+  static constexpr int RV = RK + NR * RAW;
+  static constexpr int BARS = F8 ? RV + NR * RAW : NR * STAGE;  // offset of the barrier block
   static constexpr size_t SMEM = (size_t)BARS + sizeof(Bars);
   static constexpr int THREADS = F8 ? NTHREADS + 4 * 32 : NTHREADS;
 };
@@ -311,23 +363,22 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
   }
 
   if (tid == 0) {
-    for (int s = 0; s < NS; ++s) {
+    for (int s = 0; s < L::NR; ++s) {
       mbar_init(&bars->k_full[s], 1);
       mbar_init(&bars->v_full[s], 1);
-      mbar_init(&bars->kv_empty[s], F8 ? 2 * NCONV : 1);  // FP8: freed by the converters
+      // bf16: freed by the P V commit; FP8: by the S commit and the V decoders
+      mbar_init(&bars->kv_empty[s], F8 ? NCONV + 1 : 1);
     }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&bars->kc_full[s], NCONV);
       mbar_init(&bars->vc_full[s], NCONV);
-      mbar_init(&bars->kc_empty[s], 1);
       mbar_init(&bars->vc_empty[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->s_full[s], 1);
-      mbar_init(&bars->s_free[s], NSOFT);
+      mbar_init(&bars->s_free[s], 1);
+      mbar_init(&bars->p_full[s], NSOFT);
+      mbar_init(&bars->o_done[s], 1);
     }
-    mbar_init(&bars->p_full, NSOFT);
-    mbar_init(&bars->o_done, 1);
     mbar_init(&bars->q_full, NSOFT);
     mbar_init(&bars->s_final, 1);
     mbar_init(&bars->pv_final, 1);
@@ -366,8 +417,9 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
       while (ok && seg_next(p, num_units, t, t_end, u, s)) {
         const int row0 = (int)p.kv_off[s.b];
         for (int j = s.j0; j < s.j1; ++j, ++it) {
-          const uint32_t st = it % NS;
-          if (it >= NS && !mbar_wait(&bars->kv_empty[st], ((it / NS) - 1) & 1, abort, p.flags)) {
+          const uint32_t st = it % L::NR;
+          if (it >= L::NR &&
+              !mbar_wait(&bars->kv_empty[st], ((it / L::NR) - 1) & 1, abort, p.flags)) {
             ok = false;
             break;
           }
@@ -395,8 +447,8 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
       }
       if (!ok || *abort) {
         // leave no copy in flight: wait (bounded) for the last fill of every stage
-        for (uint32_t st = 0; st < NS && st < it; ++st) {
-          const uint32_t fills = (it - 1 - st) / NS + 1;
+        for (uint32_t st = 0; st < L::NR && st < it; ++st) {
+          const uint32_t fills = (it - 1 - st) / L::NR + 1;
           const uint32_t par = (fills - 1) & 1;
           const long long t0 = clock64();
           while (!(mbar_try(&bars->k_full[st], par) && mbar_try(&bars->v_full[st], par)) &&
@@ -408,9 +460,10 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ S = Q K^T issuer
     if (lane == 0) {
-      constexpr uint32_t ID_S = F8 ? idesc_f16(KT, 0) : idesc_bf16(KT, 0);
-      // K: K-major, 128-byte rows, 8-row groups 1024 B apart; 32 B per 16-element step
-      const uint64_t kdesc0 = smem_desc(saddr(smem + (F8 ? L::CK : 0)), 16, 1024);
+      constexpr uint32_t ID_S = F8 ? idesc_e4m3(KT) : idesc_bf16(KT, 0);
+      // K: K-major, 128-byte rows, 8-row groups 1024 B apart; 32 B per K step (16 bf16 or
+      // 32 E4M3 elements)
+      const uint64_t kdesc0 = smem_desc(saddr(smem + (F8 ? L::RK : 0)), 16, 1024);
       int64_t t = t_begin;
       int u = u_first;
       Seg s;
@@ -420,23 +473,31 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
         if (!mbar_wait(&bars->q_full, seg_i & 1, abort, p.flags)) break;
         fence_after();
         for (int j = s.j0; j < s.j1; ++j, ++it) {
-          const uint32_t st = F8 ? it % L::NCK : it % NS, sb = it & 1;
-          uint64_t* kready = F8 ? &bars->kc_full[st] : &bars->k_full[st];
-          const uint32_t kpar = F8 ? (it / L::NCK) & 1 : (it / NS) & 1;
-          if (!mbar_wait(kready, kpar, abort, p.flags) ||
+          const uint32_t st = it % L::NR, sb = it & 1;
+          if (!mbar_wait(&bars->k_full[st], (it / L::NR) & 1, abort, p.flags) ||
               (it >= 2 && !mbar_wait(&bars->s_free[sb], ((it >> 1) - 1) & 1, abort, p.flags))) {
             ok = false;
             break;
           }
           fence_after();
-          const uint64_t kd = kdesc0 + ((st * (F8 ? L::TILE : L::STAGE)) >> 4);
+          const uint64_t kd = kdesc0 + ((st * (F8 ? L::RAW : L::STAGE)) >> 4);
           const uint32_t dcol = tmem + COL_S0 + sb * 128;
+          if constexpr (F8) {
+            // S = Q_hi K^T + Q_lo K^T: Q_hi in TMEM columns [COL_Q, +32), Q_lo in [+32, +64)
 #pragma unroll
-          for (int kk = 0; kk < HD / 16; ++kk)
-            mma_ts(dcol, tmem + COL_Q + kk * 8, kd + ((((kk >> 2) * L::BLK) + (kk & 3) * 32) >> 4),
-                   ID_S, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < HD / 32; ++kk) {
+              mma_ts_e4m3(dcol, tmem + COL_Q + kk * 8, kd + ((kk * 32) >> 4), ID_S,
+                          kk > 0 ? 1u : 0u);
+              mma_ts_e4m3(dcol, tmem + COL_Q + 32 + kk * 8, kd + ((kk * 32) >> 4), ID_S, 1u);
+            }
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < HD / 16; ++kk)
+              mma_ts(dcol, tmem + COL_Q + kk * 8,
+                     kd + ((((kk >> 2) * L::BLK) + (kk & 3) * 32) >> 4), ID_S, kk > 0 ? 1u : 0u);
+          }
           mma_commit(&bars->s_full[sb]);
-          if constexpr (F8) mma_commit(&bars->kc_empty[st]);
+          if constexpr (F8) mma_commit(&bars->kv_empty[st]);  // the raw K tile is read
         }
         ++seg_i;
       }
@@ -448,8 +509,9 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
   } else if (warp == 3) {
     // ------------------------------------------------------------ O += P V issuer
     // A thread of its own, so that P V starts as soon as P is ready instead of after
-    // the next S has been issued. A stage is released after its P V, which follows its
-    // S (the softmax read the scores before publishing P).
+    // the next S has been issued. P sits in the score buffer it was computed from; the
+    // P V commit frees that buffer for the S two tiles later, and the K/V stage (bf16)
+    // or decoded V stage (FP8).
     if (lane == 0) {
       constexpr uint32_t ID_PV = F8 ? idesc_f16(HD, 1) : idesc_bf16(HD, 1);
       // V: MN-major, 64-column blocks L::BLK apart (LBO), 8-key groups 1024 B apart (SBO)
@@ -461,21 +523,25 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
       bool ok = true;
       while (ok && seg_next(p, num_units, t, t_end, u, s)) {
         for (int j = s.j0; j < s.j1; ++j, ++it) {
-          const uint32_t st = F8 ? it % L::NCV : it % NS;
+          const uint32_t st = F8 ? it % L::NCV : it % L::NR;
           uint64_t* vready = F8 ? &bars->vc_full[st] : &bars->v_full[st];
-          const uint32_t vpar = F8 ? (it / L::NCV) & 1 : (it / NS) & 1;
-          if (!mbar_wait(&bars->p_full, it & 1, abort, p.flags) ||
+          const uint32_t vpar = F8 ? (it / L::NCV) & 1 : (it / L::NR) & 1;
+          const uint32_t sb = it & 1;
+          if (!mbar_wait(&bars->p_full[sb], (it >> 1) & 1, abort, p.flags) ||
               !mbar_wait(vready, vpar, abort, p.flags)) {
             ok = false;
             break;
           }
           fence_after();
           const uint64_t vd = vdesc0 + ((st * (F8 ? L::TILE : L::STAGE)) >> 4);
+          // keys [16kk, 16kk + 16): warpgroup kk / 4 wrote them at its half's first columns
+          const uint32_t pcol = tmem + COL_S0 + sb * 128;
 #pragma unroll
           for (int kk = 0; kk < KT / 16; ++kk)
-            mma_ts(tmem + COL_O, tmem + COL_P + kk * 8, vd + ((kk * 16 * 128) >> 4), ID_PV,
-                   (j == s.j0 && kk == 0) ? 0u : 1u);
-          mma_commit(&bars->o_done);
+            mma_ts(tmem + COL_O, pcol + (kk >> 2) * (KT / 2) + (kk & 3) * 8,
+                   vd + ((kk * 16 * 128) >> 4), ID_PV, (j == s.j0 && kk == 0) ? 0u : 1u);
+          mma_commit(&bars->o_done[sb]);
+          mma_commit(&bars->s_free[sb]);
           mma_commit(F8 ? &bars->vc_empty[st] : &bars->kv_empty[st]);
         }
       }
@@ -515,26 +581,58 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
       const int i_row = live ? rg / p.G : D;
       const int hl = live ? rg % p.G : 0;
       const int64_t qrow = p.q_off[s.b] + i_row;
-      const float sc = F8 ? p.scale_log2 * p.kv_scale[s.g] : p.scale_log2;
+      float sc = p.scale_log2;  // score scale in log2 units
       const float vs = F8 ? p.kv_scale[p.Hkv + s.g] : 1.f;
+      const uint4* qsrc = reinterpret_cast<const uint4*>(
+          (const __nv_bfloat16*)p.q + (qrow * p.Hq + (int64_t)s.g * p.G + hl) * HD);
 
-      // Q row -> TMEM columns [COL_Q, COL_Q + HD/2) as packed bf16 pairs, 32 columns per
-      // store (both warpgroups for d = 128, the first one for d = 64)
-      if (wg < HD / 64) {
-        const uint4* src = reinterpret_cast<const uint4*>(
-            (const __nv_bfloat16*)p.q + (qrow * p.Hq + (int64_t)s.g * p.G + hl) * HD);
-        uint32_t rq[32];
+      if constexpr (F8) {
+        // Q row x 2^e -> E4M3 hi + lo terms in TMEM columns [COL_Q, +32) and [+32, +64),
+        // this warpgroup's half of d in each. e puts the row's largest |q| in [128, 256),
+        // so the pair holds every element to within 2^-17 of that maximum (exactly, for
+        // elements within 2^-9 of it); 2^-e joins the K scale in the score scale.
+        uint32_t rq[HD / 4];  // this warpgroup's half of the row
+        uint32_t amax = 0;    // largest bf16 magnitude of the row (integer order = magnitude)
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const uint4 v = live ? __ldg(src + wg * 8 + e) : make_uint4(0, 0, 0, 0);
+        for (int e = 0; e < HD / 16; ++e) {
+          const uint4 v = live ? __ldg(qsrc + wg * (HD / 16) + e) : make_uint4(0, 0, 0, 0);
+          const uint4 o = live ? __ldg(qsrc + (wg ^ 1) * (HD / 16) + e) : make_uint4(0, 0, 0, 0);
           rq[4 * e] = v.x;
           rq[4 * e + 1] = v.y;
           rq[4 * e + 2] = v.z;
           rq[4 * e + 3] = v.w;
-        }
-        if constexpr (F8) {
+          const uint32_t both[8] = {v.x, v.y, v.z, v.w, o.x, o.y, o.z, o.w};
 #pragma unroll
-          for (int e = 0; e < 32; ++e) rq[e] = bf16x2_to_f16x2(rq[e]);
+          for (int k = 0; k < 8; ++k)
+            amax = max(amax, max(both[k] & 0x7fffu, (both[k] >> 16) & 0x7fffu));
+        }
+        // amax in [2^(eb-127), 2^(eb-126)): e = 8 - (eb - 126), clamped to keep 2^+-e normal
+        const int eb = max((int)(amax >> 7), 1);
+        const int e2 = amax == 0 ? 0 : min(max(134 - eb, -120), 120);
+        const float f = __int_as_float((e2 + 127) << 23);
+        uint32_t hi[16], lo[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const uint32_t a = rq[2 * c], b = rq[2 * c + 1];
+          const float x[4] = {__uint_as_float(a << 16) * f, __uint_as_float(a & 0xffff0000u) * f,
+                              __uint_as_float(b << 16) * f, __uint_as_float(b & 0xffff0000u) * f};
+          split_q_e4m3(x, hi[c], lo[c]);
+        }
+        tmem_st16(tq + COL_Q + wg * 16, hi);
+        tmem_st16(tq + COL_Q + 32 + wg * 16, lo);
+        tmem_wait_st();
+        sc = p.scale_log2 * p.kv_scale[s.g] * __int_as_float((127 - e2) << 23);
+      } else if (wg < HD / 64) {
+        // Q row -> TMEM columns [COL_Q, COL_Q + HD/2) as packed bf16 pairs, 32 columns per
+        // store (both warpgroups for d = 128, the first one for d = 64)
+        uint32_t rq[32];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const uint4 v = live ? __ldg(qsrc + wg * 8 + e) : make_uint4(0, 0, 0, 0);
+          rq[4 * e] = v.x;
+          rq[4 * e + 1] = v.y;
+          rq[4 * e + 2] = v.z;
+          rq[4 * e + 3] = v.w;
         }
         tmem_st32(tq + COL_Q + wg * 32, rq);
         tmem_wait_st();
@@ -558,8 +656,6 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
           tmem_wait_ld();
 #pragma unroll
           for (int c = 0; c < HC / 32; ++c) reg_fence32(raw + c * 32);
-          fence_before();
-          mbar_arrive(&bars->s_free[sb]);
           if (key0 + HC - 1 > T) {  // the window-causal mask reaches into this half tile
             const int lim = T + i_row - key0;
 #pragma unroll
@@ -581,11 +677,6 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
         }
         mx = fmaxf(mx, bars->xmax[sb][wg ^ 1][r]);
         const float mt = mx * sc;  // tile max in log2 units (sc > 0)
-        if (j > s.j0) {
-          good = wwait(&bars->o_done, (it - 1) & 1);
-          if (!good) continue;  // leave together at the next barrier
-          fence_after();
-        }
         // The decision is per row, but TMEM loads and stores are warp-collective: the whole
         // warp rescales when any of its rows needs it, with alpha = 1 for the others.
         float alpha = 1.f;
@@ -598,6 +689,14 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
           m_ref = mt;
         }
         if (__any_sync(0xffffffffu, grow)) {
+          // O is only touched once the previous tile's P V is complete (never on a unit's
+          // first tile: grow is false there). That P V's buffer barrier is at most one
+          // phase behind it: the previous tile's S was issued only after the P V two
+          // tiles before it had completed.
+          const uint32_t pb = (it - 1) & 1;
+          good = wwait(&bars->o_done[pb], ((it - 1) >> 1) & 1);
+          if (!good) continue;  // leave together at the next barrier
+          fence_after();
 #pragma unroll 1
           for (int c = 0; c < OC / 32; ++c) {
             uint32_t ro[32];
@@ -624,7 +723,7 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
           uint32_t pk[32];
 #pragma unroll
           for (int e = 0; e < 32; ++e) pk[e] = pack_p<F8>(sv[2 * e], sv[2 * e + 1]);
-          tmem_st32(tq + COL_P + wg * 32, pk);
+          tmem_st32(tq + COL_S0 + sb * 128 + wg * HC, pk);
           tmem_wait_st();
         }
         const int tkey0 = j * KT;
@@ -632,8 +731,8 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
         if (!F8 && tkey0 + KT > nkeys) {
           // last tile of the sequence: clear the V rows past its end so that P = 0 never
           // meets non-finite data (they may hold the next sequence or unwritten memory)
-          const uint32_t st = it % NS;
-          good = wwait(&bars->v_full[st], (it / NS) & 1);
+          const uint32_t st = it % L::NR;
+          good = wwait(&bars->v_full[st], (it / L::NR) & 1);
           if (!good) continue;
           const int first = nkeys - tkey0;
           uint8_t* vt = smem + st * L::STAGE + L::TILE;
@@ -647,11 +746,11 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
         }
         if (zeroed) fence_proxy_async();
         fence_before();
-        mbar_arrive(&bars->p_full);
+        mbar_arrive(&bars->p_full[sb]);
       }
       if (!ok) break;
-      if (good) {
-        good = wwait(&bars->o_done, (it - 1) & 1);
+      if (good) {  // the unit's last P V (and with it every earlier one) is complete
+        good = wwait(&bars->o_done[(it - 1) & 1], ((it - 1) >> 1) & 1);
         if (good) fence_after();
       }
       float* xl = bars->xmax[it & 1][0];  // the last tile used parity (it - 1) & 1
@@ -707,63 +806,62 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
 
   if constexpr (F8) {
     if (warp >= CONV_WARP0) {
-      // ---------------------------------------------------------- E4M3 -> f16 decoding
-      // warps 12-13 decode K tiles, 14-15 V tiles: raw 128-byte swizzled rows in, the
-      // 16-bit operand layout of the bf16 path (two 64-column swizzled blocks) out. Every
-      // code decodes to a finite value, so keys past a sequence's end need no clearing.
-      const bool is_k = warp < CONV_WARP0 + 2;
-      const int ct = (warp - CONV_WARP0 - (is_k ? 0 : 2)) * 32 + lane;
-      uint64_t* raw_full = is_k ? bars->k_full : bars->v_full;
-      uint64_t* cv_full = is_k ? bars->kc_full : bars->vc_full;
-      uint64_t* cv_empty = is_k ? bars->kc_empty : bars->vc_empty;
-      const uint32_t ncv = is_k ? L::NCK : L::NCV;
-      const uint8_t* raw0 = smem + (is_k ? L::RK : L::RV);
-      uint8_t* cv0 = smem + (is_k ? L::CK : L::CV);
+      // ---------------------------------------------------------- E4M3 -> f16 V decoding
+      // Raw 128-byte swizzled rows in, the 16-bit MN-major operand layout of the bf16 path
+      // (two 64-column swizzled blocks) out. Thread ct owns 16-byte chunk column c = ct & 7
+      // of rows rw + 16k, rw = (ct >> 3) ^ (c >> 2): each group of eight lanes takes the
+      // eight chunk columns from two rows of opposite parity, so its 16-byte loads and
+      // stores fall in eight different bank groups. Rows past the sequence's last key are
+      // written as zeros (P is zero there, and 0 x NaN would not be).
+      const int ct = (warp - CONV_WARP0) * 32 + lane;
+      const int c = ct & 7;
+      const int rw = (ct >> 3) ^ (c >> 2);
+      const int ph = rw & 7;  // swizzle phase of rows rw + 16k
+      const uint32_t src_off = rw * 128 + ((c ^ ph) << 4);
+      const uint32_t dst_off = (c >> 2) * L::BLK + rw * 128;
+      const uint32_t w0 = ((2 * (c & 3)) ^ ph) << 4, w1 = ((2 * (c & 3) + 1) ^ ph) << 4;
+      constexpr int RSTEP = 16 * 128;  // bytes between a thread's rows
       int64_t t = t_begin;
       int u = u_first;
       Seg s;
       uint32_t it = 0;
       bool ok = true;
       while (ok && seg_next(p, num_units, t, t_end, u, s)) {
+        const int nkeys = p.seq_lens[s.b] + p.draft_len[s.b] + 1;
         for (int j = s.j0; j < s.j1; ++j, ++it) {
-          const uint32_t rs = it % NS, cs = it % ncv;
-          if (!mbar_wait(&raw_full[rs], (it / NS) & 1, abort, p.flags) ||
-              (it >= ncv && !mbar_wait(&cv_empty[cs], ((it / ncv) - 1) & 1, abort, p.flags))) {
+          const uint32_t rs = it % L::NR, cs = it % L::NCV;
+          if (!mbar_wait(&bars->v_full[rs], (it / L::NR) & 1, abort, p.flags) ||
+              (it >= L::NCV &&
+               !mbar_wait(&bars->vc_empty[cs], ((it / L::NCV) - 1) & 1, abort, p.flags))) {
             ok = false;
             break;
           }
           fence_after();
-          const uint8_t* raw = raw0 + rs * L::RAW;
-          uint8_t* cv = cv0 + cs * L::TILE;
-          // 128 rows x 8 sixteen-byte chunks; each chunk -> two 16-byte f16 chunks. Thread ct
-          // owns chunk column ct & 7 of rows ct / 8 + 8k, k = 0..15: its swizzle phase is the
-          // same for all of them, so the addresses advance by 1 KiB per row step.
-          const uint8_t* rsrc = raw + (ct >> 3) * 128 + (((ct & 7) ^ ((ct >> 3) & 7)) << 4);
-          const int rr = (ct >> 3) & 7, c0 = 2 * (ct & 3);
-          uint8_t* cdst = cv + ((ct & 7) >> 2) * L::BLK + (ct >> 3) * 128;
-          const int w0 = (c0 ^ rr) << 4, w1 = ((c0 + 1) ^ rr) << 4;
-          constexpr int PER = KT * 8 / NCONV;
+          const uint8_t* rsrc = smem + L::RV + rs * L::RAW + src_off;
+          uint8_t* cdst = smem + L::CV + cs * L::TILE + dst_off;
+          uint4 w[KT / 16];
 #pragma unroll
-          for (int h8 = 0; h8 < PER; h8 += 8) {
-            uint4 w[8];
+          for (int k = 0; k < KT / 16; ++k)
+            w[k] = *reinterpret_cast<const uint4*>(rsrc + k * RSTEP);
+          mbar_arrive(&bars->kv_empty[rs]);  // the raw V tile is read
+          const int lim = nkeys - j * KT;    // rows >= lim lie past the sequence's end
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-              w[k] = *reinterpret_cast<const uint4*>(rsrc + (h8 + k) * 1024);
+          for (int k = 0; k < KT / 16; ++k) {
+            uint32_t h[8];
+            e4m3x4_to_f16x4(w[k].x, h[0], h[1]);
+            e4m3x4_to_f16x4(w[k].y, h[2], h[3]);
+            e4m3x4_to_f16x4(w[k].z, h[4], h[5]);
+            e4m3x4_to_f16x4(w[k].w, h[6], h[7]);
+            if (rw + 16 * k >= lim) {
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              uint32_t h[8];
-              e4m3x4_to_f16x4(w[k].x, h[0], h[1]);
-              e4m3x4_to_f16x4(w[k].y, h[2], h[3]);
-              e4m3x4_to_f16x4(w[k].z, h[4], h[5]);
-              e4m3x4_to_f16x4(w[k].w, h[6], h[7]);
-              uint8_t* row = cdst + (h8 + k) * 1024;
-              *reinterpret_cast<uint4*>(row + w0) = make_uint4(h[0], h[1], h[2], h[3]);
-              *reinterpret_cast<uint4*>(row + w1) = make_uint4(h[4], h[5], h[6], h[7]);
+              for (int e = 0; e < 8; ++e) h[e] = 0u;
             }
+            uint8_t* row = cdst + k * RSTEP;
+            *reinterpret_cast<uint4*>(row + w0) = make_uint4(h[0], h[1], h[2], h[3]);
+            *reinterpret_cast<uint4*>(row + w1) = make_uint4(h[4], h[5], h[6], h[7]);
           }
           fence_proxy_async();
-          mbar_arrive(&cv_full[cs]);
-          mbar_arrive(&bars->kv_empty[rs]);
+          mbar_arrive(&bars->vc_full[cs]);
         }
       }
     }

@@ -219,16 +219,55 @@ def test_running_max_grows_on_some_rows_only(kernel, kv):
     k[:, :, 0] = (np.arange(T + W) // 128)[:, None] * 12.0
     v = rng.standard_normal((T + W, Hkv, d)).astype(np.float32)
     w = synth.Workload("r", B=1, Hq=Hq, Hkv=Hkv, d=d, D=0, T=0, V=8, p=0.5, kv_dtype=kv)
-    if kv == "bf16":
-        x = dict(q=_bits(q), k=_bits(k), v=_bits(v), kv_scale=None)
-    else:
-        sk = np.abs(k).max(axis=(0, 2)) / 448.0
-        sv_ = np.abs(v).max(axis=(0, 2)) / 448.0
-        x = dict(q=_bits(q), k=synth.e4m3_codes(k / sk[None, :, None]),
-                 v=synth.e4m3_codes(v / sv_[None, :, None]),
-                 kv_scale=np.stack([sk, sv_]).astype(np.float32))
+    x = dict(q=_bits(q))
+    x.update(dict(k=_bits(k), v=_bits(v), kv_scale=None) if kv == "bf16" else _fp8_kv(k, v))
     x.update(seq_lens=np.array([T], dtype=np.int32), draft_len=np.array([D], dtype=np.int32))
     assert_close(gpu_attn(x), oracle_attn(w, x))
+
+
+def _fp8_kv(k, v):
+    """Per-KV-head E4M3 quantisation of float K and V (scale = absmax / 448)."""
+    sk = np.abs(k).max(axis=(0, 2)) / 448.0
+    sv_ = np.abs(v).max(axis=(0, 2)) / 448.0
+    return dict(k=synth.e4m3_codes(k / sk[None, :, None]),
+                v=synth.e4m3_codes(v / sv_[None, :, None]),
+                kv_scale=np.stack([sk, sv_]).astype(np.float32))
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8_e4m3"])
+def test_query_rows_of_wide_dynamic_range(kernel, kv):
+    """Query rows scaled by 2^-12 .. 2^8, the elements of each row spread over 2^-10 .. 2^2:
+    the large rows give sharp score distributions, in which an error of 1/16 in a Q element
+    moves P by tens of percent, and the tiny rows average V almost uniformly. On the 8-bit
+    score path this checks the per-row power-of-two scale and both E4M3 terms of Q."""
+    Hq, Hkv, d, T, D = 8, 1, 128, 400, 3
+    W = D + 1
+    rng = np.random.default_rng(11)
+    q = rng.standard_normal((W, Hq, d)) * np.exp2(rng.uniform(-10, 2, (W, Hq, d)))
+    q *= np.exp2(np.array([-12, -4, 0, 1, 2, 3, 6, 8], dtype=np.float64))[None, :, None]
+    k = rng.standard_normal((T + W, Hkv, d)).astype(np.float32)
+    v = rng.standard_normal((T + W, Hkv, d)).astype(np.float32)
+    w = synth.Workload("q", B=1, Hq=Hq, Hkv=Hkv, d=d, D=0, T=0, V=8, p=0.5, kv_dtype=kv)
+    x = dict(q=_bits(q), seq_lens=np.array([T], dtype=np.int32),
+             draft_len=np.array([D], dtype=np.int32))
+    x.update(dict(k=_bits(k), v=_bits(v), kv_scale=None) if kv == "bf16" else _fp8_kv(k, v))
+    assert_close(gpu_attn(x), oracle_attn(w, x))
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8_e4m3"])
+def test_nan_rows_after_the_last_sequence(kernel, kv):
+    """K/V tensors longer than the packed batch, the extra rows full of NaN codes: the last
+    sequence's last tile overlaps them, and they must not reach its output (P is 0 there,
+    but 0 x NaN is NaN)."""
+    w, x = _small(B=2, Hq=8, Hkv=2, d=128, T=(300, 190), D=(5, 3), kv=kv, seed=4)
+    pad = 200
+    for name in ("k", "v"):
+        a = x[name]
+        fill = 0x7F if a.dtype == np.uint8 else 0x7FC0  # E4M3 NaN / bf16 quiet NaN
+        x[name] = np.concatenate([a, np.full((pad,) + a.shape[1:], fill, dtype=a.dtype)])
+    got = gpu_attn(x)
+    assert np.isfinite(bf16_to_f64(got)).all()
+    assert_close(got, oracle_attn(w, x))
 
 
 def test_constant_values_select_the_kv_group(kernel):
