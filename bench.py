@@ -464,7 +464,8 @@ def run_ours(args):
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                 "ms_per_step": round(e2e_ms, 4), "steps": e2e["steps"]},
             "clocks": clk,
-            "gpu_launches": 5 * K,
+            # plan, attention, combine (verify call); argmax + acceptance (accept call)
+            "gpu_launches": 4 * K,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -25,8 +25,10 @@
  *     buffers) make the kernels skip all work and leave outputs untouched; they set a
  *     sticky flag in the workspace that sv_workspace_status() reports.
  *   - A workspace must be zero-filled once before its first use (the flags live in its
- *     first 256 bytes) and may be reused by later calls on the same stream. Two calls
- *     that run concurrently must not share a workspace.
+ *     first 256 bytes; spec_accept also keeps a completion counter and one key per row
+ *     there, which every call leaves at zero) and may be reused by later calls of the
+ *     same entry point on the same stream. Two calls that run concurrently must not
+ *     share a workspace.
  *   - Return value: SV_OK or an error code; nothing is printed and nothing is thrown.
  *
  * Packed ragged layout (uniform batches are the special case with equal lengths):
@@ -149,8 +151,7 @@ SV_API sv_status spec_accept(int32_t batch, int32_t max_draft_len, int32_t vocab
  * in a device array of SV_ACCEPT_NOALLOC_MAX_WORKSPACE bytes compiled into the library:
  *   - every GPU that loads the library holds that memory until the process exits;
  *   - a shape whose spec_accept_workspace_size() exceeds it is rejected with
- *     SV_ERR_WORKSPACE and nothing is launched (512 KiB covers, for example, 64,000
- *     window rows on a 152-SM GPU);
+ *     SV_ERR_WORKSPACE and nothing is launched (512 KiB covers 43,000 window rows);
  *   - the first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call before any
  *     stream capture;

@@ -3,13 +3,16 @@
 // "Speculative decoding (2)": the target's own token takes the place of the first
 // rejected draft).
 //
-// Kernel 1 (argmax_partial): persistent CTAs, each scanning an equal contiguous range of
-//   the packed logits with 16-byte streaming loads, a running (value, index) per thread, then
-//   warp-shuffle and shared-memory reductions with the comparator "larger value wins, equal
-//   values: smaller index wins", one candidate per row the range touches. Values are
-//   compared exactly in fp32 (bf16 widens exactly).
-// Kernel 2 (finalize): one CTA per sequence. Merges the candidates of its 1 + D_b rows,
-//   then finds the first position whose draft differs from the target's token.
+// One kernel of persistent CTAs, each scanning an equal contiguous range of the packed
+// logits with 16-byte streaming loads. Per thread and row, only each vector's maximum
+// (packed max instructions) is compared, without branches, and the best vector is kept;
+// the element index inside it is resolved once at the end of the row. Warp-shuffle
+// reductions with the comparator "larger value wins, equal values: smaller index wins"
+// give one candidate per warp and row, folded into the row's 64-bit key (order-preserving
+// value bits above the inverted index) with one atomicMax. Values are compared exactly in
+// fp32 (bf16 widens exactly). The last CTA to finish (a completion ticket in the
+// workspace) reads and clears every row's key, which is the target's token, and, per
+// sequence, finds the first position whose draft differs from it.
 #include <cuda_bf16.h>
 
 #include "internal.cuh"
@@ -18,13 +21,11 @@ namespace sv {
 namespace {
 
 constexpr int ARGMAX_THREADS = 512;
-constexpr int UNROLL = 4;
+// Two CTAs of 512 threads per SM, each thread with eight 16-byte loads in flight (64
+// registers): measured faster than four CTAs with four loads each (32 registers).
+constexpr int ARGMAX_CTAS_PER_SM = 2;
+constexpr int UNROLL = 8;
 constexpr int NONE = 0x7fffffff;  // "no candidate yet"
-
-struct Cand {
-  float v;
-  int i;
-};
 
 __device__ __forceinline__ bool better(float v1, int i1, float v2, int i2) {
   if (i1 == NONE) return false;
@@ -44,7 +45,18 @@ __device__ __forceinline__ float bf16_at(uint32_t w, int hi) {
   return __uint_as_float(hi ? (w & 0xffff0000u) : (w << 16));
 }
 
-__device__ __forceinline__ void block_argmax(float& bv, int& bi, Cand* sh) {
+__device__ __forceinline__ __nv_bfloat162 as_bf2(uint32_t w) {
+  return *reinterpret_cast<const __nv_bfloat162*>(&w);
+}
+
+// Largest of eight bf16 values (NaN ignored unless all are NaN), widened to fp32.
+__device__ __forceinline__ float vmax_bf16x8(const uint4& w) {
+  const __nv_bfloat162 m = __hmax2(__hmax2(as_bf2(w.x), as_bf2(w.y)), __hmax2(as_bf2(w.z), as_bf2(w.w)));
+  const uint32_t u = *reinterpret_cast<const uint32_t*>(&m);
+  return fmaxf(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+}
+
+__device__ __forceinline__ void warp_argmax(float& bv, int& bi) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     const float v2 = __shfl_xor_sync(0xffffffffu, bv, o);
@@ -54,53 +66,19 @@ __device__ __forceinline__ void block_argmax(float& bv, int& bi, Cand* sh) {
       bi = i2;
     }
   }
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  if (lane == 0) sh[wid] = Cand{bv, bi};
-  __syncthreads();
-  if (wid == 0) {
-    const int nw = blockDim.x >> 5;
-    bv = lane < nw ? sh[lane].v : 0.f;
-    bi = lane < nw ? sh[lane].i : NONE;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float v2 = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int i2 = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (better(v2, i2, bv, bi)) {
-        bv = v2;
-        bi = i2;
-      }
-    }
-  }
 }
 
-// Sum of (1 + D_b') and D_b' over b' < b; returns false if any D_b' is out of range.
-__device__ bool prefix_offsets(const int32_t* draft_len, int b, int max_draft, int64_t* q_off,
-                               int64_t* d_off) {
-  __shared__ long long s_q, s_d;
-  __shared__ int s_bad;
-  if (threadIdx.x == 0) {
-    s_q = 0;
-    s_d = 0;
-    s_bad = 0;
-  }
-  __syncthreads();
-  long long q = 0, d = 0;
-  int bad = 0;
-  for (int bb = threadIdx.x; bb < b; bb += blockDim.x) {
-    const int D = draft_len[bb];
-    bad |= (D < 0 || D > max_draft);
-    q += 1 + D;
-    d += D;
-  }
-  if (q) atomicAdd((unsigned long long*)&s_q, (unsigned long long)q);
-  if (d) atomicAdd((unsigned long long*)&s_d, (unsigned long long)d);
-  if (bad) s_bad = 1;
-  __syncthreads();
-  *q_off = s_q;
-  *d_off = s_d;
-  const bool ok = !s_bad;
-  __syncthreads();
-  return ok;
+
+// Row key: the value's bits mapped to an unsigned integer of the same order (-0 taken as
+// +0, so the two tie) above 0xffffffff - index, so a larger key is a larger value or the
+// same value at a smaller index. 0 means "no candidate" (below every value's key).
+__device__ __forceinline__ unsigned long long row_key(float v, int i) {
+  uint32_t u = v == 0.f ? 0u : __float_as_uint(v);
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return ((unsigned long long)u << 32) | (0xffffffffu - (uint32_t)i);
+}
+__device__ __forceinline__ int key_index(unsigned long long k) {
+  return (int)(0xffffffffu - (uint32_t)k);
 }
 
 struct AcceptArgs {
@@ -111,12 +89,20 @@ struct AcceptArgs {
   int32_t* next_token;
   int32_t* target_tokens;
   uint32_t* flags;
-  Cand* part;  // [nctas + B * (1 + max_draft)]: slot c + r = CTA c's part of row r
+  uint32_t* ticket;         // CTAs of this call that have finished; reset by the last one
+  unsigned long long* key;  // [B * (1 + max_draft)]: best (value, index) of every row so
+                            // far; read and reset to 0 by the last CTA
+  int32_t* amax;            // [B * (1 + max_draft)]: the target's token of every row
   int B, max_draft, vocab, nctas;
 };
 
-// Total window rows sum_b (1 + D_b); false if any D_b is out of range.
-__device__ bool total_rows(const int32_t* draft_len, int B, int max_draft, int64_t* rows) {
+constexpr int FIN_B = 1024;   // sequences whose D_b stay in shared memory
+constexpr int FIN_CAP = 4096;  // rows / drafts the last CTA finalizes in shared memory
+
+// Total window rows sum_b (1 + D_b); false if any D_b is out of range. D_b of the first
+// FIN_B sequences are left in s_D.
+__device__ bool total_rows(const int32_t* draft_len, int B, int max_draft, int64_t* rows,
+                           int* s_D) {
   __shared__ long long s_rows;
   __shared__ int s_bad;
   if (threadIdx.x == 0) {
@@ -130,6 +116,7 @@ __device__ bool total_rows(const int32_t* draft_len, int B, int max_draft, int64
     const int D = draft_len[bb];
     bad |= (D < 0 || D > max_draft);
     q += 1 + D;
+    if (bb < FIN_B) s_D[bb] = D;
   }
   if (q) atomicAdd((unsigned long long*)&s_rows, (unsigned long long)q);
   if (bad) s_bad = 1;
@@ -145,17 +132,11 @@ __device__ bool total_rows(const int32_t* draft_len, int B, int max_draft, int64
 // and leaves one (value, index) candidate per row it touches (a range spans at most a few
 // rows).
 template <bool BF16>
-__global__ void __launch_bounds__(ARGMAX_THREADS) argmax_partial_kernel(AcceptArgs a) {
-  __shared__ Cand sh[32];
-  pdl_trigger();
-  pdl_wait();
-  int64_t rows;
-  if (!total_rows(a.draft_len, a.B, a.max_draft, &rows)) return;  // finalize raises the flag
+__device__ void scan_range(const AcceptArgs& a, int64_t rows) {
   constexpr int ES = BF16 ? 2 : 4;
   constexpr int VE = 16 / ES;  // elements per 16-byte vector
   const int64_t V = a.vocab, N = rows * V;
   const int64_t e0 = N * blockIdx.x / a.nctas, e1 = N * (blockIdx.x + 1) / a.nctas;
-  if (e0 >= e1) return;
   for (int64_t r = e0 / V; r * V < e1; ++r) {
     const int64_t c0 = max(e0, r * V) - r * V, c1 = min(e1, (r + 1) * V) - r * V;
     const uint8_t* row = (const uint8_t*)a.logits + r * V * ES;
@@ -166,87 +147,186 @@ __global__ void __launch_bounds__(ARGMAX_THREADS) argmax_partial_kernel(AcceptAr
         return ((const float*)row)[e];
     };
     // scalar head up to a 16-byte boundary, 16-byte vectors, scalar tail
-    const int64_t h0 = (int64_t)(((16 - ((uintptr_t)(row + c0 * ES) & 15)) & 15) / ES);
-    const int64_t vb = c0 + (h0 < c1 - c0 ? h0 : c1 - c0);
-    const int64_t nvec = (c1 - vb) / VE;
-    const int64_t tb = vb + nvec * VE;
+    // (row-local indices fit in 32 bits: V < 2^31)
+    const int h0 = (int)(((16 - ((uintptr_t)(row + c0 * ES) & 15)) & 15) / ES);
+    const int vb = (int)c0 + (h0 < c1 - c0 ? h0 : (int)(c1 - c0));
+    const int nvec = ((int)c1 - vb) / VE;
+    const int tb = vb + nvec * VE;
     float bv = -INFINITY;
     int bi = NONE;
-    for (int64_t e = c0 + threadIdx.x; e < vb; e += blockDim.x) take(elem(e), (int)e, bv, bi);
+    for (int e = (int)c0 + threadIdx.x; e < vb; e += blockDim.x) take(elem(e), e, bv, bi);
+    // Vectors: only the maximum of each is compared, without branches; the best vector so
+    // far (strictly larger maximum, so the earliest of equal ones) and its words are kept,
+    // and the element index inside it is resolved once at the end.
     const uint4* vec = reinterpret_cast<const uint4*>(row + vb * ES);
-    for (int64_t base = threadIdx.x; base < nvec; base += (int64_t)blockDim.x * UNROLL) {
+    int bvec = -1;
+    uint4 bw = make_uint4(0, 0, 0, 0);
+    for (int base = threadIdx.x; base < nvec; base += blockDim.x * UNROLL) {
       uint4 w[UNROLL];
 #pragma unroll
       for (int k = 0; k < UNROLL; ++k) {
-        const int64_t vi = base + (int64_t)k * blockDim.x;
+        const int vi = base + k * blockDim.x;
         w[k] = vi < nvec ? __ldcs(vec + vi) : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
       for (int k = 0; k < UNROLL; ++k) {
-        const int64_t vi = base + (int64_t)k * blockDim.x;
-        if (vi >= nvec) break;
-        const int e = (int)(vb + vi * VE);
-        const uint32_t ww[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          if constexpr (BF16) {
-            take(bf16_at(ww[q], 0), e + 2 * q, bv, bi);
-            take(bf16_at(ww[q], 1), e + 2 * q + 1, bv, bi);
-          } else {
-            take(__uint_as_float(ww[q]), e + q, bv, bi);
-          }
-        }
+        const int vi = base + k * blockDim.x;
+        float vm;
+        if constexpr (BF16)
+          vm = vmax_bf16x8(w[k]);
+        else
+          vm = fmaxf(fmaxf(__uint_as_float(w[k].x), __uint_as_float(w[k].y)),
+                     fmaxf(__uint_as_float(w[k].z), __uint_as_float(w[k].w)));
+        const bool win = vi < nvec && (vm > bv || (bi == NONE && bvec < 0 && vm == vm));
+        bv = win ? vm : bv;
+        bvec = win ? vi : bvec;
+        bw.x = win ? w[k].x : bw.x;
+        bw.y = win ? w[k].y : bw.y;
+        bw.z = win ? w[k].z : bw.z;
+        bw.w = win ? w[k].w : bw.w;
       }
     }
-    for (int64_t e = tb + threadIdx.x; e < c1; e += blockDim.x) take(elem(e), (int)e, bv, bi);
-    block_argmax(bv, bi, sh);
-    if (threadIdx.x == 0) a.part[(size_t)blockIdx.x + r] = Cand{bv, bi};
-    __syncthreads();  // sh is reused by the next row
+    if (bvec >= 0) {  // the first element of the best vector that equals its maximum
+      const int e = vb + bvec * VE;
+      const uint32_t ww[4] = {bw.x, bw.y, bw.z, bw.w};
+      int q = VE - 1;
+#pragma unroll
+      for (int t = VE - 1; t >= 0; --t) {
+        const float x = BF16 ? bf16_at(ww[t / 2], t & 1) : __uint_as_float(ww[t]);
+        if (x == bv) q = t;
+      }
+      bi = e + q;
+    }
+    for (int e = tb + threadIdx.x; e < c1; e += blockDim.x) take(elem(e), e, bv, bi);
+    warp_argmax(bv, bi);  // one key update per warp and row: no CTA-wide barrier
+    if ((threadIdx.x & 31) == 0 && bi != NONE) atomicMax(a.key + r, row_key(bv, bi));
   }
 }
 
-__global__ void __launch_bounds__(256) accept_finalize_kernel(AcceptArgs a) {
-  __shared__ int s_amax[256];
-  __shared__ int s_first;
+// Exclusive scan over the CTA of (1 + D, D); returns the running totals through `carry`.
+__device__ __forceinline__ void block_scan2(long long& x, long long& y, long long* sh2,
+                                            long long& cx, long long& cy) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  long long ix = x, iy = y;  // inclusive within the warp
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long ux = __shfl_up_sync(0xffffffffu, ix, o);
+    const long long uy = __shfl_up_sync(0xffffffffu, iy, o);
+    if (lane >= o) {
+      ix += ux;
+      iy += uy;
+    }
+  }
+  if (lane == 31) {
+    sh2[2 * wid] = ix;
+    sh2[2 * wid + 1] = iy;
+  }
+  __syncthreads();
+  long long wx = 0, wy = 0, tx = 0, ty = 0;
+  for (int w = 0; w < nw; ++w) {
+    if (w < wid) {
+      wx += sh2[2 * w];
+      wy += sh2[2 * w + 1];
+    }
+    tx += sh2[2 * w];
+    ty += sh2[2 * w + 1];
+  }
+  x = cx + wx + ix - x;
+  y = cy + wy + iy - y;
+  cx += tx;
+  cy += ty;
+  __syncthreads();  // sh2 is reused by the next chunk
+}
+
+__device__ __forceinline__ void cp_async4(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
+                   (uint32_t)__cvta_generic_to_shared(smem_dst)),
+               "l"(gmem_src)
+               : "memory");
+}
+
+// Run by the last CTA: every row's target token, then per sequence (one warp each) the
+// accepted length. For up to FIN_CAP rows and drafts everything stays in shared memory,
+// so the only global round trip is the candidates' (the drafts are copied alongside).
+__device__ __noinline__ void finalize_all(const AcceptArgs& a, int64_t rows, const int* s_D) {
+  __shared__ long long sh2[2 * (ARGMAX_THREADS / 32)];
+  __shared__ long long s_q[ARGMAX_THREADS], s_d[ARGMAX_THREADS];
+  __shared__ int s_n[ARGMAX_THREADS];
+  __shared__ int s_amax[FIN_CAP], s_draft[FIN_CAP];
+  const int64_t ndraft = rows - a.B;  // sum of D_b
+  const bool in_smem = rows <= FIN_CAP && a.B <= FIN_B;
+  int* amax = in_smem ? s_amax : a.amax;
+  const int* draft = in_smem ? s_draft : a.draft_tokens;
+  if (in_smem) {
+    for (int j = threadIdx.x; j < ndraft; j += blockDim.x) cp_async4(s_draft + j, a.draft_tokens + j);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
+  for (int64_t r = threadIdx.x; r < rows; r += blockDim.x) {
+    const unsigned long long k = atomicExch(a.key + r, 0ull);  // clean for the next call
+    // a row made only of NaN has no candidate: unspecified, report index 0
+    const int bi = k == 0ull ? 0 : key_index(k);
+    amax[r] = bi;
+    if (a.target_tokens) a.target_tokens[r] = bi;
+  }
+  if (in_smem) asm volatile("cp.async.wait_all;" ::: "memory");
+  __syncthreads();  // amax and the drafts are visible to the whole CTA
+  long long cq = 0, cd = 0;
+  for (int b0 = 0; b0 < a.B; b0 += blockDim.x) {
+    const int b = b0 + threadIdx.x;
+    const int D = b >= a.B ? 0 : (b < FIN_B ? s_D[b] : a.draft_len[b]);
+    long long q_off = b < a.B ? 1 + D : 0, d_off = D;
+    block_scan2(q_off, d_off, sh2, cq, cd);
+    s_q[threadIdx.x] = q_off;
+    s_d[threadIdx.x] = d_off;
+    s_n[threadIdx.x] = D;
+    __syncthreads();
+    const int lane = threadIdx.x & 31, nb = min((int)blockDim.x, a.B - b0);
+    for (int bb = threadIdx.x >> 5; bb < nb; bb += blockDim.x >> 5) {
+      const int Db = s_n[bb];
+      const long long qb = s_q[bb], db = s_d[bb];
+      int n = Db;  // first draft position that differs from the target's token
+      for (int j0 = 0; j0 < Db; j0 += 32) {
+        const int j = j0 + lane;
+        const bool differs = j < Db && draft[db + j] != amax[qb + j];
+        const uint32_t m = __ballot_sync(0xffffffffu, differs);
+        if (m) {
+          n = j0 + __ffs(m) - 1;
+          break;
+        }
+      }
+      if (lane == 0) {
+        a.accept_len[b0 + bb] = n + 1;
+        a.next_token[b0 + bb] = amax[qb + n];
+      }
+    }
+    __syncthreads();  // s_q / s_d / s_n are reused by the next chunk
+  }
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(ARGMAX_THREADS, ARGMAX_CTAS_PER_SM) accept_kernel(AcceptArgs a) {
+  __shared__ int s_last;
+  __shared__ int s_D[FIN_B];
   pdl_trigger();
   pdl_wait();
-  const int b = blockIdx.x;
-  const int D = a.draft_len[b];
-  if (D < 0 || D > a.max_draft) {
+  int64_t rows;
+  const bool ok = total_rows(a.draft_len, a.B, a.max_draft, &rows, s_D);
+  if (ok) scan_range<BF16>(a, rows);
+  // completion ticket: every CTA takes one after its candidates are written
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_last = atomicAdd(a.ticket, 1u) == (uint32_t)a.nctas - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();  // the other CTAs' candidates are visible from here on
+  if (threadIdx.x == 0) atomicExch(a.ticket, 0u);
+  if (!ok) {
     if (threadIdx.x == 0) atomicOr(a.flags, FLAG_ACCEPT_SHAPE);
     return;
   }
-  int64_t q_off, d_off, rows;
-  if (!prefix_offsets(a.draft_len, b, a.max_draft, &q_off, &d_off)) return;
-  if (!total_rows(a.draft_len, a.B, a.max_draft, &rows)) return;
-  const int64_t V = a.vocab, N = rows * V;
-  for (int i = threadIdx.x; i <= D; i += blockDim.x) {
-    const int64_t r = q_off + i;
-    const int c_lo = cta_of_tile(r * V, N, a.nctas), c_hi = cta_of_tile((r + 1) * V - 1, N, a.nctas);
-    float bv = 0.f;
-    int bi = NONE;
-    for (int c = c_lo; c <= c_hi; ++c) {
-      if (!cta_has_tiles(c, N, a.nctas)) continue;
-      const Cand pc = a.part[(size_t)c + r];
-      if (better(pc.v, pc.i, bv, bi)) {
-        bv = pc.v;
-        bi = pc.i;
-      }
-    }
-    if (bi == NONE) bi = 0;  // a row made only of NaN: unspecified, report index 0
-    s_amax[i] = bi;
-    if (a.target_tokens) a.target_tokens[r] = bi;
-  }
-  if (threadIdx.x == 0) s_first = D;
-  __syncthreads();
-  for (int j = threadIdx.x; j < D; j += blockDim.x)
-    if (a.draft_tokens[d_off + j] != s_amax[j]) atomicMin(&s_first, j);
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const int n = s_first;
-    a.accept_len[b] = n + 1;
-    a.next_token[b] = s_amax[n];
-  }
+  finalize_all(a, rows, s_D);
 }
 
 }  // namespace
@@ -254,15 +334,17 @@ __global__ void __launch_bounds__(256) accept_finalize_kernel(AcceptArgs a) {
 AcceptWs accept_ws_layout(int B, int max_draft, int vocab, int num_sms) {
   AcceptWs w;
   const int64_t rows = (int64_t)B * (1 + max_draft);
-  // persistent CTAs: 4 per SM, fewer for small inputs (at least ~8K elements each)
+  // persistent CTAs: all resident at once (4 per SM), fewer for small inputs (at least
+  // ~8K elements each)
   const int64_t n_max = rows * (int64_t)vocab;
-  int64_t c = 4LL * num_sms;
+  int64_t c = (int64_t)ARGMAX_CTAS_PER_SM * num_sms;
   if (c > n_max / 8192) c = n_max / 8192;
   if (c < 1) c = 1;
   w.nctas = (int)c;
-  w.ctrl = 0;
-  w.part = 256;
-  w.total = align_up(256 + sizeof(Cand) * (size_t)(rows + c), 256);
+  w.ctrl = 0;  // flags word at +0, completion ticket at +64
+  w.key = 256;
+  w.amax = align_up(w.key + sizeof(unsigned long long) * (size_t)rows, 256);
+  w.total = align_up(w.amax + sizeof(int32_t) * (size_t)rows, 256);
   return w;
 }
 
@@ -278,16 +360,16 @@ cudaError_t launch_accept(int B, int max_draft, int vocab, int dtype, const void
   a.next_token = next_token;
   a.target_tokens = target_tokens;
   a.flags = (uint32_t*)((uint8_t*)ws + lay.ctrl);
-  a.part = (Cand*)((uint8_t*)ws + lay.part);
+  a.ticket = (uint32_t*)((uint8_t*)ws + lay.ctrl + 64);
+  a.key = (unsigned long long*)((uint8_t*)ws + lay.key);
+  a.amax = (int32_t*)((uint8_t*)ws + lay.amax);
   a.B = B;
   a.max_draft = max_draft;
   a.vocab = vocab;
   a.nctas = lay.nctas;
-  cudaError_t e = dtype == SV_BF16
-                      ? launch_pdl(argmax_partial_kernel<true>, dim3(lay.nctas), dim3(ARGMAX_THREADS), 0, s, a)
-                      : launch_pdl(argmax_partial_kernel<false>, dim3(lay.nctas), dim3(ARGMAX_THREADS), 0, s, a);
-  if (e != cudaSuccess) return e;
-  return launch_pdl(accept_finalize_kernel, dim3(B), dim3(256), 0, s, a);
+  return dtype == SV_BF16
+             ? launch_pdl(accept_kernel<true>, dim3(lay.nctas), dim3(ARGMAX_THREADS), 0, s, a)
+             : launch_pdl(accept_kernel<false>, dim3(lay.nctas), dim3(ARGMAX_THREADS), 0, s, a);
 }
 
 }  // namespace sv

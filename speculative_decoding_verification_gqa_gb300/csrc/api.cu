@@ -9,6 +9,14 @@ using namespace sv;
 
 namespace {
 
+// Virtual tiles charged for starting a unit (see internal.cuh), per attention kernel: a
+// unit switch inside a CTA's range measured about 7 us on the FP8 tcgen05 kernel (1.0 to
+// 1.1 us per tile) and 5 us on the bf16 one (1.6 to 1.8 us per tile); the values below
+// are the best of a sweep.
+constexpr int SWITCH_TILES_TC_FP8 = 9;
+constexpr int SWITCH_TILES_TC_BF16 = 5;
+constexpr int SWITCH_TILES_MMA = 2;
+
 int g_attn_kernel = 0;  // 0 automatic, 1 mma.sync, 2 tcgen05
 cudaEvent_t g_ev_start = nullptr;
 cudaEvent_t g_ev_stop = nullptr;
@@ -137,6 +145,7 @@ SV_API sv_status spec_verify_attn(const sv_attn_desc* desc, const void* q, const
   p.kv_off = (int64_t*)(ws + lay.kv_off);
   p.units = (int4*)(ws + lay.units);
   p.ubeg = (int32_t*)(ws + lay.ubeg);
+  p.cta_tab = (int2*)(ws + lay.cta_tab);
   p.part_o = (float*)(ws + lay.part_o);
   p.part_ml = (float2*)(ws + lay.part_ml);
   p.B = desc->batch;
@@ -150,6 +159,8 @@ SV_API sv_status spec_verify_attn(const sv_attn_desc* desc, const void* q, const
   p.kv_rows = desc->kv_rows;
   p.max_units = max_units_for(p.B, p.Hkv, G, p.max_draft);
   p.n_ctas = (int)(max_tiles < sms ? (max_tiles > 0 ? max_tiles : 1) : sms);
+  // measured cost of starting a unit inside a CTA's range, in tiles of that kernel
+  p.switch_tiles = which == 2 ? (fp8 ? SWITCH_TILES_TC_FP8 : SWITCH_TILES_TC_BF16) : SWITCH_TILES_MMA;
   const float scale = desc->softmax_scale > 0.f ? desc->softmax_scale
                                                 : 1.f / sqrtf((float)desc->head_dim);
   p.scale_log2 = scale * 1.4426950408889634f;

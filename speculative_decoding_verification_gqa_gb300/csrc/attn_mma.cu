@@ -138,24 +138,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_mma_kernel(const AttnParams 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   pdl_trigger();
   pdl_wait();  // the plan of this call is complete
-  const int64_t TT = p.hdr->total_tiles;
-  if (TT == 0) return;
-  const int C = p.n_ctas;
-  const int64_t t_begin = (int64_t)blockIdx.x * TT / C;
-  const int64_t t_end = (int64_t)(blockIdx.x + 1) * TT / C;
+  const int2 rb = p.cta_tab[blockIdx.x], re = p.cta_tab[blockIdx.x + 1];
+  const int64_t t_begin = rb.x, t_end = re.x;  // this CTA's tiles (see the plan kernel)
   if (t_begin >= t_end) return;
-
-  __shared__ int s_u;
-  if (tid == 0) {
-    int lo = 0, hi = p.hdr->num_units - 1;  // last unit with ubeg <= t_begin
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (p.ubeg[mid] <= t_begin) lo = mid; else hi = mid - 1;
-    }
-    s_u = lo;
-  }
-  __syncthreads();
-  int u = s_u;
+  int u = rb.y;
   const size_t elem = FP8 ? 1 : 2;
 
   for (int64_t t = t_begin; t < t_end; ++u) {

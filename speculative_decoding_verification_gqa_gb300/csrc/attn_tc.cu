@@ -62,7 +62,6 @@ struct __align__(8) Bars {
   uint64_t q_full, s_final, pv_final;
   uint32_t tmem_base;
   int abort;
-  int u0;
   // [tile parity][warpgroup][row]: half-tile row maxima; at the end of a unit the half
   // sums go through the parity not used by the unit's last tile
   float xmax[2][2][128];
@@ -351,12 +350,10 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
   pdl_trigger();
   pdl_wait();  // the plan of this call is complete
 
-  const int TT = p.hdr->total_tiles;
   const int num_units = p.hdr->num_units;
-  const int C = p.n_ctas;
-  const int64_t t_begin = (int64_t)blockIdx.x * TT / C;
-  const int64_t t_end = (int64_t)(blockIdx.x + 1) * TT / C;
-  if (TT == 0 || t_begin >= t_end) return;  // uniform across the CTA
+  const int2 rb = p.cta_tab[blockIdx.x], re = p.cta_tab[blockIdx.x + 1];
+  const int64_t t_begin = rb.x, t_end = re.x;  // this CTA's tiles (see the plan kernel)
+  if (t_begin >= t_end) return;                // uniform across the CTA
   if (saddr(smem) & 1023) {  // the swizzle phases below assume a 1 KiB-aligned base
     if (tid == 0) atomicOr(p.flags, FLAG_ATTN_SHAPE);
     return;
@@ -383,12 +380,6 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
     mbar_init(&bars->s_final, 1);
     mbar_init(&bars->pv_final, 1);
     bars->abort = 0;
-    int lo = 0, hi = num_units - 1;  // last unit whose first tile is <= t_begin
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (p.ubeg[mid] <= t_begin) lo = mid; else hi = mid - 1;
-    }
-    bars->u0 = lo;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) {
@@ -402,7 +393,7 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
   __syncthreads();
   fence_after();
   const uint32_t tmem = bars->tmem_base;
-  const int u_first = bars->u0;
+  const int u_first = rb.y;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer

@@ -5,10 +5,15 @@
 //           that share KV head g ("GQA", "GPU and LLM, chapter 5"; guideline 2 of the
 //           co-design summary: G*(1+D) rows per KV head, M = 128 fills a tile).
 //   tile  = KT consecutive cache positions of one unit's key range 0 .. T_b + D_b.
-//   Units are laid end to end on one global tile line; persistent CTA c processes the
-//   contiguous range [c*TT/C, (c+1)*TT/C) of it, so every CTA gets the same number of
-//   tiles (to within one) whatever the mix of lengths. A CTA that covers a whole unit
-//   writes the normalised output itself; otherwise each CTA covering part of the unit
+//   Units are laid end to end on one global tile line; persistent CTAs process contiguous
+//   ranges of it. Starting a unit costs a CTA about `switch_tiles` tiles' worth of time
+//   (epilogue of the previous unit, loading and splitting Q, refilling the pipeline), so
+//   the split is made on a virtual line on which every unit is preceded by switch_tiles
+//   virtual tiles: CTA c owns the virtual range [c*VT/C, (c+1)*VT/C), VT = TT +
+//   U * switch_tiles, and with it the real tiles whose virtual positions fall inside. A
+//   CTA whose range crosses into a unit therefore gets fewer real tiles. The plan kernel
+//   tabulates each CTA's first real tile and unit. A CTA that covers a whole unit writes
+//   the normalised output itself; otherwise each CTA covering part of the unit
 //   writes a partial (O unnormalised, running max m, running sum l) to slot c + u and the
 //   combine kernel merges them with the same rescaling rule as the online softmax.
 #pragma once
@@ -40,7 +45,7 @@ struct PlanHdr {
 
 // Byte offsets inside a spec_verify_attn workspace.
 struct AttnWs {
-  size_t ctrl, hdr, q_off, kv_off, units, ubeg, part_o, part_ml, total;
+  size_t ctrl, hdr, q_off, kv_off, units, ubeg, cta_tab, part_o, part_ml, total;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -61,6 +66,7 @@ inline AttnWs attn_ws_layout(int B, int Hkv, int G, int d, int max_draft, int n_
   w.kv_off = o;  o = align_up(o + sizeof(int64_t) * (B + 1), 256);
   w.units = o;   o = align_up(o + sizeof(int4) * U, 256);
   w.ubeg = o;    o = align_up(o + sizeof(int32_t) * (U + 1), 256);
+  w.cta_tab = o; o = align_up(o + sizeof(int2) * ((size_t)n_ctas + 1), 256);
   w.part_o = o;  o = align_up(o + sizeof(float) * slots * MT * d, 256);
   w.part_ml = o; o = align_up(o + sizeof(float2) * slots * MT, 256);
   w.total = o;
@@ -81,6 +87,7 @@ struct AttnParams {
   int64_t* kv_off;            // [B+1]
   int4* units;                // [U] (b, kv head, row tile, tiles in the unit)
   int32_t* ubeg;              // [U+1] first global tile of each unit
+  int2* cta_tab;              // [n_ctas+1] (first real tile, its unit) of each CTA's range
   float* part_o;              // [slots, MT, d]
   float2* part_ml;            // [slots, MT] (m in log2 units, l)
   int B, Hq, Hkv, G, d;
@@ -88,15 +95,22 @@ struct AttnParams {
   int64_t q_rows, kv_rows;
   int max_units;
   int n_ctas;
+  int switch_tiles;           // virtual tiles charged for starting a unit
   float scale_log2;           // softmax_scale * log2(e)
 };
 
-// The CTA whose tile range [c*TT/C, (c+1)*TT/C) contains global tile t.
+// Virtual-line position of real tile t of unit u (u * switch_tiles virtual tiles precede
+// unit u's start, and switch_tiles more its first real tile).
+__host__ __device__ inline int64_t vpos_of_tile(int64_t t, int u, int switch_tiles) {
+  return t + (int64_t)(u + 1) * switch_tiles;
+}
+
+// The CTA whose range [c*TT/C, (c+1)*TT/C) of a line of TT positions contains position t.
 __host__ __device__ inline int cta_of_tile(int64_t t, int64_t TT, int C) {
   return (int)(((t + 1) * (int64_t)C - 1) / TT);
 }
-// Whether CTA c has any tile (with fewer tiles than CTAs some ranges are empty; such a CTA
-// writes no partial for the units its neighbours split).
+// Whether CTA c's range of a line of TT positions is not empty (with fewer positions than
+// CTAs some ranges are empty).
 __host__ __device__ inline bool cta_has_tiles(int c, int64_t TT, int C) {
   return (int64_t)(c + 1) * TT / C > (int64_t)c * TT / C;
 }
@@ -137,7 +151,7 @@ cudaError_t launch_attn_tc(const AttnParams& p, bool fp8, cudaStream_t s);
 
 // Acceptance.
 struct AcceptWs {
-  size_t ctrl, part, total;
+  size_t ctrl, key, amax, total;
   int nctas;  // persistent argmax CTAs
 };
 AcceptWs accept_ws_layout(int B, int max_draft, int vocab, int num_sms);

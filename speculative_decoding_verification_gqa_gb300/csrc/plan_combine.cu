@@ -1,7 +1,8 @@
 // plan_combine.cu -- the two small kernels around verify attention.
 //
-// plan:    per-sequence offsets of the packed layout, the unit list and each unit's first
-//          tile on the global tile line; device-side length checks.
+// plan:    per-sequence offsets of the packed layout, the unit list, each unit's first
+//          tile on the global tile line and each CTA's range of it; device-side length
+//          checks.
 // combine: merges the split-KV partials of one unit. For partials s with running max m_s,
 //          sum l_s and unnormalised output O_s: m* = max m_s, l* = sum l_s 2^(m_s - m*),
 //          O* = sum O_s 2^(m_s - m*) / l*. This is the online-softmax update of
@@ -115,6 +116,25 @@ __global__ void __launch_bounds__(1024) plan_kernel(AttnParams p, int kt) {
       p.ubeg[carry[2]] = (int32_t)carry[3];
     }
   }
+  __syncthreads();  // ubeg and the header are visible to the whole block
+  // CTA c starts at the first real tile at or after virtual position c*VT/C
+  const int U = p.hdr->num_units;
+  const int64_t TT = p.hdr->total_tiles, X = p.switch_tiles;
+  const int64_t VT = TT + (int64_t)U * X;
+  for (int c = tid; c <= p.n_ctas; c += blockDim.x) {
+    int2 e = make_int2((int32_t)TT, U);
+    if (c < p.n_ctas && TT > 0) {
+      const int64_t v0 = (int64_t)c * VT / p.n_ctas;
+      int lo = 0, hi = U - 1;  // last unit whose virtual start ubeg[u] + u*X is <= v0
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (p.ubeg[mid] + (int64_t)mid * X <= v0) lo = mid; else hi = mid - 1;
+      }
+      const int64_t into = v0 - (p.ubeg[lo] + (int64_t)lo * X) - X;  // < 0: before its tiles
+      e = make_int2((int32_t)(p.ubeg[lo] + (into > 0 ? into : 0)), lo);
+    }
+    p.cta_tab[c] = e;
+  }
 }
 
 cudaError_t launch_plan(const AttnParams& p, int kt, cudaStream_t s) {
@@ -135,9 +155,10 @@ __global__ void __launch_bounds__(256) combine_kernel(AttnParams p) {
   const int r = (blockIdx.x % (MT / COMBINE_ROWS)) * COMBINE_ROWS + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (u >= p.hdr->num_units) return;
-  const int64_t TT = p.hdr->total_tiles;
+  const int64_t VT = p.hdr->total_tiles + (int64_t)p.hdr->num_units * p.switch_tiles;
   const int64_t ub = p.ubeg[u], ue = p.ubeg[u + 1];
-  const int c_lo = cta_of_tile(ub, TT, p.n_ctas), c_hi = cta_of_tile(ue - 1, TT, p.n_ctas);
+  const int c_lo = cta_of_tile(vpos_of_tile(ub, u, p.switch_tiles), VT, p.n_ctas);
+  const int c_hi = cta_of_tile(vpos_of_tile(ue - 1, u, p.switch_tiles), VT, p.n_ctas);
   if (c_lo == c_hi) return;  // one CTA covered the unit and wrote the output itself
   const int4 info = p.units[u];
   const int b = info.x, g = info.y, mt = info.z;
@@ -153,7 +174,7 @@ __global__ void __launch_bounds__(256) combine_kernel(AttnParams p) {
 #pragma unroll
     for (int k = 0; k < MAXP; ++k) {
       const int c = c0 + k;
-      const bool use = c <= c_hi && cta_has_tiles(c, TT, p.n_ctas);
+      const bool use = c <= c_hi && cta_has_tiles(c, VT, p.n_ctas);
       const size_t slot = (size_t)(c + u);
       ml[k] = use ? p.part_ml[slot * MT + r] : make_float2(-INFINITY, 0.f);
       const float* src = p.part_o + (slot * MT + r) * HD + lane * PER;

@@ -94,3 +94,60 @@ def test_device_side_length_check_sets_flag():
     assert sv.workspace_status(ws, clear=True) == 8
     assert (al.cpu() == -7).all() and (nt.cpu() == -7).all()
     assert sv.workspace_status(ws) == 0
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_subnormal_and_nan_values(dtype):
+    """A positive subnormal is the maximum of a row of zeros and negatives (the packed
+    vector maximum must not flush it); NaN never wins, and later equal values lose."""
+    V = 1037
+    rows = 4
+    logits = np.full((rows, V), -2.0, dtype=np.float32)
+    tiny = np.array([0x0001 if dtype == "bf16" else 0x00000001], dtype=np.uint32)
+    tiny = (tiny << 16).view(np.float32)[0] if dtype == "bf16" else tiny.view(np.float32)[0]
+    logits[0, :] = 0.0
+    logits[0, 700] = tiny
+    logits[0, 900] = tiny
+    logits[1, [3, 17, 500]] = np.nan
+    logits[1, 400] = 5.0
+    logits[1, 401] = 5.0
+    logits[2, :] = -np.inf
+    logits[2, 1036] = -1.0
+    logits[3, :] = -np.inf
+    logits[3, 0] = np.nan
+    lg = logits if dtype == "fp32" else synth.bf16_bits(logits)
+    a = dict(logits=lg, draft_tokens=np.array([700, 400, 1036], dtype=np.int32),
+             draft_len=np.array([3], dtype=np.int32))
+    al, nt, tgt = gpu_accept(a)
+    assert list(tgt) == [700, 400, 1036, 1]
+    assert al[0] == 4 and nt[0] == 1
+
+
+def test_workspace_shared_by_shapes_and_after_a_failed_check():
+    """One workspace, sized for the largest call, serves calls of different shapes (and so
+    different CTA counts) back to back, including after a call whose device-side length
+    check failed."""
+    import speculative_decoding_verification_gqa_gb300 as sv
+    ws = sv.new_workspace(sv.accept_workspace_bytes(8, 15, 128256))
+    for B, V, md in [(8, 128256, 15), (3, 1000, 4), (8, 32000, 15), (1, 64, 2)]:
+        w = synth.Workload("w", B=B, Hq=1, Hkv=1, d=8, D=md, T=1, V=V, p=0.7)
+        a = synth.accept_inputs(w, B + V)
+        lg, dt, dl = dev_accept(a)
+        if B == 3:  # D_0 > max_draft_len: the call fails on the device
+            bad = dl.clone()
+            bad[0] = md + 1
+            sv.spec_accept(lg, dt, bad, max_draft_len=md, workspace=ws)
+            assert sv.workspace_status(ws, clear=True) == 8
+        al, nt = sv.spec_accept(lg, dt, dl, max_draft_len=md, workspace=ws)
+        torch.cuda.synchronize()
+        assert sv.workspace_status(ws) == 0
+        ral, rnt, _ = oracle.spec_accept(a["logits"], a["draft_tokens"], a["draft_len"])
+        assert np.array_equal(al.cpu().numpy(), ral) and np.array_equal(nt.cpu().numpy(), rnt)
+
+
+@pytest.mark.parametrize("B,D,V", [(300, 15, 64), (1100, 3, 16)])
+def test_many_rows_and_sequences(B, D, V):
+    """More window rows (4800, 4400) than the last CTA keeps in shared memory, and more
+    sequences (1100) than it keeps draft lengths for: the global-memory fallback."""
+    w = synth.Workload("m", B=B, Hq=1, Hkv=1, d=8, D=D, T=1, V=V, p=0.8)
+    _check(synth.accept_inputs(w, 9))

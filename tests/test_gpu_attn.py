@@ -53,6 +53,8 @@ SMALL = {
     "rows_256": dict(B=1, Hq=32, Hkv=4, d=128, T=(400,), D=(31,)),
     "llama3_8b_shape": dict(B=2, Hq=32, Hkv=8, d=128, T=(1500, 333), D=(31, 31)),
     "d64_ragged": dict(B=3, Hq=16, Hkv=2, d=64, T=(513, 5, 2049), D=(8, 2, 1)),
+    # ~7 tiles per CTA on 152 CTAs: every ring stage and buffer parity is reused
+    "tiles_per_cta": dict(B=2, Hq=16, Hkv=2, d=128, T=(40000, 30000), D=(7, 3)),
 }
 
 
