@@ -42,8 +42,11 @@ __device__ int64_t block_excl_scan(int64_t v, int64_t* s_warp, int64_t* total) {
   return excl;
 }
 
+constexpr int PLAN_SMEM_UNITS = 4096;  // unit starts also kept in shared memory
+
 __global__ void __launch_bounds__(1024) plan_kernel(AttnParams p, int kt) {
   __shared__ int64_t s_warp[32];
+  __shared__ int32_t s_ubeg[PLAN_SMEM_UNITS + 1];
   __shared__ int64_t carry[4];
   __shared__ int bad;
   const int tid = threadIdx.x;
@@ -84,8 +87,10 @@ __global__ void __launch_bounds__(1024) plan_kernel(AttnParams p, int kt) {
         for (int mt = 0; mt < nmt; ++mt) {
           const int64_t u = ub + (int64_t)g * nmt + mt;
           if (u < p.max_units) {
+            const int32_t ub_u = (int32_t)(tb + ((int64_t)g * nmt + mt) * nt);
             p.units[u] = make_int4(b, g, mt, nt);
-            p.ubeg[u] = (int32_t)(tb + ((int64_t)g * nmt + mt) * nt);
+            p.ubeg[u] = ub_u;
+            if (u < PLAN_SMEM_UNITS) s_ubeg[u] = ub_u;
           }
         }
     }
@@ -121,6 +126,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(AttnParams p, int kt) {
   const int U = p.hdr->num_units;
   const int64_t TT = p.hdr->total_tiles, X = p.switch_tiles;
   const int64_t VT = TT + (int64_t)U * X;
+  const int32_t* ubeg = U <= PLAN_SMEM_UNITS ? s_ubeg : p.ubeg;
   for (int c = tid; c <= p.n_ctas; c += blockDim.x) {
     int2 e = make_int2((int32_t)TT, U);
     if (c < p.n_ctas && TT > 0) {
@@ -128,10 +134,10 @@ __global__ void __launch_bounds__(1024) plan_kernel(AttnParams p, int kt) {
       int lo = 0, hi = U - 1;  // last unit whose virtual start ubeg[u] + u*X is <= v0
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (p.ubeg[mid] + (int64_t)mid * X <= v0) lo = mid; else hi = mid - 1;
+        if (ubeg[mid] + (int64_t)mid * X <= v0) lo = mid; else hi = mid - 1;
       }
-      const int64_t into = v0 - (p.ubeg[lo] + (int64_t)lo * X) - X;  // < 0: before its tiles
-      e = make_int2((int32_t)(p.ubeg[lo] + (into > 0 ? into : 0)), lo);
+      const int64_t into = v0 - (ubeg[lo] + (int64_t)lo * X) - X;  // < 0: before its tiles
+      e = make_int2((int32_t)(ubeg[lo] + (into > 0 ? into : 0)), lo);
     }
     p.cta_tab[c] = e;
   }
