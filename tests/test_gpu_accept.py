@@ -151,3 +151,23 @@ def test_many_rows_and_sequences(B, D, V):
     sequences (1100) than it keeps draft lengths for: the global-memory fallback."""
     w = synth.Workload("m", B=B, Hq=1, Hkv=1, d=8, D=D, T=1, V=V, p=0.8)
     _check(synth.accept_inputs(w, 9))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_aligned_and_unaligned_logits(dtype):
+    """The same logits on 16-byte row boundaries and shifted by one element (every row then
+    has a scalar head and tail around its 16-byte vectors): both match the oracle."""
+    import speculative_decoding_verification_gqa_gb300 as sv
+    w = synth.Workload("a", B=6, Hq=1, Hkv=1, d=8, D=7, T=1, V=4096, p=0.75, logits_dtype=dtype)
+    a = synth.accept_inputs(w, 21)
+    lg, dt, dl = dev_accept(a)
+    flat = torch.empty(lg.numel() + 8, dtype=lg.dtype, device="cuda")
+    shifted = flat[1:1 + lg.numel()].view(lg.shape)
+    shifted.copy_(lg)
+    ral, rnt, ramax = oracle.spec_accept(a["logits"], a["draft_tokens"], a["draft_len"])
+    for x in (lg, shifted):
+        tgt = torch.full((lg.shape[0],), -1, dtype=torch.int32, device="cuda")
+        al, nt = sv.spec_accept(x, dt, dl, max_draft_len=7, target_tokens=tgt)
+        torch.cuda.synchronize()
+        assert np.array_equal(tgt.cpu().numpy(), ramax)
+        assert np.array_equal(al.cpu().numpy(), ral) and np.array_equal(nt.cpu().numpy(), rnt)
