@@ -263,6 +263,12 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# DRAM bytes (read + written) per launch of the attention kernel, from one ncu capture of
+# the current kernel on that workload (dram__bytes_read.sum + dram__bytes_write.sum). Only
+# valid for the kernel version that was captured: drop an entry when the kernel changes.
+NCU_TRAFFIC = {("c2", "tcgen05"): 562_292_224, ("c3", "tcgen05"): 551_767_808}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -437,7 +443,9 @@ def run_ours(args):
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
             "steps": K, "warmup": max(3, args.warmup), "ms_per_step": round(ms_step, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "fp8_e4m3->f16 mma, fp32 accum" if w.kv_dtype == "fp8_e4m3"
+            "dtype": ("fp8_e4m3 (QK^T: e4m3 x e4m3, Q as two e4m3 terms; PV: f16), fp32 accum"
+                      if attn_kernel == "tcgen05" else "fp8_e4m3->f16 mma, fp32 accum")
+                     if w.kv_dtype == "fp8_e4m3"
                      else "bf16 mma, fp32 accum",
             "data": "synthetic",
             "config": {"workload": describe(w, T, D),
@@ -455,7 +463,10 @@ def run_ours(args):
             "attn_tflops": round(fl / (attn_ms / 1e3) / 1e12, 2),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
                          "unit": "GB/s", "frac": round(achieved / hbm, 4),
-                         "traffic": None,
+                         "traffic": (NCU_TRAFFIC.get((args.config, attn_kernel))
+                                     if args.D is None else None),
+                         "traffic_unit": "bytes per launch (ncu)",
+                         "algorithmic_bytes": kv_bytes + qo_bytes,
                          "peak_source": src + " (STREAM-style copy)",
                          "kernel": "verify attention (%s)" % attn_kernel},
             "cpu_baseline": cpu,
