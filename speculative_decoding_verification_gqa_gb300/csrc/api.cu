@@ -9,12 +9,15 @@ using namespace sv;
 
 namespace {
 
-// Virtual tiles charged for starting a unit (see internal.cuh), per attention kernel: a
-// unit switch inside a CTA's range measured about 7 us on the FP8 tcgen05 kernel (1.0 to
-// 1.1 us per tile) and 5 us on the bf16 one (1.6 to 1.8 us per tile); the values below
-// are the best of a sweep.
-constexpr int SWITCH_TILES_TC_FP8 = 9;
-constexpr int SWITCH_TILES_TC_BF16 = 5;
+#ifndef SV_SWITCH_F8
+#define SV_SWITCH_F8 9
+#endif
+#ifndef SV_SWITCH_BF16
+#define SV_SWITCH_BF16 5
+#endif
+// Virtual tiles charged for starting a unit (see internal.cuh), per attention kernel.
+constexpr int SWITCH_TILES_TC_FP8 = SV_SWITCH_F8;
+constexpr int SWITCH_TILES_TC_BF16 = SV_SWITCH_BF16;
 constexpr int SWITCH_TILES_MMA = 2;
 
 int g_attn_kernel = 0;  // 0 automatic, 1 mma.sync, 2 tcgen05

@@ -1,29 +1,36 @@
 // attn_tc.cu -- verify attention on the fifth-generation tensor cores (tcgen05, TMEM, TMA).
 //
-// Same work decomposition as the mma.sync kernel (persistent CTAs walking contiguous ranges
-// of the global tile line; see internal.cuh), with 128-key tiles and warp-specialised roles:
+// Persistent CTAs walk contiguous ranges of the global tile line (see internal.cuh) in
+// 128-key tiles. The two softmax warpgroups split every tile by keys: warpgroup w owns
+// keys [64w, 64w + 64) of each tile, each of its threads a whole query row of them, with
+// its own running max m_w, running sum l_w, TMEM accumulator O_w and P buffer. So the
+// warpgroups never exchange maxima per tile, and each half's P V starts as soon as that
+// half's P is written. The two partial results of a unit merge once, at its end, with the
+// online-softmax rule ("GPU and LLM, chapter 5", "Online softmax").
 //
 //   warp 0      TMA producer: K and V tiles of one KV head (128 keys x d, 128-byte swizzle)
 //               into a shared-memory ring (3 stages of bf16, 4 of E4M3); a stage is
 //               released once every reader of it has finished.
-//   warp 1      S issuer (one thread): S = Q K^T into a double-buffered TMEM score tile.
-//   warp 3      P V issuer (one thread): O += P V into the TMEM accumulator.
-//               Q and P are tcgen05 A operands read straight from TMEM; K (K-major) and V
-//               (MN-major) come from shared memory through UMMA descriptors.
-//   warps 12-15 (FP8 K/V only) decode E4M3 V tiles to f16 operand tiles for P V (f16
-//               MMAs, P in f16). K is not decoded: S runs on the 8-bit tensor path with the
-//               raw E4M3 K tile as B and Q as A, Q held exactly as the sum of two E4M3
-//               terms (see split_q_e4m3), so S takes two 8-bit MMAs per 32-element step.
-//               The K scale folds into the score scale, the V scale into the normalisation.
-//   warps 4..11 softmax, two warpgroups: in each, thread r owns query row r (TMEM lane r)
-//               and one half of the columns. Per unit they write the Q row into TMEM; per
-//               tile they read their 64 scores, apply the scale and the window-causal
-//               mask, exchange half-tile maxima, update the running max m and sum l ("GPU
-//               and LLM, chapter 5", "Online softmax"), and write P = 2^(s - m) as bf16
-//               into TMEM; at the end they normalise O (or store a split partial).
+//   warp 1      S issuer (one thread): S = Q K^T (N = 128) into the score buffer, which is
+//               free again as soon as both warpgroups have read their halves. bf16:
+//               kind::f16 with Q (A) read from TMEM and K (B, K-major) from shared memory.
+//               FP8: kind::f8f6f4 on the raw E4M3 K tile, with Q held exactly as the sum of
+//               two E4M3 terms (see split_q_e4m3): two 8-bit MMAs per 32-element step.
+//   warp 3      P V issuer (one thread): O_w += P_w V[64w .. 64w + 64) for each half, with
+//               P_w (A) read from TMEM and V (B, MN-major) from shared memory.
+//   warps 4..11 softmax, warpgroups 0 (warps 4-7) and 1 (8-11). Per unit they write Q into
+//               TMEM (half of d each). Per tile a thread reads its row's 64 scores of its
+//               half, releases the score buffer, applies the scale and the window-causal
+//               mask, updates m_w and l_w, and writes P_w = 2^(s - m_w) into its P buffer
+//               (after its previous P V has consumed the last one). At the end of a unit
+//               they merge (O_0, m_0, l_0) with (O_1, m_1, l_1) and store the output, or a
+//               split partial.
+//   warps 12-15 (FP8 K/V only) decode E4M3 V tiles to f16 tiles for P V (MMAs in f16, P
+//               in f16). The K scale folds into the score scale, the V scale into the
+//               normalisation.
 //
-// The online-softmax rescale O *= 2^(m_old - m_new) is applied lazily: the reference max
-// only moves when the tile max exceeds it by more than 2^8, so P stays below 256 and the
+// The online-softmax rescale O_w *= 2^(m_old - m_new) is applied lazily: a reference max
+// only moves when a tile's max exceeds it by more than 2^8, so P stays below 256 and the
 // exact result is unchanged (numerator and denominator use the same reference).
 //
 // Every mbarrier wait is bounded: on timeout the kernel sets a flag in the workspace,
@@ -38,33 +45,33 @@
 namespace sv {
 namespace {
 
-constexpr int KT = 128;          // keys per tile
-constexpr int NS = 3;            // shared-memory ring depth, bf16 K/V
-constexpr int NS8 = 4;           // shared-memory ring depth, E4M3 K/V
+constexpr int KT = 128;           // keys per tile
+constexpr int HK = KT / 2;        // keys per warpgroup per tile
+constexpr int NS = 3;             // shared-memory ring depth, bf16 K/V
+constexpr int NS8 = 4;            // shared-memory ring depth, E4M3 K/V
 constexpr int NSMAX = 4;
+constexpr int NCV = 2;            // FP8: decoded V stages
 constexpr int NTHREADS = 384;
-constexpr int SOFTMAX_WARP0 = 4;  // warps 4..7: columns 0..63 of a tile, 8..11: 64..127
+constexpr int SOFTMAX_WARP0 = 4;  // warps 4..7: warpgroup 0, 8..11: warpgroup 1
 constexpr int NSOFT = 256;        // softmax threads (two warpgroups)
 constexpr int CONV_WARP0 = 12;    // FP8 only: warps 12-15 decode V tiles
 constexpr int NCONV = 128;        // decoding threads
 constexpr uint32_t TMEM_COLS = 512;
-// TMEM columns: O accumulator, two score tiles (each tile's P overwrites the first 32
-// columns of each warpgroup's half of it), Q as the A operand of S
-constexpr uint32_t COL_O = 0, COL_S0 = 128, COL_Q = 384;
+// TMEM columns: O_0 and O_1 (128 each), the score tile (128), Q (64: bf16 pairs, or the
+// E4M3 hi and lo terms), the warpgroups' P buffers (32 each: 64 keys of 16-bit pairs)
+constexpr uint32_t COL_O = 0, COL_S = 256, COL_Q = 384, COL_P = 448;
 constexpr long long TIMEOUT_CYCLES = 4000000000LL;  // ~2 s at 2 GHz
 constexpr float RESCALE_THRESHOLD = 8.f;            // log2 units
 
 struct __align__(8) Bars {
   uint64_t k_full[NSMAX], v_full[NSMAX], kv_empty[NSMAX];
-  uint64_t vc_full[2], vc_empty[2];  // FP8: decoded f16 V tiles
-  uint64_t s_full[2], s_free[2];  // per score buffer; freed by the P V that reads its P
-  uint64_t p_full[2], o_done[2];  // per score buffer: P published / its P V complete
+  uint64_t vc_full[NCV], vc_empty[NCV];  // FP8: decoded f16 V tiles
+  uint64_t s_full, s_free;               // the score tile: written / read by both halves
+  uint64_t p_full[2], o_done[2];         // per warpgroup: P published / its P V complete
   uint64_t q_full, s_final, pv_final;
   uint32_t tmem_base;
   int abort;
-  // [tile parity][warpgroup][row]: half-tile row maxima; at the end of a unit the half
-  // sums go through the parity not used by the unit's last tile
-  float xmax[2][2][128];
+  float xm[2][128], xl[2][128];  // end of a unit: each warpgroup's (m, l) per row
 };
 
 __device__ __forceinline__ uint32_t saddr(const void* p) {
@@ -208,6 +215,13 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
       SV_W8(0), SV_W8(8)
       : "memory");
 }
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15}, [%16];"
+      : SV_R8(0), SV_R8(8)
+      : "r"(taddr));
+}
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -220,6 +234,11 @@ __device__ __forceinline__ void reg_fence32(uint32_t* r) {
                "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
                "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
                "+r"(r[30]), "+r"(r[31]));
+}
+__device__ __forceinline__ void reg_fence16(uint32_t* r) {
+  asm volatile("" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+               "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+               "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]));
 }
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
@@ -319,22 +338,22 @@ __device__ __forceinline__ bool seg_next(const AttnParams& p, int num_units, int
 
 // Shared memory. bf16 K/V: NS stages of (K tile, V tile), filled by TMA and read by the
 // MMAs. FP8 K/V: an NS8-stage ring of raw E4M3 K and V tiles filled by TMA (K read by the
-// S MMAs as it is), and a 2-stage ring of V tiles decoded to f16 for the P V MMAs.
+// S MMAs as it is), and an NCV-stage ring of V tiles decoded to f16 for the P V MMAs.
 template <int HD, bool F8>
 struct TcLayout {
   static_assert(!F8 || HD == 128, "E4M3 rows of one head are one 128-byte swizzle row");
   static constexpr int NR = F8 ? NS8 : NS;        // TMA ring stages
-  static constexpr int BLK = KT * 128;            // one 64-column block of a 128-key tile
-  static constexpr int NBLK = HD / 64;            // column blocks per tile
+  static constexpr int BLK = KT * 128;            // one 128-byte-wide column block of a tile
+  static constexpr int NBLK = HD / 64;            // 16-bit column blocks per tile
   static constexpr int TILE = KT * HD * 2;        // one 16-bit K or V tile
   static constexpr int STAGE = 2 * TILE;          // bf16: K then V
   static constexpr int RAW = KT * HD;             // one E4M3 tile
-  static constexpr int NCV = 2;                   // FP8: decoded V stages
   static constexpr int CV = 0;                    // FP8 offsets
   static constexpr int RK = CV + NCV * TILE;
   static constexpr int RV = RK + NR * RAW;
   static constexpr int BARS = F8 ? RV + NR * RAW : NR * STAGE;  // offset of the barrier block
   static constexpr size_t SMEM = (size_t)BARS + sizeof(Bars);
+  static_assert(SMEM <= 227 * 1024, "dynamic shared memory above the per-CTA limit");
   static constexpr int THREADS = F8 ? NTHREADS + 4 * 32 : NTHREADS;
 };
 
@@ -366,15 +385,15 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
       // bf16: freed by the P V commit; FP8: by the S commit and the V decoders
       mbar_init(&bars->kv_empty[s], F8 ? NCONV + 1 : 1);
     }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < NCV; ++s) {
       mbar_init(&bars->vc_full[s], NCONV);
       mbar_init(&bars->vc_empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&bars->s_full[s], 1);
-      mbar_init(&bars->s_free[s], 1);
-      mbar_init(&bars->p_full[s], NSOFT);
-      mbar_init(&bars->o_done[s], 1);
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->s_free, NSOFT);
+    for (int w = 0; w < 2; ++w) {
+      mbar_init(&bars->p_full[w], NSOFT / 2);
+      mbar_init(&bars->o_done[w], 1);
     }
     mbar_init(&bars->q_full, NSOFT);
     mbar_init(&bars->s_final, 1);
@@ -464,15 +483,15 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
         if (!mbar_wait(&bars->q_full, seg_i & 1, abort, p.flags)) break;
         fence_after();
         for (int j = s.j0; j < s.j1; ++j, ++it) {
-          const uint32_t st = it % L::NR, sb = it & 1;
+          const uint32_t st = it % L::NR;
           if (!mbar_wait(&bars->k_full[st], (it / L::NR) & 1, abort, p.flags) ||
-              (it >= 2 && !mbar_wait(&bars->s_free[sb], ((it >> 1) - 1) & 1, abort, p.flags))) {
+              (it >= 1 && !mbar_wait(&bars->s_free, (it - 1) & 1, abort, p.flags))) {
             ok = false;
             break;
           }
           fence_after();
           const uint64_t kd = kdesc0 + ((st * (F8 ? L::RAW : L::STAGE)) >> 4);
-          const uint32_t dcol = tmem + COL_S0 + sb * 128;
+          const uint32_t dcol = tmem + COL_S;
           if constexpr (F8) {
             // S = Q_hi K^T + Q_lo K^T: Q_hi in TMEM columns [COL_Q, +32), Q_lo in [+32, +64)
 #pragma unroll
@@ -487,7 +506,7 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
               mma_ts(dcol, tmem + COL_Q + kk * 8,
                      kd + ((((kk >> 2) * L::BLK) + (kk & 3) * 32) >> 4), ID_S, kk > 0 ? 1u : 0u);
           }
-          mma_commit(&bars->s_full[sb]);
+          mma_commit(&bars->s_full);
           if constexpr (F8) mma_commit(&bars->kv_empty[st]);  // the raw K tile is read
         }
         ++seg_i;
@@ -498,11 +517,7 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
       }
     }
   } else if (warp == 3) {
-    // ------------------------------------------------------------ O += P V issuer
-    // A thread of its own, so that P V starts as soon as P is ready instead of after
-    // the next S has been issued. P sits in the score buffer it was computed from; the
-    // P V commit frees that buffer for the S two tiles later, and the K/V stage (bf16)
-    // or decoded V stage (FP8).
+    // ------------------------------------------------------------ O_w += P V issuer
     if (lane == 0) {
       constexpr uint32_t ID_PV = F8 ? idesc_f16(HD, 1) : idesc_bf16(HD, 1);
       // V: MN-major, 64-column blocks L::BLK apart (LBO), 8-key groups 1024 B apart (SBO)
@@ -513,26 +528,32 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
       uint32_t it = 0;
       bool ok = true;
       while (ok && seg_next(p, num_units, t, t_end, u, s)) {
+        bool first[2] = {true, true};  // each accumulator starts afresh in every unit
         for (int j = s.j0; j < s.j1; ++j, ++it) {
-          const uint32_t st = F8 ? it % L::NCV : it % L::NR;
+          const uint32_t st = F8 ? it % NCV : it % L::NR;
           uint64_t* vready = F8 ? &bars->vc_full[st] : &bars->v_full[st];
-          const uint32_t vpar = F8 ? (it / L::NCV) & 1 : (it / L::NR) & 1;
-          const uint32_t sb = it & 1;
-          if (!mbar_wait(&bars->p_full[sb], (it >> 1) & 1, abort, p.flags) ||
-              !mbar_wait(vready, vpar, abort, p.flags)) {
+          const uint32_t vpar = F8 ? (it / NCV) & 1 : (it / L::NR) & 1;
+          if (!mbar_wait(vready, vpar, abort, p.flags)) {
             ok = false;
             break;
           }
-          fence_after();
           const uint64_t vd = vdesc0 + ((st * (F8 ? L::TILE : L::STAGE)) >> 4);
-          // keys [16kk, 16kk + 16): warpgroup kk / 4 wrote them at its half's first columns
-          const uint32_t pcol = tmem + COL_S0 + sb * 128;
+          for (int w = 0; w < 2 && ok; ++w) {
+            if (!mbar_wait(&bars->p_full[w], it & 1, abort, p.flags)) {
+              ok = false;
+              break;
+            }
+            fence_after();
+            // keys [64w + 16kk, +16): rows 64w + 16kk of the V tile (128 bytes each)
 #pragma unroll
-          for (int kk = 0; kk < KT / 16; ++kk)
-            mma_ts(tmem + COL_O, pcol + (kk >> 2) * (KT / 2) + (kk & 3) * 8,
-                   vd + ((kk * 16 * 128) >> 4), ID_PV, (j == s.j0 && kk == 0) ? 0u : 1u);
-          mma_commit(&bars->o_done[sb]);
-          mma_commit(&bars->s_free[sb]);
+            for (int kk = 0; kk < HK / 16; ++kk)
+              mma_ts(tmem + COL_O + w * 128, tmem + COL_P + w * (HK / 2) + kk * 8,
+                     vd + (((w * HK + kk * 16) * 128) >> 4), ID_PV,
+                     (first[w] && kk == 0) ? 0u : 1u);
+            first[w] = false;
+            mma_commit(&bars->o_done[w]);
+          }
+          if (!ok) break;
           mma_commit(F8 ? &bars->vc_empty[st] : &bars->kv_empty[st]);
         }
       }
@@ -543,16 +564,11 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
     }
   } else if (warp >= SOFTMAX_WARP0 && warp < SOFTMAX_WARP0 + NSOFT / 32) {
     // ------------------------------------------------------------ softmax / epilogue
-    // Two warpgroups share every query row: warpgroup h handles columns [64h, 64h + 64) of
-    // each score tile and the same half of the output columns. They exchange half-tile
-    // row maxima through shared memory at one named barrier per tile, so both apply the
-    // same reference max; the half sums are added once per unit.
     const int wg = (warp - SOFTMAX_WARP0) >> 2;
     const int r = (warp & 3) * 32 + lane;  // query row = TMEM lane
-    const int st_id = wg * 128 + r;        // 0..255 within the softmax threads
     const uint32_t tq = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    constexpr int HC = KT / 2;             // score columns per warpgroup
-    constexpr int OC = HD / 2;             // output columns per warpgroup
+    const uint32_t colS = COL_S + wg * HK;
+    constexpr int OC = HD / 2;             // output columns per warpgroup in the epilogue
     auto wwait = [&](uint64_t* bar, uint32_t par) -> bool {
       return __all_sync(0xffffffffu, mbar_wait(bar, par, abort, p.flags));
     };
@@ -631,104 +647,98 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
       fence_before();
       mbar_arrive(&bars->q_full);
 
+      // this warpgroup's half of every tile of the unit
       float m_ref = -INFINITY, lh = 0.f;
+      uint32_t it_last = 0;
       bool good = true;
       for (int j = s.j0; j < s.j1; ++j, ++it) {
-        const uint32_t sb = it & 1;
-        float sv[HC];
-        float mx = -INFINITY;
-        const int key0 = j * KT + wg * HC;
-        if (good && (good = wwait(&bars->s_full[sb], (it >> 1) & 1))) {
-          fence_after();
+        if (!good) continue;
+        it_last = it;
+        if (!(good = wwait(&bars->s_full, it & 1))) continue;
+        fence_after();
+        float sv[HK];
+        {
           uint32_t* raw = reinterpret_cast<uint32_t*>(sv);
 #pragma unroll
-          for (int c = 0; c < HC / 32; ++c)
-            tmem_ld32(tq + COL_S0 + sb * 128 + wg * HC + c * 32, raw + c * 32);
+          for (int c = 0; c < HK / 32; ++c) tmem_ld32(tq + colS + c * 32, raw + c * 32);
           tmem_wait_ld();
 #pragma unroll
-          for (int c = 0; c < HC / 32; ++c) reg_fence32(raw + c * 32);
-          if (key0 + HC - 1 > T) {  // the window-causal mask reaches into this half tile
-            const int lim = T + i_row - key0;
-#pragma unroll
-            for (int c = 0; c < HC; ++c)
-              if (c > lim) sv[c] = -INFINITY;
-          }
-          float m8[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) m8[e] = sv[e];
-#pragma unroll
-          for (int c = 8; c < HC; ++c) m8[c & 7] = fmaxf(m8[c & 7], sv[c]);
-          mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                     fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-          bars->xmax[sb][wg][r] = mx;
+          for (int c = 0; c < HK / 32; ++c) reg_fence32(raw + c * 32);
         }
-        if (!softmax_pair_and(good)) {
-          ok = false;
-          break;
+        fence_before();
+        mbar_arrive(&bars->s_free);  // the scores are in registers: the next S may start
+        const int key0 = j * KT + wg * HK;
+        if (key0 + HK - 1 > T) {  // the window-causal mask reaches into this half tile
+          const int lim = T + i_row - key0;
+#pragma unroll
+          for (int c = 0; c < HK; ++c)
+            if (c > lim) sv[c] = -INFINITY;
         }
-        mx = fmaxf(mx, bars->xmax[sb][wg ^ 1][r]);
+        float m8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) m8[e] = sv[e];
+#pragma unroll
+        for (int c = 8; c < HK; ++c) m8[c & 7] = fmaxf(m8[c & 7], sv[c]);
+        const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
         const float mt = mx * sc;  // tile max in log2 units (sc > 0)
         // The decision is per row, but TMEM loads and stores are warp-collective: the whole
         // warp rescales when any of its rows needs it, with alpha = 1 for the others.
         float alpha = 1.f;
         const bool grow = m_ref != -INFINITY && mt > m_ref + RESCALE_THRESHOLD;
         if (m_ref == -INFINITY) {
-          m_ref = mt;  // O holds nothing yet for this row (zeros or about to be overwritten)
+          m_ref = mt;  // O_w holds nothing yet for this row (zeros or about to be overwritten)
         } else if (grow) {
           alpha = ex2(m_ref - mt);
           lh *= alpha;
           m_ref = mt;
         }
-        if (__any_sync(0xffffffffu, grow)) {
-          // O is only touched once the previous tile's P V is complete (never on a unit's
-          // first tile: grow is false there). That P V's buffer barrier is at most one
-          // phase behind it: the previous tile's S was issued only after the P V two
-          // tiles before it had completed.
-          const uint32_t pb = (it - 1) & 1;
-          good = wwait(&bars->o_done[pb], ((it - 1) >> 1) & 1);
-          if (!good) continue;  // leave together at the next barrier
+        // O_w and the P buffer are reused once this warpgroup's previous P V is complete.
+        // Its barrier cannot be two phases behind: that tile's P was stored only after
+        // the P V before it had completed.
+        if (it >= 1) {
+          if (!(good = wwait(&bars->o_done[wg], (it - 1) & 1))) continue;
           fence_after();
+        }
+        if (__any_sync(0xffffffffu, grow)) {  // (never on a unit's first tile)
 #pragma unroll 1
-          for (int c = 0; c < OC / 32; ++c) {
-            uint32_t ro[32];
-            tmem_ld32(tq + COL_O + wg * OC + c * 32, ro);
+          for (int c = 0; c < HD / 16; ++c) {  // 16 columns at a time: sv stays in registers
+            uint32_t ro[16];
+            tmem_ld16(tq + COL_O + wg * 128 + c * 16, ro);
             tmem_wait_ld();
-            reg_fence32(ro);
+            reg_fence16(ro);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) ro[e] = __float_as_uint(__uint_as_float(ro[e]) * alpha);
-            tmem_st32(tq + COL_O + wg * OC + c * 32, ro);
+            for (int e = 0; e < 16; ++e) ro[e] = __float_as_uint(__uint_as_float(ro[e]) * alpha);
+            tmem_st16(tq + COL_O + wg * 128 + c * 16, ro);
           }
-          tmem_wait_st();
         }
         const float nmu = m_ref == -INFINITY ? 0.f : -m_ref;
         float s8[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) s8[e] = 0.f;
 #pragma unroll
-        for (int c = 0; c < HC; ++c) {
+        for (int c = 0; c < HK; ++c) {
           sv[c] = ex2(fmaf(sv[c], sc, nmu));
           s8[c & 7] += sv[c];
         }
         lh += ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
         {
-          uint32_t pk[32];
+          uint32_t pk[HK / 2];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) pk[e] = pack_p<F8>(sv[2 * e], sv[2 * e + 1]);
-          tmem_st32(tq + COL_S0 + sb * 128 + wg * HC, pk);
+          for (int e = 0; e < HK / 2; ++e) pk[e] = pack_p<F8>(sv[2 * e], sv[2 * e + 1]);
+          tmem_st32(tq + COL_P + wg * (HK / 2), pk);
           tmem_wait_st();
         }
-        const int tkey0 = j * KT;
         bool zeroed = false;
-        if (!F8 && tkey0 + KT > nkeys) {
-          // last tile of the sequence: clear the V rows past its end so that P = 0 never
-          // meets non-finite data (they may hold the next sequence or unwritten memory)
+        if (!F8 && key0 + HK > nkeys) {
+          // last tile of the sequence: clear this half's V rows past its end so that P = 0
+          // never meets non-finite data (they may hold the next sequence or unwritten memory)
           const uint32_t st = it % L::NR;
-          good = wwait(&bars->v_full[st], (it / L::NR) & 1);
-          if (!good) continue;
-          const int first = nkeys - tkey0;
+          if (!(good = wwait(&bars->v_full[st], (it / L::NR) & 1))) continue;
+          const int first = max(nkeys - key0, 0) + wg * HK;  // first row to clear
           uint8_t* vt = smem + st * L::STAGE + L::TILE;
-          const int chunks = (KT - first) * 8;  // 16-byte chunks per 64-column block
-          for (int q = st_id; q < chunks * L::NBLK; q += NSOFT) {
+          const int chunks = (wg * HK + HK - first) * 8;  // 16-byte chunks per column block
+          for (int q = r; q < chunks * L::NBLK; q += NSOFT / 2) {
             const int blk = q / chunks, rem = q % chunks;
             *reinterpret_cast<uint4*>(vt + blk * L::BLK + (first + rem / 8) * 128 + (rem % 8) * 16) =
                 make_uint4(0, 0, 0, 0);
@@ -737,60 +747,66 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
         }
         if (zeroed) fence_proxy_async();
         fence_before();
-        mbar_arrive(&bars->p_full[sb]);
+        mbar_arrive(&bars->p_full[wg]);
       }
-      if (!ok) break;
-      if (good) {  // the unit's last P V (and with it every earlier one) is complete
-        good = wwait(&bars->o_done[(it - 1) & 1], ((it - 1) >> 1) & 1);
+      // this warpgroup's last P V of the unit (and with it every earlier one) is complete
+      if (good) {
+        good = wwait(&bars->o_done[wg], it_last & 1);
         if (good) fence_after();
       }
-      float* xl = bars->xmax[it & 1][0];  // the last tile used parity (it - 1) & 1
-      xl[wg * 128 + r] = lh;
-      if (!softmax_pair_and(good)) break;
-      const float l = lh + xl[(wg ^ 1) * 128 + r];
+      bars->xm[wg][r] = m_ref;
+      bars->xl[wg][r] = lh;
+      if (!softmax_pair_and(good)) {
+        ok = false;
+        break;
+      }
+      fence_after();  // the other warpgroup's accumulator is complete too
 
-      // ---- epilogue: this warpgroup's half of the output columns
+      // ---- epilogue: merge the two accumulators; this warpgroup's half of the columns
+      const float m0 = bars->xm[0][r], m1 = bars->xm[1][r];
+      const float m = fmaxf(m0, m1);
+      const float a0 = m0 == -INFINITY ? 0.f : ex2(m0 - m);
+      const float a1 = m1 == -INFINITY ? 0.f : ex2(m1 - m);
+      const float l = a0 * bars->xl[0][r] + a1 * bars->xl[1][r];
       const bool whole = s.j0 == 0 && s.j1 == s.nt;
-      if (whole) {
-        const float inv = vs / l;
-        __nv_bfloat16* dst = (__nv_bfloat16*)p.out +
-                             ((p.q_off[s.b] + i_row) * p.Hq + (int64_t)s.g * p.G + hl) * HD +
-                             wg * OC;
+      const float inv = whole ? vs / l : 1.f;
+      auto merged = [&](uint32_t o0, uint32_t o1) {  // an accumulator without tiles is skipped
+        return (a0 != 0.f ? a0 * __uint_as_float(o0) : 0.f) +
+               (a1 != 0.f ? a1 * __uint_as_float(o1) : 0.f);
+      };
 #pragma unroll 1
-        for (int c = 0; c < OC / 32; ++c) {
-          uint32_t ro[32];
-          tmem_ld32(tq + COL_O + wg * OC + c * 32, ro);
-          tmem_wait_ld();
-          reg_fence32(ro);
-          if (live) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e)
-              pk[e] = pack_bf16(__uint_as_float(ro[2 * e]) * inv, __uint_as_float(ro[2 * e + 1]) * inv);
-            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              d4[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
-          }
-        }
-      } else {
-        const size_t slot = (size_t)blockIdx.x + s.u;
-        float* dst = p.part_o + (slot * MT + r) * HD + wg * OC;
-#pragma unroll 1
-        for (int c = 0; c < OC / 32; ++c) {
-          uint32_t ro[32];
-          tmem_ld32(tq + COL_O + wg * OC + c * 32, ro);
-          tmem_wait_ld();
-          reg_fence32(ro);
-          if (live) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+      for (int c = 0; c < OC / 16; ++c) {
+        uint32_t r0[16], r1[16];
+        tmem_ld16(tq + COL_O + wg * OC + c * 16, r0);
+        tmem_ld16(tq + COL_O + 128 + wg * OC + c * 16, r1);
+        tmem_wait_ld();
+        reg_fence16(r0);
+        reg_fence16(r1);
+        if (live) {
+          if (whole) {
+            __nv_bfloat16* dst = (__nv_bfloat16*)p.out +
+                                 ((p.q_off[s.b] + i_row) * p.Hq + (int64_t)s.g * p.G + hl) * HD +
+                                 wg * OC + c * 16;
+            uint32_t pk[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e)
-              d4[e] = make_uint4(ro[4 * e], ro[4 * e + 1], ro[4 * e + 2], ro[4 * e + 3]);
+              pk[e] = pack_bf16(merged(r0[2 * e], r1[2 * e]) * inv,
+                                merged(r0[2 * e + 1], r1[2 * e + 1]) * inv);
+            uint4* d4 = reinterpret_cast<uint4*>(dst);
+            d4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            d4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          } else {
+            const size_t slot = (size_t)blockIdx.x + s.u;
+            float4* d4 = reinterpret_cast<float4*>(p.part_o + (slot * MT + r) * HD + wg * OC + c * 16);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              d4[e] = make_float4(merged(r0[4 * e], r1[4 * e]), merged(r0[4 * e + 1], r1[4 * e + 1]),
+                                  merged(r0[4 * e + 2], r1[4 * e + 2]),
+                                  merged(r0[4 * e + 3], r1[4 * e + 3]));
           }
         }
-        if (live && wg == 0) p.part_ml[slot * MT + r] = make_float2(m_ref, l);
       }
+      if (!whole && live && wg == 0) p.part_ml[((size_t)blockIdx.x + s.u) * MT + r] = make_float2(m, l);
       fence_before();  // TMEM reads above complete before the next unit's MMAs
     }
   }
@@ -820,10 +836,9 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
       while (ok && seg_next(p, num_units, t, t_end, u, s)) {
         const int nkeys = p.seq_lens[s.b] + p.draft_len[s.b] + 1;
         for (int j = s.j0; j < s.j1; ++j, ++it) {
-          const uint32_t rs = it % L::NR, cs = it % L::NCV;
+          const uint32_t rs = it % L::NR, cs = it % NCV;
           if (!mbar_wait(&bars->v_full[rs], (it / L::NR) & 1, abort, p.flags) ||
-              (it >= L::NCV &&
-               !mbar_wait(&bars->vc_empty[cs], ((it / L::NCV) - 1) & 1, abort, p.flags))) {
+              (it >= NCV && !mbar_wait(&bars->vc_empty[cs], ((it / NCV) - 1) & 1, abort, p.flags))) {
             ok = false;
             break;
           }
