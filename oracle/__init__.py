@@ -18,6 +18,8 @@ Functions and the passages they follow (page title, then section):
 * ``accept`` -- first-mismatch acceptance: "Co-Designing AI Models Using Speculative
   Decoding" summary, "basic structure" (AL in [1, 1+D]); "GPU and LLM, chapter 5",
   "Speculative decoding (2)" (the target's own token replaces the first rejected draft).
+* ``draft_signals`` -- per row, the confidence (largest softmax probability) and the
+  entropy (nats) of the softmax: "SpecKV" summary, "technical core", item 1.
 * ``bf16_to_f64`` / ``e4m3_to_f64`` -- decoders written from the binary32 and OCP E4M3
   format definitions.
 """
@@ -71,6 +73,8 @@ def _load():
             lib.orc_argmax_rows.restype = i32
             lib.orc_accept.argtypes = [i32, p, p, p, p, p]
             lib.orc_accept.restype = i32
+            lib.orc_draft_signals.argtypes = [i64, i64, i32, p, p, p, i32]
+            lib.orc_draft_signals.restype = i32
             _lib = lib
     return _lib
 
@@ -191,3 +195,22 @@ def spec_accept(logits, draft_tokens, draft_len, nthreads=0):
     amax = argmax_rows(logits, nthreads)
     al, nt = accept(amax, draft_tokens, draft_len)
     return al, nt, amax
+
+
+def draft_signals(logits, nthreads=0):
+    """logits: [rows, V] fp32, or uint16 bf16 bits. Returns (confidence, entropy), fp64
+    [rows] each: the largest probability and the entropy in nats of each row's softmax."""
+    logits = np.ascontiguousarray(logits)
+    if logits.dtype == np.uint16:
+        dt = 0
+    elif logits.dtype == np.float32:
+        dt = 2
+    else:
+        raise TypeError("logits must be float32 or uint16 (bf16 bits)")
+    rows, vocab = logits.shape
+    conf = np.empty(rows, dtype=np.float64)
+    ent = np.empty(rows, dtype=np.float64)
+    if _load().orc_draft_signals(rows, vocab, dt, _ptr(logits), _ptr(conf), _ptr(ent),
+                                 int(nthreads)):
+        raise ValueError("oracle rejected the arguments")
+    return conf, ent

@@ -14,6 +14,9 @@
  *        (the m / l / O update, exact rather than approximate), "GQA: several Q heads share
  *        one K/V head", "Speculative decoding (2): verify together" (3 accepted, the 4th
  *        rejected, the target's own token inserted; one forward over k+1 positions).
+ *   [P4] "SpecKV: Adaptive Speculative Decoding with Compression-Aware Gamma Selection"
+ *        (summary page), section "technical core", item 1: the draft model's confidence
+ *        and entropy, the inputs of the gamma controller.
  *
  * Readings where the pages are silent:
  *   - The 1+D window rows' K/V are already in the cache at positions T..T+D; window row i
@@ -22,6 +25,8 @@
  *   - FP8 values are OCP E4M3 codes times a per-KV-head fp32 scale (kv_scale[0][g] for K,
  *     kv_scale[1][g] for V).
  *   - Argmax ties go to the lowest index; -0.0 equals +0.0.
+ *   - Draft signals: confidence = the largest probability of the row's softmax (the first
+ *     of the page's two options); entropy = the Shannon entropy of that softmax in nats.
  *
  * Layouts (packed ragged batch): q and out [sum_b W_b, Hq, d]; k and v
  * [sum_b (T_b + W_b), Hkv, d]; W_b = 1 + D_b; sequences in batch order.
@@ -291,4 +296,46 @@ int orc_accept(int B, const int32_t* draft_len, const int32_t* draft_tokens,
     d_off += D;
   }
   return 0;
+}
+
+/* Draft signals of every row ([P4] "technical core", item 1). The softmax of the row is
+ * materialised in fp64, p_j = exp(x_j - m) / sum_k exp(x_k - m) with m the row maximum;
+ * confidence = max_j p_j; entropy = -sum_j p_j ln p_j over the p_j > 0 (0 ln 0 = 0).
+ * dtype 0: bf16 bit patterns; 2: fp32. Rows must hold at least one finite value. */
+int orc_draft_signals(int64_t rows, int64_t vocab, int dtype, const void* logits,
+                      double* confidence, double* entropy, int nthreads) {
+  if (rows < 0 || vocab <= 0 || (dtype != 0 && dtype != 2)) return 1;
+  int bad = 0;
+#ifdef _OPENMP
+  if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel for num_threads(nthreads) schedule(static) reduction(| : bad)
+#endif
+  for (int64_t r = 0; r < rows; ++r) {
+    double* p = (double*)malloc(sizeof(double) * (size_t)vocab);
+    if (!p) {
+      bad = 1;
+      continue;
+    }
+    double m = -INFINITY;
+    for (int64_t j = 0; j < vocab; ++j) {
+      p[j] = dtype == 0 ? orc_bf16_to_f64(((const uint16_t*)logits)[r * vocab + j])
+                        : (double)((const float*)logits)[r * vocab + j];
+      if (p[j] > m) m = p[j];
+    }
+    double z = 0.0;
+    for (int64_t j = 0; j < vocab; ++j) {
+      p[j] = exp(p[j] - m);
+      z += p[j];
+    }
+    double pmax = 0.0, h = 0.0;
+    for (int64_t j = 0; j < vocab; ++j) {
+      const double pj = p[j] / z;
+      if (pj > pmax) pmax = pj;
+      if (pj > 0.0) h -= pj * log(pj);
+    }
+    confidence[r] = pmax;
+    entropy[r] = h;
+    free(p);
+  }
+  return bad;
 }

@@ -350,3 +350,62 @@ def test_expected_acceptance_length(alpha, k, printed, dec):
 def test_accept_rejects_bad_sizes():
     with pytest.raises(ValueError):
         oracle.accept(np.zeros(3, np.int32), np.zeros(3, np.int32), np.array([3]))
+
+
+# ------------------------------------------------------------------ draft signals
+
+def test_draft_signals_uniform_and_equal_maxima():
+    """Equal logits: confidence 1/V, entropy ln V. k equal maxima with the rest at -inf:
+    confidence 1/k, entropy ln k."""
+    V = 1000
+    conf, ent = oracle.draft_signals(np.full((2, V), 0.25, dtype=np.float32))
+    assert np.allclose(conf, 1.0 / V, rtol=1e-12) and np.allclose(ent, math.log(V), rtol=1e-12)
+    for k in (1, 2, 7):
+        x = np.full((1, V), -np.inf, dtype=np.float32)
+        x[0, np.arange(k) * 97] = 3.0
+        conf, ent = oracle.draft_signals(x)
+        assert conf[0] == pytest.approx(1.0 / k, rel=1e-12)
+        assert ent[0] == pytest.approx(math.log(k), abs=1e-12)
+
+
+@pytest.mark.parametrize("a", [0.0, 0.5, -3.0, 12.0])
+def test_draft_signals_two_point_closed_form(a):
+    """Two finite logits (a, 0), the rest -inf: p = 1/(1 + e^-a); confidence max(p, 1-p),
+    entropy -p ln p - (1-p) ln(1-p)."""
+    x = np.full((1, 50), -np.inf, dtype=np.float32)
+    x[0, 3], x[0, 40] = a, 0.0
+    p = 1.0 / (1.0 + math.exp(-a))
+    conf, ent = oracle.draft_signals(x)
+    assert conf[0] == pytest.approx(max(p, 1 - p), rel=1e-12)
+    h = -p * math.log(p) - (1 - p) * math.log(1 - p)
+    assert ent[0] == pytest.approx(h, rel=1e-10, abs=1e-15)
+
+
+def test_draft_signals_match_library_softmax_entropy():
+    """Random rows against scipy's softmax and entropy (natural log), fp32 and bf16."""
+    scipy_special = pytest.importorskip("scipy.special")
+    scipy_stats = pytest.importorskip("scipy.stats")
+    rng = np.random.default_rng(5)
+    x = (rng.standard_normal((6, 3001)) * rng.uniform(0.1, 6.0, (6, 1))).astype(np.float32)
+    for logits, vals in ((x, x.astype(np.float64)),
+                         (synth.bf16_bits(x), None)):
+        if vals is None:
+            vals = (logits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        conf, ent = oracle.draft_signals(logits)
+        p = scipy_special.softmax(vals, axis=1)
+        assert np.allclose(conf, p.max(axis=1), rtol=1e-12)
+        assert np.allclose(ent, scipy_stats.entropy(p, axis=1), rtol=1e-10)
+
+
+def test_draft_signals_shift_invariance_and_bounds():
+    """Adding a constant to a row changes neither signal; 1/V <= confidence <= 1,
+    0 <= entropy <= ln V, and confidence >= exp(-entropy) (min-entropy <= entropy)."""
+    rng = np.random.default_rng(6)
+    V = 777
+    x = (rng.standard_normal((8, V)) * 3).astype(np.float32)
+    c0, h0 = oracle.draft_signals(x)
+    c1, h1 = oracle.draft_signals(x + np.float32(17.0))
+    assert np.allclose(c0, c1, rtol=1e-5) and np.allclose(h0, h1, rtol=1e-5, atol=1e-6)
+    assert np.all(c0 >= 1.0 / V) and np.all(c0 <= 1.0)
+    assert np.all(h0 >= 0) and np.all(h0 <= math.log(V) + 1e-12)
+    assert np.all(c0 >= np.exp(-h0) - 1e-12)
