@@ -383,6 +383,25 @@ def run_ours(args):
     verify_ms = float(np.median([e[0].elapsed_time(e[1]) for e in e3]))
     accept_ms = float(np.median([e[1].elapsed_time(e[2]) for e in e3]))
 
+    # draft signals (confidence, entropy per row) over the step's logits matrix, as a
+    # stand-in for the draft model's logits of the same shape (not part of the step)
+    rows_l, V_l = d["logits"].shape
+    sig_c = torch.empty(rows_l, dtype=torch.float32, device=dev)
+    sig_e = torch.empty(rows_l, dtype=torch.float32, device=dev)
+    ws_sig = sv.new_workspace(sv.signals_workspace_bytes(rows_l, V_l), dev)
+    for _ in range(3):
+        sv.spec_draft_signals(d["logits"], confidence=sig_c, entropy=sig_e, workspace=ws_sig,
+                              stream=stream)
+    es = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K3)]
+    for i in range(K3):
+        es[i][0].record(stream)
+        sv.spec_draft_signals(d["logits"], confidence=sig_c, entropy=sig_e, workspace=ws_sig,
+                              stream=stream)
+        es[i][1].record(stream)
+    torch.cuda.synchronize()
+    signals_ms = float(np.median([e[0].elapsed_time(e[1]) for e in es]))
+    logits_bytes = d["logits"].numel() * d["logits"].element_size()
+
     # end to end: pinned host inputs -> device, step, result back to pinned host memory
     e2e = None
     if not args.no_e2e:
@@ -460,6 +479,11 @@ def run_ours(args):
             "attn_ms": round(attn_ms, 5),
             "verify_call_ms": round(verify_ms, 5),
             "accept_call_ms": round(accept_ms, 5),
+            "draft_signals": {"ms": round(signals_ms, 5),
+                              "GB_per_s": round(logits_bytes / (signals_ms / 1e3) / 1e9, 1),
+                              "rows": rows_l, "vocab": V_l,
+                              "note": "spec_draft_signals on a logits matrix of the step's "
+                                      "shape; not part of the step"},
             "attn_tflops": round(fl / (attn_ms / 1e3) / 1e12, 2),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
                          "unit": "GB/s", "frac": round(achieved / hbm, 4),

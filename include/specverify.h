@@ -170,6 +170,32 @@ SV_API sv_status spec_accept_noalloc(int32_t batch, int32_t max_draft_len, int32
                                      int32_t* accept_len, int32_t* next_token,
                                      int32_t* target_tokens, void* stream);
 
+/* Bytes of workspace spec_draft_signals needs on the current CUDA device. 0 if invalid. */
+SV_API size_t spec_draft_signals_workspace_size(int32_t rows, int32_t vocab);
+
+/*
+ * spec_draft_signals -- the draft signals of "SpecKV: Adaptive Speculative Decoding with
+ * Compression-Aware Gamma Selection" (summary, "technical core", item 1), the inputs of
+ * its speculation-length controller, for every row of a logits matrix (in that use, the
+ * draft model's logits at each drafted position):
+ *   confidence[r] = max_j p_j,  entropy[r] = -sum_j p_j ln p_j (nats),
+ *   p = softmax(logits[r, :]).
+ * The page names the largest probability as one reading of "confidence"; the entropy's
+ * base is not given and is taken as e.
+ *
+ *   logits       bf16 or fp32 [rows, vocab], row-major; every row must hold at least one
+ *                finite value (NaN elements are ignored)
+ *   confidence, entropy  fp32 [rows] (outputs)
+ *   workspace >= spec_draft_signals_workspace_size(rows, vocab) bytes, 256-byte aligned,
+ *                zero-filled before its first use (it keeps a completion counter that
+ *                every call leaves at zero)
+ * One pass over the logits, fp32 arithmetic: a running max, sum of exponentials and
+ * exponent-weighted sum per part of a row, merged with the online-softmax rule.
+ */
+SV_API sv_status spec_draft_signals(int32_t rows, int32_t vocab, int32_t logits_dtype,
+                                    const void* logits, float* confidence, float* entropy,
+                                    void* workspace, size_t workspace_bytes, void* stream);
+
 /* Synchronises `stream`, then reads the sticky device-side flags of a workspace used by
  * either call: SV_OK, SV_ERR_DEVICE_SHAPE or SV_ERR_TIMEOUT. clear != 0 resets them. */
 SV_API sv_status sv_workspace_status(void* workspace, int clear, void* stream);

@@ -26,7 +26,8 @@ STATUS = {0: "SV_OK", 1: "SV_ERR_NULL", 2: "SV_ERR_SHAPE", 3: "SV_ERR_DTYPE",
           4: "SV_ERR_ALIGN", 5: "SV_ERR_WORKSPACE", 6: "SV_ERR_CUDA", 7: "SV_ERR_TIMEOUT",
           8: "SV_ERR_DEVICE_SHAPE"}
 EXPORTS = ("spec_verify_attn_workspace_size", "spec_verify_attn", "spec_accept_workspace_size",
-           "spec_accept", "sv_workspace_status", "sv_status_string", "sv_set_attn_kernel",
+           "spec_accept", "spec_draft_signals_workspace_size", "spec_draft_signals",
+           "sv_workspace_status", "sv_status_string", "sv_set_attn_kernel",
            "sv_set_profile_events", "sv_version")
 
 
@@ -68,6 +69,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.spec_accept_workspace_size.restype = sz
         lib.spec_accept.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         lib.spec_accept.restype = ctypes.c_int
+        lib.spec_draft_signals_workspace_size.argtypes = [i32, i32]
+        lib.spec_draft_signals_workspace_size.restype = sz
+        lib.spec_draft_signals.argtypes = [i32, i32, i32, vp, vp, vp, vp, sz, vp]
+        lib.spec_draft_signals.restype = ctypes.c_int
         lib.sv_workspace_status.argtypes = [vp, ctypes.c_int, vp]
         lib.sv_workspace_status.restype = ctypes.c_int
         lib.sv_status_string.argtypes = [ctypes.c_int]
@@ -126,6 +131,13 @@ def accept_workspace_bytes(batch: int, max_draft_len: int, vocab: int) -> int:
     n = load_library().spec_accept_workspace_size(batch, max_draft_len, vocab)
     if n == 0:
         raise SpecVerifyError(2, "spec_accept_workspace_size")
+    return n
+
+
+def signals_workspace_bytes(rows: int, vocab: int) -> int:
+    n = load_library().spec_draft_signals_workspace_size(rows, vocab)
+    if n == 0:
+        raise SpecVerifyError(2, "spec_draft_signals_workspace_size")
     return n
 
 
@@ -193,6 +205,28 @@ def spec_accept(logits, draft_tokens, draft_len, *, max_draft_len: int, accept_l
         workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, "spec_accept")
     return accept_len, next_token
+
+
+def spec_draft_signals(logits, *, confidence=None, entropy=None, workspace=None, stream=None):
+    """logits [rows, V] bf16 or fp32 (e.g. the draft model's logits at each drafted
+    position). Returns (confidence, entropy), fp32 [rows] each: the largest probability
+    and the entropy (nats) of each row's softmax."""
+    _need(logits, "logits", (torch.bfloat16, torch.float32))
+    rows, V = logits.shape
+    if confidence is None:
+        confidence = torch.empty(rows, dtype=torch.float32, device=logits.device)
+    if entropy is None:
+        entropy = torch.empty(rows, dtype=torch.float32, device=logits.device)
+    for t, n in ((confidence, "confidence"), (entropy, "entropy")):
+        _need(t, n, (torch.float32,))
+    if workspace is None:
+        workspace = new_workspace(signals_workspace_bytes(rows, V), logits.device)
+    dt = SV_BF16 if logits.dtype == torch.bfloat16 else SV_FP32
+    st = load_library().spec_draft_signals(
+        rows, V, dt, _ptr(logits), _ptr(confidence), _ptr(entropy), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "spec_draft_signals")
+    return confidence, entropy
 
 
 def workspace_status(workspace: torch.Tensor, clear: bool = False, stream=None) -> int:

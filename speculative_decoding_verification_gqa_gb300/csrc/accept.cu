@@ -16,6 +16,7 @@
 #include <cuda_bf16.h>
 
 #include "internal.cuh"
+#include "logits_vec.cuh"
 
 namespace sv {
 namespace {
@@ -39,21 +40,6 @@ __device__ __forceinline__ void take(float x, int idx, float& bv, int& bi) {
     bv = x;
     bi = idx;
   }
-}
-
-__device__ __forceinline__ float bf16_at(uint32_t w, int hi) {
-  return __uint_as_float(hi ? (w & 0xffff0000u) : (w << 16));
-}
-
-__device__ __forceinline__ __nv_bfloat162 as_bf2(uint32_t w) {
-  return *reinterpret_cast<const __nv_bfloat162*>(&w);
-}
-
-// Largest of eight bf16 values (NaN ignored unless all are NaN), widened to fp32.
-__device__ __forceinline__ float vmax_bf16x8(const uint4& w) {
-  const __nv_bfloat162 m = __hmax2(__hmax2(as_bf2(w.x), as_bf2(w.y)), __hmax2(as_bf2(w.z), as_bf2(w.w)));
-  const uint32_t u = *reinterpret_cast<const uint32_t*>(&m);
-  return fmaxf(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
 }
 
 __device__ __forceinline__ void warp_argmax(float& bv, int& bi) {

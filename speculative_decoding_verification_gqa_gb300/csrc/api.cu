@@ -210,6 +210,33 @@ SV_API sv_status spec_accept(int32_t batch, int32_t max_draft_len, int32_t vocab
   return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
+SV_API size_t spec_draft_signals_workspace_size(int32_t rows, int32_t vocab) {
+  if (rows < 0 || vocab <= 0) return 0;
+  const int sms = current_sms();
+  if (sms <= 0) return 0;
+  return signals_ws_layout(rows, vocab, sms).total;
+}
+
+SV_API sv_status spec_draft_signals(int32_t rows, int32_t vocab, int32_t logits_dtype,
+                                    const void* logits, float* confidence, float* entropy,
+                                    void* workspace, size_t workspace_bytes, void* stream) {
+  if (rows < 0 || vocab <= 0) return SV_ERR_SHAPE;
+  if (logits_dtype != SV_BF16 && logits_dtype != SV_FP32) return SV_ERR_DTYPE;
+  if (rows == 0) return SV_OK;
+  if (!logits || !confidence || !entropy || !workspace) return SV_ERR_NULL;
+  const uintptr_t es = logits_dtype == SV_BF16 ? 2 : 4;
+  if (!aligned(logits, es) || !aligned(confidence, 4) || !aligned(entropy, 4) ||
+      !aligned(workspace, 256))
+    return SV_ERR_ALIGN;
+  const int sms = current_sms();
+  if (sms <= 0) return SV_ERR_CUDA;
+  const SigWs lay = signals_ws_layout(rows, vocab, sms);
+  if (workspace_bytes < lay.total) return SV_ERR_WORKSPACE;
+  const cudaError_t e = launch_signals(rows, vocab, logits_dtype, logits, confidence, entropy,
+                                       workspace, lay, (cudaStream_t)stream);
+  return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
 SV_API sv_status sv_workspace_status(void* workspace, int clear, void* stream) {
   if (!workspace) return SV_ERR_NULL;
   cudaStream_t s = (cudaStream_t)stream;

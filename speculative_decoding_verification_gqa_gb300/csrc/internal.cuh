@@ -160,4 +160,14 @@ cudaError_t launch_accept(int B, int max_draft, int vocab, int dtype, const void
                           int32_t* accept_len, int32_t* next_token, int32_t* target_tokens,
                           void* ws, const AcceptWs& lay, cudaStream_t s);
 
+// Draft signals.
+struct SigWs {
+  size_t ctrl, part, total;
+  int nctas;
+};
+SigWs signals_ws_layout(int64_t rows, int vocab, int num_sms);
+cudaError_t launch_signals(int64_t rows, int vocab, int dtype, const void* logits,
+                           float* confidence, float* entropy, void* ws, const SigWs& lay,
+                           cudaStream_t s);
+
 }  // namespace sv
