@@ -14,6 +14,9 @@ Functions and the passages they follow (page title, then section):
   softmax(Q K^T) V) and "Speculative decoding (2)" (one forward over the 1+D positions).
 * ``verify_attn_online`` -- the same result through the online-softmax update of
   "GPU and LLM, chapter 5", "Online softmax: carry the max and the sum".
+* ``verify_attn(window=W)`` -- sliding-window verify attention: "GPU and LLM, chapter 5",
+  "Sliding window: do not keep the distant past" (each position sees the W most recent
+  positions, itself included).
 * ``argmax_rows`` -- naive first-index argmax (target's greedy choice per window row).
 * ``accept`` -- first-mismatch acceptance: "Co-Designing AI Models Using Speculative
   Decoding" summary, "basic structure" (AL in [1, 1+D]); "GPU and LLM, chapter 5",
@@ -65,9 +68,9 @@ def _load():
             lib.orc_e4m3_to_f64.restype = dbl
             lib.orc_num_threads.restype = i32
             attn = [i32, i32, i32, i32, p, p, i32, p, p, p, p, dbl, p, p, p, i32]
-            lib.orc_verify_attn.argtypes = attn
+            lib.orc_verify_attn.argtypes = attn + [i32]
             lib.orc_verify_attn.restype = i32
-            lib.orc_verify_attn_online.argtypes = attn + [i32]
+            lib.orc_verify_attn_online.argtypes = attn + [i32, i32]
             lib.orc_verify_attn_online.restype = i32
             lib.orc_argmax_rows.argtypes = [i64, i64, i32, p, p, i32]
             lib.orc_argmax_rows.restype = i32
@@ -129,11 +132,12 @@ def _attn_args(q, k, v, seq_lens, draft_len, kv_scale, Hq, Hkv, d, scale, units,
 
 
 def verify_attn(q, k, v, seq_lens, draft_len, *, Hq, Hkv, d, kv_scale=None, scale=None,
-                units=None, rows=None, nthreads=0, online_tile=0, out=None):
+                units=None, rows=None, nthreads=0, online_tile=0, out=None, window=0):
     """fp64 verify attention. q: bf16 bits [sum W, Hq, d]; k, v: bf16 bits or e4m3 codes
     [sum (T+W), Hkv, d]. Returns fp64 [sum W, Hq, d]. ``units`` (an iterable of
     (b, kv_head)) and ``rows`` (a bool array [sum W, Hq]) restrict the outputs computed;
-    the others are NaN."""
+    the others are NaN. ``window`` = 0 lets window row i see keys 0 .. T+i; a sliding
+    window of W >= 1 positions keeps only keys max(0, T+i-W+1) .. T+i."""
     (q, k, v, seq_lens, draft_len, kv_scale, scale, mask, rmask, fp8, B,
      rows) = _attn_args(q, k, v, seq_lens, draft_len, kv_scale, Hq, Hkv, d, scale, units,
                         rows)
@@ -142,10 +146,12 @@ def verify_attn(q, k, v, seq_lens, draft_len, *, Hq, Hkv, d, kv_scale=None, scal
     lib = _load()
     args = [B, Hq, Hkv, d, _ptr(seq_lens), _ptr(draft_len), int(fp8), _ptr(q), _ptr(k),
             _ptr(v), _ptr(kv_scale), scale, _ptr(mask), _ptr(rmask), _ptr(out), int(nthreads)]
+    if window < 0:
+        raise ValueError("window must be >= 0")
     if online_tile:
-        rc = lib.orc_verify_attn_online(*args, int(online_tile))
+        rc = lib.orc_verify_attn_online(*args, int(online_tile), int(window))
     else:
-        rc = lib.orc_verify_attn(*args)
+        rc = lib.orc_verify_attn(*args, int(window))
     if rc:
         raise ValueError("oracle rejected the arguments")
     return out

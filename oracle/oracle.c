@@ -27,6 +27,10 @@
  *   - Argmax ties go to the lowest index; -0.0 equals +0.0.
  *   - Draft signals: confidence = the largest probability of the row's softmax (the first
  *     of the page's two options); entropy = the Shannon entropy of that softmax in nats.
+ *   - Sliding window ([P3] "Sliding window: do not keep the distant past"): with a window
+ *     of W >= 1 positions the query at position p sees only the W most recent positions,
+ *     itself included, i.e. keys max(0, p - W + 1) .. p; for window row i, p = T + i.
+ *     W = 0 means no window (every earlier key).
  *
  * Layouts (packed ragged batch): q and out [sum_b W_b, Hq, d]; k and v
  * [sum_b (T_b + W_b), Hkv, d]; W_b = 1 + D_b; sequences in batch order.
@@ -84,6 +88,7 @@ typedef struct {
   int64_t* kv_off;  /* [B+1] prefix sums of T_b + W_b */
   const int32_t* seq_lens;
   const int32_t* draft_len;
+  int window;      /* 0: none; W >= 1: only the W most recent positions are visible */
   double lut[256]; /* e4m3 code -> value, from orc_e4m3_to_f64 */
 } orc_ctx;
 
@@ -97,8 +102,9 @@ static double kv_elem(const orc_ctx* c, const void* base, int which, int64_t row
 
 static int setup(orc_ctx* c, int B, int Hq, int Hkv, int d, const int32_t* seq_lens,
                  const int32_t* draft_len, int kv_fp8, const uint16_t* q, const void* k,
-                 const void* v, const float* kv_scale, double scale) {
-  if (B < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv != 0) return 1;
+                 const void* v, const float* kv_scale, double scale, int window) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv != 0 || window < 0) return 1;
+  c->window = window;
   if (kv_fp8 && !kv_scale) return 1;
   c->B = B; c->Hq = Hq; c->Hkv = Hkv; c->d = d; c->G = Hq / Hkv;
   c->kv_fp8 = kv_fp8; c->q = q; c->k = k; c->v = v; c->kv_scale = kv_scale;
@@ -117,30 +123,40 @@ static int setup(orc_ctx* c, int B, int Hq, int Hkv, int d, const int32_t* seq_l
 
 static void teardown(orc_ctx* c) { free(c->q_off); free(c->kv_off); }
 
+/* First key visible to window row i of sequence b: 0, or with a sliding window of W
+ * positions the oldest of the W positions ending at T + i. */
+static int64_t first_key(const orc_ctx* c, int b, int i) {
+  if (c->window <= 0) return 0;
+  int64_t lo = (int64_t)c->seq_lens[b] + i - c->window + 1;
+  return lo > 0 ? lo : 0;
+}
+
 /* One output row, materialised softmax ([P3] attention = softmax(q K^T) V over the
- * visible keys; the window-causal mask keeps keys 0..T+i). */
+ * visible keys; the window-causal mask keeps keys first_key .. T+i, and s[n] holds the
+ * score of key first_key + n). */
 static void row_materialised(const orc_ctx* c, int b, int h, int i, double* s,
                              double* out_row) {
   const int g = h / c->G, d = c->d;
+  const int64_t j_lo = first_key(c, b, i);
   const int64_t nkeys = (int64_t)c->seq_lens[b] + i + 1;
   const int64_t qrow = c->q_off[b] + i;
   const uint16_t* qv = c->q + (qrow * c->Hq + h) * (int64_t)d;
   double mx = -INFINITY;
-  for (int64_t j = 0; j < nkeys; ++j) {
+  for (int64_t j = j_lo; j < nkeys; ++j) {
     double acc = 0.0;
     for (int col = 0; col < d; ++col)
       acc += orc_bf16_to_f64(qv[col]) * kv_elem(c, c->k, 0, c->kv_off[b] + j, g, col);
-    s[j] = acc * c->scale;
-    if (s[j] > mx) mx = s[j];
+    s[j - j_lo] = acc * c->scale;
+    if (s[j - j_lo] > mx) mx = s[j - j_lo];
   }
   double denom = 0.0;
-  for (int64_t j = 0; j < nkeys; ++j) {
-    s[j] = exp(s[j] - mx);
-    denom += s[j];
+  for (int64_t j = j_lo; j < nkeys; ++j) {
+    s[j - j_lo] = exp(s[j - j_lo] - mx);
+    denom += s[j - j_lo];
   }
   for (int col = 0; col < d; ++col) out_row[col] = 0.0;
-  for (int64_t j = 0; j < nkeys; ++j) {
-    double p = s[j] / denom;
+  for (int64_t j = j_lo; j < nkeys; ++j) {
+    double p = s[j - j_lo] / denom;
     for (int col = 0; col < d; ++col)
       out_row[col] += p * kv_elem(c, c->v, 1, c->kv_off[b] + j, g, col);
   }
@@ -157,7 +173,7 @@ static void row_online(const orc_ctx* c, int b, int h, int i, int tile, double* 
   const uint16_t* qv = c->q + (qrow * c->Hq + h) * (int64_t)d;
   double m = -INFINITY, l = 0.0;
   for (int col = 0; col < d; ++col) out_row[col] = 0.0;
-  for (int64_t j0 = 0; j0 < nkeys; j0 += tile) {
+  for (int64_t j0 = first_key(c, b, i); j0 < nkeys; j0 += tile) {
     int64_t j1 = j0 + tile < nkeys ? j0 + tile : nkeys;
     double tmax = -INFINITY;
     for (int64_t j = j0; j < j1; ++j) {
@@ -186,9 +202,10 @@ static int run_attn(int B, int Hq, int Hkv, int d, const int32_t* seq_lens,
                     const int32_t* draft_len, int kv_fp8, const uint16_t* q, const void* k,
                     const void* v, const float* kv_scale, double scale,
                     const uint8_t* unit_mask, const uint8_t* row_mask, double* out,
-                    int nthreads, int tile) {
+                    int nthreads, int tile, int window) {
   orc_ctx c;
-  if (setup(&c, B, Hq, Hkv, d, seq_lens, draft_len, kv_fp8, q, k, v, kv_scale, scale)) {
+  if (setup(&c, B, Hq, Hkv, d, seq_lens, draft_len, kv_fp8, q, k, v, kv_scale, scale,
+            window)) {
     return 1;
   }
   int64_t max_keys = 1;
@@ -234,14 +251,15 @@ static int run_attn(int B, int Hq, int Hkv, int d, const int32_t* seq_lens,
 /* Verify attention, materialised softmax. unit_mask [B*Hkv] selects (b, kv-head) units and
  * row_mask [sum W * Hq] selects (query row, head) outputs to compute (NULL: all); outputs
  * not selected are left untouched. kv_fp8 = 0: k/v are bf16 bit patterns; 1: E4M3 codes
- * with kv_scale [2, Hkv]. Returns 0 on success. */
+ * with kv_scale [2, Hkv]. window = 0: every earlier key; W >= 1: a sliding window of the W
+ * most recent positions. Returns 0 on success. */
 int orc_verify_attn(int B, int Hq, int Hkv, int d, const int32_t* seq_lens,
                     const int32_t* draft_len, int kv_fp8, const uint16_t* q, const void* k,
                     const void* v, const float* kv_scale, double scale,
                     const uint8_t* unit_mask, const uint8_t* row_mask, double* out,
-                    int nthreads) {
+                    int nthreads, int window) {
   return run_attn(B, Hq, Hkv, d, seq_lens, draft_len, kv_fp8, q, k, v, kv_scale, scale,
-                  unit_mask, row_mask, out, nthreads, 0);
+                  unit_mask, row_mask, out, nthreads, 0, window);
 }
 
 /* The same attention through the tile-by-tile online-softmax update (tile >= 1 keys). */
@@ -249,10 +267,10 @@ int orc_verify_attn_online(int B, int Hq, int Hkv, int d, const int32_t* seq_len
                            const int32_t* draft_len, int kv_fp8, const uint16_t* q,
                            const void* k, const void* v, const float* kv_scale,
                            double scale, const uint8_t* unit_mask, const uint8_t* row_mask,
-                           double* out, int nthreads, int tile) {
+                           double* out, int nthreads, int tile, int window) {
   if (tile < 1) return 1;
   return run_attn(B, Hq, Hkv, d, seq_lens, draft_len, kv_fp8, q, k, v, kv_scale, scale,
-                  unit_mask, row_mask, out, nthreads, tile);
+                  unit_mask, row_mask, out, nthreads, tile, window);
 }
 
 /* Row-wise argmax, naive loop, first index wins ties (strict '>' keeps the earliest).

@@ -156,6 +156,114 @@ def test_equal_keys_give_mean_of_visible_values():
         assert abs(out[i, :, 1] - 1.0).max() <= 1e-12
 
 
+# ------------------------------------------------------------- sliding window
+
+def _sdpa_window_reference(w, x, W):
+    """Torch fp64 SDPA with the sliding-window mask built from the reading 'the query at
+    position p sees keys p-W+1 .. p' (p = T+i for window row i)."""
+    q = torch.from_numpy(_decode_bf16(x["q"]))
+    if x["k"].dtype == np.uint8:
+        dec = lambda c: torch.from_numpy(c).view(torch.float8_e4m3fn).to(torch.float64)
+        sk = torch.from_numpy(x["kv_scale"].astype(np.float64))
+        k = dec(x["k"]) * sk[0][None, :, None]
+        v = dec(x["v"]) * sk[1][None, :, None]
+    else:
+        k = torch.from_numpy(_decode_bf16(x["k"]))
+        v = torch.from_numpy(_decode_bf16(x["v"]))
+    outs = []
+    qo = ko = 0
+    for T, D in zip(x["seq_lens"].tolist(), x["draft_len"].tolist()):
+        R = D + 1
+        qb = q[qo:qo + R].permute(1, 0, 2)
+        kb = k[ko:ko + T + R].permute(1, 0, 2).repeat_interleave(w.G, dim=0)
+        vb = v[ko:ko + T + R].permute(1, 0, 2).repeat_interleave(w.G, dim=0)
+        j = torch.arange(T + R)[None, :]
+        p = T + torch.arange(R)[:, None]
+        mask = (j <= p) & (j > p - W)
+        o = torch.nn.functional.scaled_dot_product_attention(qb, kb, vb, attn_mask=mask)
+        outs.append(o.permute(1, 0, 2))
+        qo += R
+        ko += T + R
+    return torch.cat(outs).numpy()
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8_e4m3"])
+@pytest.mark.parametrize("W", [1, 2, 5, 16, 41, 1000])
+def test_sliding_window_matches_library_attention(kv, W):
+    w, x = _small(B=3, Hq=8, Hkv=2, d=32, T=(1, 17, 40), D=(4, 0, 9), seed=7, kv=kv)
+    ref = _sdpa_window_reference(w, x, W)
+    got = _run(w, x, window=W)
+    assert np.max(np.abs(got - ref)) <= 1e-12
+
+
+def test_sliding_window_equal_keys_give_mean_of_last_w_values():
+    """All keys identical -> uniform weights over the window: row i averages V rows
+    max(0, T+i-W+1) .. T+i. V row j carries j in column 0, so an off-by-one lower or
+    upper bound changes the mean."""
+    Hq, Hkv, d, T, D = 2, 1, 8, 10, 3
+    R = D + 1
+    q = _bits_of(np.random.default_rng(0).standard_normal((R, Hq, d)))
+    k = _bits_of(np.ones((T + R, Hkv, d)) * 0.5)
+    vals = np.zeros((T + R, Hkv, d), dtype=np.float32)
+    vals[:, 0, 0] = np.arange(T + R)
+    vals[:, 0, 1] = 1.0
+    for W in (1, 2, 3, 7, 11, 12, 13, 14, 50):
+        out = oracle.verify_attn(q, k, _bits_of(vals), [T], [D], Hq=Hq, Hkv=Hkv, d=d,
+                                 window=W)
+        for i in range(R):
+            lo = max(0, T + i - W + 1)
+            assert abs(out[i, :, 0] - (lo + T + i) / 2.0).max() <= 1e-12
+            assert abs(out[i, :, 1] - 1.0).max() <= 1e-12
+
+
+def test_window_of_one_returns_the_rows_own_value():
+    """W = 1: each query sees only its own position, so the output is that V row."""
+    w, x = _small(B=2, Hq=4, Hkv=2, d=16, T=(5, 0), D=(3, 2), seed=8)
+    got = _run(w, x, window=1)
+    v = _decode_bf16(x["v"])
+    qo = ko = 0
+    for T, D in zip(x["seq_lens"].tolist(), x["draft_len"].tolist()):
+        for i in range(D + 1):
+            for h in range(w.Hq):
+                assert np.array_equal(got[qo + i, h], v[ko + T + i, h // w.G])
+        qo += D + 1
+        ko += T + D + 1
+
+
+def test_window_covering_every_key_is_full_attention():
+    """W >= T+D+1 keeps every key: the result equals the unwindowed one exactly."""
+    w, x = _small(B=2, Hq=4, Hkv=1, d=16, T=(6, 12), D=(2, 5), seed=9)
+    full = _run(w, x)
+    for W in (18, 19, 10 ** 6):
+        assert np.array_equal(_run(w, x, window=W), full)
+    assert not np.array_equal(_run(w, x, window=17), full)  # the last row loses key 0
+
+
+@pytest.mark.parametrize("tile", [1, 4, 7])
+def test_sliding_window_online_equals_materialised(tile):
+    w, x = _small(B=3, Hq=8, Hkv=2, d=32, T=(1, 17, 40), D=(4, 0, 9), seed=10)
+    for W in (3, 9, 30):
+        a = _run(w, x, window=W)
+        b = _run(w, x, window=W, online_tile=tile)
+        assert np.max(np.abs(a - b)) <= 1e-12
+
+
+def test_sliding_window_never_reads_positions_before_it():
+    """Cache rows of positions before T-W+1 are outside every row's window: NaN there
+    leaves every output finite and unchanged."""
+    w, x = _small(B=2, Hq=4, Hkv=2, d=16, T=(30, 22), D=(3, 6), seed=11)
+    W = 8
+    ref = _run(w, x, window=W)
+    k, v = x["k"].copy(), x["v"].copy()
+    ko = 0
+    for T, D in zip(x["seq_lens"].tolist(), x["draft_len"].tolist()):
+        k[ko:ko + T - W + 1] = 0x7FC0  # bf16 NaN
+        v[ko:ko + T - W + 1] = 0x7FC0
+        ko += T + D + 1
+    got = _run(w, dict(x, k=k, v=v), window=W)
+    assert np.isfinite(got).all() and np.array_equal(got, ref)
+
+
 def test_constant_values_per_kv_head_select_the_group():
     """V constant per KV head -> every query head h returns its group's constant c[h//G]."""
     B, Hq, Hkv, d, T, D = 2, 8, 4, 16, 6, 2
