@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--side-window", type=int, default=4096,
+                    help="also time the verify call with this sliding window (0: skip)")
     return ap.parse_args()
 
 
@@ -81,11 +83,15 @@ def describe(w, T, D):
     return "%s: %s, %s KV, logits V=%d %s" % (w.name, shape, w.kv_dtype, w.V, w.logits_dtype)
 
 
-def algorithmic_bytes(w, T, D):
-    """K+V bytes actually required (each KV element read once) and Q+out bytes."""
+def algorithmic_bytes(w, T, D, window=0):
+    """K+V bytes actually required (each KV element read once) and Q+out bytes. With a
+    sliding window of W positions a sequence needs only positions max(0, T-W+1) .. T+D."""
     kv_elem = 1 if w.kv_dtype == "fp8_e4m3" else 2
     W = D.astype(np.int64) + 1
-    kv = int(2 * w.Hkv * w.d * kv_elem * np.sum(T.astype(np.int64) + W))
+    rows = T.astype(np.int64) + W
+    if window > 0:
+        rows = rows - np.maximum(T.astype(np.int64) - window + 1, 0)
+    kv = int(2 * w.Hkv * w.d * kv_elem * np.sum(rows))
     qo = int(2 * np.sum(W) * w.Hq * w.d * 2)
     return kv, qo
 
@@ -402,6 +408,54 @@ def run_ours(args):
     signals_ms = float(np.median([e[0].elapsed_time(e[1]) for e in es]))
     logits_bytes = d["logits"].numel() * d["logits"].element_size()
 
+    # sliding-window verify attention on the same inputs (not part of the step)
+    side_win = None
+    if args.side_window > 0:
+        Wn = args.side_window
+        out_w = torch.empty_like(out)
+        ws_w = sv.new_workspace(sv.verify_workspace_bytes(
+            sv.api.attn_desc(d["q"], d["k"], w.B, md, ms, sliding_window=Wn)), dev)
+
+        def win_call():
+            sv.spec_verify_attn(d["q"], d["k"], d["v"], d["T"], d["D"], max_draft_len=md,
+                                max_seq_len=ms, kv_scale=d.get("sc"), out=out_w, workspace=ws_w,
+                                sliding_window=Wn, stream=stream)
+
+        for _ in range(3):
+            win_call()
+        ew = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K3)]
+        for e in ew:  # create the events the library records into
+            e[2].record(stream)
+            e[3].record(stream)
+        # the window's K/V may fit in L2: evict them before each call by reading a buffer
+        # twice L2's size (reads leave clean lines, so no write-back lands in the call)
+        flush = torch.ones(int(2 * L2_BYTES) // 4, dtype=torch.float32, device=dev)
+        sink = torch.empty((), dtype=torch.float32, device=dev)
+        for i in range(K3):
+            torch.sum(flush, out=sink)
+            ew[i][0].record(stream)
+            sv.set_profile_events(ew[i][2], ew[i][3])
+            win_call()
+            ew[i][1].record(stream)
+        sv.set_profile_events(None, None)
+        torch.cuda.synchronize()
+        if sv.workspace_status(ws_w) != 0:
+            raise RuntimeError("device-side check failed in the sliding-window call")
+        win_ms = float(np.median([e[0].elapsed_time(e[1]) for e in ew]))
+        win_attn_ms = float(np.median([e[2].elapsed_time(e[3]) for e in ew]))
+        kvw, qow = algorithmic_bytes(w, T, D, window=Wn)
+        side_win = {"window": Wn, "verify_call_ms": round(win_ms, 5),
+                    "attn_ms": round(win_attn_ms, 5), "kv_bytes": kvw,
+                    "GB_per_s": round((kvw + qow) / (win_ms / 1e3) / 1e9, 1),
+                    "attn_GB_per_s": round((kvw + qow) / (win_attn_ms / 1e3) / 1e9, 1),
+                    "attn_frac": round((kvw + qow) / (win_attn_ms / 1e3) / 1e9 / peaks()[0], 4),
+                    "note": "spec_verify_attn with sliding_window on the step's inputs, L2 "
+                            "evicted before each call; verify_call_ms = plan + attention + "
+                            "combine, attn_ms = the attention kernel alone; bytes = K/V "
+                            "positions max(0, T-W+1)..T+D plus Q and out; not part of the "
+                            "step"}
+        del flush
+
     # end to end: pinned host inputs -> device, step, result back to pinned host memory
     e2e = None
     if not args.no_e2e:
@@ -484,6 +538,7 @@ def run_ours(args):
                               "rows": rows_l, "vocab": V_l,
                               "note": "spec_draft_signals on a logits matrix of the step's "
                                       "shape; not part of the step"},
+            "sliding_window": side_win,
             "attn_tflops": round(fl / (attn_ms / 1e3) / 1e12, 2),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
                          "unit": "GB/s", "frac": round(achieved / hbm, 4),

@@ -79,11 +79,14 @@ typedef struct {
   int32_t num_kv_heads;   /* Hkv >= 1 */
   int32_t head_dim;       /* d: 64 or 128 */
   int32_t max_draft_len;  /* upper bound on every D_b, 0 <= D_b <= max_draft_len <= 255 */
-  int32_t max_seq_len;    /* upper bound on every T_b */
+  int32_t max_seq_len;    /* upper bound on every T_b, <= 2^31 - 1025 */
   int64_t q_rows;         /* rows allocated in q and out, >= sum_b (1 + D_b) */
-  int64_t kv_rows;        /* rows allocated in k_cache and v_cache, >= sum_b (T_b+1+D_b) */
+  int64_t kv_rows;        /* rows allocated in k_cache and v_cache, >= sum_b (T_b+1+D_b),
+                             <= 2^31 - 1025 */
   int32_t kv_dtype;       /* SV_BF16, or SV_FP8_E4M3 (OCP E4M3 codes) */
   float softmax_scale;    /* scale on q.k; 0 selects 1/sqrt(head_dim) */
+  int32_t sliding_window; /* 0: every earlier key; W >= 1: sliding-window attention over
+                             the W most recent positions (see spec_verify_attn) */
 } sv_attn_desc;
 
 /* Bytes of workspace spec_verify_attn needs for `desc` on the CURRENT CUDA device
@@ -95,9 +98,15 @@ SV_API size_t spec_verify_attn_workspace_size(const sv_attn_desc* desc);
  *
  * For every sequence b, KV head g, query head h in [g*G, (g+1)*G) and window row
  * i in [0, D_b]:
- *   s_j = scale * q[q_off[b]+i, h, :] . K[kv_off[b]+j, g, :],   j = 0 .. T_b + i
+ *   s_j = scale * q[q_off[b]+i, h, :] . K[kv_off[b]+j, g, :],   j = lo .. T_b + i
  *   out[q_off[b]+i, h, :] = sum_j softmax(s)_j * V[kv_off[b]+j, g, :]
  * computed tile by tile with the online-softmax update, so no score table reaches HBM.
+ * lo = 0, or with sliding_window = W >= 1, lo = max(0, T_b + i - W + 1): the query at
+ * position T_b + i sees the W most recent positions, itself included ("GPU and LLM,
+ * chapter 5", "Sliding window: do not keep the distant past"). Key tiles wholly before
+ * a unit's window are skipped, so a call reads about min(T_b + 1 + D_b, W + D_b) cache
+ * rows per sequence and KV head. Cache rows of positions before T_b - W + 1 are never
+ * used and may hold any bits (they may be reclaimed).
  *
  *   q        bf16 [q_rows, Hq, d]
  *   k_cache  bf16 or E4M3 codes [kv_rows, Hkv, d]; v_cache likewise

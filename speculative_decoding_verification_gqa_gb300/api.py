@@ -42,7 +42,8 @@ class AttnDesc(ctypes.Structure):
                 ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("max_draft_len", ctypes.c_int32), ("max_seq_len", ctypes.c_int32),
                 ("q_rows", ctypes.c_int64), ("kv_rows", ctypes.c_int64),
-                ("kv_dtype", ctypes.c_int32), ("softmax_scale", ctypes.c_float)]
+                ("kv_dtype", ctypes.c_int32), ("softmax_scale", ctypes.c_float),
+                ("sliding_window", ctypes.c_int32)]
 
 
 _lock = threading.Lock()
@@ -111,13 +112,13 @@ def _need(t: torch.Tensor, name: str, dtypes):
 
 
 def attn_desc(q: torch.Tensor, k_cache: torch.Tensor, batch: int, max_draft_len: int,
-              max_seq_len: int, softmax_scale: float = 0.0) -> AttnDesc:
+              max_seq_len: int, softmax_scale: float = 0.0, sliding_window: int = 0) -> AttnDesc:
     fp8 = k_cache.dtype in (torch.uint8, torch.float8_e4m3fn)
     return AttnDesc(batch=batch, num_q_heads=q.shape[1], num_kv_heads=k_cache.shape[1],
                     head_dim=q.shape[2], max_draft_len=max_draft_len, max_seq_len=max_seq_len,
                     q_rows=q.shape[0], kv_rows=k_cache.shape[0],
                     kv_dtype=SV_FP8_E4M3 if fp8 else SV_BF16,
-                    softmax_scale=float(softmax_scale))
+                    softmax_scale=float(softmax_scale), sliding_window=int(sliding_window))
 
 
 def verify_workspace_bytes(desc: AttnDesc) -> int:
@@ -148,10 +149,12 @@ def new_workspace(nbytes: int, device=None) -> torch.Tensor:
 
 def spec_verify_attn(q, k_cache, v_cache, seq_lens, draft_len, *, max_draft_len: int,
                      max_seq_len: int, kv_scale=None, out=None, workspace=None,
-                     softmax_scale: float = 0.0, stream=None) -> torch.Tensor:
+                     softmax_scale: float = 0.0, sliding_window: int = 0,
+                     stream=None) -> torch.Tensor:
     """q [rows, Hq, d] bf16; k_cache/v_cache [kv_rows, Hkv, d] bf16, or uint8 /
     float8_e4m3fn E4M3 codes with kv_scale fp32 [2, Hkv]; seq_lens, draft_len int32 [B].
-    Returns out [rows, Hq, d] bf16 (only the packed rows sum_b (1 + D_b) are written)."""
+    Returns out [rows, Hq, d] bf16 (only the packed rows sum_b (1 + D_b) are written).
+    ``sliding_window`` = W >= 1 restricts window row i to keys max(0, T+i-W+1) .. T+i."""
     _need(q, "q", (torch.bfloat16,))
     _need(k_cache, "k_cache", (torch.bfloat16, torch.uint8, torch.float8_e4m3fn))
     _need(v_cache, "v_cache", (k_cache.dtype,))
@@ -161,7 +164,8 @@ def spec_verify_attn(q, k_cache, v_cache, seq_lens, draft_len, *, max_draft_len:
         _need(kv_scale, "kv_scale", (torch.float32,))
     if q.dim() != 3 or k_cache.dim() != 3 or v_cache.shape != k_cache.shape:
         raise ValueError("q must be [rows, Hq, d], k/v caches [kv_rows, Hkv, d]")
-    desc = attn_desc(q, k_cache, seq_lens.shape[0], max_draft_len, max_seq_len, softmax_scale)
+    desc = attn_desc(q, k_cache, seq_lens.shape[0], max_draft_len, max_seq_len, softmax_scale,
+                     sliding_window)
     if out is None:
         out = torch.empty_like(q)
     _need(out, "out", (torch.bfloat16,))

@@ -20,6 +20,10 @@ constexpr int SWITCH_TILES_TC_FP8 = SV_SWITCH_F8;
 constexpr int SWITCH_TILES_TC_BF16 = SV_SWITCH_BF16;
 constexpr int SWITCH_TILES_MMA = 2;
 
+// Positions and cache rows are 32-bit on the device (tile arithmetic, TMA coordinates).
+constexpr int32_t MAX_SEQ_LEN = 0x7fffffff - 1024;
+constexpr int64_t MAX_KV_ROWS = 0x7fffffff - 1024;
+
 int g_attn_kernel = 0;  // 0 automatic, 1 mma.sync, 2 tcgen05
 cudaEvent_t g_ev_start = nullptr;
 cudaEvent_t g_ev_stop = nullptr;
@@ -38,7 +42,8 @@ sv_status check_desc(const sv_attn_desc* d) {
   if (d->batch < 0 || d->num_kv_heads < 1 || d->num_q_heads < 1 ||
       d->num_q_heads % d->num_kv_heads != 0 || d->num_q_heads > 4096 ||
       d->max_draft_len < 0 || d->max_draft_len > 255 || d->max_seq_len < 0 ||
-      d->q_rows < 0 || d->kv_rows < 0)
+      d->max_seq_len > MAX_SEQ_LEN || d->q_rows < 0 || d->kv_rows < 0 ||
+      d->kv_rows > MAX_KV_ROWS || d->sliding_window < 0)
     return SV_ERR_SHAPE;
   if (d->head_dim != 64 && d->head_dim != 128) return SV_ERR_SHAPE;
   if (!(d->softmax_scale >= 0.f) || isinf(d->softmax_scale)) return SV_ERR_SHAPE;
@@ -158,6 +163,10 @@ SV_API sv_status spec_verify_attn(const sv_attn_desc* desc, const void* q, const
   p.d = desc->head_dim;
   p.max_draft = desc->max_draft_len;
   p.max_seq = desc->max_seq_len;
+  // a window covering every position of the longest sequence is no window
+  p.window = (int64_t)desc->sliding_window > (int64_t)desc->max_seq_len + desc->max_draft_len
+                 ? 0
+                 : desc->sliding_window;
   p.q_rows = desc->q_rows;
   p.kv_rows = desc->kv_rows;
   p.max_units = max_units_for(p.B, p.Hkv, G, p.max_draft);

@@ -147,17 +147,23 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_mma_kernel(const AttnParams 
   for (int64_t t = t_begin; t < t_end; ++u) {
     if (u >= p.hdr->num_units) break;  // cannot happen for a valid plan
     const int4 info = p.units[u];
-    const int b = info.x, g = info.y, mt = info.z, nt = info.w;
+    const int b = info.x, g = info.y, mt = info.z;
     const int64_t ub = p.ubeg[u];
-    const int j0 = (int)(t - ub);
-    const int j1 = (int)(min(t_end, ub + nt) - ub);
-    if (j1 <= j0) break;  // cannot happen for a valid plan
-    t = ub + j1;
+    const int nt = p.ubeg[u + 1] - (int)ub;
+    const int l0 = (int)(t - ub);
+    const int l1 = (int)(min(t_end, ub + nt) - ub);
+    if (l1 <= l0) break;  // cannot happen for a valid plan
+    t = ub + l1;
     const int T = p.seq_lens[b];
     const int D = p.draft_len[b];
+    // key tiles [j0, j1) of the sequence (tile j holds positions j*KT ..), out of the
+    // unit's tiles [kb, kb + nt)
+    const int kb = info.w / KT;
+    const int j0 = kb + l0, j1 = kb + l1;
     const int rows_total = p.G * (D + 1);
     const int rows = min(MT, rows_total - mt * MT);
     const int nkeys = T + D + 1;
+    const int kvis = first_visible_key(T, p.window);  // earlier rows left the window
     const int64_t qo = p.q_off[b], ko = p.kv_off[b];
     const float ks = FP8 ? p.kv_scale[g] : 1.f;
     const float sc = p.scale_log2 * ks;
@@ -178,7 +184,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_mma_kernel(const AttnParams 
       *reinterpret_cast<uint4*>(sQ + L::swz(r, c)) = val;
     }
 
-    // ---- K/V tile loader (cp.async, zero fill beyond the sequence's last key)
+    // ---- K/V tile loader (cp.async; zero fill beyond the sequence's last key and, under a
+    // sliding window, before its first visible key: P = 0 there must not meet NaN)
     auto load_tile = [&](int j, int stage) {
       uint8_t* dK = sKV + stage * STAGE_BYTES;
       uint8_t* dV = dK + STAGE_BYTES / 2;
@@ -188,7 +195,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_mma_kernel(const AttnParams 
         for (int idx = tid; idx < KT * CH8; idx += NTHREADS) {
           const int r = idx / CH8, c = idx % CH8;
           const int key = key0 + r;
-          const bool ok = key < nkeys;
+          const bool ok = key >= kvis && key < nkeys;
           const size_t off = ok ? (((ko + key) * p.Hkv + g) * (size_t)HD + c * 16) : 0;
           cp_async16(smem_u32(dK + r * HD + c * 16), (const uint8_t*)p.k + off, ok);
           cp_async16(smem_u32(dV + r * HD + c * 16), (const uint8_t*)p.v + off, ok);
@@ -197,7 +204,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_mma_kernel(const AttnParams 
         for (int idx = tid; idx < KT * L::CH; idx += NTHREADS) {
           const int r = idx / L::CH, c = idx % L::CH;
           const int key = key0 + r;
-          const bool ok = key < nkeys;
+          const bool ok = key >= kvis && key < nkeys;
           const size_t off = ok ? (((ko + key) * p.Hkv + g) * (size_t)HD + c * 8) * elem : 0;
           cp_async16(smem_u32(dK + L::swz(r, c)), (const uint8_t*)p.k + off, ok);
           cp_async16(smem_u32(dV + L::swz(r, c)), (const uint8_t*)p.v + off, ok);
@@ -227,6 +234,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_mma_kernel(const AttnParams 
     const int rgA = mt * MT + rA, rgB = mt * MT + rB;
     const int iA = rgA < rows_total ? rgA / p.G : D;  // padding rows see every key
     const int iB = rgB < rows_total ? rgB / p.G : D;
+    // sliding window: first visible key of each row, and the largest over the unit
+    const int loA = p.window > 0 ? max(T + iA + 1 - p.window, 0) : 0;
+    const int loB = p.window > 0 ? max(T + iB + 1 - p.window, 0) : 0;
+    const int lo_max = p.window > 0 ? max(T + D + 1 - p.window, 0) : 0;
     float o[NO][4];
 #pragma unroll
     for (int n = 0; n < NO; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
@@ -290,8 +301,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_mma_kernel(const AttnParams 
         }
       }
       // ---- scale (log2 units) and window-causal mask: key j visible to row i iff j <= T+i
+      // (and, under a sliding window, j >= T+i-window+1)
       const int key0 = j * KT;
-      const bool edge = key0 + KT > T;
+      const bool edge = key0 + KT > T || key0 < lo_max;
 #pragma unroll
       for (int n = 0; n < NS; ++n) {
 #pragma unroll
@@ -300,7 +312,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_mma_kernel(const AttnParams 
           if (edge) {
             const int key = key0 + n * 8 + 2 * (lane & 3) + (e & 1);
             const int lim = T + (e < 2 ? iA : iB);
-            if (key > lim) x = -INFINITY;
+            if (key > lim || key < (e < 2 ? loA : loB)) x = -INFINITY;
           }
           s[n][e] = x;
         }
@@ -370,7 +382,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_mma_kernel(const AttnParams 
       lB += __shfl_xor_sync(0xffffffffu, lB, 1);
       lB += __shfl_xor_sync(0xffffffffu, lB, 2);
       const int col = 2 * (lane & 3);
-      if (j0 == 0 && j1 == nt) {
+      if (j0 == kb && j1 == kb + nt) {
         // this CTA saw every key of the unit: normalise and store bf16
         const float vs = FP8 ? p.kv_scale[p.Hkv + g] : 1.f;
 #pragma unroll

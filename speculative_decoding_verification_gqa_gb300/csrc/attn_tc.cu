@@ -215,6 +215,12 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
       SV_W8(0), SV_W8(8)
       : "memory");
 }
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(
+                   taddr),
+               SV_W8(0)
+               : "memory");
+}
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
@@ -313,11 +319,16 @@ __device__ __forceinline__ void split_q_e4m3(const float* x, uint32_t& whi, uint
   wlo = l01 | (l23 << 16);
 }
 
+// One unit's share of a CTA's range: the unit's tiles [j0, j1), tile j holding cache
+// positions kbase + j*KT .. (kbase: the first position of the unit's first tile, 0 without
+// a sliding window); whole when they are all of the unit's tiles.
 struct Seg {
-  int u, b, g, mt, nt, j0, j1;
+  int u, b, g, mt, j0, j1, kbase;
+  bool whole;
 };
 
 // Next (unit, tile range) of this CTA's contiguous range of the global tile line.
+template <bool WIN>
 __device__ __forceinline__ bool seg_next(const AttnParams& p, int num_units, int64_t& t,
                                          int64_t t_end, int& u, Seg& s) {
   if (t >= t_end || u >= num_units) return false;
@@ -327,10 +338,12 @@ __device__ __forceinline__ bool seg_next(const AttnParams& p, int num_units, int
   s.b = info.x;
   s.g = info.y;
   s.mt = info.z;
-  s.nt = info.w;
+  s.kbase = WIN ? info.w : 0;
+  const int nt = p.ubeg[u + 1] - (int)ub;
   s.j0 = (int)(t - ub);
-  s.j1 = (int)(min(t_end, ub + info.w) - ub);
+  s.j1 = (int)(min(t_end, ub + nt) - ub);
   if (s.j1 <= s.j0) return false;
+  s.whole = s.j0 == 0 && s.j1 == nt;
   t = ub + s.j1;
   ++u;
   return true;
@@ -357,11 +370,14 @@ struct TcLayout {
   static constexpr int THREADS = F8 ? NTHREADS + 4 * 32 : NTHREADS;
 };
 
-template <int HD, bool F8>
+// WIN: a sliding window is in force (p.window > 0); without it the window's lower mask
+// edge, the per-unit key base and the clearing of V rows before the window compile away.
+template <int HD, bool F8, bool WIN>
 __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
     attn_tc_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv) {
   using L = TcLayout<HD, F8>;
+  const int window = WIN ? p.window : 0;
   extern __shared__ __align__(1024) uint8_t smem[];  // 128-byte swizzled tiles: 1 KiB aligned
   Bars* bars = (Bars*)(smem + L::BARS);
   volatile int* abort = &bars->abort;
@@ -424,8 +440,8 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
       Seg s;
       uint32_t it = 0;
       bool ok = true;
-      while (ok && seg_next(p, num_units, t, t_end, u, s)) {
-        const int row0 = (int)p.kv_off[s.b];
+      while (ok && seg_next<WIN>(p, num_units, t, t_end, u, s)) {
+        const int row0 = (int)p.kv_off[s.b] + s.kbase;
         for (int j = s.j0; j < s.j1; ++j, ++it) {
           const uint32_t st = it % L::NR;
           if (it >= L::NR &&
@@ -479,7 +495,7 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
       Seg s;
       uint32_t it = 0, seg_i = 0;
       bool ok = true;
-      while (ok && seg_next(p, num_units, t, t_end, u, s)) {
+      while (ok && seg_next<WIN>(p, num_units, t, t_end, u, s)) {
         if (!mbar_wait(&bars->q_full, seg_i & 1, abort, p.flags)) break;
         fence_after();
         for (int j = s.j0; j < s.j1; ++j, ++it) {
@@ -527,7 +543,7 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
       Seg s;
       uint32_t it = 0;
       bool ok = true;
-      while (ok && seg_next(p, num_units, t, t_end, u, s)) {
+      while (ok && seg_next<WIN>(p, num_units, t, t_end, u, s)) {
         bool first[2] = {true, true};  // each accumulator starts afresh in every unit
         for (int j = s.j0; j < s.j1; ++j, ++it) {
           const uint32_t st = F8 ? it % NCV : it % L::NR;
@@ -577,8 +593,9 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
     Seg s;
     uint32_t it = 0;
     bool ok = true;
-    while (ok && seg_next(p, num_units, t, t_end, u, s)) {
-      const int T = p.seq_lens[s.b];
+    while (ok && seg_next<WIN>(p, num_units, t, t_end, u, s)) {
+      // cache positions below are relative to the unit's first tile (kbase)
+      const int T = p.seq_lens[s.b] - s.kbase;
       const int D = p.draft_len[s.b];
       const int rows_total = p.G * (D + 1);
       const int rows = min(MT, rows_total - s.mt * MT);
@@ -586,6 +603,7 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
       const int rg = s.mt * MT + r;
       const bool live = r < rows;
       const int i_row = live ? rg / p.G : D;
+      const int hi_row = T + i_row;  // the row's last visible key
       const int hl = live ? rg % p.G : 0;
       const int64_t qrow = p.q_off[s.b] + i_row;
       float sc = p.scale_log2;  // score scale in log2 units
@@ -617,16 +635,19 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
         const int eb = max((int)(amax >> 7), 1);
         const int e2 = amax == 0 ? 0 : min(max(134 - eb, -120), 120);
         const float f = __int_as_float((e2 + 127) << 23);
-        uint32_t hi[16], lo[16];
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const uint32_t a = rq[2 * c], b = rq[2 * c + 1];
-          const float x[4] = {__uint_as_float(a << 16) * f, __uint_as_float(a & 0xffff0000u) * f,
-                              __uint_as_float(b << 16) * f, __uint_as_float(b & 0xffff0000u) * f};
-          split_q_e4m3(x, hi[c], lo[c]);
+        for (int hh = 0; hh < 2; ++hh) {  // 8 columns (32 elements) at a time
+          uint32_t hi[8], lo[8];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint32_t a = rq[16 * hh + 2 * c], b = rq[16 * hh + 2 * c + 1];
+            const float x[4] = {__uint_as_float(a << 16) * f, __uint_as_float(a & 0xffff0000u) * f,
+                                __uint_as_float(b << 16) * f, __uint_as_float(b & 0xffff0000u) * f};
+            split_q_e4m3(x, hi[c], lo[c]);
+          }
+          tmem_st8(tq + COL_Q + wg * 16 + 8 * hh, hi);
+          tmem_st8(tq + COL_Q + 32 + wg * 16 + 8 * hh, lo);
         }
-        tmem_st16(tq + COL_Q + wg * 16, hi);
-        tmem_st16(tq + COL_Q + 32 + wg * 16, lo);
         tmem_wait_st();
         sc = p.scale_log2 * p.kv_scale[s.g] * __int_as_float((127 - e2) << 23);
       } else if (wg < HD / 64) {
@@ -668,11 +689,20 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
         fence_before();
         mbar_arrive(&bars->s_free);  // the scores are in registers: the next S may start
         const int key0 = j * KT + wg * HK;
-        if (key0 + HK - 1 > T) {  // the window-causal mask reaches into this half tile
-          const int lim = T + i_row - key0;
+        // the window-causal mask (key <= T + i) or the sliding window's lower edge
+        // (key >= T + i - window + 1) reaches into this half tile for this row
+        const int lo_row = hi_row + 1 - window;  // (used only under a sliding window)
+        if (key0 + HK - 1 > hi_row) {
+          const int lim = hi_row - key0;
 #pragma unroll
           for (int c = 0; c < HK; ++c)
             if (c > lim) sv[c] = -INFINITY;
+        }
+        if (WIN && key0 < lo_row) {
+          const int low = lo_row - key0;
+#pragma unroll
+          for (int c = 0; c < HK; ++c)
+            if (c < low) sv[c] = -INFINITY;
         }
         float m8[8];
 #pragma unroll
@@ -730,19 +760,29 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
           tmem_wait_st();
         }
         bool zeroed = false;
-        if (!F8 && key0 + HK > nkeys) {
-          // last tile of the sequence: clear this half's V rows past its end so that P = 0
-          // never meets non-finite data (they may hold the next sequence or unwritten memory)
+        // under a sliding window, keys before T - window + 1 left every row's window
+        const int kvis = WIN ? T + 1 - window : -1;
+        if (!F8 && (key0 + HK > nkeys || key0 < kvis)) {
+          // clear this half's V rows past the sequence's end (they may hold the next
+          // sequence or unwritten memory) and, under a sliding window, before the first
+          // visible key (left the window: any bits), so that P = 0 never meets non-finite
+          // data
           const uint32_t st = it % L::NR;
           if (!(good = wwait(&bars->v_full[st], (it / L::NR) & 1))) continue;
-          const int first = max(nkeys - key0, 0) + wg * HK;  // first row to clear
           uint8_t* vt = smem + st * L::STAGE + L::TILE;
-          const int chunks = (wg * HK + HK - first) * 8;  // 16-byte chunks per column block
-          for (int q = r; q < chunks * L::NBLK; q += NSOFT / 2) {
-            const int blk = q / chunks, rem = q % chunks;
-            *reinterpret_cast<uint4*>(vt + blk * L::BLK + (first + rem / 8) * 128 + (rem % 8) * 16) =
-                make_uint4(0, 0, 0, 0);
-          }
+          auto clear_rows = [&](int first, int end) {  // tile rows [first, end)
+            const int chunks = (end - first) * 8;  // 16-byte chunks per column block
+            for (int q = r; q < chunks * L::NBLK; q += NSOFT / 2) {
+              const int blk = q / chunks, rem = q % chunks;
+              *reinterpret_cast<uint4*>(vt + blk * L::BLK + (first + rem / 8) * 128 + (rem % 8) * 16) =
+                  make_uint4(0, 0, 0, 0);
+            }
+          };
+          const int h0 = wg * HK, h1 = h0 + HK;  // this half's rows of the tile
+          const int lo_end = min(max(kvis - key0, 0), HK) + h0;
+          const int hi_first = max(min(nkeys - key0, HK), 0) + h0;
+          if (lo_end > h0) clear_rows(h0, lo_end);
+          if (hi_first < h1) clear_rows(max(hi_first, lo_end), h1);
           zeroed = true;
         }
         if (zeroed) fence_proxy_async();
@@ -768,7 +808,7 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
       const float a0 = m0 == -INFINITY ? 0.f : ex2(m0 - m);
       const float a1 = m1 == -INFINITY ? 0.f : ex2(m1 - m);
       const float l = a0 * bars->xl[0][r] + a1 * bars->xl[1][r];
-      const bool whole = s.j0 == 0 && s.j1 == s.nt;
+      const bool whole = s.whole;
       const float inv = whole ? vs / l : 1.f;
       auto merged = [&](uint32_t o0, uint32_t o1) {  // an accumulator without tiles is skipped
         return (a0 != 0.f ? a0 * __uint_as_float(o0) : 0.f) +
@@ -818,8 +858,9 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
       // (two 64-column swizzled blocks) out. Thread ct owns 16-byte chunk column c = ct & 7
       // of rows rw + 16k, rw = (ct >> 3) ^ (c >> 2): each group of eight lanes takes the
       // eight chunk columns from two rows of opposite parity, so its 16-byte loads and
-      // stores fall in eight different bank groups. Rows past the sequence's last key are
-      // written as zeros (P is zero there, and 0 x NaN would not be).
+      // stores fall in eight different bank groups. Rows past the sequence's last key, and
+      // rows before its first visible key under a sliding window, are written as zeros (P
+      // is zero there, and 0 x NaN would not be).
       const int ct = (warp - CONV_WARP0) * 32 + lane;
       const int c = ct & 7;
       const int rw = (ct >> 3) ^ (c >> 2);
@@ -833,8 +874,11 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
       Seg s;
       uint32_t it = 0;
       bool ok = true;
-      while (ok && seg_next(p, num_units, t, t_end, u, s)) {
-        const int nkeys = p.seq_lens[s.b] + p.draft_len[s.b] + 1;
+      while (ok && seg_next<WIN>(p, num_units, t, t_end, u, s)) {
+        // cache positions relative to the unit's first tile
+        const int T = p.seq_lens[s.b] - s.kbase;
+        const int nkeys = T + p.draft_len[s.b] + 1;
+        const int kvis = WIN ? T + 1 - window : -1;
         for (int j = s.j0; j < s.j1; ++j, ++it) {
           const uint32_t rs = it % L::NR, cs = it % NCV;
           if (!mbar_wait(&bars->v_full[rs], (it / L::NR) & 1, abort, p.flags) ||
@@ -851,6 +895,7 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
             w[k] = *reinterpret_cast<const uint4*>(rsrc + k * RSTEP);
           mbar_arrive(&bars->kv_empty[rs]);  // the raw V tile is read
           const int lim = nkeys - j * KT;    // rows >= lim lie past the sequence's end
+          const int low = kvis - j * KT;     // rows < low left the sliding window
 #pragma unroll
           for (int k = 0; k < KT / 16; ++k) {
             uint32_t h[8];
@@ -858,7 +903,7 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
             e4m3x4_to_f16x4(w[k].y, h[2], h[3]);
             e4m3x4_to_f16x4(w[k].z, h[4], h[5]);
             e4m3x4_to_f16x4(w[k].w, h[6], h[7]);
-            if (rw + 16 * k >= lim) {
+            if (rw + 16 * k >= lim || rw + 16 * k < low) {
 #pragma unroll
               for (int e = 0; e < 8; ++e) h[e] = 0u;
             }
@@ -924,18 +969,23 @@ bool make_kv_map(CUtensorMap* map, const void* base, int64_t kv_rows, int hkv, i
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int HD, bool F8>
+template <int HD, bool F8, bool WIN>
 cudaError_t launch_hd(const AttnParams& p, cudaStream_t s) {
   using L = TcLayout<HD, F8>;
   CUtensorMap mk, mv;
   if (!make_kv_map(&mk, p.k, p.kv_rows, p.Hkv, HD, F8) ||
       !make_kv_map(&mv, p.v, p.kv_rows, p.Hkv, HD, F8))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<HD, F8>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::SMEM);
+  auto kernel = attn_tc_kernel<HD, F8, WIN>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::SMEM);
   if (e != cudaSuccess) return e;
-  return launch_pdl(attn_tc_kernel<HD, F8>, dim3(p.n_ctas), dim3(L::THREADS), L::SMEM, s, p, mk,
-                    mv);
+  return launch_pdl(kernel, dim3(p.n_ctas), dim3(L::THREADS), L::SMEM, s, p, mk, mv);
+}
+
+template <int HD, bool F8>
+cudaError_t launch_hd(const AttnParams& p, cudaStream_t s) {
+  return p.window > 0 ? launch_hd<HD, F8, true>(p, s) : launch_hd<HD, F8, false>(p, s);
 }
 
 }  // namespace

@@ -4,7 +4,11 @@
 //   unit  = (sequence b, KV head g, row tile mt): up to 128 of the G*(1+D_b) query rows
 //           that share KV head g ("GQA", "GPU and LLM, chapter 5"; guideline 2 of the
 //           co-design summary: G*(1+D) rows per KV head, M = 128 fills a tile).
-//   tile  = KT consecutive cache positions of one unit's key range 0 .. T_b + D_b.
+//   tile  = KT consecutive cache positions of one unit's key range. Tiles are aligned to
+//           multiples of KT from the sequence's first position; a unit's tiles run from
+//           the one holding its first visible key (0, or under a sliding window of W
+//           positions the oldest key of its first window row, T_b + i_lo - W + 1) to the
+//           one holding T_b + D_b.
 //   Units are laid end to end on one global tile line; persistent CTAs process contiguous
 //   ranges of it. Starting a unit costs a CTA about `switch_tiles` tiles' worth of time
 //   (epilogue of the previous unit, loading and splitting Q, refilling the pipeline), so
@@ -85,8 +89,10 @@ struct AttnParams {
   PlanHdr* hdr;
   int64_t* q_off;             // [B+1]
   int64_t* kv_off;            // [B+1]
-  int4* units;                // [U] (b, kv head, row tile, tiles in the unit)
-  int32_t* ubeg;              // [U+1] first global tile of each unit
+  int4* units;                // [U] (b, kv head, row tile, first cache position of the
+                              // unit's first tile)
+  int32_t* ubeg;              // [U+1] first global tile of each unit (unit u has
+                              // ubeg[u+1] - ubeg[u] tiles)
   int2* cta_tab;              // [n_ctas+1] (first real tile, its unit) of each CTA's range
   float* part_o;              // [slots, MT, d]
   float2* part_ml;            // [slots, MT] (m in log2 units, l)
@@ -96,8 +102,25 @@ struct AttnParams {
   int max_units;
   int n_ctas;
   int switch_tiles;           // virtual tiles charged for starting a unit
+  int window;                 // sliding window in positions (0: every earlier key); set to 0
+                              // when it covers max_seq + max_draft + 1 positions
   float scale_log2;           // softmax_scale * log2(e)
 };
+
+// First key tile of row tile mt of a sequence with T cached keys. Window row i sees keys
+// max(0, T + i - window + 1) .. T + i ("GPU and LLM, chapter 5", "Sliding window": only the
+// W most recent positions); the tile's smallest window row is mt * MT / G.
+// (32-bit arithmetic: T <= 2^31 - 1025 and the window row mt * MT / G <= 255.)
+__host__ __device__ inline int unit_first_tile(int T, int mt, int G, int window, int kt) {
+  if (window <= 0) return 0;
+  const int lo = T + mt * MT / G + 1 - window;
+  return lo > 0 ? lo / kt : 0;
+}
+// First cache position whose K/V rows a sequence's window rows can see: positions before
+// it may hold any bits (their V rows are zeroed on the chip before they meet P = 0).
+__host__ __device__ inline int first_visible_key(int T, int window) {
+  return window > 0 && T - window + 1 > 0 ? T - window + 1 : 0;
+}
 
 // Virtual-line position of real tile t of unit u (u * switch_tiles virtual tiles precede
 // unit u's start, and switch_tiles more its first real tile).

@@ -59,19 +59,21 @@ __global__ void __launch_bounds__(1024) plan_kernel(AttnParams p, int kt) {
   __syncthreads();
   for (int base = 0; base < p.B; base += blockDim.x) {
     const int b = base + tid;
-    int64_t w = 0, kvn = 0, nunits = 0, ntiles = 0;
-    int nmt = 0, nt = 0;
+    int64_t w = 0, kvn = 0, nunits = 0, ntiles = 0, per_g = 0;
+    int nmt = 0, nt = 0, T = 0;
     if (b < p.B) {
-      const int T = p.seq_lens[b], D = p.draft_len[b];
+      T = p.seq_lens[b];
+      const int D = p.draft_len[b];
       if (T < 0 || T > p.max_seq || D < 0 || D > p.max_draft) {
         bad = 1;
       } else {
         w = 1 + D;
         kvn = T + w;
         nmt = (int)((p.G * w + MT - 1) / MT);
-        nt = (int)((kvn + kt - 1) / kt);
+        nt = (int)((kvn + kt - 1) / kt);  // tiles up to the one holding T + D
+        for (int mt = 0; mt < nmt; ++mt) per_g += nt - unit_first_tile(T, mt, p.G, p.window, kt);
         nunits = (int64_t)p.Hkv * nmt;
-        ntiles = nunits * nt;
+        ntiles = (int64_t)p.Hkv * per_g;
       }
     }
     int64_t tq, tkv, tu, tt;
@@ -83,16 +85,20 @@ __global__ void __launch_bounds__(1024) plan_kernel(AttnParams p, int kt) {
       p.q_off[b] = carry[0] + eq;
       p.kv_off[b] = carry[1] + ekv;
       const int64_t ub = carry[2] + eu, tb = carry[3] + et;
-      for (int g = 0; g < p.Hkv; ++g)
+      for (int g = 0; g < p.Hkv; ++g) {
+        int64_t t0 = tb + (int64_t)g * per_g;
         for (int mt = 0; mt < nmt; ++mt) {
           const int64_t u = ub + (int64_t)g * nmt + mt;
+          const int kb = unit_first_tile(T, mt, p.G, p.window, kt);
+          const int ntu = nt - kb;
           if (u < p.max_units) {
-            const int32_t ub_u = (int32_t)(tb + ((int64_t)g * nmt + mt) * nt);
-            p.units[u] = make_int4(b, g, mt, nt);
-            p.ubeg[u] = ub_u;
-            if (u < PLAN_SMEM_UNITS) s_ubeg[u] = ub_u;
+            p.units[u] = make_int4(b, g, mt, kb * kt);
+            p.ubeg[u] = (int32_t)t0;
+            if (u < PLAN_SMEM_UNITS) s_ubeg[u] = (int32_t)t0;
           }
+          t0 += ntu;
         }
+      }
     }
     __syncthreads();
     if (tid == 0) {

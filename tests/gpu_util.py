@@ -36,12 +36,12 @@ def dev_attn(x, device="cuda"):
     return q, k, v, sc, T, D
 
 
-def gpu_attn(x, *, max_draft=None, max_seq=None, workspace=None, out=None):
+def gpu_attn(x, *, max_draft=None, max_seq=None, workspace=None, out=None, window=0):
     q, k, v, sc, T, D = dev_attn(x)
     md = int(x["draft_len"].max()) if max_draft is None else max_draft
     ms = int(x["seq_lens"].max()) if max_seq is None else max_seq
     o = sv.spec_verify_attn(q, k, v, T, D, max_draft_len=md, max_seq_len=ms, kv_scale=sc,
-                            workspace=workspace, out=out)
+                            workspace=workspace, out=out, sliding_window=window)
     torch.cuda.synchronize()
     return o.view(torch.int16).cpu().numpy().view(np.uint16)
 
@@ -79,9 +79,10 @@ def assert_close(gpu_bits, ref):
     return ma, mr
 
 
-def oracle_attn(w, x, units=None):
+def oracle_attn(w, x, units=None, window=0):
     return oracle.verify_attn(x["q"], x["k"], x["v"], x["seq_lens"], x["draft_len"], Hq=w.Hq,
-                              Hkv=w.Hkv, d=w.d, kv_scale=x["kv_scale"], units=units)
+                              Hkv=w.Hkv, d=w.d, kv_scale=x["kv_scale"], units=units,
+                              window=window)
 
 
 def dev_accept(a, device="cuda"):

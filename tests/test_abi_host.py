@@ -70,6 +70,9 @@ def _attn(lib, desc, **ptrs):
     (dict(kv_dtype=7), 3),
     (dict(softmax_scale=float("nan")), 2),
     (dict(softmax_scale=-1.0), 2),
+    (dict(sliding_window=-1), 2),
+    (dict(max_seq_len=2 ** 31 - 1024), 2),
+    (dict(kv_rows=2 ** 31), 2),
 ])
 def test_attn_rejects_bad_descriptors(lib, bad, status):
     assert _attn(lib, _desc(**bad)) == status
@@ -106,3 +109,23 @@ def test_no_device_means_no_workspace_size(lib):
         pytest.skip("a GPU is present")
     assert lib.spec_verify_attn_workspace_size(ctypes.byref(_desc())) == 0
     assert lib.spec_accept_workspace_size(2, 3, 100) == 0
+
+
+def test_descriptor_layout_matches_the_header(tmp_path):
+    """The ctypes mirror of sv_attn_desc has the C struct's size and field offsets (a C
+    program compiled against include/specverify.h prints them)."""
+    import subprocess
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    fields = [f for f, _ in api.AttnDesc._fields_]
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "specverify.h"\n'
+                   'int main(void) {\n  printf("%zu", sizeof(sv_attn_desc));\n' +
+                   "".join('  printf(" %%zu", offsetof(sv_attn_desc, %s));\n' % f for f in fields) +
+                   "  return 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-I", os.path.join(root, "include"), "-o", str(exe), str(src)],
+                   check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], check=True, capture_output=True,
+                                          text=True).stdout.split()]
+    assert got[0] == ctypes.sizeof(api.AttnDesc)
+    assert got[1:] == [getattr(api.AttnDesc, f).offset for f in fields]
