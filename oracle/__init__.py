@@ -17,6 +17,10 @@ Functions and the passages they follow (page title, then section):
 * ``verify_attn(window=W)`` -- sliding-window verify attention: "GPU and LLM, chapter 5",
   "Sliding window: do not keep the distant past" (each position sees the W most recent
   positions, itself included).
+* ``verify_attn_paged`` -- the same attention over a paged cache: "GPU and LLM, chapter
+  5", "PagedAttention (2): manage with fixed-size pages" (fixed-size blocks of positions
+  anywhere in memory, found through a per-sequence block table). The rows are gathered
+  back into the packed layout, then ``verify_attn`` runs on them.
 * ``argmax_rows`` -- naive first-index argmax (target's greedy choice per window row).
 * ``accept`` -- first-mismatch acceptance: "Co-Designing AI Models Using Speculative
   Decoding" summary, "basic structure" (AL in [1, 1+D]); "GPU and LLM, chapter 5",
@@ -155,6 +159,38 @@ def verify_attn(q, k, v, seq_lens, draft_len, *, Hq, Hkv, d, kv_scale=None, scal
     if rc:
         raise ValueError("oracle rejected the arguments")
     return out
+
+
+def verify_attn_paged(q, k_pages, v_pages, block_table, seq_lens, draft_len, *, Hq, Hkv, d,
+                      kv_scale=None, window=0, **kw):
+    """fp64 verify attention over a paged cache. k_pages, v_pages: [num_blocks, block_size,
+    Hkv, d] (bf16 bits or e4m3 codes); block_table int32 [B, max_blocks]: position j of
+    sequence b is row j % block_size of block block_table[b, j // block_size]. Entries
+    that are negative or out of range are never followed: the positions they cover
+    become NaN rows, which a correct attention never reads (positions outside every
+    window row's sliding window)."""
+    k_pages = np.asarray(k_pages)
+    v_pages = np.asarray(v_pages)
+    nb, bs = k_pages.shape[0], k_pages.shape[1]
+    table = np.asarray(block_table, dtype=np.int64)
+    T = np.asarray(seq_lens, dtype=np.int64)
+    R = T + np.asarray(draft_len, dtype=np.int64) + 1
+    kflat = k_pages.reshape(nb * bs, Hkv, d)
+    vflat = v_pages.reshape(nb * bs, Hkv, d)
+    nan = 0x7F if k_pages.dtype == np.uint8 else 0x7FC0
+    k = np.full((int(R.sum()), Hkv, d), nan, dtype=k_pages.dtype)
+    v = np.full((int(R.sum()), Hkv, d), nan, dtype=v_pages.dtype)
+    row0 = 0
+    for b in range(len(T)):
+        j = np.arange(int(R[b]))
+        blk = table[b, j // bs]
+        ok = (blk >= 0) & (blk < nb)
+        src = blk[ok] * bs + j[ok] % bs
+        k[row0 + j[ok]] = kflat[src]
+        v[row0 + j[ok]] = vflat[src]
+        row0 += int(R[b])
+    return verify_attn(q, k, v, seq_lens, draft_len, Hq=Hq, Hkv=Hkv, d=d, kv_scale=kv_scale,
+                       window=window, **kw)
 
 
 def verify_attn_online(q, k, v, seq_lens, draft_len, *, tile, **kw):

@@ -17,6 +17,10 @@ Recipes (one per workload; see ``CONFIGS``):
   ids. An id that merely ties the maximum therefore counts as a mismatch.
 * Ragged batches: T_b uniform on [1024, 65536], D_b uniform on {1, 2, 4, 8} and a match
   probability p_b uniform on (0.4, 0.9) per sequence; sequences are packed back to back.
+* Paged caches (``paged_layout``): the packed K/V rows of each sequence cut into blocks of
+  ``block_size`` positions, the blocks placed at seeded random physical slots of a pool
+  that also holds spare blocks; unused rows (the tail of each sequence's last block, spare
+  blocks) hold a fill pattern (NaN by default) and unused block-table entries are -1.
 
 Streams: every array is drawn from its own ``SeedSequence(seed, spawn_key=(tag, chunk))``
 so that results do not depend on the number of threads used to draw them.
@@ -237,3 +241,54 @@ def packed_offsets(seq_lens: Sequence[int], draft_len: Sequence[int]):
     W = np.asarray(draft_len, dtype=np.int64) + 1
     KV = np.asarray(seq_lens, dtype=np.int64) + W
     return (np.concatenate([[0], np.cumsum(W)]), np.concatenate([[0], np.cumsum(KV)]))
+
+
+_TAG_PAGES = 41
+
+
+def paged_layout(x, block_size: int, seed: int, spare_blocks: int = 3, fill: str = "nan",
+                 reclaim_before_window: int = 0):
+    """Moves the packed K/V of ``attn_inputs`` into a paged pool.
+
+    Returns dict(k_pages, v_pages, block_table, block_size): k_pages, v_pages
+    [num_blocks, block_size, Hkv, d] (the packed arrays' dtype); block_table int32
+    [B, max_blocks] where logical block n of sequence b (positions n*block_size ..) lives
+    in physical block block_table[b, n]; entries past a sequence's last block are -1.
+    With reclaim_before_window = W > 0, blocks holding only positions before T_b - W + 1
+    (outside every window row's sliding window) are given back to the pool: their entries
+    are -1 and their slots hold the fill pattern."""
+    if block_size < 1:
+        raise ValueError("block_size must be >= 1")
+    k, v = x["k"], x["v"]
+    T = np.asarray(x["seq_lens"], dtype=np.int64)
+    R = T + np.asarray(x["draft_len"], dtype=np.int64) + 1  # cache rows per sequence
+    nblk = (R + block_size - 1) // block_size
+    used = int(nblk.sum())
+    num_blocks = used + int(spare_blocks)
+    perm = _ss(seed, _TAG_PAGES).permutation(num_blocks)
+    Hkv, d = k.shape[1], k.shape[2]
+    if k.dtype == np.uint8:
+        pat = {"nan": 0x7F, "zero": 0}[fill]
+    else:
+        pat = {"nan": 0x7FC0, "zero": 0}[fill]
+    kp = np.full((num_blocks, block_size, Hkv, d), pat, dtype=k.dtype)
+    vp = np.full((num_blocks, block_size, Hkv, d), pat, dtype=v.dtype)
+    table = np.full((len(T), max(int(nblk.max()) if len(T) else 1, 1)), -1, dtype=np.int32)
+    row0 = 0
+    nxt = 0
+    for b in range(len(T)):
+        first_kept = 0
+        if reclaim_before_window > 0:
+            first_kept = max(int(T[b]) - reclaim_before_window + 1, 0) // block_size
+        for n in range(int(nblk[b])):
+            phys = int(perm[nxt])
+            nxt += 1
+            if n < first_kept:
+                continue  # reclaimed: the slot keeps the fill pattern
+            lo = n * block_size
+            hi = min(lo + block_size, int(R[b]))
+            kp[phys, :hi - lo] = k[row0 + lo:row0 + hi]
+            vp[phys, :hi - lo] = v[row0 + lo:row0 + hi]
+            table[b, n] = phys
+        row0 += int(R[b])
+    return dict(k_pages=kp, v_pages=vp, block_table=table, block_size=block_size)

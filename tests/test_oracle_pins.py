@@ -264,6 +264,59 @@ def test_sliding_window_never_reads_positions_before_it():
     assert np.isfinite(got).all() and np.array_equal(got, ref)
 
 
+# ------------------------------------------------------------------- paged cache
+
+def _paged_oracle(w, x, pg, **kw):
+    return oracle.verify_attn_paged(x["q"], pg["k_pages"], pg["v_pages"], pg["block_table"],
+                                    x["seq_lens"], x["draft_len"], Hq=w.Hq, Hkv=w.Hkv, d=w.d,
+                                    kv_scale=x["kv_scale"], **kw)
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8_e4m3"])
+@pytest.mark.parametrize("bs", [1, 4, 16, 64])
+def test_paged_equals_packed_for_any_block_placement(kv, bs):
+    """Blocks at random physical slots among NaN-filled spares give exactly the packed
+    result: every position is found through the table and nothing else is read."""
+    w, x = _small(B=3, Hq=8, Hkv=2, d=32, T=(1, 17, 40), D=(4, 0, 9), seed=12, kv=kv)
+    pg = synth.paged_layout(x, bs, seed=5, spare_blocks=4)
+    assert np.array_equal(_paged_oracle(w, x, pg), _run(w, x))
+
+
+def test_paged_brute_force_walk_of_the_block_table():
+    """One output row recomputed in numpy by walking the block table position by position
+    (softmax over the fetched keys, weighted sum of the fetched values)."""
+    w, x = _small(B=2, Hq=4, Hkv=2, d=16, T=(23, 9), D=(3, 2), seed=13)
+    bs = 8
+    pg = synth.paged_layout(x, bs, seed=6, spare_blocks=2)
+    got = _paged_oracle(w, x, pg)
+    kp = _decode_bf16(pg["k_pages"])
+    vp = _decode_bf16(pg["v_pages"])
+    q = _decode_bf16(x["q"])
+    qo = 0
+    for b, (T, D) in enumerate(zip(x["seq_lens"].tolist(), x["draft_len"].tolist())):
+        for i in range(D + 1):
+            for h in range(w.Hq):
+                g = h // w.G
+                keys = [kp[pg["block_table"][b, j // bs], j % bs, g] for j in range(T + i + 1)]
+                vals = [vp[pg["block_table"][b, j // bs], j % bs, g] for j in range(T + i + 1)]
+                s_ = np.array([q[qo + i, h] @ kk for kk in keys]) / math.sqrt(w.d)
+                p_ = np.exp(s_ - s_.max())
+                ref = (p_ / p_.sum()) @ np.array(vals)
+                assert np.max(np.abs(got[qo + i, h] - ref)) <= 1e-12
+        qo += D + 1
+
+
+@pytest.mark.parametrize("bs", [4, 16])
+def test_paged_with_window_and_reclaimed_blocks(bs):
+    """Blocks wholly before every row's sliding window handed back to the pool (table
+    entries -1, slots NaN): the windowed result equals the packed windowed one."""
+    w, x = _small(B=3, Hq=8, Hkv=2, d=32, T=(70, 17, 45), D=(4, 0, 9), seed=14)
+    W = 20
+    pg = synth.paged_layout(x, bs, seed=7, spare_blocks=2, reclaim_before_window=W)
+    assert (pg["block_table"][0, :2] == -1).all()  # positions 0..7 of sequence 0 are gone
+    assert np.array_equal(_paged_oracle(w, x, pg, window=W), _run(w, x, window=W))
+
+
 def test_constant_values_per_kv_head_select_the_group():
     """V constant per KV head -> every query head h returns its group's constant c[h//G]."""
     B, Hq, Hkv, d, T, D = 2, 8, 4, 16, 6, 2
