@@ -51,6 +51,9 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--side-window", type=int, default=4096,
                     help="also time the verify call with this sliding window (0: skip)")
+    ap.add_argument("--side-block", type=int, default=16,
+                    help="also time the verify call over a paged copy of the cache with "
+                         "blocks of this many positions (0: skip)")
     return ap.parse_args()
 
 
@@ -432,7 +435,7 @@ def run_ours(args):
         flush = torch.ones(int(2 * L2_BYTES) // 4, dtype=torch.float32, device=dev)
         sink = torch.empty((), dtype=torch.float32, device=dev)
         for i in range(K3):
-            torch.sum(flush, out=sink)
+            sink.copy_(flush.sum())
             ew[i][0].record(stream)
             sv.set_profile_events(ew[i][2], ew[i][3])
             win_call()
@@ -455,6 +458,52 @@ def run_ours(args):
                             "positions max(0, T-W+1)..T+D plus Q and out; not part of the "
                             "step"}
         del flush
+
+    # verify attention over a paged copy of the same cache (not part of the step)
+    side_paged = None
+    if args.side_block > 0:
+        pg = synth.paged_layout(x, args.side_block, seed + 5, spare_blocks=256)
+        to_dev = (lambda a: torch.from_numpy(a).to(dev)) if kvdt == torch.uint8 else \
+            (lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev))
+        kp, vp = to_dev(pg["k_pages"]), to_dev(pg["v_pages"])
+        bt = torch.from_numpy(pg["block_table"]).to(dev)
+        del pg
+        out_p = torch.empty_like(out)
+        ws_p = sv.new_workspace(sv.verify_workspace_bytes(desc), dev)
+
+        def paged_call():
+            sv.spec_verify_attn_paged(d["q"], kp, vp, bt, d["T"], d["D"], max_draft_len=md,
+                                      max_seq_len=ms, kv_scale=d.get("sc"), out=out_p,
+                                      workspace=ws_p, stream=stream)
+
+        for _ in range(3):
+            paged_call()
+        ep = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K3)]
+        for e in ep:
+            e[2].record(stream)
+            e[3].record(stream)
+        for i in range(K3):
+            ep[i][0].record(stream)
+            sv.set_profile_events(ep[i][2], ep[i][3])
+            paged_call()
+            ep[i][1].record(stream)
+        sv.set_profile_events(None, None)
+        torch.cuda.synchronize()
+        if sv.workspace_status(ws_p) != 0:
+            raise RuntimeError("device-side check failed in the paged call")
+        same = bool(torch.equal(out_p, out))
+        p_ms = float(np.median([e[0].elapsed_time(e[1]) for e in ep]))
+        p_attn = float(np.median([e[2].elapsed_time(e[3]) for e in ep]))
+        side_paged = {"block_size": args.side_block, "verify_call_ms": round(p_ms, 5),
+                      "attn_ms": round(p_attn, 5),
+                      "attn_GB_per_s": round((kv_bytes + qo_bytes) / (p_attn / 1e3) / 1e9, 1),
+                      "attn_frac": round((kv_bytes + qo_bytes) / (p_attn / 1e3) / 1e9
+                                         / peaks()[0], 4),
+                      "same_bits_as_packed": same,
+                      "note": "spec_verify_attn_paged on the step's K/V cut into blocks at "
+                              "seeded random slots of a pool with 256 spare blocks; inputs "
+                              "larger than L2; not part of the step"}
+        del kp, vp
 
     # end to end: pinned host inputs -> device, step, result back to pinned host memory
     e2e = None
@@ -539,6 +588,7 @@ def run_ours(args):
                               "note": "spec_draft_signals on a logits matrix of the step's "
                                       "shape; not part of the step"},
             "sliding_window": side_win,
+            "paged": side_paged,
             "attn_tflops": round(fl / (attn_ms / 1e3) / 1e12, 2),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
                          "unit": "GB/s", "frac": round(achieved / hbm, 4),

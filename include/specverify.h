@@ -123,6 +123,39 @@ SV_API sv_status spec_verify_attn(const sv_attn_desc* desc, const void* q, const
                            const int32_t* draft_len, const float* kv_scale, void* out,
                            void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * spec_verify_attn_paged -- spec_verify_attn over a paged KV cache ("GPU and LLM, chapter 5",
+ * "PagedAttention (2): manage with fixed-size pages": the cache is cut into blocks of a
+ * fixed number of positions placed anywhere in a pool, and a per-sequence block table
+ * records where each block is).
+ *
+ * The result is that of spec_verify_attn (sliding_window included) with the cache row of
+ * position j of sequence b (j = 0 .. T_b + D_b) read from
+ *   k_pages[block_table[b * max_blocks_per_seq + j / block_size], j % block_size, g, :]
+ * (v_pages likewise). The caller has written the window's K/V (positions T_b .. T_b + D_b)
+ * into the pool before the call, as for the packed cache.
+ *
+ *   k_pages, v_pages  bf16 or E4M3 codes [num_blocks, block_size, Hkv, d], 16-byte aligned
+ *   num_blocks        blocks in the pool, >= 1; num_blocks * block_size <= 2^31 - 1025
+ *   block_size        positions per block: a power of two in [8, 65536]
+ *   block_table       int32 [B, max_blocks_per_seq], row-major, 4-byte aligned; entries
+ *                     for logical blocks 0 .. (T_b + D_b) / block_size must name blocks of
+ *                     the pool, except, under a sliding window, blocks holding only
+ *                     positions before T_b - W + 1, which are never read (they may be
+ *                     reclaimed and their entries hold anything); later entries are
+ *                     never read
+ * desc->kv_rows is ignored. The workspace is that of spec_verify_attn for the same desc.
+ * A sequence needing more than max_blocks_per_seq blocks, or a table entry outside
+ * [0, num_blocks) that must be read, is reported by sv_workspace_status (SV_ERR_DEVICE_
+ * SHAPE); such an entry reads as zeros and no memory outside the pool is touched.
+ */
+SV_API sv_status spec_verify_attn_paged(const sv_attn_desc* desc, const void* q,
+                                 const void* k_pages, const void* v_pages, int64_t num_blocks,
+                                 int32_t block_size, const int32_t* block_table,
+                                 int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                 const int32_t* draft_len, const float* kv_scale, void* out,
+                                 void* workspace, size_t workspace_bytes, void* stream);
+
 /* Bytes of workspace spec_accept needs on the current CUDA device. 0 if invalid. */
 SV_API size_t spec_accept_workspace_size(int32_t batch, int32_t max_draft_len, int32_t vocab);
 

@@ -6,6 +6,7 @@ PyTorch supplies device memory and the current stream. Entry points mirror the C
 include/specverify.h:
 
 * ``spec_verify_attn`` -- GQA verify attention over cached prefix + draft window.
+* ``spec_verify_attn_paged`` -- the same over a paged cache (block pool + block table).
 * ``spec_accept`` -- greedy acceptance (argmax per window row, first mismatch).
 """
 from __future__ import annotations
@@ -25,7 +26,8 @@ SV_BF16, SV_FP8_E4M3, SV_FP32 = 0, 1, 2
 STATUS = {0: "SV_OK", 1: "SV_ERR_NULL", 2: "SV_ERR_SHAPE", 3: "SV_ERR_DTYPE",
           4: "SV_ERR_ALIGN", 5: "SV_ERR_WORKSPACE", 6: "SV_ERR_CUDA", 7: "SV_ERR_TIMEOUT",
           8: "SV_ERR_DEVICE_SHAPE"}
-EXPORTS = ("spec_verify_attn_workspace_size", "spec_verify_attn", "spec_accept_workspace_size",
+EXPORTS = ("spec_verify_attn_workspace_size", "spec_verify_attn", "spec_verify_attn_paged",
+           "spec_accept_workspace_size",
            "spec_accept", "spec_draft_signals_workspace_size", "spec_draft_signals",
            "sv_workspace_status", "sv_status_string", "sv_set_attn_kernel",
            "sv_set_profile_events", "sv_version")
@@ -66,6 +68,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.spec_verify_attn.argtypes = [ctypes.POINTER(AttnDesc), vp, vp, vp, vp, vp, vp, vp,
                                          vp, sz, vp]
         lib.spec_verify_attn.restype = ctypes.c_int
+        i64 = ctypes.c_int64
+        lib.spec_verify_attn_paged.argtypes = [ctypes.POINTER(AttnDesc), vp, vp, vp, i64, i32,
+                                               vp, i32, vp, vp, vp, vp, vp, sz, vp]
+        lib.spec_verify_attn_paged.restype = ctypes.c_int
         lib.spec_accept_workspace_size.argtypes = [i32, i32, i32]
         lib.spec_accept_workspace_size.restype = sz
         lib.spec_accept.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, sz, vp]
@@ -178,6 +184,44 @@ def spec_verify_attn(q, k_cache, v_cache, seq_lens, draft_len, *, max_draft_len:
         _ptr(draft_len), _ptr(kv_scale), _ptr(out), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, "spec_verify_attn")
+    return out
+
+
+def spec_verify_attn_paged(q, k_pages, v_pages, block_table, seq_lens, draft_len, *,
+                           max_draft_len: int, max_seq_len: int, kv_scale=None, out=None,
+                           workspace=None, softmax_scale: float = 0.0, sliding_window: int = 0,
+                           stream=None) -> torch.Tensor:
+    """spec_verify_attn over a paged cache. k_pages/v_pages [num_blocks, block_size, Hkv, d]
+    (bf16, or uint8 / float8_e4m3fn codes with kv_scale); block_table int32 [B, max_blocks]:
+    position j of sequence b is row j % block_size of block block_table[b, j // block_size]."""
+    _need(q, "q", (torch.bfloat16,))
+    _need(k_pages, "k_pages", (torch.bfloat16, torch.uint8, torch.float8_e4m3fn))
+    _need(v_pages, "v_pages", (k_pages.dtype,))
+    _need(block_table, "block_table", (torch.int32,))
+    _need(seq_lens, "seq_lens", (torch.int32,))
+    _need(draft_len, "draft_len", (torch.int32,))
+    if kv_scale is not None:
+        _need(kv_scale, "kv_scale", (torch.float32,))
+    if q.dim() != 3 or k_pages.dim() != 4 or v_pages.shape != k_pages.shape:
+        raise ValueError("q must be [rows, Hq, d], k/v pages [num_blocks, block_size, Hkv, d]")
+    if block_table.dim() != 2 or block_table.shape[0] != seq_lens.shape[0]:
+        raise ValueError("block_table must be [B, max_blocks]")
+    nb, bs = k_pages.shape[0], k_pages.shape[1]
+    flat = k_pages.view(nb * bs, k_pages.shape[2], k_pages.shape[3])
+    desc = attn_desc(q, flat, seq_lens.shape[0], max_draft_len, max_seq_len, softmax_scale,
+                     sliding_window)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", (torch.bfloat16,))
+    if out.shape != q.shape:
+        raise ValueError("out must have q's shape")
+    if workspace is None:
+        workspace = new_workspace(verify_workspace_bytes(desc), q.device)
+    st = load_library().spec_verify_attn_paged(
+        ctypes.byref(desc), _ptr(q), _ptr(k_pages), _ptr(v_pages), nb, bs, _ptr(block_table),
+        block_table.shape[1], _ptr(seq_lens), _ptr(draft_len), _ptr(kv_scale), _ptr(out),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "spec_verify_attn_paged")
     return out
 
 

@@ -110,15 +110,29 @@ SV_API size_t spec_verify_attn_workspace_size(const sv_attn_desc* desc) {
   return layout_for(desc, sms).total;
 }
 
-SV_API sv_status spec_verify_attn(const sv_attn_desc* desc, const void* q, const void* k_cache,
-                                  const void* v_cache, const int32_t* seq_lens,
-                                  const int32_t* draft_len, const float* kv_scale, void* out,
-                                  void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// A paged cache (block_size 0: the packed layout).
+struct PagedArgs {
+  const int32_t* table;
+  int32_t stride;
+  int32_t block_size;
+  int64_t num_blocks;
+};
+
+sv_status verify_impl(const sv_attn_desc* desc, const void* q, const void* k_cache,
+                      const void* v_cache, const PagedArgs& pg, const int32_t* seq_lens,
+                      const int32_t* draft_len, const float* kv_scale, void* out,
+                      void* workspace, size_t workspace_bytes, void* stream) {
   sv_status st = check_desc(desc);
   if (st != SV_OK) return st;
   if (desc->batch == 0) return SV_OK;
   if (!q || !k_cache || !v_cache || !seq_lens || !draft_len || !out || !workspace)
     return SV_ERR_NULL;
+  if (pg.block_size > 0 && !pg.table) return SV_ERR_NULL;
+  if (pg.block_size > 0 && !aligned(pg.table, 4)) return SV_ERR_ALIGN;
   const bool fp8 = desc->kv_dtype == SV_FP8_E4M3;
   if (fp8 && !kv_scale) return SV_ERR_NULL;
   if (!fp8 && kv_scale) return SV_ERR_SHAPE;
@@ -168,7 +182,13 @@ SV_API sv_status spec_verify_attn(const sv_attn_desc* desc, const void* q, const
                  ? 0
                  : desc->sliding_window;
   p.q_rows = desc->q_rows;
-  p.kv_rows = desc->kv_rows;
+  p.kv_rows = pg.block_size > 0 ? pg.num_blocks * pg.block_size : desc->kv_rows;
+  p.block_table = pg.table;
+  p.bt_stride = pg.stride;
+  p.block_size = pg.block_size;
+  p.bs_log2 = 0;
+  while (pg.block_size > 0 && (1 << p.bs_log2) < pg.block_size) ++p.bs_log2;
+  p.num_blocks = pg.num_blocks;
   p.max_units = max_units_for(p.B, p.Hkv, G, p.max_draft);
   p.n_ctas = (int)(max_tiles < sms ? (max_tiles > 0 ? max_tiles : 1) : sms);
   // measured cost of starting a unit inside a CTA's range, in tiles of that kernel
@@ -185,6 +205,34 @@ SV_API sv_status spec_verify_attn(const sv_attn_desc* desc, const void* q, const
   if (g_ev_stop && cudaEventRecord(g_ev_stop, s) != cudaSuccess) return SV_ERR_CUDA;
   if (launch_combine(p, s) != cudaSuccess) return SV_ERR_CUDA;
   return SV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+SV_API sv_status spec_verify_attn(const sv_attn_desc* desc, const void* q, const void* k_cache,
+                                  const void* v_cache, const int32_t* seq_lens,
+                                  const int32_t* draft_len, const float* kv_scale, void* out,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
+  const PagedArgs packed = {nullptr, 0, 0, 0};
+  return verify_impl(desc, q, k_cache, v_cache, packed, seq_lens, draft_len, kv_scale, out,
+                     workspace, workspace_bytes, stream);
+}
+
+SV_API sv_status spec_verify_attn_paged(const sv_attn_desc* desc, const void* q,
+                                        const void* k_pages, const void* v_pages,
+                                        int64_t num_blocks, int32_t block_size,
+                                        const int32_t* block_table, int32_t max_blocks_per_seq,
+                                        const int32_t* seq_lens, const int32_t* draft_len,
+                                        const float* kv_scale, void* out, void* workspace,
+                                        size_t workspace_bytes, void* stream) {
+  if (block_size < 8 || block_size > (1 << 16) || (block_size & (block_size - 1)) != 0 ||
+      num_blocks < 1 || num_blocks > MAX_KV_ROWS / block_size || max_blocks_per_seq < 1)
+    return SV_ERR_SHAPE;
+  const PagedArgs pg = {block_table, max_blocks_per_seq, block_size, num_blocks};
+  return verify_impl(desc, q, k_pages, v_pages, pg, seq_lens, draft_len, kv_scale, out,
+                     workspace, workspace_bytes, stream);
 }
 
 SV_API size_t spec_accept_workspace_size(int32_t batch, int32_t max_draft_len, int32_t vocab) {

@@ -185,7 +185,22 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_mma_kernel(const AttnParams 
     }
 
     // ---- K/V tile loader (cp.async; zero fill beyond the sequence's last key and, under a
-    // sliding window, before its first visible key: P = 0 there must not meet NaN)
+    // sliding window, before its first visible key: P = 0 there must not meet NaN). The
+    // cache row of position `key`: packed, ko + key; paged, row key % block_size of the
+    // block the block table names (an entry outside the pool sets the shape flag and
+    // reads as zeros).
+    const int32_t* tab = p.block_table + (size_t)b * p.bt_stride;
+    auto cache_row = [&](int key, bool& ok) -> int64_t {
+      if (p.block_size == 0) return ko + key;
+      if (!ok) return 0;
+      const int blk = __ldg(tab + (key >> p.bs_log2));
+      if (blk < 0 || blk >= p.num_blocks) {
+        atomicOr(p.flags, FLAG_ATTN_SHAPE);
+        ok = false;
+        return 0;
+      }
+      return (int64_t)blk * p.block_size + (key & (p.block_size - 1));
+    };
     auto load_tile = [&](int j, int stage) {
       uint8_t* dK = sKV + stage * STAGE_BYTES;
       uint8_t* dV = dK + STAGE_BYTES / 2;
@@ -195,8 +210,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_mma_kernel(const AttnParams 
         for (int idx = tid; idx < KT * CH8; idx += NTHREADS) {
           const int r = idx / CH8, c = idx % CH8;
           const int key = key0 + r;
-          const bool ok = key >= kvis && key < nkeys;
-          const size_t off = ok ? (((ko + key) * p.Hkv + g) * (size_t)HD + c * 16) : 0;
+          bool ok = key >= kvis && key < nkeys;
+          const int64_t row = cache_row(key, ok);
+          const size_t off = ok ? ((row * p.Hkv + g) * (size_t)HD + c * 16) : 0;
           cp_async16(smem_u32(dK + r * HD + c * 16), (const uint8_t*)p.k + off, ok);
           cp_async16(smem_u32(dV + r * HD + c * 16), (const uint8_t*)p.v + off, ok);
         }
@@ -204,8 +220,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) attn_mma_kernel(const AttnParams 
         for (int idx = tid; idx < KT * L::CH; idx += NTHREADS) {
           const int r = idx / L::CH, c = idx % L::CH;
           const int key = key0 + r;
-          const bool ok = key >= kvis && key < nkeys;
-          const size_t off = ok ? (((ko + key) * p.Hkv + g) * (size_t)HD + c * 8) * elem : 0;
+          bool ok = key >= kvis && key < nkeys;
+          const int64_t row = cache_row(key, ok);
+          const size_t off = ok ? ((row * p.Hkv + g) * (size_t)HD + c * 8) * elem : 0;
           cp_async16(smem_u32(dK + L::swz(r, c)), (const uint8_t*)p.k + off, ok);
           cp_async16(smem_u32(dV + L::swz(r, c)), (const uint8_t*)p.v + off, ok);
         }

@@ -440,8 +440,53 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
       Seg s;
       uint32_t it = 0;
       bool ok = true;
+      // Packed cache: one box of KT rows per tile. Paged cache: KT / box boxes of box =
+      // min(block_size, KT) rows, each from the physical block the block table names; a
+      // box holding no position a row of the unit can see (past the sequence's end, or
+      // wholly before its sliding window) is not looked up and loads from a negative
+      // row, which fills it with zeros.
+      const int box = p.block_size > 0 ? min(p.block_size, KT) : KT;
+      auto load_k = [&](uint32_t st, int n, int g, int grow) {
+        const uint32_t roff = (uint32_t)(n * box * 128);
+        if constexpr (F8) {
+          tma_load_3d(saddr(smem + L::RK + st * L::RAW) + roff, &tmk, &bars->k_full[st], 0, g,
+                      grow);
+        } else {
+#pragma unroll
+          for (int c = 0; c < L::NBLK; ++c)
+            tma_load_3d(saddr(smem + st * L::STAGE) + c * L::BLK + roff, &tmk, &bars->k_full[st],
+                        c * 64, g, grow);
+        }
+      };
+      auto load_v = [&](uint32_t st, int n, int g, int grow) {
+        const uint32_t roff = (uint32_t)(n * box * 128);
+        if constexpr (F8) {
+          tma_load_3d(saddr(smem + L::RV + st * L::RAW) + roff, &tmv, &bars->v_full[st], 0, g,
+                      grow);
+        } else {
+#pragma unroll
+          for (int c = 0; c < L::NBLK; ++c)
+            tma_load_3d(saddr(smem + st * L::STAGE) + L::TILE + c * L::BLK + roff, &tmv,
+                        &bars->v_full[st], c * 64, g, grow);
+        }
+      };
       while (ok && seg_next<WIN>(p, num_units, t, t_end, u, s)) {
         const int row0 = (int)p.kv_off[s.b] + s.kbase;
+        const int T = p.seq_lens[s.b];
+        const int nkeys = T + p.draft_len[s.b] + 1;
+        const int kvis = first_visible_key(T, window);
+        const int32_t* tab = p.block_table + (size_t)s.b * p.bt_stride;
+        // first cache row of box n of tile j (paged)
+        auto paged_row = [&](int j, int n) -> int {
+          const int pos = s.kbase + j * KT + n * box;
+          if (pos >= nkeys || pos + box <= kvis) return -box;
+          const int blk = __ldg(tab + (pos >> p.bs_log2));
+          if (blk < 0 || blk >= p.num_blocks) {  // a table entry outside the pool
+            atomicOr(p.flags, FLAG_ATTN_SHAPE);
+            return -box;
+          }
+          return blk * p.block_size + (pos & (p.block_size - 1));
+        };
         for (int j = s.j0; j < s.j1; ++j, ++it) {
           const uint32_t st = it % L::NR;
           if (it >= L::NR &&
@@ -449,25 +494,18 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
             ok = false;
             break;
           }
-          if constexpr (F8) {
-            // one box per tensor: 128 keys x 128 one-byte codes
-            mbar_expect_tx(&bars->k_full[st], L::RAW);
-            tma_load_3d(saddr(smem + L::RK + st * L::RAW), &tmk, &bars->k_full[st], 0, s.g,
-                        row0 + j * KT);
-            mbar_expect_tx(&bars->v_full[st], L::RAW);
-            tma_load_3d(saddr(smem + L::RV + st * L::RAW), &tmv, &bars->v_full[st], 0, s.g,
-                        row0 + j * KT);
+          // the boxes of a tile add up to one full tile per tensor
+          mbar_expect_tx(&bars->k_full[st], F8 ? L::RAW : L::TILE);
+          if (p.block_size == 0) {
+            load_k(st, 0, s.g, row0 + j * KT);
           } else {
-            const uint32_t kdst = saddr(smem + st * L::STAGE);
-            const uint32_t vdst = kdst + L::TILE;
-            mbar_expect_tx(&bars->k_full[st], L::TILE);
-#pragma unroll
-            for (int c = 0; c < L::NBLK; ++c)
-              tma_load_3d(kdst + c * L::BLK, &tmk, &bars->k_full[st], c * 64, s.g, row0 + j * KT);
-            mbar_expect_tx(&bars->v_full[st], L::TILE);
-#pragma unroll
-            for (int c = 0; c < L::NBLK; ++c)
-              tma_load_3d(vdst + c * L::BLK, &tmv, &bars->v_full[st], c * 64, s.g, row0 + j * KT);
+            for (int n = 0; n < KT / box; ++n) load_k(st, n, s.g, paged_row(j, n));
+          }
+          mbar_expect_tx(&bars->v_full[st], F8 ? L::RAW : L::TILE);
+          if (p.block_size == 0) {
+            load_v(st, 0, s.g, row0 + j * KT);
+          } else {
+            for (int n = 0; n < KT / box; ++n) load_v(st, n, s.g, paged_row(j, n));
           }
         }
       }
@@ -952,13 +990,17 @@ EncodeTiledFn encode_fn() {
 
 // [kv_rows, Hkv, HD] -> boxes of 128 bytes x 1 head x KT rows, 128-byte swizzle: 64 bf16
 // columns, or 128 one-byte E4M3 codes.
-bool make_kv_map(CUtensorMap* map, const void* base, int64_t kv_rows, int hkv, int hd, bool fp8) {
+// Rows of `box_rows` cache positions of one KV head (box_rows: KT, or a paged cache's
+// block size when that is smaller; a multiple of 8 keeps every box on a whole 1 KiB
+// swizzle period in shared memory).
+bool make_kv_map(CUtensorMap* map, const void* base, int64_t kv_rows, int hkv, int hd, bool fp8,
+                 int box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t es = fp8 ? 1 : 2;
   const cuuint64_t dims[3] = {(cuuint64_t)hd, (cuuint64_t)hkv, (cuuint64_t)kv_rows};
   const cuuint64_t strides[2] = {(cuuint64_t)hd * es, (cuuint64_t)hkv * hd * es};
-  const cuuint32_t box[3] = {(cuuint32_t)(128 / es), 1, KT};
+  const cuuint32_t box[3] = {(cuuint32_t)(128 / es), 1, (cuuint32_t)box_rows};
   const cuuint32_t estr[3] = {1, 1, 1};
   return fn(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
             const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -973,8 +1015,9 @@ template <int HD, bool F8, bool WIN>
 cudaError_t launch_hd(const AttnParams& p, cudaStream_t s) {
   using L = TcLayout<HD, F8>;
   CUtensorMap mk, mv;
-  if (!make_kv_map(&mk, p.k, p.kv_rows, p.Hkv, HD, F8) ||
-      !make_kv_map(&mv, p.v, p.kv_rows, p.Hkv, HD, F8))
+  const int box = p.block_size > 0 ? min(p.block_size, KT) : KT;
+  if (!make_kv_map(&mk, p.k, p.kv_rows, p.Hkv, HD, F8, box) ||
+      !make_kv_map(&mv, p.v, p.kv_rows, p.Hkv, HD, F8, box))
     return cudaErrorInvalidValue;
   auto kernel = attn_tc_kernel<HD, F8, WIN>;
   cudaError_t e =

@@ -79,8 +79,8 @@ inline AttnWs attn_ws_layout(int B, int Hkv, int G, int d, int max_draft, int n_
 
 struct AttnParams {
   const void* q;
-  const void* k;
-  const void* v;
+  const void* k;               // packed cache [kv_rows, Hkv, d], or the block pool
+  const void* v;               // [num_blocks * block_size, Hkv, d] of a paged cache
   void* out;
   const float* kv_scale;      // [2, Hkv] or nullptr
   const int32_t* seq_lens;    // [B]
@@ -102,6 +102,13 @@ struct AttnParams {
   int max_units;
   int n_ctas;
   int switch_tiles;           // virtual tiles charged for starting a unit
+  const int32_t* block_table;  // paged cache: [B, bt_stride] physical block of each logical
+                               // block (position j of sequence b: row j % block_size of
+                               // block block_table[b * bt_stride + j / block_size])
+  int bt_stride;
+  int block_size;             // positions per block, a power of two; 0: packed cache
+  int bs_log2;
+  int64_t num_blocks;
   int window;                 // sliding window in positions (0: every earlier key); set to 0
                               // when it covers max_seq + max_draft + 1 positions
   float scale_log2;           // softmax_scale * log2(e)

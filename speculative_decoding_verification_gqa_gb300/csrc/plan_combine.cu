@@ -64,8 +64,10 @@ __global__ void __launch_bounds__(1024) plan_kernel(AttnParams p, int kt) {
     if (b < p.B) {
       T = p.seq_lens[b];
       const int D = p.draft_len[b];
-      if (T < 0 || T > p.max_seq || D < 0 || D > p.max_draft) {
-        bad = 1;
+      if (T < 0 || T > p.max_seq || D < 0 || D > p.max_draft ||
+          (p.block_size > 0 &&
+           (((int64_t)T + D + p.block_size) >> p.bs_log2) > p.bt_stride)) {
+        bad = 1;  // a length out of range, or more blocks than the block table's row holds
       } else {
         w = 1 + D;
         kvn = T + w;
@@ -110,7 +112,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(AttnParams p, int kt) {
     __syncthreads();
   }
   if (tid == 0) {
-    const bool err = bad || carry[0] > p.q_rows || carry[1] > p.kv_rows ||
+    const bool err = bad || carry[0] > p.q_rows || (p.block_size == 0 && carry[1] > p.kv_rows) ||
                      carry[2] > p.max_units || carry[3] >= (int64_t)0x7fffffff;
     p.q_off[p.B] = carry[0];
     p.kv_off[p.B] = carry[1];

@@ -129,3 +129,31 @@ def test_descriptor_layout_matches_the_header(tmp_path):
                                           text=True).stdout.split()]
     assert got[0] == ctypes.sizeof(api.AttnDesc)
     assert got[1:] == [getattr(api.AttnDesc, f).offset for f in fields]
+
+
+def _paged(lib, desc, nb=64, bs=16, table=FAKE, mb=8, **ptrs):
+    p = dict(q=FAKE, k=FAKE, v=FAKE, T=FAKE, D=FAKE, sc=None, out=FAKE, ws=FAKE)
+    p.update(ptrs)
+    return lib.spec_verify_attn_paged(ctypes.byref(desc), p["q"], p["k"], p["v"], nb, bs, table,
+                                      mb, p["T"], p["D"], p["sc"], p["out"], p["ws"], 1 << 30,
+                                      None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(bs=12), 2),            # not a power of two
+    (dict(bs=4), 2),             # below 8 positions
+    (dict(bs=1 << 17), 2),
+    (dict(nb=0), 2),
+    (dict(nb=2 ** 31 // 16), 2),  # pool rows beyond 32-bit coordinates
+    (dict(mb=0), 2),
+    (dict(table=None), 1),
+    (dict(table=ctypes.c_void_p(0x10002)), 4),
+])
+def test_paged_rejects_bad_arguments(lib, kw, status):
+    assert _paged(lib, _desc(), **kw) == status
+
+
+def test_paged_checks_the_descriptor_too(lib):
+    assert _paged(lib, _desc(head_dim=96)) == 2
+    assert _paged(lib, _desc(), q=None) == 1
+    assert _paged(lib, _desc(batch=0), q=None) == 0
