@@ -432,92 +432,93 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
+    // Packed cache: lane 0 loads one box of KT rows per tile and tensor. Paged cache: a
+    // tile is KT / box boxes of box = min(block_size, KT) rows, each from the physical
+    // block the block table names, spread over the lanes (lane n looks up and loads box
+    // n, so the lookups overlap each other and the wait for the stage); a box holding no
+    // position a row of the unit can see (past the sequence's end, or wholly before its
+    // sliding window) is not looked up and loads from a negative row, which fills it with
+    // zeros. Lane 0 waits for the stage and arms its barriers.
     if (lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmk) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmv) : "memory");
-      int64_t t = t_begin;
-      int u = u_first;
-      Seg s;
-      uint32_t it = 0;
-      bool ok = true;
-      // Packed cache: one box of KT rows per tile. Paged cache: KT / box boxes of box =
-      // min(block_size, KT) rows, each from the physical block the block table names; a
-      // box holding no position a row of the unit can see (past the sequence's end, or
-      // wholly before its sliding window) is not looked up and loads from a negative
-      // row, which fills it with zeros.
-      const int box = p.block_size > 0 ? min(p.block_size, KT) : KT;
-      auto load_k = [&](uint32_t st, int n, int g, int grow) {
-        const uint32_t roff = (uint32_t)(n * box * 128);
-        if constexpr (F8) {
-          tma_load_3d(saddr(smem + L::RK + st * L::RAW) + roff, &tmk, &bars->k_full[st], 0, g,
-                      grow);
-        } else {
+    }
+    int64_t t = t_begin;
+    int u = u_first;
+    Seg s;
+    uint32_t it = 0;
+    bool ok = true;
+    const int box = p.block_size > 0 ? min(p.block_size, KT) : KT;
+    const int nbox = KT / box;  // boxes per tile, one per lane
+    auto load_k = [&](uint32_t st, int n, int g, int grow) {
+      const uint32_t roff = (uint32_t)(n * box * 128);
+      if constexpr (F8) {
+        tma_load_3d(saddr(smem + L::RK + st * L::RAW) + roff, &tmk, &bars->k_full[st], 0, g,
+                    grow);
+      } else {
 #pragma unroll
-          for (int c = 0; c < L::NBLK; ++c)
-            tma_load_3d(saddr(smem + st * L::STAGE) + c * L::BLK + roff, &tmk, &bars->k_full[st],
-                        c * 64, g, grow);
-        }
-      };
-      auto load_v = [&](uint32_t st, int n, int g, int grow) {
-        const uint32_t roff = (uint32_t)(n * box * 128);
-        if constexpr (F8) {
-          tma_load_3d(saddr(smem + L::RV + st * L::RAW) + roff, &tmv, &bars->v_full[st], 0, g,
-                      grow);
-        } else {
-#pragma unroll
-          for (int c = 0; c < L::NBLK; ++c)
-            tma_load_3d(saddr(smem + st * L::STAGE) + L::TILE + c * L::BLK + roff, &tmv,
-                        &bars->v_full[st], c * 64, g, grow);
-        }
-      };
-      while (ok && seg_next<WIN>(p, num_units, t, t_end, u, s)) {
-        const int row0 = (int)p.kv_off[s.b] + s.kbase;
-        const int T = p.seq_lens[s.b];
-        const int nkeys = T + p.draft_len[s.b] + 1;
-        const int kvis = first_visible_key(T, window);
-        const int32_t* tab = p.block_table + (size_t)s.b * p.bt_stride;
-        // first cache row of box n of tile j (paged)
-        auto paged_row = [&](int j, int n) -> int {
-          const int pos = s.kbase + j * KT + n * box;
-          if (pos >= nkeys || pos + box <= kvis) return -box;
-          const int blk = __ldg(tab + (pos >> p.bs_log2));
-          if (blk < 0 || blk >= p.num_blocks) {  // a table entry outside the pool
-            atomicOr(p.flags, FLAG_ATTN_SHAPE);
-            return -box;
-          }
-          return blk * p.block_size + (pos & (p.block_size - 1));
-        };
-        for (int j = s.j0; j < s.j1; ++j, ++it) {
-          const uint32_t st = it % L::NR;
-          if (it >= L::NR &&
-              !mbar_wait(&bars->kv_empty[st], ((it / L::NR) - 1) & 1, abort, p.flags)) {
-            ok = false;
-            break;
-          }
-          // the boxes of a tile add up to one full tile per tensor
-          mbar_expect_tx(&bars->k_full[st], F8 ? L::RAW : L::TILE);
-          if (p.block_size == 0) {
-            load_k(st, 0, s.g, row0 + j * KT);
-          } else {
-            for (int n = 0; n < KT / box; ++n) load_k(st, n, s.g, paged_row(j, n));
-          }
-          mbar_expect_tx(&bars->v_full[st], F8 ? L::RAW : L::TILE);
-          if (p.block_size == 0) {
-            load_v(st, 0, s.g, row0 + j * KT);
-          } else {
-            for (int n = 0; n < KT / box; ++n) load_v(st, n, s.g, paged_row(j, n));
-          }
-        }
+        for (int c = 0; c < L::NBLK; ++c)
+          tma_load_3d(saddr(smem + st * L::STAGE) + c * L::BLK + roff, &tmk, &bars->k_full[st],
+                      c * 64, g, grow);
       }
-      if (!ok || *abort) {
-        // leave no copy in flight: wait (bounded) for the last fill of every stage
-        for (uint32_t st = 0; st < L::NR && st < it; ++st) {
-          const uint32_t fills = (it - 1 - st) / L::NR + 1;
-          const uint32_t par = (fills - 1) & 1;
-          const long long t0 = clock64();
-          while (!(mbar_try(&bars->k_full[st], par) && mbar_try(&bars->v_full[st], par)) &&
-                 clock64() - t0 < TIMEOUT_CYCLES) {
-          }
+    };
+    auto load_v = [&](uint32_t st, int n, int g, int grow) {
+      const uint32_t roff = (uint32_t)(n * box * 128);
+      if constexpr (F8) {
+        tma_load_3d(saddr(smem + L::RV + st * L::RAW) + roff, &tmv, &bars->v_full[st], 0, g,
+                    grow);
+      } else {
+#pragma unroll
+        for (int c = 0; c < L::NBLK; ++c)
+          tma_load_3d(saddr(smem + st * L::STAGE) + L::TILE + c * L::BLK + roff, &tmv,
+                      &bars->v_full[st], c * 64, g, grow);
+      }
+    };
+    while (ok && seg_next<WIN>(p, num_units, t, t_end, u, s)) {
+      const int row0 = (int)p.kv_off[s.b] + s.kbase;
+      const int T = p.seq_lens[s.b];
+      const int nkeys = T + p.draft_len[s.b] + 1;
+      const int kvis = first_visible_key(T, window);
+      const int32_t* tab = p.block_table + (size_t)s.b * p.bt_stride;
+      // first cache row of box n of tile j (paged)
+      auto paged_row = [&](int j, int n) -> int {
+        const int pos = s.kbase + j * KT + n * box;
+        if (pos >= nkeys || pos + box <= kvis) return -box;
+        const int blk = __ldg(tab + (pos >> p.bs_log2));
+        if (blk < 0 || blk >= p.num_blocks) {  // a table entry outside the pool
+          atomicOr(p.flags, FLAG_ATTN_SHAPE);
+          return -box;
+        }
+        return blk * p.block_size + (pos & (p.block_size - 1));
+      };
+      for (int j = s.j0; j < s.j1; ++j, ++it) {
+        const uint32_t st = it % L::NR;
+        const bool mine = p.block_size == 0 ? lane == 0 : lane < nbox;
+        const int grow = p.block_size == 0 ? row0 + j * KT : (mine ? paged_row(j, lane) : 0);
+        bool w = true;
+        if (it >= L::NR && lane == 0)
+          w = mbar_wait(&bars->kv_empty[st], ((it / L::NR) - 1) & 1, abort, p.flags);
+        if (!__shfl_sync(0xffffffffu, w, 0)) {
+          ok = false;
+          break;
+        }
+        // the boxes of a tile add up to one full tile per tensor
+        if (lane == 0) mbar_expect_tx(&bars->k_full[st], F8 ? L::RAW : L::TILE);
+        __syncwarp();
+        if (mine) load_k(st, lane, s.g, grow);
+        if (lane == 0) mbar_expect_tx(&bars->v_full[st], F8 ? L::RAW : L::TILE);
+        __syncwarp();
+        if (mine) load_v(st, lane, s.g, grow);
+      }
+    }
+    if (lane == 0 && (!ok || *abort)) {
+      // leave no copy in flight: wait (bounded) for the last fill of every stage
+      for (uint32_t st = 0; st < L::NR && st < it; ++st) {
+        const uint32_t fills = (it - 1 - st) / L::NR + 1;
+        const uint32_t par = (fills - 1) & 1;
+        const long long t0 = clock64();
+        while (!(mbar_try(&bars->k_full[st], par) && mbar_try(&bars->v_full[st], par)) &&
+               clock64() - t0 < TIMEOUT_CYCLES) {
         }
       }
     }
