@@ -19,6 +19,19 @@ namespace {
 constexpr int SWITCH_TILES_TC_FP8 = SV_SWITCH_F8;
 constexpr int SWITCH_TILES_TC_BF16 = SV_SWITCH_BF16;
 constexpr int SWITCH_TILES_MMA = 2;
+// Per-tile compute floor of each kernel, in CTAs streaming at once (a 128-key tile's
+// compute time x HBM bandwidth / the tile's bytes: bf16 about 0.9 us x 6.8 TB/s / 64 KB,
+// E4M3 about 0.89 us x 6.8 TB/s / 32 KB). The mma.sync kernel is never run one CTA per
+// unit.
+#ifndef SV_TILE_FLOOR_BF16
+#define SV_TILE_FLOOR_BF16 93
+#endif
+#ifndef SV_TILE_FLOOR_F8
+#define SV_TILE_FLOOR_F8 185
+#endif
+#ifndef SV_UNIT_CTAS
+#define SV_UNIT_CTAS -1
+#endif
 
 // Positions and cache rows are 32-bit on the device (tile arithmetic, TMA coordinates).
 constexpr int32_t MAX_SEQ_LEN = 0x7fffffff - 1024;
@@ -193,6 +206,8 @@ sv_status verify_impl(const sv_attn_desc* desc, const void* q, const void* k_cac
   p.n_ctas = (int)(max_tiles < sms ? (max_tiles > 0 ? max_tiles : 1) : sms);
   // measured cost of starting a unit inside a CTA's range, in tiles of that kernel
   p.switch_tiles = which == 2 ? (fp8 ? SWITCH_TILES_TC_FP8 : SWITCH_TILES_TC_BF16) : SWITCH_TILES_MMA;
+  p.tile_floor = which == 2 ? (fp8 ? SV_TILE_FLOOR_F8 : SV_TILE_FLOOR_BF16) : 0;
+  p.unit_ctas_mode = SV_UNIT_CTAS;
   const float scale = desc->softmax_scale > 0.f ? desc->softmax_scale
                                                 : 1.f / sqrtf((float)desc->head_dim);
   p.scale_log2 = scale * 1.4426950408889634f;

@@ -20,6 +20,12 @@
 //   the normalised output itself; otherwise each CTA covering part of the unit
 //   writes a partial (O unnormalised, running max m, running sum l) to slot c + u and the
 //   combine kernel merges them with the same rescaling rule as the online softmax.
+//   When there are no more units than CTAs, the plan may instead give CTA c exactly unit
+//   c: no unit starts inside a range and nothing is combined, at the price of idle CTAs.
+//   It does so when a per-tile time model says so: a tile takes max(tile_floor, n) time
+//   units while n CTAs stream at once (their share of HBM bandwidth, or the tile's
+//   compute time), so the split line takes (TT + U * switch_tiles) / C * max(tile_floor,
+//   C) and one CTA per unit takes (the longest unit's tiles) * max(tile_floor, U).
 #pragma once
 
 #include <cuda_runtime.h>
@@ -42,7 +48,7 @@ struct PlanHdr {
   int32_t num_units;
   int32_t total_tiles;
   int32_t kt;
-  int32_t pad0;
+  int32_t unit_ctas;  // 1: CTA c covers exactly unit c (no split, nothing to combine)
   int64_t sum_w;
   int64_t sum_kv;
 };
@@ -102,6 +108,9 @@ struct AttnParams {
   int max_units;
   int n_ctas;
   int switch_tiles;           // virtual tiles charged for starting a unit
+  int tile_floor;             // CTAs streaming at once at which a tile's share of HBM time
+                              // equals its compute time (0: never one CTA per unit)
+  int unit_ctas_mode;         // -1: choose by the cost model; 0: never; 1: whenever U <= CTAs
   const int32_t* block_table;  // paged cache: [B, bt_stride] physical block of each logical
                                // block (position j of sequence b: row j % block_size of
                                // block block_table[b * bt_stride + j / block_size])

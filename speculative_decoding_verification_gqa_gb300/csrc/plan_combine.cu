@@ -48,13 +48,14 @@ __global__ void __launch_bounds__(1024) plan_kernel(AttnParams p, int kt) {
   __shared__ int64_t s_warp[32];
   __shared__ int32_t s_ubeg[PLAN_SMEM_UNITS + 1];
   __shared__ int64_t carry[4];
-  __shared__ int bad;
+  __shared__ int bad, s_maxt;
   const int tid = threadIdx.x;
   pdl_trigger();
   pdl_wait();
   if (tid == 0) {
     carry[0] = carry[1] = carry[2] = carry[3] = 0;
     bad = 0;
+    s_maxt = 0;
   }
   __syncthreads();
   for (int base = 0; base < p.B; base += blockDim.x) {
@@ -74,6 +75,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(AttnParams p, int kt) {
         nmt = (int)((p.G * w + MT - 1) / MT);
         nt = (int)((kvn + kt - 1) / kt);  // tiles up to the one holding T + D
         for (int mt = 0; mt < nmt; ++mt) per_g += nt - unit_first_tile(T, mt, p.G, p.window, kt);
+        atomicMax(&s_maxt, nt - unit_first_tile(T, 0, p.G, p.window, kt));  // longest unit
         nunits = (int64_t)p.Hkv * nmt;
         ntiles = (int64_t)p.Hkv * per_g;
       }
@@ -129,12 +131,29 @@ __global__ void __launch_bounds__(1024) plan_kernel(AttnParams p, int kt) {
       p.ubeg[carry[2]] = (int32_t)carry[3];
     }
   }
+  if (tid == 0) {
+    // one CTA per unit, or the split tile line (cost model in internal.cuh)
+    const int64_t U = p.hdr->num_units, TT = p.hdr->total_tiles, C = p.n_ctas;
+    bool one = U > 0 && U <= C && p.unit_ctas_mode != 0 && p.tile_floor > 0;
+    if (one && p.unit_ctas_mode < 0) {
+      const double f = p.tile_floor;
+      const double t_split = (double)(TT + U * p.switch_tiles) / C * fmax(f, (double)C);
+      const double t_units = (double)s_maxt * fmax(f, (double)U);
+      one = t_units < t_split;
+    }
+    p.hdr->unit_ctas = one ? 1 : 0;
+  }
   __syncthreads();  // ubeg and the header are visible to the whole block
-  // CTA c starts at the first real tile at or after virtual position c*VT/C
   const int U = p.hdr->num_units;
   const int64_t TT = p.hdr->total_tiles, X = p.switch_tiles;
-  const int64_t VT = TT + (int64_t)U * X;
   const int32_t* ubeg = U <= PLAN_SMEM_UNITS ? s_ubeg : p.ubeg;
+  if (p.hdr->unit_ctas) {
+    for (int c = tid; c <= p.n_ctas; c += blockDim.x)
+      p.cta_tab[c] = c < U ? make_int2(ubeg[c], c) : make_int2((int32_t)TT, U);
+    return;
+  }
+  // CTA c starts at the first real tile at or after virtual position c*VT/C
+  const int64_t VT = TT + (int64_t)U * X;
   for (int c = tid; c <= p.n_ctas; c += blockDim.x) {
     int2 e = make_int2((int32_t)TT, U);
     if (c < p.n_ctas && TT > 0) {
@@ -168,7 +187,7 @@ __global__ void __launch_bounds__(256) combine_kernel(AttnParams p) {
   const int u = blockIdx.x / (MT / COMBINE_ROWS);
   const int r = (blockIdx.x % (MT / COMBINE_ROWS)) * COMBINE_ROWS + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  if (u >= p.hdr->num_units) return;
+  if (u >= p.hdr->num_units || p.hdr->unit_ctas) return;  // (one CTA per unit: all whole)
   const int64_t VT = p.hdr->total_tiles + (int64_t)p.hdr->num_units * p.switch_tiles;
   const int64_t ub = p.ubeg[u], ue = p.ubeg[u + 1];
   const int c_lo = cta_of_tile(vpos_of_tile(ub, u, p.switch_tiles), VT, p.n_ctas);
