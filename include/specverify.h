@@ -250,6 +250,14 @@ SV_API const char* sv_status_string(sv_status status);
  * if the value is unknown or the kernel is not built. Process-wide. */
 SV_API int sv_set_attn_kernel(int which);
 
+/* How spec_verify_attn spreads its units (sequence, KV head, 128-row tile) over CTAs,
+ * for measurement and tests: -1 = by the library's per-tile time model (default), 0 =
+ * always one tile line split evenly over the CTAs, k >= 1 = k CTAs per unit, each with
+ * an equal share of its tiles, whenever units * k fits the grid (otherwise as 0). Results
+ * agree to rounding across modes. Returns the previous value, or -2 if mode is outside
+ * [-1, 1024]. Process-wide. */
+SV_API int sv_set_unit_ctas(int mode);
+
 /* Profiling hook: when both are non-NULL, every later spec_verify_attn records `start`
  * just before and `stop` just after its main attention kernel, on the call's stream
  * (cudaEvent_t handles owned by the caller). Pass NULLs to turn it off. Process-wide. */

@@ -29,7 +29,7 @@ STATUS = {0: "SV_OK", 1: "SV_ERR_NULL", 2: "SV_ERR_SHAPE", 3: "SV_ERR_DTYPE",
 EXPORTS = ("spec_verify_attn_workspace_size", "spec_verify_attn", "spec_verify_attn_paged",
            "spec_accept_workspace_size",
            "spec_accept", "spec_draft_signals_workspace_size", "spec_draft_signals",
-           "sv_workspace_status", "sv_status_string", "sv_set_attn_kernel",
+           "sv_workspace_status", "sv_status_string", "sv_set_attn_kernel", "sv_set_unit_ctas",
            "sv_set_profile_events", "sv_version")
 
 
@@ -86,6 +86,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.sv_status_string.restype = ctypes.c_char_p
         lib.sv_set_attn_kernel.argtypes = [ctypes.c_int]
         lib.sv_set_attn_kernel.restype = ctypes.c_int
+        lib.sv_set_unit_ctas.argtypes = [ctypes.c_int]
+        lib.sv_set_unit_ctas.restype = ctypes.c_int
         lib.sv_set_profile_events.argtypes = [vp, vp]
         lib.sv_set_profile_events.restype = None
         lib.sv_version.restype = ctypes.c_int
@@ -287,6 +289,15 @@ def set_attn_kernel(which: int) -> int:
     prev = load_library().sv_set_attn_kernel(int(which))
     if prev < 0:
         raise ValueError("attention kernel %d is not available" % which)
+    return prev
+
+
+def set_unit_ctas(mode: int) -> int:
+    """-1 cost model (default), 0 split tile line, k >= 1 k CTAs per unit. Returns the
+    previous mode."""
+    prev = load_library().sv_set_unit_ctas(int(mode))
+    if prev < -1:
+        raise ValueError("unit-CTA mode must be in [-1, 1024]")
     return prev
 
 

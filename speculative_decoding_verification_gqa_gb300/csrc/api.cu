@@ -38,6 +38,7 @@ constexpr int32_t MAX_SEQ_LEN = 0x7fffffff - 1024;
 constexpr int64_t MAX_KV_ROWS = 0x7fffffff - 1024;
 
 int g_attn_kernel = 0;  // 0 automatic, 1 mma.sync, 2 tcgen05
+int g_unit_ctas = SV_UNIT_CTAS;  // -1 cost model, 0 split tile line, k > 0 k CTAs per unit
 cudaEvent_t g_ev_start = nullptr;
 cudaEvent_t g_ev_stop = nullptr;
 
@@ -104,6 +105,13 @@ SV_API int sv_set_attn_kernel(int which) {
   if (which == 2 && !attn_tc_available()) return -1;
   const int prev = g_attn_kernel;
   g_attn_kernel = which;
+  return prev;
+}
+
+SV_API int sv_set_unit_ctas(int mode) {
+  if (mode < -1 || mode > 1024) return -2;
+  const int prev = g_unit_ctas;
+  g_unit_ctas = mode;
   return prev;
 }
 
@@ -207,7 +215,7 @@ sv_status verify_impl(const sv_attn_desc* desc, const void* q, const void* k_cac
   // measured cost of starting a unit inside a CTA's range, in tiles of that kernel
   p.switch_tiles = which == 2 ? (fp8 ? SWITCH_TILES_TC_FP8 : SWITCH_TILES_TC_BF16) : SWITCH_TILES_MMA;
   p.tile_floor = which == 2 ? (fp8 ? SV_TILE_FLOOR_F8 : SV_TILE_FLOOR_BF16) : 0;
-  p.unit_ctas_mode = SV_UNIT_CTAS;
+  p.unit_ctas_mode = g_unit_ctas;
   const float scale = desc->softmax_scale > 0.f ? desc->softmax_scale
                                                 : 1.f / sqrtf((float)desc->head_dim);
   p.scale_log2 = scale * 1.4426950408889634f;

@@ -20,12 +20,14 @@
 //   the normalised output itself; otherwise each CTA covering part of the unit
 //   writes a partial (O unnormalised, running max m, running sum l) to slot c + u and the
 //   combine kernel merges them with the same rescaling rule as the online softmax.
-//   When there are no more units than CTAs, the plan may instead give CTA c exactly unit
-//   c: no unit starts inside a range and nothing is combined, at the price of idle CTAs.
-//   It does so when a per-tile time model says so: a tile takes max(tile_floor, n) time
-//   units while n CTAs stream at once (their share of HBM bandwidth, or the tile's
-//   compute time), so the split line takes (TT + U * switch_tiles) / C * max(tile_floor,
-//   C) and one CTA per unit takes (the longest unit's tiles) * max(tile_floor, U).
+//   When there are no more units than CTAs, the plan may instead give each unit k CTAs
+//   (k <= C / U), CTA u*k + i taking the i-th of k equal parts of unit u's tiles: no unit
+//   starts inside a range, and only k partials per unit are combined (none for k = 1),
+//   at the price of idle CTAs. It does so when a per-tile time model says so: a tile
+//   takes max(tile_floor, n) time units while n CTAs stream at once (their share of HBM
+//   bandwidth, or the tile's compute time), so the split line takes (TT + U *
+//   switch_tiles) / C * max(tile_floor, C) and k CTAs per unit ceil(the longest unit's
+//   tiles / k) * max(tile_floor, U * k).
 #pragma once
 
 #include <cuda_runtime.h>
@@ -48,7 +50,8 @@ struct PlanHdr {
   int32_t num_units;
   int32_t total_tiles;
   int32_t kt;
-  int32_t unit_ctas;  // 1: CTA c covers exactly unit c (no split, nothing to combine)
+  int32_t unit_ctas;  // k > 0: CTA u*k + i covers the i-th of k equal parts of unit u
+                      // (k = 1: nothing to combine); 0: the split tile line
   int64_t sum_w;
   int64_t sum_kv;
 };
@@ -110,7 +113,8 @@ struct AttnParams {
   int switch_tiles;           // virtual tiles charged for starting a unit
   int tile_floor;             // CTAs streaming at once at which a tile's share of HBM time
                               // equals its compute time (0: never one CTA per unit)
-  int unit_ctas_mode;         // -1: choose by the cost model; 0: never; 1: whenever U <= CTAs
+  int unit_ctas_mode;         // -1: choose by the cost model; 0: never; k > 0: k CTAs per
+                              // unit whenever U * k <= CTAs
   const int32_t* block_table;  // paged cache: [B, bt_stride] physical block of each logical
                                // block (position j of sequence b: row j % block_size of
                                // block block_table[b * bt_stride + j / block_size])

@@ -129,27 +129,46 @@ __global__ void __launch_bounds__(1024) plan_kernel(AttnParams p, int kt) {
       p.hdr->num_units = (int32_t)carry[2];
       p.hdr->total_tiles = (int32_t)carry[3];
       p.ubeg[carry[2]] = (int32_t)carry[3];
+      if (carry[2] <= PLAN_SMEM_UNITS) s_ubeg[carry[2]] = (int32_t)carry[3];  // the end too
     }
   }
   if (tid == 0) {
-    // one CTA per unit, or the split tile line (cost model in internal.cuh)
+    // k CTAs per unit, or the split tile line (cost model in internal.cuh)
     const int64_t U = p.hdr->num_units, TT = p.hdr->total_tiles, C = p.n_ctas;
-    bool one = U > 0 && U <= C && p.unit_ctas_mode != 0 && p.tile_floor > 0;
-    if (one && p.unit_ctas_mode < 0) {
-      const double f = p.tile_floor;
-      const double t_split = (double)(TT + U * p.switch_tiles) / C * fmax(f, (double)C);
-      const double t_units = (double)s_maxt * fmax(f, (double)U);
-      one = t_units < t_split;
+    int k = 0;
+    if (U > 0 && U <= C && p.tile_floor > 0) {
+      if (p.unit_ctas_mode > 0) {
+        k = (int)min((int64_t)p.unit_ctas_mode, C / U);
+      } else if (p.unit_ctas_mode < 0) {
+        const double f = p.tile_floor;
+        double best = (double)(TT + U * p.switch_tiles) / C * fmax(f, (double)C);
+        for (int kk = 1; kk <= C / U; ++kk) {
+          const double t = (double)((s_maxt + kk - 1) / kk) * fmax(f, (double)(U * kk));
+          if (t < best) {
+            best = t;
+            k = kk;
+          }
+        }
+      }
     }
-    p.hdr->unit_ctas = one ? 1 : 0;
+    p.hdr->unit_ctas = k;
   }
   __syncthreads();  // ubeg and the header are visible to the whole block
   const int U = p.hdr->num_units;
   const int64_t TT = p.hdr->total_tiles, X = p.switch_tiles;
   const int32_t* ubeg = U <= PLAN_SMEM_UNITS ? s_ubeg : p.ubeg;
-  if (p.hdr->unit_ctas) {
-    for (int c = tid; c <= p.n_ctas; c += blockDim.x)
-      p.cta_tab[c] = c < U ? make_int2(ubeg[c], c) : make_int2((int32_t)TT, U);
+  if (p.hdr->unit_ctas > 0) {
+    // CTA c = u * k + i takes the i-th of k equal parts of unit u's tiles
+    const int k = p.hdr->unit_ctas;
+    for (int c = tid; c <= p.n_ctas; c += blockDim.x) {
+      int2 e = make_int2((int32_t)TT, U);
+      if (c < U * k) {
+        const int u = c / k, i = c % k;
+        const int32_t n = ubeg[u + 1] - ubeg[u];
+        e = make_int2(ubeg[u] + (int32_t)((int64_t)n * i / k), u);
+      }
+      p.cta_tab[c] = e;
+    }
     return;
   }
   // CTA c starts at the first real tile at or after virtual position c*VT/C
@@ -187,12 +206,17 @@ __global__ void __launch_bounds__(256) combine_kernel(AttnParams p) {
   const int u = blockIdx.x / (MT / COMBINE_ROWS);
   const int r = (blockIdx.x % (MT / COMBINE_ROWS)) * COMBINE_ROWS + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  if (u >= p.hdr->num_units || p.hdr->unit_ctas) return;  // (one CTA per unit: all whole)
+  const int kc = p.hdr->unit_ctas;  // CTAs per unit (0: the split tile line)
+  if (u >= p.hdr->num_units || kc == 1) return;  // (one CTA per unit: every unit is whole)
   const int64_t VT = p.hdr->total_tiles + (int64_t)p.hdr->num_units * p.switch_tiles;
   const int64_t ub = p.ubeg[u], ue = p.ubeg[u + 1];
-  const int c_lo = cta_of_tile(vpos_of_tile(ub, u, p.switch_tiles), VT, p.n_ctas);
-  const int c_hi = cta_of_tile(vpos_of_tile(ue - 1, u, p.switch_tiles), VT, p.n_ctas);
-  if (c_lo == c_hi) return;  // one CTA covered the unit and wrote the output itself
+  // the CTAs that covered the unit: u*k .. u*k + k - 1 (k CTAs per unit), or those whose
+  // ranges of the split tile line hold its tiles
+  const int c_lo = kc > 0 ? u * kc : cta_of_tile(vpos_of_tile(ub, u, p.switch_tiles), VT, p.n_ctas);
+  const int c_hi = kc > 0 ? u * kc + kc - 1
+                          : cta_of_tile(vpos_of_tile(ue - 1, u, p.switch_tiles), VT, p.n_ctas);
+  // one CTA covered the unit and wrote the output itself
+  if (c_lo == c_hi || (kc > 0 && ue - ub == 1)) return;
   const int4 info = p.units[u];
   const int b = info.x, g = info.y, mt = info.z;
   const int rows_total = p.G * (1 + p.draft_len[b]);
@@ -207,7 +231,8 @@ __global__ void __launch_bounds__(256) combine_kernel(AttnParams p) {
 #pragma unroll
     for (int k = 0; k < MAXP; ++k) {
       const int c = c0 + k;
-      const bool use = c <= c_hi && cta_has_tiles(c, VT, p.n_ctas);
+      const bool use = c <= c_hi && (kc > 0 ? (ue - ub) * (c - c_lo + 1) / kc > (ue - ub) * (c - c_lo) / kc
+                                            : cta_has_tiles(c, VT, p.n_ctas));
       const size_t slot = (size_t)(c + u);
       ml[k] = use ? p.part_ml[slot * MT + r] : make_float2(-INFINITY, 0.f);
       const float* src = p.part_o + (slot * MT + r) * HD + lane * PER;

@@ -157,3 +157,11 @@ def test_paged_checks_the_descriptor_too(lib):
     assert _paged(lib, _desc(head_dim=96)) == 2
     assert _paged(lib, _desc(), q=None) == 1
     assert _paged(lib, _desc(batch=0), q=None) == 0
+
+
+def test_unit_cta_policy_setter(lib):
+    prev = lib.sv_set_unit_ctas(2)
+    assert lib.sv_set_unit_ctas(prev) == 2
+    assert lib.sv_set_unit_ctas(-2) == -2
+    assert lib.sv_set_unit_ctas(1025) == -2
+    assert lib.sv_set_unit_ctas(prev) == prev

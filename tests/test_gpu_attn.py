@@ -304,3 +304,33 @@ def test_dominant_key_wins(kernel):
     out2 = _run_raw(_bits(q), _bits(k2), vb, [T], [D])
     assert np.abs(out2[D] - bf16_to_f64(vb)[T + D, 0][None, :]).max() <= 1e-2
     assert np.abs(out2[0] - bf16_to_f64(vb)[T + D, 0][None, :]).max() > 0.1
+
+
+# ------------------------------------------------------------- unit-to-CTA policies
+
+@pytest.fixture(params=[0, 1, 2, 3, -1], ids=["split", "k1", "k2", "k3", "model"])
+def unit_ctas(request):
+    prev = sv.set_unit_ctas(request.param)
+    yield request.param
+    sv.set_unit_ctas(prev)
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8_e4m3"])
+@pytest.mark.parametrize("name", ["ragged", "rows_256", "d64_ragged", "tile_edges", "c1"])
+def test_every_unit_cta_policy(kernel, unit_ctas, name, kv):
+    """The split tile line, k CTAs per unit (k = 1, 2, 3: equal parts, the last unit's end
+    included) and the model's choice give the oracle's result."""
+    w, x = _small(kv=kv, seed=21, **SMALL[name])
+    assert_close(gpu_attn(x), oracle_attn(w, x))
+
+
+@pytest.mark.parametrize("k", [1, 2])
+def test_unit_cta_policy_on_a_full_size_workload(kernel, k):
+    """c3 (64 units of 257 tiles) with 1 and 2 CTAs per unit, on sampled units."""
+    prev = sv.set_unit_ctas(k)
+    try:
+        w, x = _full("c3")
+        got = gpu_attn(x)
+    finally:
+        sv.set_unit_ctas(prev)
+    assert_close(got, oracle_attn(w, x, units=[(0, 0), (7, 7), (3, 5)]))
