@@ -491,7 +491,6 @@ def run_ours(args):
         torch.cuda.synchronize()
         if sv.workspace_status(ws_p) != 0:
             raise RuntimeError("device-side check failed in the paged call")
-        same = bool(torch.equal(out_p, out))
         p_ms = float(np.median([e[0].elapsed_time(e[1]) for e in ep]))
         p_attn = float(np.median([e[2].elapsed_time(e[3]) for e in ep]))
         side_paged = {"block_size": args.side_block, "verify_call_ms": round(p_ms, 5),
@@ -499,7 +498,6 @@ def run_ours(args):
                       "attn_GB_per_s": round((kv_bytes + qo_bytes) / (p_attn / 1e3) / 1e9, 1),
                       "attn_frac": round((kv_bytes + qo_bytes) / (p_attn / 1e3) / 1e9
                                          / peaks()[0], 4),
-                      "same_bits_as_packed": same,
                       "note": "spec_verify_attn_paged on the step's K/V cut into blocks at "
                               "seeded random slots of a pool with 256 spare blocks; inputs "
                               "larger than L2; not part of the step"}

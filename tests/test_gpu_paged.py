@@ -54,6 +54,16 @@ def gpu_paged(x, pg, *, window=0, workspace=None, table=None):
     return o.view(torch.int16).cpu().numpy().view(np.uint16)
 
 
+def same_policy_packed(x):
+    """The packed call under the split tile line, the policy the paged calls with blocks
+    shorter than a tile always use: the same tiles, hence the same bits."""
+    prev = sv.set_unit_ctas(0)
+    try:
+        return gpu_attn(x)
+    finally:
+        sv.set_unit_ctas(prev)
+
+
 def paged_oracle(w, x, pg, window=0, units=None):
     return oracle.verify_attn_paged(x["q"], pg["k_pages"], pg["v_pages"], pg["block_table"],
                                     x["seq_lens"], x["draft_len"], Hq=w.Hq, Hkv=w.Hkv, d=w.d,
@@ -68,10 +78,15 @@ RAGGED = dict(B=4, Hq=8, Hkv=2, d=128, T=(1000, 37, 300, 2500), D=(5, 0, 15, 9))
 def test_ragged_batch_against_paged_oracle(kernel, kv, bs):
     w, x = _small(kv=kv, seed=bs, **RAGGED)
     pg = synth.paged_layout(x, bs, seed=bs + 1, spare_blocks=5)
-    got = gpu_paged(x, pg)
+    prev = sv.set_unit_ctas(0)
+    try:
+        got = gpu_paged(x, pg)
+    finally:
+        sv.set_unit_ctas(prev)
     assert_close(got, paged_oracle(w, x, pg))
     # the same positions through the packed layout: the same tiles, the same bits
-    assert np.array_equal(got, gpu_attn(x))
+    assert np.array_equal(got, same_policy_packed(x))
+    assert_close(gpu_paged(x, pg), paged_oracle(w, x, pg))  # the default policy
 
 
 @pytest.mark.parametrize("d", [64, 128])
@@ -132,10 +147,10 @@ def _full(cfg):
 @pytest.mark.parametrize("cfg", ["c2", "c3"])
 def test_full_size_16_position_blocks(kernel, cfg):
     """The workloads with 16-position blocks scattered over the pool: bit-identical to the
-    packed call, and the oracle on sampled (sequence, KV head) units."""
+    packed call on the same (split) tile line, and the oracle on sampled units."""
     w, x, pg = _full(cfg)
     got = gpu_paged(x, pg)
-    assert np.array_equal(got, gpu_attn(x))
+    assert np.array_equal(got, same_policy_packed(x))
     B = len(x["seq_lens"])
     units = [(0, 0), (B - 1, w.Hkv - 1), (B // 2, 1)]
     assert_close(got, oracle_attn(w, x, units=units))
