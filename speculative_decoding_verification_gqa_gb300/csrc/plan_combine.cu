@@ -48,7 +48,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(AttnParams p, int kt) {
   __shared__ int64_t s_warp[32];
   __shared__ int32_t s_ubeg[PLAN_SMEM_UNITS + 1];
   __shared__ int64_t carry[4];
-  __shared__ int bad, s_maxt;
+  __shared__ int bad, s_maxt, s_nmt_lo, s_nmt_hi;
   const int tid = threadIdx.x;
   pdl_trigger();
   pdl_wait();
@@ -56,6 +56,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(AttnParams p, int kt) {
     carry[0] = carry[1] = carry[2] = carry[3] = 0;
     bad = 0;
     s_maxt = 0;
+    s_nmt_lo = 0x7fffffff;
+    s_nmt_hi = 0;
   }
   __syncthreads();
   for (int base = 0; base < p.B; base += blockDim.x) {
@@ -76,6 +78,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(AttnParams p, int kt) {
         nt = (int)((kvn + kt - 1) / kt);  // tiles up to the one holding T + D
         for (int mt = 0; mt < nmt; ++mt) per_g += nt - unit_first_tile(T, mt, p.G, p.window, kt);
         atomicMax(&s_maxt, nt - unit_first_tile(T, 0, p.G, p.window, kt));  // longest unit
+        atomicMin(&s_nmt_lo, nmt);
+        atomicMax(&s_nmt_hi, nmt);
         nunits = (int64_t)p.Hkv * nmt;
         ntiles = (int64_t)p.Hkv * per_g;
       }
@@ -130,6 +134,42 @@ __global__ void __launch_bounds__(1024) plan_kernel(AttnParams p, int kt) {
       p.hdr->total_tiles = (int32_t)carry[3];
       p.ubeg[carry[2]] = (int32_t)carry[3];
       if (carry[2] <= PLAN_SMEM_UNITS) s_ubeg[carry[2]] = (int32_t)carry[3];  // the end too
+    }
+  }
+  __syncthreads();  // the header is visible to the whole block
+  // Every sequence with the same number nm > 1 of row tiles per KV head: reorder the units
+  // row-tile-major (all row tiles 0, then all row tiles 1, ...). The row tiles of one
+  // (sequence, KV head) read the same K/V; on the split tile line the CTAs of slice mt
+  // then walk the same key tiles at the same time as those of slice 0, so the K/V of all
+  // but one of them comes from L2 instead of HBM.
+  const int nm = s_nmt_hi;
+  if (p.hdr->num_units > 0 && nm > 1 && s_nmt_lo == nm) {
+    if (tid == 0) carry[3] = 0;
+    __syncthreads();
+    for (int mt = 0; mt < nm; ++mt) {
+      for (int base = 0; base < p.B; base += blockDim.x) {
+        const int b = base + tid;
+        int T = 0, nt = 0, kb = 0;
+        if (b < p.B) {
+          T = p.seq_lens[b];
+          nt = (int)(((int64_t)T + p.draft_len[b] + kt) / kt);  // tiles up to T + D
+          kb = unit_first_tile(T, mt, p.G, p.window, kt);
+        }
+        int64_t tt;
+        const int64_t et = block_excl_scan(b < p.B ? (int64_t)p.Hkv * (nt - kb) : 0, s_warp, &tt);
+        if (b < p.B) {
+          for (int g = 0; g < p.Hkv; ++g) {
+            const int64_t u = ((int64_t)mt * p.B + b) * p.Hkv + g;
+            const int32_t t0 = (int32_t)(carry[3] + et + (int64_t)g * (nt - kb));
+            p.units[u] = make_int4(b, g, mt, kb * kt);
+            p.ubeg[u] = t0;
+            if (u < PLAN_SMEM_UNITS) s_ubeg[u] = t0;
+          }
+        }
+        __syncthreads();
+        if (tid == 0) carry[3] += tt;
+        __syncthreads();
+      }
     }
   }
   if (tid == 0) {
