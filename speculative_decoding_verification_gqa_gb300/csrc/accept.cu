@@ -287,6 +287,8 @@ __device__ __noinline__ void finalize_all(const AcceptArgs& a, int64_t rows, con
     }
     __syncthreads();  // s_q / s_d / s_n are reused by the next chunk
   }
+  if (!in_smem)  // leave the workspace as it was found (zero) for the next call
+    for (int64_t r = threadIdx.x; r < rows; r += blockDim.x) amax[r] = 0;
 }
 
 template <bool BF16>

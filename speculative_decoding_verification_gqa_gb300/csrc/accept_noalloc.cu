@@ -4,8 +4,8 @@
 // reserve all of their device memory once at start-up and then give each operator only
 // its inputs and outputs (plugin-style interfaces without a scratch argument), so any
 // per-call cudaMalloc would break their memory plan. For them, spec_accept_noalloc keeps
-// the acceptance step's scratch (the per-split (value, index) partials of the vocab
-// argmax and the flag word) in a fixed array compiled into the library.
+// the acceptance step's scratch (one (value, index) key per window row, a completion
+// ticket, the flag word) in a fixed array compiled into the library.
 //
 // Cost and limits: every GPU that loads the library holds kNoallocScratchBytes of device
 // memory until the process exits; shapes that need more scratch are rejected. All calls
@@ -53,9 +53,9 @@ extern "C" SV_API sv_status spec_accept_noalloc(int32_t batch, int32_t max_draft
   const sv_status st = scratch_on_current_device(&scratch);
   if (st != SV_OK) return st;
   // Same checks and kernels as spec_accept; a shape whose scratch exceeds the array fails
-  // its workspace-size check with SV_ERR_WORKSPACE before anything is launched. Nothing in
-  // the array has to start at zero: every partial the kernels read is written earlier in
-  // the same call, and the flag word is only ever OR-ed into.
+  // its workspace-size check with SV_ERR_WORKSPACE before anything is launched. The array
+  // starts at zero (static storage) and every call leaves it at zero apart from the flag
+  // word, which is only ever OR-ed into.
   return spec_accept(batch, max_draft_len, vocab, logits_dtype, logits, draft_tokens,
                      draft_len, accept_len, next_token, target_tokens, scratch,
                      kNoallocScratchBytes, stream);

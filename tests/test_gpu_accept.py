@@ -171,3 +171,22 @@ def test_aligned_and_unaligned_logits(dtype):
         torch.cuda.synchronize()
         assert np.array_equal(tgt.cpu().numpy(), ramax)
         assert np.array_equal(al.cpu().numpy(), ral) and np.array_equal(nt.cpu().numpy(), rnt)
+
+
+@pytest.mark.parametrize("B,D,V", [(16, 31, 128256), (300, 15, 64), (5, 0, 1000), (1, 255, 300)])
+def test_every_call_leaves_the_workspace_at_zero(B, D, V):
+    """The last CTA clears the row keys, the completion ticket and any target-token
+    scratch, so a zero-filled workspace is zero again after every call (here including
+    sequences spread over many CTAs, more rows than the last CTA keeps in shared memory,
+    no drafts at all, and the longest window)."""
+    import speculative_decoding_verification_gqa_gb300 as sv
+    w = synth.Workload("z", B=B, Hq=1, Hkv=1, d=8, D=D, T=1, V=V, p=0.9)
+    a = synth.accept_inputs(w, 31)
+    lg, dt, dl = dev_accept(a)
+    ws = sv.new_workspace(sv.accept_workspace_bytes(B, D, V))
+    for _ in range(2):
+        al, nt = sv.spec_accept(lg, dt, dl, max_draft_len=D, workspace=ws)
+        torch.cuda.synchronize()
+        assert int(torch.count_nonzero(ws)) == 0
+        ral, rnt, _ = oracle.spec_accept(a["logits"], a["draft_tokens"], a["draft_len"])
+        assert np.array_equal(al.cpu().numpy(), ral) and np.array_equal(nt.cpu().numpy(), rnt)
