@@ -233,21 +233,14 @@ cudaError_t launch_plan(const AttnParams& p, int kt, cudaStream_t s) {
   return launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, s, p, kt);
 }
 
-// Eight query rows per CTA, 32 lanes per row, each lane d/32 consecutive columns; the CTAs
-// of units that a single attention CTA covered exit at once.
+// Work item = eight query rows of one unit: one warp per row, each lane d/32 consecutive
+// columns; the rows of units that a single attention CTA covered are skipped at once.
 constexpr int COMBINE_ROWS = 8;
 
 template <int HD>
-__global__ void __launch_bounds__(256) combine_kernel(AttnParams p) {
+__device__ __forceinline__ void combine_row(const AttnParams& p, int u, int r, int lane, int kc) {
   constexpr int PER = HD / 32;
   constexpr int MAXP = 4;  // partials loaded in one batch
-  pdl_trigger();
-  pdl_wait();
-  const int u = blockIdx.x / (MT / COMBINE_ROWS);
-  const int r = (blockIdx.x % (MT / COMBINE_ROWS)) * COMBINE_ROWS + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  const int kc = p.hdr->unit_ctas;  // CTAs per unit (0: the split tile line)
-  if (u >= p.hdr->num_units || kc == 1) return;  // (one CTA per unit: every unit is whole)
   const int64_t VT = p.hdr->total_tiles + (int64_t)p.hdr->num_units * p.switch_tiles;
   const int64_t ub = p.ubeg[u], ue = p.ubeg[u + 1];
   // the CTAs that covered the unit: u*k .. u*k + k - 1 (k CTAs per unit), or those whose
@@ -323,9 +316,26 @@ __global__ void __launch_bounds__(256) combine_kernel(AttnParams p) {
   }
 }
 
+// Work items (unit, block of COMBINE_ROWS rows) in a grid-stride loop over a grid that is
+// resident at once, so that a call with nothing to combine (one CTA per unit) ends at once.
+template <int HD>
+__global__ void __launch_bounds__(256) combine_kernel(AttnParams p) {
+  pdl_trigger();
+  pdl_wait();
+  const int kc = p.hdr->unit_ctas;  // CTAs per unit (0: the split tile line)
+  if (kc == 1) return;              // one CTA per unit: every unit is whole
+  const int items = p.hdr->num_units * (MT / COMBINE_ROWS);
+  for (int it = blockIdx.x; it < items; it += gridDim.x)
+    combine_row<HD>(p, it / (MT / COMBINE_ROWS),
+                    (it % (MT / COMBINE_ROWS)) * COMBINE_ROWS + (threadIdx.x >> 5),
+                    threadIdx.x & 31, kc);
+}
+
 cudaError_t launch_combine(const AttnParams& p, cudaStream_t s) {
   if (p.max_units <= 0) return cudaSuccess;
-  const unsigned grid = (unsigned)p.max_units * (MT / COMBINE_ROWS);
+  // at most 8 CTAs of 256 threads per CTA of the attention grid (about one SM each)
+  const unsigned items = (unsigned)p.max_units * (MT / COMBINE_ROWS);
+  const unsigned grid = min(items, 8u * (unsigned)(p.n_ctas > 0 ? p.n_ctas : 1));
   return p.d == 128 ? launch_pdl(combine_kernel<128>, dim3(grid), dim3(256), 0, s, p)
                     : launch_pdl(combine_kernel<64>, dim3(grid), dim3(256), 0, s, p);
 }
