@@ -31,6 +31,39 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "spec-verify attention: KV GB/s vs HBM peak; accepted tokens/s"
+
+
+# ---------------------------------------------------------------- ranks (replicas only)
+# One process per GPU under torchrun. Each rank verifies its own batch (no data-path
+# collective); the only exchange is the max of the timings over ranks.
+
+def rank_info():
+    """(world size, rank, local rank) from the torchrun environment (1, 0, 0 without)."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def replica_seed(seed: int, rank: int) -> int:
+    """Input seed of a rank: every replica verifies a different batch."""
+    return seed + 7919 * rank
+
+
+def max_over_ranks(values, device=None):
+    """Element-wise maximum of `values` over all ranks of the default process group (the
+    values themselves without one). NCCL reduces on `device`, gloo on the host."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    dev = device if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_rate(world: int, units_per_rank: float, seconds: float) -> float:
+    """Units of all ranks per second of the slowest rank (weak scaling)."""
+    return world * units_per_rank / seconds
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_BYTES = 129e6
@@ -230,8 +263,8 @@ def cpu_oracle_sample(w, x, a, budget_s, seed, acc_rows=None):
 
 def run_reference(args):
     from speculative_decoding_verification_gqa_gb300 import synth
-    rank = int(os.environ.get("RANK", "0"))
-    if rank != 0:
+    _, rank, _ = rank_info()
+    if rank != 0:  # the reference arm runs on rank 0 only; the other ranks exit at once
         return
     w, T, D, p = workload(args)
     x = synth.attn_inputs(w, args.seed, seq_lens=T, draft_len=D)
@@ -285,9 +318,7 @@ def run_ours(args):
     import speculative_decoding_verification_gqa_gb300 as sv
     from speculative_decoding_verification_gqa_gb300 import build, synth
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    world, rank, local = rank_info()
     if world > 1:
         torch.cuda.set_device(local)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
@@ -304,7 +335,7 @@ def run_ours(args):
     attn_kernel = {1: "mma.sync", 2: "tcgen05"}[_active_kernel(sv)]
 
     w, T, D, p = workload(args)
-    seed = args.seed + 7919 * rank  # each rank verifies its own batch (replicas)
+    seed = replica_seed(args.seed, rank)  # each rank verifies its own batch (replicas)
     x = synth.attn_inputs(w, seed, seq_lens=T, draft_len=D)
     a = synth.accept_inputs(w, seed, draft_len=D, p=p)
     kv_bytes, qo_bytes = algorithmic_bytes(w, T, D)
@@ -537,16 +568,13 @@ def run_ours(args):
         e2e = {"ms": e2e_ms, "h2d": h2d, "d2h": d2h, "steps": K2}
 
     # max over ranks
-    vals = torch.tensor([ms_step, attn_ms, e2e["ms"] if e2e else 0.0], dtype=torch.float64,
-                        device=dev)
-    if world > 1:
-        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
-    ms_step, attn_ms, e2e_ms = vals.tolist()
+    ms_step, attn_ms, e2e_ms = max_over_ranks([ms_step, attn_ms, e2e["ms"] if e2e else 0.0],
+                                              device=dev)
 
     if rank == 0:
         hbm, tf, src = peaks()
         sec = ms_step / 1e3
-        value = world * kv_bytes / sec / 1e9
+        value = whole_job_rate(world, kv_bytes, sec) / 1e9
         achieved = (kv_bytes + qo_bytes) / (attn_ms / 1e3) / 1e9
         cpu = None
         if not args.no_cpu_baseline:
@@ -573,8 +601,8 @@ def run_ours(args):
                              % (kv_bytes / 1e6, a["logits"].nbytes / 1e6)
                              if kv_bytes > L2_BYTES else "inputs smaller than L2",
                        "parallelism": "replicas" if world > 1 else "1 GPU"},
-            "accepted_tokens_per_s": round(world * accepted_per_step / sec, 1),
-            "verified_query_tokens_per_s": round(world * int(W.sum()) / sec, 1),
+            "accepted_tokens_per_s": round(whole_job_rate(world, accepted_per_step, sec), 1),
+            "verified_query_tokens_per_s": round(whole_job_rate(world, int(W.sum()), sec), 1),
             "kv_bytes_per_step": kv_bytes,
             "attn_kernel": attn_kernel,
             "attn_ms": round(attn_ms, 5),
@@ -598,7 +626,8 @@ def run_ours(args):
                          "kernel": "verify attention (%s)" % attn_kernel},
             "cpu_baseline": cpu,
             "e2e": None if e2e is None else {
-                "value": round(world * kv_bytes / (e2e_ms / 1e3) / 1e9, 2), "unit": "GB/s",
+                "value": round(whole_job_rate(world, kv_bytes, e2e_ms / 1e3) / 1e9, 2),
+                "unit": "GB/s",
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                 "ms_per_step": round(e2e_ms, 4), "steps": e2e["steps"]},
             "clocks": clk,

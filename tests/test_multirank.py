@@ -1,0 +1,78 @@
+"""The multi-GPU path of the benchmark is N independent replicas (no data-path
+collective): each rank verifies its own batch and the ranks only agree on the slowest
+timing. These tests run that host logic as world_size-2 gloo process groups on the CPU."""
+import os
+import socket
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out):
+    import torch.distributed as dist
+    sys.path.insert(0, ROOT)
+    import bench
+    from speculative_decoding_verification_gqa_gb300 import synth
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        w_, r_, l_ = bench.rank_info()
+        # each rank reports its own step time; every rank must see the slowest one
+        got = bench.max_over_ranks([1.0 + rank, 5.0 - rank, 0.0])
+        # replicas: each rank's inputs come from its own seed
+        seed = bench.replica_seed(0, rank)
+        x = synth.attn_inputs(synth.CONFIGS["c1"], seed)
+        out.put((rank, (w_, r_, l_), got, seed, x["q"][:4].copy()))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_ranks_take_the_slowest_time_and_distinct_batches():
+    ctx = mp.get_context("spawn")
+    out = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, out)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = {}
+    for _ in procs:
+        r, info, got, seed, q = out.get(timeout=120)
+        res[r] = (info, got, seed, q)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for r in range(2):
+        assert res[r][0] == (2, r, r)
+        assert res[r][1] == [2.0, 5.0, 0.0]  # element-wise max over both ranks
+    assert res[0][2] != res[1][2]
+    assert not np.array_equal(res[0][3], res[1][3])
+
+
+def test_single_process_max_is_identity_and_job_rate_is_weak_scaling():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.max_over_ranks([3.0, 1.5]) == [3.0, 1.5]
+    assert bench.whole_job_rate(4, 10.0, 2.0) == 20.0  # 4 ranks x 10 units in 2 s
+    assert bench.replica_seed(7, 0) == 7
+
+
+def test_reference_arm_runs_on_rank_zero_only():
+    """Under torchrun every rank runs bench.py; the reference arm works on rank 0 alone and
+    the others exit 0 at once without printing."""
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--config", "c1", "--steps", "1", "--warmup", "0"],
+                       env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0 and r.stdout.strip() == ""
