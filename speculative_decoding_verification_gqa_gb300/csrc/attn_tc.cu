@@ -10,7 +10,8 @@
 //
 //   warp 0      TMA producer: K and V tiles of one KV head (128 keys x d, 128-byte swizzle)
 //               into a shared-memory ring (3 stages of bf16, 4 of E4M3); a stage is
-//               released once every reader of it has finished.
+//               released once every reader of it has finished. A paged cache's tile is
+//               one box per block, each looked up and loaded by its own lane.
 //   warp 1      S issuer (one thread): S = Q K^T (N = 128) into the score buffer, which is
 //               free again as soon as both warpgroups have read their halves. bf16:
 //               kind::f16 with Q (A) read from TMEM and K (B, K-major) from shared memory.
@@ -21,7 +22,8 @@
 //   warps 4..11 softmax, warpgroups 0 (warps 4-7) and 1 (8-11). Per unit they write Q into
 //               TMEM (half of d each). Per tile a thread reads its row's 64 scores of its
 //               half, releases the score buffer, applies the scale and the window-causal
-//               mask, updates m_w and l_w, and writes P_w = 2^(s - m_w) into its P buffer
+//               mask (and a sliding window's lower edge), updates m_w and l_w, and writes
+//               P_w = 2^(s - m_w) into its P buffer
 //               (after its previous P V has consumed the last one). At the end of a unit
 //               they merge (O_0, m_0, l_0) with (O_1, m_1, l_1) and store the output, or a
 //               split partial.
