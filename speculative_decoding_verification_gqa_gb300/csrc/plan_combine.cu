@@ -14,38 +14,47 @@
 
 namespace sv {
 
-// Exclusive scan of one int64 per thread over a 1024-thread block.
-__device__ int64_t block_excl_scan(int64_t v, int64_t* s_warp, int64_t* total) {
+constexpr int PLAN_THREADS = 256;
+
+// Exclusive scans over the block of N int64 values per thread at once (one pair of
+// barriers for all of them); total[k] receives the block's sum of v[k].
+template <int N>
+__device__ void block_excl_scan(const int64_t (&v)[N], int64_t (&ex)[N], int64_t (&total)[N],
+                                int64_t (*s_warp)[N]) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int nw = blockDim.x >> 5;
-  int64_t x = v;
+  int64_t x[N];
+#pragma unroll
+  for (int k = 0; k < N; ++k) x[k] = v[k];
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    int64_t y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) s_warp[wid] = x;
-  __syncthreads();
-  if (wid == 0) {
-    int64_t w = lane < nw ? s_warp[lane] : 0;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      int64_t y = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += y;
+    for (int k = 0; k < N; ++k) {
+      const int64_t y = __shfl_up_sync(0xffffffffu, x[k], o);
+      if (lane >= o) x[k] += y;
     }
-    s_warp[lane] = w;
   }
+  if (lane == 31)
+#pragma unroll
+    for (int k = 0; k < N; ++k) s_warp[wid][k] = x[k];
   __syncthreads();
-  const int64_t excl = x - v + (wid > 0 ? s_warp[wid - 1] : 0);
-  *total = s_warp[nw - 1];
-  __syncthreads();
-  return excl;
+#pragma unroll
+  for (int k = 0; k < N; ++k) {
+    int64_t before = 0, all = 0;
+    for (int w2 = 0; w2 < nw; ++w2) {
+      before += w2 < wid ? s_warp[w2][k] : 0;
+      all += s_warp[w2][k];
+    }
+    ex[k] = x[k] - v[k] + before;
+    total[k] = all;
+  }
+  __syncthreads();  // s_warp is reused by the next scan
 }
 
 constexpr int PLAN_SMEM_UNITS = 4096;  // unit starts also kept in shared memory
 
-__global__ void __launch_bounds__(1024) plan_kernel(AttnParams p, int kt) {
-  __shared__ int64_t s_warp[32];
+__global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(AttnParams p, int kt) {
+  __shared__ int64_t s_warp[PLAN_THREADS / 32][4];
   __shared__ int32_t s_ubeg[PLAN_SMEM_UNITS + 1];
   __shared__ int64_t carry[4];
   __shared__ int bad, s_maxt, s_nmt_lo, s_nmt_hi;
@@ -84,11 +93,11 @@ __global__ void __launch_bounds__(1024) plan_kernel(AttnParams p, int kt) {
         ntiles = (int64_t)p.Hkv * per_g;
       }
     }
-    int64_t tq, tkv, tu, tt;
-    const int64_t eq = block_excl_scan(w, s_warp, &tq);
-    const int64_t ekv = block_excl_scan(kvn, s_warp, &tkv);
-    const int64_t eu = block_excl_scan(nunits, s_warp, &tu);
-    const int64_t et = block_excl_scan(ntiles, s_warp, &tt);
+    const int64_t vals[4] = {w, kvn, nunits, ntiles};
+    int64_t ex[4], tot[4];
+    block_excl_scan<4>(vals, ex, tot, s_warp);
+    const int64_t eq = ex[0], ekv = ex[1], eu = ex[2], et = ex[3];
+    const int64_t tq = tot[0], tkv = tot[1], tu = tot[2], tt = tot[3];
     if (b < p.B) {
       p.q_off[b] = carry[0] + eq;
       p.kv_off[b] = carry[1] + ekv;
@@ -155,8 +164,10 @@ __global__ void __launch_bounds__(1024) plan_kernel(AttnParams p, int kt) {
           nt = (int)(((int64_t)T + p.draft_len[b] + kt) / kt);  // tiles up to T + D
           kb = unit_first_tile(T, mt, p.G, p.window, kt);
         }
-        int64_t tt;
-        const int64_t et = block_excl_scan(b < p.B ? (int64_t)p.Hkv * (nt - kb) : 0, s_warp, &tt);
+        const int64_t v1[1] = {b < p.B ? (int64_t)p.Hkv * (nt - kb) : 0};
+        int64_t e1[1], t1[1];
+        block_excl_scan<1>(v1, e1, t1, reinterpret_cast<int64_t (*)[1]>(&s_warp[0][0]));
+        const int64_t et = e1[0], tt = t1[0];
         if (b < p.B) {
           for (int g = 0; g < p.Hkv; ++g) {
             const int64_t u = ((int64_t)mt * p.B + b) * p.Hkv + g;
@@ -230,7 +241,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(AttnParams p, int kt) {
 }
 
 cudaError_t launch_plan(const AttnParams& p, int kt, cudaStream_t s) {
-  return launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, s, p, kt);
+  return launch_pdl(plan_kernel, dim3(1), dim3(PLAN_THREADS), 0, s, p, kt);
 }
 
 // Work item = eight query rows of one unit: one warp per row, each lane d/32 consecutive
