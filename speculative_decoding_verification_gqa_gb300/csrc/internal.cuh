@@ -28,6 +28,10 @@
 //   bandwidth, or the tile's compute time), so the split line takes (TT + U *
 //   switch_tiles) / C * max(tile_floor, C) and k CTAs per unit ceil(the longest unit's
 //   tiles / k) * max(tile_floor, U * k).
+//   Unit order on the line: by sequence, then KV head, then row tile; but when every
+//   sequence has the same number (> 1) of row tiles, row-tile-major (all row tiles 0,
+//   then all row tiles 1, ...), so that the CTAs of each row-tile slice of the split line
+//   read the same K/V at the same time and share it through L2.
 #pragma once
 
 #include <cuda_runtime.h>
