@@ -334,3 +334,42 @@ def test_unit_cta_policy_on_a_full_size_workload(kernel, k):
     finally:
         sv.set_unit_ctas(prev)
     assert_close(got, oracle_attn(w, x, units=[(0, 0), (7, 7), (3, 5)]))
+
+
+# ------------------------------------------------------- many sequences (plan chunks)
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8_e4m3"])
+def test_many_short_ragged_sequences(kernel, kv):
+    """700 sequences (more than the plan kernel handles in one pass over its threads):
+    ragged prefixes and draft lengths, several units per CTA on the split line."""
+    rng = np.random.default_rng(41)
+    B = 700
+    T = rng.integers(0, 400, size=B)
+    D = rng.integers(0, 8, size=B)
+    w, x = _small(B=B, Hq=8, Hkv=2, d=128, T=tuple(T), D=tuple(D), kv=kv, seed=41)
+    got = gpu_attn(x)
+    units = [(0, 0), (255, 1), (256, 0), (511, 1), (512, 0), (699, 1)] + \
+            [(int(b), int(rng.integers(2))) for b in rng.integers(0, B, size=6)]
+    assert_close(got, oracle_attn(w, x, units=units))
+    assert np.isfinite(bf16_to_f64(got)).all()
+
+
+def test_many_sequences_with_two_row_tiles(kernel):
+    """300 sequences with G (1 + D) = 136 rows each: every sequence has two row tiles, so
+    the plan reorders the units row-tile-major over several passes of its threads."""
+    B = 300
+    w, x = _small(B=B, Hq=8, Hkv=1, d=128, T=(150,) * B, D=(16,) * B, seed=43)
+    got = gpu_attn(x)
+    units = [(0, 0), (1, 0), (255, 0), (256, 0), (299, 0), (137, 0)]
+    assert_close(got, oracle_attn(w, x, units=units))
+
+
+def test_many_sequences_with_a_sliding_window(kernel):
+    rng = np.random.default_rng(47)
+    B = 520
+    T = rng.integers(100, 700, size=B)
+    D = rng.integers(0, 16, size=B)
+    w, x = _small(B=B, Hq=8, Hkv=2, d=128, T=tuple(T), D=tuple(D), seed=47)
+    got = gpu_attn(x, window=200)
+    units = [(0, 0), (300, 1), (519, 1), (257, 0)]
+    assert_close(got, oracle_attn(w, x, units=units, window=200))
