@@ -44,3 +44,55 @@ def test_draft_match_rate():
     rate = np.mean(greedy == a["draft_tokens"])
     assert abs(rate - 0.7) < 0.02
     assert a["draft_tokens"].min() >= 0 and a["draft_tokens"].max() < 40
+
+
+def _paged_case(bs, reclaim=0, spare=3, kv="bf16"):
+    w = synth.Workload("p", B=4, Hq=4, Hkv=2, d=16, D=0, T=0, V=8, p=0.5, kv_dtype=kv)
+    x = synth.attn_inputs(w, 3, seq_lens=np.array([0, 37, 100, 5]),
+                          draft_len=np.array([4, 0, 7, 2]))
+    return x, synth.paged_layout(x, bs, seed=9, spare_blocks=spare, reclaim_before_window=reclaim)
+
+
+def test_paged_layout_round_trips_every_position():
+    """Position j of sequence b sits at row j % bs of block table[b, j // bs], blocks are
+    distinct and inside the pool, entries past a sequence's last block are -1, and unused
+    rows hold the NaN fill."""
+    for bs in (1, 4, 16, 64):
+        x, pg = _paged_case(bs)
+        kp, tab = pg["k_pages"], pg["block_table"]
+        T = x["seq_lens"].astype(int)
+        R = T + x["draft_len"].astype(int) + 1
+        used = []
+        row0 = 0
+        for b in range(len(T)):
+            nblk = -(-R[b] // bs)
+            assert (tab[b, nblk:] == -1).all()
+            used += list(tab[b, :nblk])
+            for j in range(R[b]):
+                assert np.array_equal(kp[tab[b, j // bs], j % bs], x["k"][row0 + j])
+                assert np.array_equal(pg["v_pages"][tab[b, j // bs], j % bs], x["v"][row0 + j])
+            if R[b] % bs:
+                assert (kp[tab[b, nblk - 1], R[b] % bs:] == 0x7FC0).all()
+            row0 += R[b]
+        assert len(set(used)) == len(used)
+        assert min(used) >= 0 and max(used) < kp.shape[0]
+        assert kp.shape[0] == len(used) + 3
+
+
+def test_paged_layout_reclaims_exactly_the_blocks_before_the_window():
+    W, bs = 20, 8
+    x, pg = _paged_case(bs, reclaim=W)
+    tab = pg["block_table"]
+    T = x["seq_lens"].astype(int)
+    for b in range(len(T)):
+        first_kept = max(T[b] - W + 1, 0) // bs  # blocks holding only earlier positions
+        assert (tab[b, :first_kept] == -1).all()
+        R = T[b] + int(x["draft_len"][b]) + 1
+        assert (tab[b, first_kept:-(-R // bs)] >= 0).all()
+
+
+def test_paged_layout_fp8_fill_is_the_e4m3_nan_code():
+    x, pg = _paged_case(16, kv="fp8_e4m3")
+    kp, tab = pg["k_pages"], pg["block_table"]
+    spare = sorted(set(range(kp.shape[0])) - set(tab[tab >= 0].tolist()))
+    assert len(spare) == 3 and (kp[spare] == 0x7F).all()
