@@ -574,9 +574,51 @@ def run_ours(args):
         e2e_ms = e0.elapsed_time(e1) / K2
         e2e = {"ms": e2e_ms, "h2d": h2d, "d2h": d2h, "steps": K2}
 
+        # The same with the cached prefix resident on the device, as across decoding steps:
+        # each step uploads only what is new (the window's Q rows, the window's K/V rows,
+        # lengths, drafts, logits; the window rows travel in one pinned buffer and are
+        # scattered into the cache on the device) and reads back the same results.
+        qo_h, ko_h = synth.packed_offsets(x["seq_lens"], x["draft_len"])
+        win_rows = np.concatenate([np.arange(ko_h[b] + T[b], ko_h[b + 1])
+                                   for b in range(len(T))]).astype(np.int64)
+        win_idx = torch.from_numpy(win_rows).to(dev)
+        hk = h["k"].view(h["k"].shape[0], -1)
+        hv = h["v"].view(h["v"].shape[0], -1)
+        win_h = torch.cat([hk[win_rows], hv[win_rows]]).pin_memory()
+        win_d = torch.empty(win_h.shape, dtype=win_h.dtype, device=dev)
+        small = ("q", "T", "D", "logits", "draft") + (("sc",) if "sc" in h else ())
+        h2d_r = win_h.numel() * win_h.element_size() + sum(
+            h[k_].numel() * h[k_].element_size() for k_ in small)
+        nw = len(win_rows)
+
+        def e2e_resident_step():
+            for k_ in small:
+                d[k_].copy_(h[k_], non_blocking=True)
+            win_d.copy_(win_h, non_blocking=True)
+            d["k"].view(d["k"].shape[0], -1).index_copy_(0, win_idx, win_d[:nw])
+            d["v"].view(d["v"].shape[0], -1).index_copy_(0, win_idx, win_d[nw:])
+            step()
+            res_h["al"].copy_(al, non_blocking=True)
+            res_h["nt"].copy_(nt, non_blocking=True)
+            res_h["out"].copy_(out, non_blocking=True)
+
+        for _ in range(2):
+            e2e_resident_step()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        e0.record(stream)
+        for _ in range(K2):
+            e2e_resident_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e["ms_resident"] = e0.elapsed_time(e1) / K2
+        e2e["h2d_resident"] = h2d_r
+
     # max over ranks
-    ms_step, attn_ms, e2e_ms = max_over_ranks([ms_step, attn_ms, e2e["ms"] if e2e else 0.0],
-                                              device=dev)
+    ms_step, attn_ms, e2e_ms, e2e_res_ms = max_over_ranks(
+        [ms_step, attn_ms, e2e["ms"] if e2e else 0.0, e2e["ms_resident"] if e2e else 0.0],
+        device=dev)
 
     if rank == 0:
         hbm, tf, src = peaks()
@@ -640,7 +682,17 @@ def run_ours(args):
                 "value": round(whole_job_rate(world, kv_bytes, e2e_ms / 1e3) / 1e9, 2),
                 "unit": "GB/s",
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
-                "ms_per_step": round(e2e_ms, 4), "steps": e2e["steps"]},
+                "ms_per_step": round(e2e_ms, 4), "steps": e2e["steps"],
+                "note": "every step uploads all of its inputs, the whole K/V cache included"},
+            "e2e_resident_cache": None if e2e is None else {
+                "value": round(whole_job_rate(world, kv_bytes, e2e_res_ms / 1e3) / 1e9, 2),
+                "unit": "GB/s",
+                "h2d_bytes_per_step": e2e["h2d_resident"], "d2h_bytes_per_step": e2e["d2h"],
+                "ms_per_step": round(e2e_res_ms, 4), "steps": e2e["steps"],
+                "note": "the cached prefix stays on the device across steps; every step "
+                        "uploads its new inputs (window Q and K/V rows, lengths, drafts, "
+                        "logits) and reads back the acceptance results and the attention "
+                        "output"},
             "clocks": clk,
             # plan, attention, combine (verify call); argmax + acceptance (accept call)
             "gpu_launches": 4 * K,
