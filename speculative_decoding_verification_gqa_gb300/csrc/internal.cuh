@@ -116,7 +116,7 @@ struct AttnParams {
   int n_ctas;
   int switch_tiles;           // virtual tiles charged for starting a unit
   int tile_floor;             // CTAs streaming at once at which a tile's share of HBM time
-                              // equals its compute time (0: never one CTA per unit)
+                              // equals its compute time (0: the model keeps the split line)
   int unit_ctas_mode;         // -1: choose by the cost model; 0: never; k > 0: k CTAs per
                               // unit whenever U * k <= CTAs
   const int32_t* block_table;  // paged cache: [B, bt_stride] physical block of each logical

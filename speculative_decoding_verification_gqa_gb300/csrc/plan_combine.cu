@@ -187,10 +187,10 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(AttnParams p, int kt
     // k CTAs per unit, or the split tile line (cost model in internal.cuh)
     const int64_t U = p.hdr->num_units, TT = p.hdr->total_tiles, C = p.n_ctas;
     int k = 0;
-    if (U > 0 && U <= C && p.tile_floor > 0) {
-      if (p.unit_ctas_mode > 0) {
+    if (U > 0 && U <= C) {
+      if (p.unit_ctas_mode > 0) {  // forced by the caller
         k = (int)min((int64_t)p.unit_ctas_mode, C / U);
-      } else if (p.unit_ctas_mode < 0) {
+      } else if (p.unit_ctas_mode < 0 && p.tile_floor > 0) {  // the model, where it applies
         const double f = p.tile_floor;
         double best = (double)(TT + U * p.switch_tiles) / C * fmax(f, (double)C);
         for (int kk = 1; kk <= C / U; ++kk) {

@@ -154,3 +154,17 @@ def test_full_size_16_position_blocks(kernel, cfg):
     B = len(x["seq_lens"])
     units = [(0, 0), (B - 1, w.Hkv - 1), (B // 2, 1)]
     assert_close(got, oracle_attn(w, x, units=units))
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_paged_under_every_unit_cta_policy(kernel, mode):
+    """Forced unit-to-CTA policies apply to paged calls too (the model alone keeps them on
+    the split line for blocks shorter than a tile)."""
+    w, x = _small(kv="bf16", seed=19, **RAGGED)
+    pg = synth.paged_layout(x, 16, seed=20, spare_blocks=2)
+    prev = sv.set_unit_ctas(mode)
+    try:
+        got = gpu_paged(x, pg)
+    finally:
+        sv.set_unit_ctas(prev)
+    assert_close(got, paged_oracle(w, x, pg))
