@@ -21,8 +21,8 @@ constexpr int SWITCH_TILES_TC_BF16 = SV_SWITCH_BF16;
 constexpr int SWITCH_TILES_MMA = 2;
 // Per-tile compute floor of each kernel, in CTAs streaming at once (a 128-key tile's
 // compute time x HBM bandwidth / the tile's bytes: bf16 about 0.9 us x 6.8 TB/s / 64 KB,
-// E4M3 about 0.89 us x 6.8 TB/s / 32 KB). The mma.sync kernel is never run one CTA per
-// unit.
+// E4M3 about 0.89 us x 6.8 TB/s / 32 KB). The cost model is not applied to the mma.sync
+// kernel (it keeps the split line unless a policy is forced).
 #ifndef SV_TILE_FLOOR_BF16
 #define SV_TILE_FLOOR_BF16 93
 #endif
