@@ -260,7 +260,9 @@ SV_API int sv_set_unit_ctas(int mode);
 
 /* Profiling hook: when both are non-NULL, every later spec_verify_attn records `start`
  * just before and `stop` just after its main attention kernel, on the call's stream
- * (cudaEvent_t handles owned by the caller). Pass NULLs to turn it off. Process-wide. */
+ * (cudaEvent_t handles owned by the caller). Pass NULLs to turn it off. Process-wide.
+ * The events sit between the call's kernels and so cost them their launch overlap
+ * (several microseconds per call): time whole calls with the hook off. */
 SV_API void sv_set_profile_events(void* start_event, void* stop_event);
 
 /* Library version: major * 10000 + minor * 100 + patch. */

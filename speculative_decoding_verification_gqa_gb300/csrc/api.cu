@@ -83,7 +83,7 @@ int pick_kernel(const sv_attn_desc* d) {
 
 extern "C" {
 
-SV_API int sv_version(void) { return 100; }
+SV_API int sv_version(void) { return 200; }  // 0.2.0: paged K/V, sliding window, unit policies
 
 SV_API const char* sv_status_string(sv_status s) {
   switch (s) {
