@@ -414,6 +414,34 @@ def run_ours(args):
     ms_step = t_start.elapsed_time(t_stop) / K
     attn_ms = float(np.mean([a_.elapsed_time(b_) for a_, b_ in zip(ev_a, ev_b)]))
 
+    # The same step through spec_verify_attn_host_lengths (lengths also in host memory, as
+    # an engine's scheduler holds them: the work plan travels with the attention launch and
+    # no planning kernel runs). Timed like the step, without events inside it.
+    T_host = torch.from_numpy(x["seq_lens"].astype(np.int32))
+    D_host = torch.from_numpy(x["draft_len"].astype(np.int32))
+
+    def step_host_lengths():
+        sv.spec_verify_attn_host_lengths(d["q"], d["k"], d["v"], d["T"], d["D"], T_host, D_host,
+                                         max_draft_len=md, max_seq_len=ms,
+                                         kv_scale=d.get("sc"), out=out, workspace=ws_attn,
+                                         stream=stream)
+        sv.spec_accept(d["logits"], d["draft"], d["D"], max_draft_len=md, accept_len=al,
+                       next_token=nt, workspace=ws_acc, stream=stream)
+
+    for _ in range(3):
+        step_host_lengths()
+    torch.cuda.synchronize()
+    h0 = torch.cuda.Event(enable_timing=True)
+    h1 = torch.cuda.Event(enable_timing=True)
+    h0.record(stream)
+    for _ in range(K):
+        step_host_lengths()
+    h1.record(stream)
+    torch.cuda.synchronize()
+    if sv.workspace_status(ws_attn) != 0:
+        raise RuntimeError("device-side check failed in the host-lengths step")
+    ms_step_hl = h0.elapsed_time(h1) / K
+
     # split of a step between the two calls (separate pass, after the timed region)
     K3 = max(1, min(K, 200))
     e3 = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K3)]
@@ -616,9 +644,9 @@ def run_ours(args):
         e2e["h2d_resident"] = h2d_r
 
     # max over ranks
-    ms_step, attn_ms, e2e_ms, e2e_res_ms = max_over_ranks(
-        [ms_step, attn_ms, e2e["ms"] if e2e else 0.0, e2e["ms_resident"] if e2e else 0.0],
-        device=dev)
+    ms_step, attn_ms, e2e_ms, e2e_res_ms, ms_step_hl = max_over_ranks(
+        [ms_step, attn_ms, e2e["ms"] if e2e else 0.0, e2e["ms_resident"] if e2e else 0.0,
+         ms_step_hl], device=dev)
 
     if rank == 0:
         hbm, tf, src = peaks()
@@ -662,6 +690,13 @@ def run_ours(args):
                               "rows": rows_l, "vocab": V_l,
                               "note": "spec_draft_signals on a logits matrix of the step's "
                                       "shape; not part of the step"},
+            "host_lengths": {
+                "ms_per_step": round(ms_step_hl, 5),
+                "value": round(whole_job_rate(world, kv_bytes, ms_step_hl / 1e3) / 1e9, 2),
+                "unit": "GB/s",
+                "note": "the same step through spec_verify_attn_host_lengths (lengths also "
+                        "in host memory: the work plan is made on the host and passed "
+                        "with the attention launch, no planning kernel)"},
             "sliding_window": side_win,
             "paged": side_paged,
             "attn_tflops": round(fl / (attn_ms / 1e3) / 1e12, 2),

@@ -124,6 +124,28 @@ SV_API sv_status spec_verify_attn(const sv_attn_desc* desc, const void* q, const
                            void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * spec_verify_attn_host_lengths -- spec_verify_attn for callers that also hold the
+ * lengths in host memory (an engine's scheduler usually does). The work plan (units,
+ * their tiles, each CTA's range) is computed on the host from seq_lens_host and
+ * draft_len_host and passed with the attention kernel's launch, so no planning kernel
+ * runs on the GPU before the attention kernel (about 6 us per call on the workloads
+ * measured). Same arguments, layouts and results as spec_verify_attn, plus:
+ *   seq_lens_host, draft_len_host  int32 [B] in HOST memory, equal to seq_lens and
+ *                                  draft_len (which are still read on the device)
+ * Lengths out of range are reported at once with SV_ERR_SHAPE (host-side check). When
+ * the tcgen05 kernel is not used, or the batch is beyond the host plan's capacity (256
+ * sequences, 640 units of 128 query rows, 192 CTAs), the call plans on the device
+ * exactly like spec_verify_attn.
+ */
+SV_API sv_status spec_verify_attn_host_lengths(const sv_attn_desc* desc, const void* q,
+                                        const void* k_cache, const void* v_cache,
+                                        const int32_t* seq_lens, const int32_t* draft_len,
+                                        const int32_t* seq_lens_host,
+                                        const int32_t* draft_len_host, const float* kv_scale,
+                                        void* out, void* workspace, size_t workspace_bytes,
+                                        void* stream);
+
+/*
  * spec_verify_attn_paged -- spec_verify_attn over a paged KV cache ("GPU and LLM, chapter 5",
  * "PagedAttention (2): manage with fixed-size pages": the cache is cut into blocks of a
  * fixed number of positions placed anywhere in a pool, and a per-sequence block table

@@ -7,6 +7,8 @@ include/specverify.h:
 
 * ``spec_verify_attn`` -- GQA verify attention over cached prefix + draft window.
 * ``spec_verify_attn_paged`` -- the same over a paged cache (block pool + block table).
+* ``spec_verify_attn_host_lengths`` -- the same with host copies of the lengths (plan on
+  the host, no planning kernel).
 * ``spec_accept`` -- greedy acceptance (argmax per window row, first mismatch).
 """
 from __future__ import annotations
@@ -27,6 +29,7 @@ STATUS = {0: "SV_OK", 1: "SV_ERR_NULL", 2: "SV_ERR_SHAPE", 3: "SV_ERR_DTYPE",
           4: "SV_ERR_ALIGN", 5: "SV_ERR_WORKSPACE", 6: "SV_ERR_CUDA", 7: "SV_ERR_TIMEOUT",
           8: "SV_ERR_DEVICE_SHAPE"}
 EXPORTS = ("spec_verify_attn_workspace_size", "spec_verify_attn", "spec_verify_attn_paged",
+           "spec_verify_attn_host_lengths",
            "spec_accept_workspace_size",
            "spec_accept", "spec_draft_signals_workspace_size", "spec_draft_signals",
            "sv_workspace_status", "sv_status_string", "sv_set_attn_kernel", "sv_set_unit_ctas",
@@ -72,6 +75,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.spec_verify_attn_paged.argtypes = [ctypes.POINTER(AttnDesc), vp, vp, vp, i64, i32,
                                                vp, i32, vp, vp, vp, vp, vp, sz, vp]
         lib.spec_verify_attn_paged.restype = ctypes.c_int
+        lib.spec_verify_attn_host_lengths.argtypes = [ctypes.POINTER(AttnDesc), vp, vp, vp, vp,
+                                                      vp, vp, vp, vp, vp, vp, sz, vp]
+        lib.spec_verify_attn_host_lengths.restype = ctypes.c_int
         lib.spec_accept_workspace_size.argtypes = [i32, i32, i32]
         lib.spec_accept_workspace_size.restype = sz
         lib.spec_accept.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, sz, vp]
@@ -186,6 +192,46 @@ def spec_verify_attn(q, k_cache, v_cache, seq_lens, draft_len, *, max_draft_len:
         _ptr(draft_len), _ptr(kv_scale), _ptr(out), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, "spec_verify_attn")
+    return out
+
+
+def spec_verify_attn_host_lengths(q, k_cache, v_cache, seq_lens, draft_len, seq_lens_host,
+                                  draft_len_host, *, max_draft_len: int, max_seq_len: int,
+                                  kv_scale=None, out=None, workspace=None,
+                                  softmax_scale: float = 0.0, sliding_window: int = 0,
+                                  stream=None) -> torch.Tensor:
+    """spec_verify_attn with the lengths also in host memory (int32 CPU tensors equal to
+    seq_lens and draft_len): the work plan is made on the host and travels with the
+    attention launch."""
+    for t, n in ((seq_lens_host, "seq_lens_host"), (draft_len_host, "draft_len_host")):
+        if t.device.type != "cpu" or t.dtype != torch.int32 or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous int32 CPU tensor" % n)
+    _need(q, "q", (torch.bfloat16,))
+    _need(k_cache, "k_cache", (torch.bfloat16, torch.uint8, torch.float8_e4m3fn))
+    _need(v_cache, "v_cache", (k_cache.dtype,))
+    _need(seq_lens, "seq_lens", (torch.int32,))
+    _need(draft_len, "draft_len", (torch.int32,))
+    if kv_scale is not None:
+        _need(kv_scale, "kv_scale", (torch.float32,))
+    if q.dim() != 3 or k_cache.dim() != 3 or v_cache.shape != k_cache.shape:
+        raise ValueError("q must be [rows, Hq, d], k/v caches [kv_rows, Hkv, d]")
+    if seq_lens_host.numel() != seq_lens.numel() or draft_len_host.numel() != draft_len.numel():
+        raise ValueError("host and device length arrays differ in size")
+    desc = attn_desc(q, k_cache, seq_lens.shape[0], max_draft_len, max_seq_len, softmax_scale,
+                     sliding_window)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", (torch.bfloat16,))
+    if out.shape != q.shape:
+        raise ValueError("out must have q's shape")
+    if workspace is None:
+        workspace = new_workspace(verify_workspace_bytes(desc), q.device)
+    st = load_library().spec_verify_attn_host_lengths(
+        ctypes.byref(desc), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens),
+        _ptr(draft_len), ctypes.c_void_p(seq_lens_host.data_ptr()),
+        ctypes.c_void_p(draft_len_host.data_ptr()), _ptr(kv_scale), _ptr(out), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "spec_verify_attn_host_lengths")
     return out
 
 

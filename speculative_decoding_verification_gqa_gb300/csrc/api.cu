@@ -146,7 +146,9 @@ struct PagedArgs {
 sv_status verify_impl(const sv_attn_desc* desc, const void* q, const void* k_cache,
                       const void* v_cache, const PagedArgs& pg, const int32_t* seq_lens,
                       const int32_t* draft_len, const float* kv_scale, void* out,
-                      void* workspace, size_t workspace_bytes, void* stream) {
+                      void* workspace, size_t workspace_bytes, void* stream,
+                      const int32_t* seq_lens_host = nullptr,
+                      const int32_t* draft_len_host = nullptr) {
   sv_status st = check_desc(desc);
   if (st != SV_OK) return st;
   if (desc->batch == 0) return SV_OK;
@@ -154,6 +156,11 @@ sv_status verify_impl(const sv_attn_desc* desc, const void* q, const void* k_cac
     return SV_ERR_NULL;
   if (pg.block_size > 0 && !pg.table) return SV_ERR_NULL;
   if (pg.block_size > 0 && !aligned(pg.table, 4)) return SV_ERR_ALIGN;
+  if (seq_lens_host && draft_len_host)  // host copies of the lengths: checked here, at once
+    for (int b = 0; b < desc->batch; ++b)
+      if (seq_lens_host[b] < 0 || seq_lens_host[b] > desc->max_seq_len || draft_len_host[b] < 0 ||
+          draft_len_host[b] > desc->max_draft_len)
+        return SV_ERR_SHAPE;
   const bool fp8 = desc->kv_dtype == SV_FP8_E4M3;
   if (fp8 && !kv_scale) return SV_ERR_NULL;
   if (!fp8 && kv_scale) return SV_ERR_SHAPE;
@@ -225,9 +232,20 @@ sv_status verify_impl(const sv_attn_desc* desc, const void* q, const void* k_cac
   p.scale_log2 = scale * 1.4426950408889634f;
 
   cudaStream_t s = (cudaStream_t)stream;
-  if (launch_plan(p, kt, s) != cudaSuccess) return SV_ERR_CUDA;
+  // Host lengths: plan on the host and pass the plan with the attention launch (tcgen05
+  // kernel, packed cache), unless it does not fit a HostPlan.
+  static thread_local HostPlan hp;
+  bool host_planned = false;
+  if (seq_lens_host && draft_len_host && which == 2 && pg.block_size == 0) {
+    const sv_status hs = host_plan(p, kt, seq_lens_host, draft_len_host, &hp);
+    if (hs == SV_ERR_SHAPE) return SV_ERR_SHAPE;
+    host_planned = hs == SV_OK;
+  }
+  if (!host_planned && launch_plan(p, kt, s) != cudaSuccess) return SV_ERR_CUDA;
   if (g_ev_start && cudaEventRecord(g_ev_start, s) != cudaSuccess) return SV_ERR_CUDA;
-  const cudaError_t e = which == 2 ? launch_attn_tc(p, fp8, s) : launch_attn_mma(p, fp8, s);
+  const cudaError_t e = host_planned ? launch_attn_tc_hp(p, fp8, hp, s)
+                        : which == 2 ? launch_attn_tc(p, fp8, s)
+                                     : launch_attn_mma(p, fp8, s);
   if (e != cudaSuccess) return SV_ERR_CUDA;
   if (g_ev_stop && cudaEventRecord(g_ev_stop, s) != cudaSuccess) return SV_ERR_CUDA;
   if (launch_combine(p, s) != cudaSuccess) return SV_ERR_CUDA;
@@ -245,6 +263,21 @@ SV_API sv_status spec_verify_attn(const sv_attn_desc* desc, const void* q, const
   const PagedArgs packed = {nullptr, 0, 0, 0};
   return verify_impl(desc, q, k_cache, v_cache, packed, seq_lens, draft_len, kv_scale, out,
                      workspace, workspace_bytes, stream);
+}
+
+SV_API sv_status spec_verify_attn_host_lengths(const sv_attn_desc* desc, const void* q,
+                                               const void* k_cache, const void* v_cache,
+                                               const int32_t* seq_lens,
+                                               const int32_t* draft_len,
+                                               const int32_t* seq_lens_host,
+                                               const int32_t* draft_len_host,
+                                               const float* kv_scale, void* out,
+                                               void* workspace, size_t workspace_bytes,
+                                               void* stream) {
+  if (desc && desc->batch > 0 && (!seq_lens_host || !draft_len_host)) return SV_ERR_NULL;
+  const PagedArgs packed = {nullptr, 0, 0, 0};
+  return verify_impl(desc, q, k_cache, v_cache, packed, seq_lens, draft_len, kv_scale, out,
+                     workspace, workspace_bytes, stream, seq_lens_host, draft_len_host);
 }
 
 SV_API sv_status spec_verify_attn_paged(const sv_attn_desc* desc, const void* q,

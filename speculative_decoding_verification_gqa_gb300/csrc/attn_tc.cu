@@ -321,6 +321,32 @@ __device__ __forceinline__ void split_q_e4m3(const float* x, uint32_t& whi, uint
   wlo = l01 | (l23 << 16);
 }
 
+// Where a CTA reads the work plan: the workspace, written by the planning kernel, or a
+// HostPlan passed with the launch (kernel parameter space, read through the constant
+// cache; every read below is uniform across the threads that make it).
+struct WsPlan {
+  const AttnParams& p;
+  __device__ int num_units() const { return p.hdr->num_units; }
+  __device__ int2 cta(int c) const { return p.cta_tab[c]; }
+  __device__ int4 unit(int u) const { return p.units[u]; }
+  __device__ int32_t ubeg(int u) const { return p.ubeg[u]; }
+  __device__ int64_t q_off(int b) const { return p.q_off[b]; }
+  __device__ int64_t kv_off(int b) const { return p.kv_off[b]; }
+  __device__ int T(int b) const { return p.seq_lens[b]; }
+  __device__ int D(int b) const { return p.draft_len[b]; }
+};
+struct ParamPlan {
+  const HostPlan& h;
+  __device__ int num_units() const { return h.num_units; }
+  __device__ int2 cta(int c) const { return h.cta_tab[c]; }
+  __device__ int4 unit(int u) const { return h.units[u]; }
+  __device__ int32_t ubeg(int u) const { return h.ubeg[u]; }
+  __device__ int64_t q_off(int b) const { return h.q_off[b]; }
+  __device__ int64_t kv_off(int b) const { return h.kv_off[b]; }
+  __device__ int T(int b) const { return h.T[b]; }
+  __device__ int D(int b) const { return h.D[b]; }
+};
+
 // One unit's share of a CTA's range: the unit's tiles [j0, j1), tile j holding cache
 // positions kbase + j*KT .. (kbase: the first position of the unit's first tile, 0 without
 // a sliding window); whole when they are all of the unit's tiles.
@@ -330,18 +356,18 @@ struct Seg {
 };
 
 // Next (unit, tile range) of this CTA's contiguous range of the global tile line.
-template <bool WIN>
-__device__ __forceinline__ bool seg_next(const AttnParams& p, int num_units, int64_t& t,
+template <bool WIN, class Plan>
+__device__ __forceinline__ bool seg_next(const Plan& pl, int num_units, int64_t& t,
                                          int64_t t_end, int& u, Seg& s) {
   if (t >= t_end || u >= num_units) return false;
-  const int4 info = p.units[u];
-  const int64_t ub = p.ubeg[u];
+  const int4 info = pl.unit(u);
+  const int64_t ub = pl.ubeg(u);
   s.u = u;
   s.b = info.x;
   s.g = info.y;
   s.mt = info.z;
   s.kbase = WIN ? info.w : 0;
-  const int nt = p.ubeg[u + 1] - (int)ub;
+  const int nt = pl.ubeg(u + 1) - (int)ub;
   s.j0 = (int)(t - ub);
   s.j1 = (int)(min(t_end, ub + nt) - ub);
   if (s.j1 <= s.j0) return false;
@@ -374,10 +400,9 @@ struct TcLayout {
 
 // WIN: a sliding window is in force (p.window > 0); without it the window's lower mask
 // edge, the per-unit key base and the clearing of V rows before the window compile away.
-template <int HD, bool F8, bool WIN>
-__global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
-    attn_tc_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmk,
-                   const __grid_constant__ CUtensorMap tmv) {
+template <int HD, bool F8, bool WIN, class Plan>
+__device__ __forceinline__ void attn_tc_body(const AttnParams& p, const CUtensorMap& tmk,
+                                             const CUtensorMap& tmv, const Plan& pl) {
   using L = TcLayout<HD, F8>;
   const int window = WIN ? p.window : 0;
   extern __shared__ __align__(1024) uint8_t smem[];  // 128-byte swizzled tiles: 1 KiB aligned
@@ -387,8 +412,8 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
   pdl_trigger();
   pdl_wait();  // the plan of this call is complete
 
-  const int num_units = p.hdr->num_units;
-  const int2 rb = p.cta_tab[blockIdx.x], re = p.cta_tab[blockIdx.x + 1];
+  const int num_units = pl.num_units();
+  const int2 rb = pl.cta(blockIdx.x), re = pl.cta(blockIdx.x + 1);
   const int64_t t_begin = rb.x, t_end = re.x;  // this CTA's tiles (see the plan kernel)
   if (t_begin >= t_end) return;                // uniform across the CTA
   if (saddr(smem) & 1023) {  // the swizzle phases below assume a 1 KiB-aligned base
@@ -476,10 +501,10 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
                       &bars->v_full[st], c * 64, g, grow);
       }
     };
-    while (ok && seg_next<WIN>(p, num_units, t, t_end, u, s)) {
-      const int row0 = (int)p.kv_off[s.b] + s.kbase;
-      const int T = p.seq_lens[s.b];
-      const int nkeys = T + p.draft_len[s.b] + 1;
+    while (ok && seg_next<WIN>(pl, num_units, t, t_end, u, s)) {
+      const int row0 = (int)pl.kv_off(s.b) + s.kbase;
+      const int T = pl.T(s.b);
+      const int nkeys = T + pl.D(s.b) + 1;
       const int kvis = first_visible_key(T, window);
       const int32_t* tab = p.block_table + (size_t)s.b * p.bt_stride;
       // first cache row of box n of tile j (paged)
@@ -536,7 +561,7 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
       Seg s;
       uint32_t it = 0, seg_i = 0;
       bool ok = true;
-      while (ok && seg_next<WIN>(p, num_units, t, t_end, u, s)) {
+      while (ok && seg_next<WIN>(pl, num_units, t, t_end, u, s)) {
         if (!mbar_wait(&bars->q_full, seg_i & 1, abort, p.flags)) break;
         fence_after();
         for (int j = s.j0; j < s.j1; ++j, ++it) {
@@ -584,7 +609,7 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
       Seg s;
       uint32_t it = 0;
       bool ok = true;
-      while (ok && seg_next<WIN>(p, num_units, t, t_end, u, s)) {
+      while (ok && seg_next<WIN>(pl, num_units, t, t_end, u, s)) {
         bool first[2] = {true, true};  // each accumulator starts afresh in every unit
         for (int j = s.j0; j < s.j1; ++j, ++it) {
           const uint32_t st = F8 ? it % NCV : it % L::NR;
@@ -634,10 +659,10 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
     Seg s;
     uint32_t it = 0;
     bool ok = true;
-    while (ok && seg_next<WIN>(p, num_units, t, t_end, u, s)) {
+    while (ok && seg_next<WIN>(pl, num_units, t, t_end, u, s)) {
       // cache positions below are relative to the unit's first tile (kbase)
-      const int T = p.seq_lens[s.b] - s.kbase;
-      const int D = p.draft_len[s.b];
+      const int T = pl.T(s.b) - s.kbase;
+      const int D = pl.D(s.b);
       const int rows_total = p.G * (D + 1);
       const int rows = min(MT, rows_total - s.mt * MT);
       const int nkeys = T + D + 1;
@@ -646,7 +671,7 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
       const int i_row = live ? rg / p.G : D;
       const int hi_row = T + i_row;  // the row's last visible key
       const int hl = live ? rg % p.G : 0;
-      const int64_t qrow = p.q_off[s.b] + i_row;
+      const int64_t qrow = pl.q_off(s.b) + i_row;
       float sc = p.scale_log2;  // score scale in log2 units
       const float vs = F8 ? p.kv_scale[p.Hkv + s.g] : 1.f;
       const uint4* qsrc = reinterpret_cast<const uint4*>(
@@ -866,7 +891,7 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
         if (live) {
           if (whole) {
             __nv_bfloat16* dst = (__nv_bfloat16*)p.out +
-                                 ((p.q_off[s.b] + i_row) * p.Hq + (int64_t)s.g * p.G + hl) * HD +
+                                 ((pl.q_off(s.b) + i_row) * p.Hq + (int64_t)s.g * p.G + hl) * HD +
                                  wg * OC + c * 16;
             uint32_t pk[8];
 #pragma unroll
@@ -915,10 +940,10 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
       Seg s;
       uint32_t it = 0;
       bool ok = true;
-      while (ok && seg_next<WIN>(p, num_units, t, t_end, u, s)) {
+      while (ok && seg_next<WIN>(pl, num_units, t, t_end, u, s)) {
         // cache positions relative to the unit's first tile
-        const int T = p.seq_lens[s.b] - s.kbase;
-        const int nkeys = T + p.draft_len[s.b] + 1;
+        const int T = pl.T(s.b) - s.kbase;
+        const int nkeys = T + pl.D(s.b) + 1;
         const int kvis = WIN ? T + 1 - window : -1;
         for (int j = s.j0; j < s.j1; ++j, ++it) {
           const uint32_t rs = it % L::NR, cs = it % NCV;
@@ -967,6 +992,37 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
                  "r"(TMEM_COLS)
                  : "memory");
   }
+}
+
+// Device-planned launch: the plan in the workspace, written by the planning kernel.
+template <int HD, bool F8, bool WIN>
+__global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
+    attn_tc_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmk,
+                   const __grid_constant__ CUtensorMap tmv) {
+  attn_tc_body<HD, F8, WIN>(p, tmk, tmv, WsPlan{p});
+}
+
+// Host-planned launch: the plan travels with the launch. CTA 0 also copies what the
+// combine kernel reads (unit list, unit starts, query offsets, counts) into the workspace.
+template <int HD, bool F8, bool WIN>
+__global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
+    attn_tc_kernel_hp(const AttnParams p, const __grid_constant__ CUtensorMap tmk,
+                      const __grid_constant__ CUtensorMap tmv,
+                      const __grid_constant__ HostPlan hp) {
+  if (blockIdx.x == 0) {
+    pdl_wait();  // the previous call's combine has read the workspace
+    for (int u = threadIdx.x; u <= hp.num_units; u += blockDim.x) {
+      if (u < hp.num_units) p.units[u] = hp.units[u];
+      p.ubeg[u] = hp.ubeg[u];
+    }
+    for (int b = threadIdx.x; b <= p.B; b += blockDim.x) p.q_off[b] = hp.q_off[b];
+    if (threadIdx.x == 0) {
+      p.hdr->num_units = hp.num_units;
+      p.hdr->total_tiles = hp.total_tiles;
+      p.hdr->unit_ctas = hp.unit_ctas;
+    }
+  }
+  attn_tc_body<HD, F8, WIN>(p, tmk, tmv, ParamPlan{hp});
 }
 
 // ---------------------------------------------------------------- host side
@@ -1034,12 +1090,41 @@ cudaError_t launch_hd(const AttnParams& p, cudaStream_t s) {
   return p.window > 0 ? launch_hd<HD, F8, true>(p, s) : launch_hd<HD, F8, false>(p, s);
 }
 
+template <int HD, bool F8, bool WIN>
+cudaError_t launch_hd_hp(const AttnParams& p, const HostPlan& hp, cudaStream_t s) {
+  using L = TcLayout<HD, F8>;
+  CUtensorMap mk, mv;
+  if (!make_kv_map(&mk, p.k, p.kv_rows, p.Hkv, HD, F8, KT) ||
+      !make_kv_map(&mv, p.v, p.kv_rows, p.Hkv, HD, F8, KT))
+    return cudaErrorInvalidValue;
+  auto kernel = attn_tc_kernel_hp<HD, F8, WIN>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::SMEM);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(kernel, dim3(p.n_ctas), dim3(L::THREADS), L::SMEM, s, p, mk, mv, hp);
+}
+
+template <int HD, bool F8>
+cudaError_t launch_hd_hp(const AttnParams& p, const HostPlan& hp, cudaStream_t s) {
+  return p.window > 0 ? launch_hd_hp<HD, F8, true>(p, hp, s)
+                      : launch_hd_hp<HD, F8, false>(p, hp, s);
+}
+
 }  // namespace
 
 bool attn_tc_available() { return encode_fn() != nullptr; }
 int attn_tc_kt() { return KT; }
 
 bool attn_tc_supports(int head_dim, bool fp8) { return head_dim == 128 || !fp8; }
+
+cudaError_t launch_attn_tc_hp(const AttnParams& p, bool fp8, const HostPlan& hp,
+                              cudaStream_t s) {
+  if (!attn_tc_supports(p.d, fp8) || p.kv_rows <= 0 || p.kv_rows > 0x7fffffffLL ||
+      p.block_size != 0)
+    return cudaErrorNotSupported;
+  if (fp8) return launch_hd_hp<128, true>(p, hp, s);
+  return p.d == 128 ? launch_hd_hp<128, false>(p, hp, s) : launch_hd_hp<64, false>(p, hp, s);
+}
 
 cudaError_t launch_attn_tc(const AttnParams& p, bool fp8, cudaStream_t s) {
   if (!attn_tc_supports(p.d, fp8) || p.kv_rows <= 0 || p.kv_rows > 0x7fffffffLL)

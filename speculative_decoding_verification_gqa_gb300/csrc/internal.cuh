@@ -186,6 +186,27 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// A work plan computed on the host from host copies of the lengths, passed by value with
+// the attention launch (a kernel parameter, read through the constant cache), so that no
+// planning kernel runs. The same plan as the planning kernel's: unit list and starts,
+// offsets, the unit-to-CTA policy and each CTA's range.
+constexpr int HP_MAX_B = 256;   // sequences
+constexpr int HP_MAX_U = 640;   // units
+constexpr int HP_MAX_C = 192;   // CTAs
+struct HostPlan {
+  int32_t num_units, total_tiles, unit_ctas, pad;
+  int32_t T[HP_MAX_B], D[HP_MAX_B];
+  int64_t q_off[HP_MAX_B + 1], kv_off[HP_MAX_B + 1];
+  int4 units[HP_MAX_U];
+  int32_t ubeg[HP_MAX_U + 1];
+  int2 cta_tab[HP_MAX_C + 1];
+};
+// Fills `hp` for the call `p` (kt: the attention kernel's tile) from host lengths T[B],
+// D[B]. Returns SV_OK, SV_ERR_SHAPE for lengths out of range or packed sizes beyond the
+// buffers, or SV_ERR_WORKSPACE when the plan does not fit a HostPlan.
+sv_status host_plan(const AttnParams& p, int kt, const int32_t* T, const int32_t* D,
+                    HostPlan* hp);
+
 // Launchers (each returns the cudaGetLastError() of its launch).
 cudaError_t launch_plan(const AttnParams& p, int kt, cudaStream_t s);
 cudaError_t launch_combine(const AttnParams& p, cudaStream_t s);
@@ -195,6 +216,7 @@ bool attn_tc_available();
 bool attn_tc_supports(int head_dim, bool fp8);
 int attn_tc_kt();
 cudaError_t launch_attn_tc(const AttnParams& p, bool fp8, cudaStream_t s);
+cudaError_t launch_attn_tc_hp(const AttnParams& p, bool fp8, const HostPlan& hp, cudaStream_t s);
 
 // Acceptance.
 struct AcceptWs {

@@ -10,6 +10,8 @@
 //          of across tiles (log2 units: the scores were pre-multiplied by log2(e)).
 #include <cuda_bf16.h>
 
+#include <algorithm>
+
 #include "internal.cuh"
 
 namespace sv {
@@ -238,6 +240,104 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(AttnParams p, int kt
     }
     p.cta_tab[c] = e;
   }
+}
+
+sv_status host_plan(const AttnParams& p, int kt, const int32_t* Tv, const int32_t* Dv,
+                    HostPlan* hp) {
+  // the steps of plan_kernel, one sequence after another
+  if (p.B > HP_MAX_B || p.n_ctas > HP_MAX_C) return SV_ERR_WORKSPACE;
+  int64_t sum_w = 0, sum_kv = 0, U = 0, TT = 0;
+  int maxt = 0, nmt_lo = 0x7fffffff, nmt_hi = 0;
+  for (int b = 0; b < p.B; ++b) {
+    const int T = Tv[b], D = Dv[b];
+    if (T < 0 || T > p.max_seq || D < 0 || D > p.max_draft) return SV_ERR_SHAPE;
+    const int w = 1 + D;
+    const int nmt = (p.G * w + MT - 1) / MT;
+    const int nt = (int)(((int64_t)T + w + kt - 1) / kt);
+    hp->T[b] = T;
+    hp->D[b] = D;
+    hp->q_off[b] = sum_w;
+    hp->kv_off[b] = sum_kv;
+    sum_w += w;
+    sum_kv += (int64_t)T + w;
+    U += (int64_t)p.Hkv * nmt;
+    maxt = std::max(maxt, nt - unit_first_tile(T, 0, p.G, p.window, kt));
+    nmt_lo = std::min(nmt_lo, nmt);
+    nmt_hi = std::max(nmt_hi, nmt);
+  }
+  hp->q_off[p.B] = sum_w;
+  hp->kv_off[p.B] = sum_kv;
+  if (sum_w > p.q_rows || sum_kv > p.kv_rows || U > p.max_units) return SV_ERR_SHAPE;
+  if (U > HP_MAX_U) return SV_ERR_WORKSPACE;
+  // units and their starts on the tile line: by sequence, KV head, row tile; row-tile-major
+  // when every sequence has the same number (> 1) of row tiles
+  const bool by_slice = p.B > 0 && nmt_hi > 1 && nmt_lo == nmt_hi;
+  int64_t u = 0;
+  auto add_unit = [&](int b, int g, int mt) {
+    const int T = hp->T[b];
+    const int nt = (int)(((int64_t)T + hp->D[b] + kt) / kt);
+    const int kb = unit_first_tile(T, mt, p.G, p.window, kt);
+    hp->units[u] = make_int4(b, g, mt, kb * kt);
+    hp->ubeg[u] = (int32_t)TT;
+    TT += nt - kb;
+    ++u;
+  };
+  if (by_slice) {
+    for (int mt = 0; mt < nmt_hi; ++mt)
+      for (int b = 0; b < p.B; ++b)
+        for (int g = 0; g < p.Hkv; ++g) add_unit(b, g, mt);
+  } else {
+    for (int b = 0; b < p.B; ++b) {
+      const int nmt = (p.G * (1 + hp->D[b]) + MT - 1) / MT;
+      for (int g = 0; g < p.Hkv; ++g)
+        for (int mt = 0; mt < nmt; ++mt) add_unit(b, g, mt);
+    }
+  }
+  if (TT >= (int64_t)0x7fffffff) return SV_ERR_SHAPE;
+  hp->ubeg[U] = (int32_t)TT;
+  hp->num_units = (int32_t)U;
+  hp->total_tiles = (int32_t)TT;
+  // the unit-to-CTA policy (the same model and arithmetic as plan_kernel)
+  const int64_t C = p.n_ctas;
+  int k = 0;
+  if (U > 0 && U <= C) {
+    if (p.unit_ctas_mode > 0) {
+      k = (int)std::min((int64_t)p.unit_ctas_mode, C / U);
+    } else if (p.unit_ctas_mode < 0 && p.tile_floor > 0) {
+      const double f = p.tile_floor;
+      double best = (double)(TT + U * p.switch_tiles) / C * fmax(f, (double)C);
+      for (int kk = 1; kk <= C / U; ++kk) {
+        const double t = (double)((maxt + kk - 1) / kk) * fmax(f, (double)(U * kk));
+        if (t < best) {
+          best = t;
+          k = kk;
+        }
+      }
+    }
+  }
+  hp->unit_ctas = k;
+  for (int c = 0; c <= C; ++c) {
+    int2 e = make_int2((int32_t)TT, (int32_t)U);
+    if (k > 0) {
+      if (c < U * k) {
+        const int uu = c / k, i = c % k;
+        const int32_t n = hp->ubeg[uu + 1] - hp->ubeg[uu];
+        e = make_int2(hp->ubeg[uu] + (int32_t)((int64_t)n * i / k), uu);
+      }
+    } else if (c < C && TT > 0) {
+      const int64_t X = p.switch_tiles, VT = TT + U * X;
+      const int64_t v0 = (int64_t)c * VT / C;
+      int lo = 0, hi = (int)U - 1;  // last unit whose virtual start ubeg[u] + u*X is <= v0
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (hp->ubeg[mid] + (int64_t)mid * X <= v0) lo = mid; else hi = mid - 1;
+      }
+      const int64_t into = v0 - (hp->ubeg[lo] + (int64_t)lo * X) - X;
+      e = make_int2((int32_t)(hp->ubeg[lo] + (into > 0 ? into : 0)), lo);
+    }
+    hp->cta_tab[c] = e;
+  }
+  return SV_OK;
 }
 
 cudaError_t launch_plan(const AttnParams& p, int kt, cudaStream_t s) {
