@@ -260,6 +260,55 @@ SV_API sv_status spec_draft_signals(int32_t rows, int32_t vocab, int32_t logits_
                                     const void* logits, float* confidence, float* entropy,
                                     void* workspace, size_t workspace_bytes, void* stream);
 
+/* Work plan of one attention call (sv_plan_preview). */
+typedef struct {
+  int32_t num_units;    /* U: units = (sequence, KV head, row tile of <= 128 query rows) */
+  int32_t total_tiles;  /* TT: key tiles of all units, laid end to end on one tile line */
+  int32_t tile_keys;    /* KT: cache positions per key tile */
+  int32_t num_ctas;     /* C: persistent attention CTAs */
+  int32_t unit_ctas;    /* k >= 1: CTA u*k + i takes the i-th of k equal parts of unit u's
+                           tiles; 0: CTA c takes a contiguous range of the tile line, ranges
+                           balanced with `switch_tiles` charged for each unit started */
+  int32_t switch_tiles; /* tiles' worth of time charged for starting a unit */
+} sv_plan_info;
+
+/*
+ * sv_plan_preview -- the work plan that spec_verify_attn (or the _paged or _host_lengths
+ * call) makes for the given lengths, computed on the host; needs no device. For capacity
+ * planning, tuning and tests. Units are ordered by sequence, KV head, row tile, except
+ * that when every sequence has the same number (> 1) of row tiles they are ordered
+ * row-tile-major. A unit's tiles start at the tile holding the first key its rows see
+ * (position 0, or under a sliding window of W positions max(0, T_b + i - W + 1) for its
+ * first window row i) and end at the tile holding T_b + D_b. The unit-to-CTA policy
+ * follows sv_set_unit_ctas, as the call does.
+ *
+ *   desc          as for the call (q_rows and, for a packed cache, kv_rows are checked)
+ *   block_size    0 for a packed cache, else the paged cache's block size (the block
+ *                 table itself is not checked)
+ *   seq_lens_host, draft_len_host  int32 [B] in host memory
+ *   num_sms       SMs of the device the call would run on, 1 .. 192
+ *   attn_kernel   1 = mma.sync kernel, 2 = tcgen05 kernel (the kernel sets KT and the
+ *                 policy's time model; automatic selection takes 2 for d = 128, and
+ *                 for d = 64 with bf16 K/V)
+ *   info          out: the counts above
+ *   units         out or NULL: int32 [capacity_units][4] = (b, KV head, row tile, first
+ *                 cache position of the unit's first tile), in tile-line order
+ *   unit_begin    out or NULL: int32 [capacity_units + 1]; unit u holds tiles
+ *                 unit_begin[u] .. unit_begin[u + 1] - 1 of the line
+ *   cta_begin     out or NULL: int32 [num_ctas + 1][2] = (first tile, its unit) of each
+ *                 CTA's range; entry num_ctas is (TT, U). A CTA's range ends where the
+ *                 next one's begins.
+ * Returns SV_ERR_SHAPE for a length or size out of range (as the calls would report),
+ * SV_ERR_WORKSPACE when units or unit_begin is given and U > capacity_units (info is
+ * filled), or when the plan is beyond the host plan's capacity (256 sequences, 640
+ * units, 192 CTAs).
+ */
+SV_API sv_status sv_plan_preview(const sv_attn_desc* desc, int32_t block_size,
+                                 const int32_t* seq_lens_host, const int32_t* draft_len_host,
+                                 int32_t num_sms, int32_t attn_kernel, sv_plan_info* info,
+                                 int32_t* units, int32_t* unit_begin, int32_t* cta_begin,
+                                 int32_t capacity_units);
+
 /* Synchronises `stream`, then reads the sticky device-side flags of a workspace used by
  * either call: SV_OK, SV_ERR_DEVICE_SHAPE or SV_ERR_TIMEOUT. clear != 0 resets them. */
 SV_API sv_status sv_workspace_status(void* workspace, int clear, void* stream);

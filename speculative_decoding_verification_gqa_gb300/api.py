@@ -33,13 +33,19 @@ EXPORTS = ("spec_verify_attn_workspace_size", "spec_verify_attn", "spec_verify_a
            "spec_accept_workspace_size",
            "spec_accept", "spec_draft_signals_workspace_size", "spec_draft_signals",
            "sv_workspace_status", "sv_status_string", "sv_set_attn_kernel", "sv_set_unit_ctas",
-           "sv_set_profile_events", "sv_version")
+           "sv_set_profile_events", "sv_version", "sv_plan_preview")
 
 
 class SpecVerifyError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
         super().__init__("%s failed: %s (%d)" % (where, STATUS.get(status, "?"), status))
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [("num_units", ctypes.c_int32), ("total_tiles", ctypes.c_int32),
+                ("tile_keys", ctypes.c_int32), ("num_ctas", ctypes.c_int32),
+                ("unit_ctas", ctypes.c_int32), ("switch_tiles", ctypes.c_int32)]
 
 
 class AttnDesc(ctypes.Structure):
@@ -97,6 +103,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.sv_set_profile_events.argtypes = [vp, vp]
         lib.sv_set_profile_events.restype = None
         lib.sv_version.restype = ctypes.c_int
+        lib.sv_plan_preview.argtypes = [ctypes.POINTER(AttnDesc), i32, vp, vp, i32, i32,
+                                        ctypes.POINTER(PlanInfo), vp, vp, vp, i32]
+        lib.sv_plan_preview.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -355,6 +364,36 @@ def set_profile_events(start=None, stop=None):
     else:
         lib.sv_set_profile_events(ctypes.c_void_p(start.cuda_event),
                                   ctypes.c_void_p(stop.cuda_event))
+
+
+def plan_preview(desc: AttnDesc, seq_lens, draft_len, *, num_sms: int, attn_kernel: int = 2,
+                 block_size: int = 0) -> dict:
+    """The work plan a verify-attention call with these host lengths (int sequences) makes
+    on a device of ``num_sms`` SMs, computed on the host by the library. Returns a dict:
+    the sv_plan_info counts, ``units`` int32 [U, 4] (b, KV head, row tile, first cache
+    position of the unit's first tile), ``unit_begin`` int32 [U + 1] and ``cta_begin``
+    int32 [C + 1, 2] (first tile, its unit)."""
+    import numpy as np
+    T = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    D = np.ascontiguousarray(draft_len, dtype=np.int32)
+    if T.shape != (desc.batch,) or D.shape != (desc.batch,):
+        raise ValueError("seq_lens and draft_len must hold desc.batch lengths")
+    lib = load_library()
+    info = PlanInfo()
+    st = lib.sv_plan_preview(ctypes.byref(desc), block_size, T.ctypes.data, D.ctypes.data,
+                             num_sms, attn_kernel, ctypes.byref(info), None, None, None, 0)
+    _check(st, "sv_plan_preview")
+    U, C = info.num_units, info.num_ctas
+    units = np.zeros((max(U, 1), 4), dtype=np.int32)
+    ubeg = np.zeros(U + 1, dtype=np.int32)
+    cta = np.zeros((C + 1, 2), dtype=np.int32)
+    st = lib.sv_plan_preview(ctypes.byref(desc), block_size, T.ctypes.data, D.ctypes.data,
+                             num_sms, attn_kernel, ctypes.byref(info), units.ctypes.data,
+                             ubeg.ctypes.data, cta.ctypes.data, U)
+    _check(st, "sv_plan_preview")
+    out = {name: getattr(info, name) for name, _ in PlanInfo._fields_}
+    out.update(units=units[:U], unit_begin=ubeg, cta_begin=cta)
+    return out
 
 
 def default_scale(head_dim: int) -> float:

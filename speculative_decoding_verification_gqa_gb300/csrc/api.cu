@@ -83,7 +83,7 @@ int pick_kernel(const sv_attn_desc* d) {
 
 extern "C" {
 
-SV_API int sv_version(void) { return 200; }  // 0.2.0: paged K/V, sliding window, unit policies
+SV_API int sv_version(void) { return 300; }  // 0.3.0: plan preview
 
 SV_API const char* sv_status_string(sv_status s) {
   switch (s) {
@@ -143,6 +143,50 @@ struct PagedArgs {
   int64_t num_blocks;
 };
 
+// The sizes, limits and work-distribution policy of one attention call on `sms` SMs with
+// kernel `which` (1 mma.sync, 2 tcgen05); every pointer is left null.
+AttnParams shape_params(const sv_attn_desc* desc, const PagedArgs& pg, int which, int sms) {
+  const bool fp8 = desc->kv_dtype == SV_FP8_E4M3;
+  const int kt = which == 2 ? attn_tc_kt() : attn_mma_kt();
+  const int G = desc->num_q_heads / desc->num_kv_heads;
+  const int64_t rows_per_kv = (int64_t)G * (1 + desc->max_draft_len);
+  const int64_t max_tiles = (int64_t)desc->batch * desc->num_kv_heads * ((rows_per_kv + MT - 1) / MT) *
+                            ((desc->max_seq_len + 1 + desc->max_draft_len + kt - 1) / kt);
+  AttnParams p = {};
+  p.B = desc->batch;
+  p.Hq = desc->num_q_heads;
+  p.Hkv = desc->num_kv_heads;
+  p.G = G;
+  p.d = desc->head_dim;
+  p.max_draft = desc->max_draft_len;
+  p.max_seq = desc->max_seq_len;
+  // a window covering every position of the longest sequence is no window
+  p.window = (int64_t)desc->sliding_window > (int64_t)desc->max_seq_len + desc->max_draft_len
+                 ? 0
+                 : desc->sliding_window;
+  p.q_rows = desc->q_rows;
+  p.kv_rows = pg.block_size > 0 ? pg.num_blocks * pg.block_size : desc->kv_rows;
+  p.bt_stride = pg.stride;
+  p.block_size = pg.block_size;
+  p.bs_log2 = 0;
+  while (pg.block_size > 0 && (1 << p.bs_log2) < pg.block_size) ++p.bs_log2;
+  p.num_blocks = pg.num_blocks;
+  p.max_units = max_units_for(p.B, p.Hkv, G, p.max_draft);
+  p.n_ctas = (int)(max_tiles < sms ? (max_tiles > 0 ? max_tiles : 1) : sms);
+  // measured cost of starting a unit inside a CTA's range, in tiles of that kernel
+  p.switch_tiles = which == 2 ? (fp8 ? SWITCH_TILES_TC_FP8 : SWITCH_TILES_TC_BF16) : SWITCH_TILES_MMA;
+  // A paged tile of blocks shorter than a tile is several TMA boxes and lookups, which
+  // caps one CTA's rate (about 1.85 us per bf16 tile with 16-position blocks against
+  // 1.42 us packed): such calls spread over every CTA, on the split tile line.
+  const bool small_blocks = pg.block_size > 0 && pg.block_size < kt;
+  p.tile_floor = which == 2 && !small_blocks ? (fp8 ? SV_TILE_FLOOR_F8 : SV_TILE_FLOOR_BF16) : 0;
+  p.unit_ctas_mode = g_unit_ctas;
+  const float scale = desc->softmax_scale > 0.f ? desc->softmax_scale
+                                                : 1.f / sqrtf((float)desc->head_dim);
+  p.scale_log2 = scale * 1.4426950408889634f;
+  return p;
+}
+
 sv_status verify_impl(const sv_attn_desc* desc, const void* q, const void* k_cache,
                       const void* v_cache, const PagedArgs& pg, const int32_t* seq_lens,
                       const int32_t* draft_len, const float* kv_scale, void* out,
@@ -175,13 +219,8 @@ sv_status verify_impl(const sv_attn_desc* desc, const void* q, const void* k_cac
 
   const int which = pick_kernel(desc);
   const int kt = which == 2 ? attn_tc_kt() : attn_mma_kt();
-  const int G = desc->num_q_heads / desc->num_kv_heads;
-  const int64_t rows_per_kv = (int64_t)G * (1 + desc->max_draft_len);
-  const int64_t max_tiles = (int64_t)desc->batch * desc->num_kv_heads * ((rows_per_kv + MT - 1) / MT) *
-                            ((desc->max_seq_len + 1 + desc->max_draft_len + kt - 1) / kt);
-
+  AttnParams p = shape_params(desc, pg, which, sms);
   uint8_t* ws = (uint8_t*)workspace;
-  AttnParams p;
   p.q = q;
   p.k = k_cache;
   p.v = v_cache;
@@ -198,38 +237,7 @@ sv_status verify_impl(const sv_attn_desc* desc, const void* q, const void* k_cac
   p.cta_tab = (int2*)(ws + lay.cta_tab);
   p.part_o = (float*)(ws + lay.part_o);
   p.part_ml = (float2*)(ws + lay.part_ml);
-  p.B = desc->batch;
-  p.Hq = desc->num_q_heads;
-  p.Hkv = desc->num_kv_heads;
-  p.G = G;
-  p.d = desc->head_dim;
-  p.max_draft = desc->max_draft_len;
-  p.max_seq = desc->max_seq_len;
-  // a window covering every position of the longest sequence is no window
-  p.window = (int64_t)desc->sliding_window > (int64_t)desc->max_seq_len + desc->max_draft_len
-                 ? 0
-                 : desc->sliding_window;
-  p.q_rows = desc->q_rows;
-  p.kv_rows = pg.block_size > 0 ? pg.num_blocks * pg.block_size : desc->kv_rows;
   p.block_table = pg.table;
-  p.bt_stride = pg.stride;
-  p.block_size = pg.block_size;
-  p.bs_log2 = 0;
-  while (pg.block_size > 0 && (1 << p.bs_log2) < pg.block_size) ++p.bs_log2;
-  p.num_blocks = pg.num_blocks;
-  p.max_units = max_units_for(p.B, p.Hkv, G, p.max_draft);
-  p.n_ctas = (int)(max_tiles < sms ? (max_tiles > 0 ? max_tiles : 1) : sms);
-  // measured cost of starting a unit inside a CTA's range, in tiles of that kernel
-  p.switch_tiles = which == 2 ? (fp8 ? SWITCH_TILES_TC_FP8 : SWITCH_TILES_TC_BF16) : SWITCH_TILES_MMA;
-  // A paged tile of blocks shorter than a tile is several TMA boxes and lookups, which
-  // caps one CTA's rate (about 1.85 us per bf16 tile with 16-position blocks against
-  // 1.42 us packed): such calls spread over every CTA, on the split tile line.
-  const bool small_blocks = pg.block_size > 0 && pg.block_size < kt;
-  p.tile_floor = which == 2 && !small_blocks ? (fp8 ? SV_TILE_FLOOR_F8 : SV_TILE_FLOOR_BF16) : 0;
-  p.unit_ctas_mode = g_unit_ctas;
-  const float scale = desc->softmax_scale > 0.f ? desc->softmax_scale
-                                                : 1.f / sqrtf((float)desc->head_dim);
-  p.scale_log2 = scale * 1.4426950408889634f;
 
   cudaStream_t s = (cudaStream_t)stream;
   // Host lengths: plan on the host and pass the plan with the attention launch (tcgen05
@@ -293,6 +301,49 @@ SV_API sv_status spec_verify_attn_paged(const sv_attn_desc* desc, const void* q,
   const PagedArgs pg = {block_table, max_blocks_per_seq, block_size, num_blocks};
   return verify_impl(desc, q, k_pages, v_pages, pg, seq_lens, draft_len, kv_scale, out,
                      workspace, workspace_bytes, stream);
+}
+
+SV_API sv_status sv_plan_preview(const sv_attn_desc* desc, int32_t block_size,
+                                 const int32_t* seq_lens_host, const int32_t* draft_len_host,
+                                 int32_t num_sms, int32_t attn_kernel, sv_plan_info* info,
+                                 int32_t* units, int32_t* unit_begin, int32_t* cta_begin,
+                                 int32_t capacity_units) {
+  sv_status st = check_desc(desc);
+  if (st != SV_OK) return st;
+  if (!info) return SV_ERR_NULL;
+  if (desc->batch > 0 && (!seq_lens_host || !draft_len_host)) return SV_ERR_NULL;
+  if (num_sms < 1 || capacity_units < 0 || (attn_kernel != 1 && attn_kernel != 2) ||
+      (block_size != 0 &&
+       (block_size < 8 || block_size > (1 << 16) || (block_size & (block_size - 1)) != 0)))
+    return SV_ERR_SHAPE;
+  if (attn_kernel == 2 && !attn_tc_supports(desc->head_dim, desc->kv_dtype == SV_FP8_E4M3))
+    return SV_ERR_SHAPE;
+  // a paged pool's size does not enter the plan: the largest pool the limits allow
+  const PagedArgs pg = {nullptr, 1 << 30, block_size,
+                        block_size > 0 ? MAX_KV_ROWS / block_size : 0};
+  const AttnParams p = shape_params(desc, pg, attn_kernel, num_sms);
+  const int kt = attn_kernel == 2 ? attn_tc_kt() : attn_mma_kt();
+  *info = sv_plan_info{0, 0, kt, p.n_ctas, 0, p.switch_tiles};
+  if (desc->batch == 0) return SV_OK;
+  static thread_local HostPlan hp;
+  st = host_plan(p, kt, seq_lens_host, draft_len_host, &hp);
+  if (st != SV_OK) return st;
+  info->num_units = hp.num_units;
+  info->total_tiles = hp.total_tiles;
+  info->unit_ctas = hp.unit_ctas;
+  if ((units || unit_begin) && hp.num_units > capacity_units) return SV_ERR_WORKSPACE;
+  for (int u = 0; units && u < hp.num_units; ++u) {
+    units[4 * u] = hp.units[u].x;
+    units[4 * u + 1] = hp.units[u].y;
+    units[4 * u + 2] = hp.units[u].z;
+    units[4 * u + 3] = hp.units[u].w;
+  }
+  for (int u = 0; unit_begin && u <= hp.num_units; ++u) unit_begin[u] = hp.ubeg[u];
+  for (int c = 0; cta_begin && c <= p.n_ctas; ++c) {
+    cta_begin[2 * c] = hp.cta_tab[c].x;
+    cta_begin[2 * c + 1] = hp.cta_tab[c].y;
+  }
+  return SV_OK;
 }
 
 SV_API size_t spec_accept_workspace_size(int32_t batch, int32_t max_draft_len, int32_t vocab) {

@@ -267,7 +267,8 @@ sv_status host_plan(const AttnParams& p, int kt, const int32_t* Tv, const int32_
   }
   hp->q_off[p.B] = sum_w;
   hp->kv_off[p.B] = sum_kv;
-  if (sum_w > p.q_rows || sum_kv > p.kv_rows || U > p.max_units) return SV_ERR_SHAPE;
+  if (sum_w > p.q_rows || (p.block_size == 0 && sum_kv > p.kv_rows) || U > p.max_units)
+    return SV_ERR_SHAPE;
   if (U > HP_MAX_U) return SV_ERR_WORKSPACE;
   // units and their starts on the tile line: by sequence, KV head, row tile; row-tile-major
   // when every sequence has the same number (> 1) of row tiles

@@ -111,24 +111,26 @@ def test_no_device_means_no_workspace_size(lib):
     assert lib.spec_accept_workspace_size(2, 3, 100) == 0
 
 
-def test_descriptor_layout_matches_the_header(tmp_path):
-    """The ctypes mirror of sv_attn_desc has the C struct's size and field offsets (a C
-    program compiled against include/specverify.h prints them)."""
+@pytest.mark.parametrize("ctype,cname", [(api.AttnDesc, "sv_attn_desc"),
+                                          (api.PlanInfo, "sv_plan_info")])
+def test_struct_layouts_match_the_header(tmp_path, ctype, cname):
+    """The ctypes mirrors of the header's structs have the C structs' sizes and field
+    offsets (a C program compiled against include/specverify.h prints them)."""
     import subprocess
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    fields = [f for f, _ in api.AttnDesc._fields_]
+    fields = [f for f, _ in ctype._fields_]
     src = tmp_path / "layout.c"
     src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "specverify.h"\n'
-                   'int main(void) {\n  printf("%zu", sizeof(sv_attn_desc));\n' +
-                   "".join('  printf(" %%zu", offsetof(sv_attn_desc, %s));\n' % f for f in fields) +
+                   'int main(void) {\n  printf("%%zu", sizeof(%s));\n' % cname +
+                   "".join('  printf(" %%zu", offsetof(%s, %s));\n' % (cname, f) for f in fields) +
                    "  return 0;\n}\n")
     exe = tmp_path / "layout"
     subprocess.run(["gcc", "-I", os.path.join(root, "include"), "-o", str(exe), str(src)],
                    check=True)
     got = [int(x) for x in subprocess.run([str(exe)], check=True, capture_output=True,
                                           text=True).stdout.split()]
-    assert got[0] == ctypes.sizeof(api.AttnDesc)
-    assert got[1:] == [getattr(api.AttnDesc, f).offset for f in fields]
+    assert got[0] == ctypes.sizeof(ctype)
+    assert got[1:] == [getattr(ctype, f).offset for f in fields]
 
 
 def _paged(lib, desc, nb=64, bs=16, table=FAKE, mb=8, **ptrs):
