@@ -477,6 +477,38 @@ def run_ours(args):
     signals_ms = float(np.median([e[0].elapsed_time(e[1]) for e in es]))
     logits_bytes = d["logits"].numel() * d["logits"].element_size()
 
+    # The two logits scans beside torch's own row reductions over the same logits, each
+    # call after L2 is evicted (a buffer twice L2's size read), as a yardstick for a
+    # one-shot read of this size (not part of the step)
+    flush_l = torch.ones(int(2 * L2_BYTES) // 4, dtype=torch.float32, device=dev)
+    sink_l = torch.empty((), dtype=torch.float32, device=dev)
+    scans = {
+        "spec_accept": lambda: sv.spec_accept(d["logits"], d["draft"], d["D"], max_draft_len=md,
+                                              accept_len=al, next_token=nt, workspace=ws_acc,
+                                              stream=stream),
+        "spec_draft_signals": lambda: sv.spec_draft_signals(d["logits"], confidence=sig_c,
+                                                            entropy=sig_e, workspace=ws_sig,
+                                                            stream=stream),
+        "torch_argmax_dim1": lambda: torch.argmax(d["logits"], dim=1),
+        "torch_amax_dim1": lambda: torch.amax(d["logits"], dim=1),
+    }
+    logits_scan = {}
+    for name, fn in scans.items():
+        fn()
+        ec = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K3)]
+        for i in range(K3):
+            sink_l.copy_(flush_l.sum())
+            ec[i][0].record(stream)
+            fn()
+            ec[i][1].record(stream)
+        torch.cuda.synchronize()
+        logits_scan[name + "_us"] = round(
+            1e3 * float(np.median([a_.elapsed_time(b_) for a_, b_ in ec])), 2)
+    logits_scan["bytes"] = logits_bytes
+    logits_scan["note"] = ("each call after L2 is evicted; torch's reductions read the same "
+                           "logits; not part of the step")
+    del flush_l
+
     # sliding-window verify attention on the same inputs (not part of the step)
     side_win = None
     if args.side_window > 0:
@@ -664,6 +696,16 @@ def run_ours(args):
                              % (r["rows"], 100 * r["f_attn"], r["seqs_acc"], 100 * r["f_acc"],
                                 r["seconds"], r["t_step"])}
         W = D.astype(np.int64) + 1
+        try:  # the attention call's work plan, as the library makes it for these lengths
+            pl = sv.plan_preview(sv.api.attn_desc(d["q"], d["k"], w.B, md, ms), T, D,
+                                 num_sms=torch.cuda.get_device_properties(dev).multi_processor_count,
+                                 attn_kernel=2 if attn_kernel == "tcgen05" else 1)
+            attn_plan = {"units": pl["num_units"], "tiles": pl["total_tiles"],
+                         "ctas": pl["num_ctas"], "ctas_per_unit": pl["unit_ctas"] or None,
+                         "policy": ("%d CTA(s) per unit" % pl["unit_ctas"]) if pl["unit_ctas"]
+                                   else "one tile line split over the CTAs"}
+        except sv.SpecVerifyError:
+            attn_plan = None
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
             "steps": K, "warmup": max(3, args.warmup), "ms_per_step": round(ms_step, 5),
@@ -682,6 +724,7 @@ def run_ours(args):
             "verified_query_tokens_per_s": round(whole_job_rate(world, int(W.sum()), sec), 1),
             "kv_bytes_per_step": kv_bytes,
             "attn_kernel": attn_kernel,
+            "attn_plan": attn_plan,
             "attn_ms": round(attn_ms, 5),
             "verify_call_ms": round(verify_ms, 5),
             "accept_call_ms": round(accept_ms, 5),
@@ -690,6 +733,7 @@ def run_ours(args):
                               "rows": rows_l, "vocab": V_l,
                               "note": "spec_draft_signals on a logits matrix of the step's "
                                       "shape; not part of the step"},
+            "logits_scans": logits_scan,
             "host_lengths": {
                 "ms_per_step": round(ms_step_hl, 5),
                 "value": round(whole_job_rate(world, kv_bytes, ms_step_hl / 1e3) / 1e9, 2),

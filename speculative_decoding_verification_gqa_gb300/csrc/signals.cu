@@ -20,8 +20,18 @@
 namespace sv {
 namespace {
 
-constexpr int SIG_THREADS = 512;
-constexpr int SIG_UNROLL = 4;  // 16-byte loads in flight per thread
+#ifndef SV_SIG_THREADS
+#define SV_SIG_THREADS 512
+#endif
+#ifndef SV_SIG_UNROLL
+#define SV_SIG_UNROLL 4
+#endif
+#ifndef SV_SIG_CTAS_PER_SM
+#define SV_SIG_CTAS_PER_SM 2
+#endif
+constexpr int SIG_THREADS = SV_SIG_THREADS;
+constexpr int SIG_UNROLL = SV_SIG_UNROLL;  // 16-byte loads in flight per thread
+constexpr int SIG_CTAS_PER_SM = SV_SIG_CTAS_PER_SM;  // all resident at once
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
 constexpr float T_FLOOR = -150.f;  // 2^-150 is 0 in fp32: keeps (t - m) * 0 finite
@@ -78,7 +88,7 @@ __device__ __forceinline__ void raise_max(float mt, float& m, float& z, float& s
 }
 
 template <bool BF16>
-__global__ void __launch_bounds__(SIG_THREADS, 2) signals_kernel(SigArgs a) {
+__global__ void __launch_bounds__(SIG_THREADS, SIG_CTAS_PER_SM) signals_kernel(SigArgs a) {
   __shared__ Part sh[SIG_THREADS / 32];
   __shared__ int s_last;
   pdl_trigger();
@@ -198,7 +208,7 @@ __global__ void __launch_bounds__(SIG_THREADS, 2) signals_kernel(SigArgs a) {
 SigWs signals_ws_layout(int64_t rows, int vocab, int num_sms) {
   SigWs w;
   const int64_t n = rows * (int64_t)vocab;
-  int64_t c = 2LL * num_sms;  // two CTAs of 512 threads per SM, all resident at once
+  int64_t c = (int64_t)SIG_CTAS_PER_SM * num_sms;
   if (c > n / 8192) c = n / 8192;
   if (c < 1) c = 1;
   w.nctas = (int)c;
