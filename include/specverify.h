@@ -336,6 +336,16 @@ SV_API int sv_set_unit_ctas(int mode);
  * (several microseconds per call): time whole calls with the hook off. */
 SV_API void sv_set_profile_events(void* start_event, void* stop_event);
 
+/* Fault injection for tests, on the host: after `after` more kernel launches of the
+ * library, the next launch fails without reaching the GPU and the call that makes it
+ * returns SV_ERR_CUDA (spec_verify_attn and the paged call launch three kernels in this
+ * order: plan, attention, combine; the host-lengths call attention and combine;
+ * spec_accept and spec_draft_signals one each). The call's earlier launches have run;
+ * its outputs are then unspecified, and its workspace serves the next call as it is. One
+ * failure per arming; after < 0 disarms. Returns the launches that were still to go
+ * before a pending failure, or -1 if none was pending. Process-wide. */
+SV_API int sv_inject_launch_failure(int after);
+
 /* Library version: major * 10000 + minor * 100 + patch. */
 SV_API int sv_version(void);
 

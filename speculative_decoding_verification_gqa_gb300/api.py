@@ -33,7 +33,8 @@ EXPORTS = ("spec_verify_attn_workspace_size", "spec_verify_attn", "spec_verify_a
            "spec_accept_workspace_size",
            "spec_accept", "spec_draft_signals_workspace_size", "spec_draft_signals",
            "sv_workspace_status", "sv_status_string", "sv_set_attn_kernel", "sv_set_unit_ctas",
-           "sv_set_profile_events", "sv_version", "sv_plan_preview")
+           "sv_set_profile_events", "sv_version", "sv_plan_preview",
+           "sv_inject_launch_failure")
 
 
 class SpecVerifyError(RuntimeError):
@@ -106,6 +107,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.sv_plan_preview.argtypes = [ctypes.POINTER(AttnDesc), i32, vp, vp, i32, i32,
                                         ctypes.POINTER(PlanInfo), vp, vp, vp, i32]
         lib.sv_plan_preview.restype = ctypes.c_int
+        lib.sv_inject_launch_failure.argtypes = [ctypes.c_int]
+        lib.sv_inject_launch_failure.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -354,6 +357,14 @@ def set_unit_ctas(mode: int) -> int:
     if prev < -1:
         raise ValueError("unit-CTA mode must be in [-1, 1024]")
     return prev
+
+
+def inject_launch_failure(after: int) -> int:
+    """Test hook: after ``after`` more kernel launches of the library, the next one fails
+    on the host, and the call that makes it raises SpecVerifyError (SV_ERR_CUDA); a
+    negative ``after`` disarms. Returns the launches that were still to go before a
+    pending failure, or -1."""
+    return load_library().sv_inject_launch_failure(int(after))
 
 
 def set_profile_events(start=None, stop=None):

@@ -3,6 +3,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "internal.cuh"
 
 using namespace sv;
@@ -37,6 +39,8 @@ constexpr int SWITCH_TILES_MMA = 2;
 constexpr int32_t MAX_SEQ_LEN = 0x7fffffff - 1024;
 constexpr int64_t MAX_KV_ROWS = 0x7fffffff - 1024;
 
+// Launches until the armed failure, plus one (0: nothing armed). Tests only.
+std::atomic<int> g_fail_countdown{0};
 int g_attn_kernel = 0;  // 0 automatic, 1 mma.sync, 2 tcgen05
 int g_unit_ctas = SV_UNIT_CTAS;  // -1 cost model, 0 split tile line, k > 0 k CTAs per unit
 cudaEvent_t g_ev_start = nullptr;
@@ -81,7 +85,20 @@ int pick_kernel(const sv_attn_desc* d) {
 
 }  // namespace
 
+bool sv::take_injected_launch_failure() {
+  int n = g_fail_countdown.load(std::memory_order_relaxed);
+  while (n > 0)
+    if (g_fail_countdown.compare_exchange_weak(n, n - 1, std::memory_order_relaxed))
+      return n == 1;
+  return false;
+}
+
 extern "C" {
+
+SV_API int sv_inject_launch_failure(int after) {
+  const int prev = g_fail_countdown.exchange(after >= 0 && after < (1 << 30) ? after + 1 : 0);
+  return prev - 1;
+}
 
 SV_API int sv_version(void) { return 300; }  // 0.3.0: plan preview
 

@@ -170,9 +170,14 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
+// Host-side fault injection (sv_inject_launch_failure): counts a launch, and returns true
+// for the one that was armed to fail.
+bool take_injected_launch_failure();
+
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                        cudaStream_t s, Args&&... args) {
+  if (take_injected_launch_failure()) return cudaErrorLaunchFailure;  // nothing launched
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;

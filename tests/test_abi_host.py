@@ -167,3 +167,11 @@ def test_unit_cta_policy_setter(lib):
     assert lib.sv_set_unit_ctas(-2) == -2
     assert lib.sv_set_unit_ctas(1025) == -2
     assert lib.sv_set_unit_ctas(prev) == prev
+
+
+def test_launch_failure_hook_arms_and_disarms(lib):
+    assert lib.sv_inject_launch_failure(-1) == -1  # nothing pending
+    assert lib.sv_inject_launch_failure(2) == -1
+    assert lib.sv_inject_launch_failure(0) == 2   # re-armed: the previous arming was pending
+    assert lib.sv_inject_launch_failure(-1) == 0  # disarmed
+    assert lib.sv_inject_launch_failure(-5) == -1
