@@ -27,6 +27,11 @@ Functions and the passages they follow (page title, then section):
   "Speculative decoding (2)" (the target's own token replaces the first rejected draft).
 * ``draft_signals`` -- per row, the confidence (largest softmax probability) and the
   entropy (nats) of the softmax: "SpecKV" summary, "technical core", item 1.
+* ``accept_stochastic`` -- distribution-preserving acceptance: "GPU and LLM, chapter 5",
+  "Speculative decoding (2)" (the acceptance rule leaves the output distribution that of
+  the large model alone); the rule of the paper that page cites (Leviathan et al., 2023):
+  keep draft x with probability min(1, p(x)/q(x)), at the first rejection draw from the
+  normalised max(0, p - q), with every draft kept draw from the target's last row.
 * ``bf16_to_f64`` / ``e4m3_to_f64`` -- decoders written from the binary32 and OCP E4M3
   format definitions.
 """
@@ -82,6 +87,8 @@ def _load():
             lib.orc_accept.restype = i32
             lib.orc_draft_signals.argtypes = [i64, i64, i32, p, p, p, i32]
             lib.orc_draft_signals.restype = i32
+            lib.orc_accept_stochastic.argtypes = [i32, i64, i32, p, p, p, p, p, p, dbl, p, p, p]
+            lib.orc_accept_stochastic.restype = i32
             _lib = lib
     return _lib
 
@@ -256,3 +263,41 @@ def draft_signals(logits, nthreads=0):
                                  int(nthreads)):
         raise ValueError("oracle rejected the arguments")
     return conf, ent
+
+
+def accept_stochastic(target_logits, draft_logits, draft_tokens, draft_len, u_accept,
+                      u_sample, temperature=1.0):
+    """target_logits [sum (1 + D_b), V] and draft_logits [sum D_b, V], fp32 or uint16 bf16
+    bits (the same type); draft_tokens int32 [sum D_b]; u_accept float32 [sum D_b] and
+    u_sample float32 [B], uniform in [0, 1). Returns (accept_len, next_token, margin): the
+    acceptance length in [1, 1 + D_b], the emitted token, and the smallest decision
+    margin of each sequence (relative; see oracle.c)."""
+    t = np.ascontiguousarray(target_logits)
+    dl = np.ascontiguousarray(draft_logits)
+    if t.dtype != dl.dtype or t.dtype not in (np.uint16, np.float32):
+        raise TypeError("logits must both be float32 or both uint16 (bf16 bits)")
+    dt = 0 if t.dtype == np.uint16 else 2
+    draft_len = np.ascontiguousarray(draft_len, dtype=np.int32)
+    draft_tokens = np.ascontiguousarray(draft_tokens, dtype=np.int32)
+    u_accept = np.ascontiguousarray(u_accept, dtype=np.float32)
+    u_sample = np.ascontiguousarray(u_sample, dtype=np.float32)
+    B = draft_len.shape[0]
+    nd = int(np.sum(draft_len.astype(np.int64)))
+    V = t.shape[1]
+    if t.shape[0] != nd + B or (nd and dl.shape != (nd, V)) or draft_tokens.shape[0] != nd \
+            or u_accept.shape[0] != nd or u_sample.shape[0] != B:
+        raise ValueError("inconsistent shapes")
+    if nd == 0:
+        dl = np.zeros((1, V), dtype=t.dtype)
+        draft_tokens = np.zeros(1, dtype=np.int32)
+        u_accept = np.zeros(1, dtype=np.float32)
+    al = np.empty(B, dtype=np.int32)
+    nt = np.empty(B, dtype=np.int32)
+    mg = np.empty(B, dtype=np.float64)
+    lib = _load()
+    if lib.orc_accept_stochastic(B, V, dt, _ptr(t), _ptr(dl), _ptr(draft_tokens),
+                                 _ptr(draft_len), _ptr(u_accept), _ptr(u_sample),
+                                 ctypes.c_double(float(temperature)), _ptr(al), _ptr(nt),
+                                 _ptr(mg)):
+        raise ValueError("oracle rejected the arguments")
+    return al, nt, mg

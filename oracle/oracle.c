@@ -31,6 +31,17 @@
  *     of W >= 1 positions the query at position p sees only the W most recent positions,
  *     itself included, i.e. keys max(0, p - W + 1) .. p; for window row i, p = T + i.
  *     W = 0 means no window (every earlier key).
+ *   - Stochastic acceptance ([P3] "Speculative decoding (2)": the acceptance rule keeps
+ *     the distribution of the output exactly that of the large model alone; the rule
+ *     itself is not printed). The rule with that property from the paper the page cites
+ *     (Leviathan, Kalman and Matias, "Fast Inference from Transformers via Speculative
+ *     Decoding", 2023): with p the target's and q the drafter's softmax (logits divided
+ *     by a temperature) at a draft position, the draft x is kept with probability
+ *     min(1, p(x) / q(x)); at the first rejection the emitted token is drawn from the
+ *     normalised max(0, p - q); with every draft kept, from the target's last row. The
+ *     uniform draws are inputs: draft x_j is kept iff u_j q(x_j) < p(x_j), and a token is
+ *     drawn as the smallest index k whose running sum of weights exceeds u times their
+ *     total.
  *
  * Layouts (packed ragged batch): q and out [sum_b W_b, Hq, d]; k and v
  * [sum_b (T_b + W_b), Hkv, d]; W_b = 1 + D_b; sequences in batch order.
@@ -355,5 +366,130 @@ int orc_draft_signals(int64_t rows, int64_t vocab, int dtype, const void* logits
     entropy[r] = h;
     free(p);
   }
+  return bad;
+}
+
+/* Logit j of row r divided by the temperature, in fp64 (dtype 0: bf16 bits; 2: fp32). */
+static double scaled_logit(const void* base, int dtype, int64_t r, int64_t vocab, int64_t j,
+                           double inv_temp) {
+  const double x = dtype == 0 ? orc_bf16_to_f64(((const uint16_t*)base)[r * vocab + j])
+                              : (double)((const float*)base)[r * vocab + j];
+  return x * inv_temp;
+}
+
+/* The softmax of one row, materialised: p[j] = exp(x_j - m) / sum_k exp(x_k - m), with
+ * x = logits / temperature and m the row maximum. Returns 1 if the row has no finite
+ * value. */
+static int softmax_row(const void* base, int dtype, int64_t r, int64_t vocab, double inv_temp,
+                       double* p) {
+  double m = -INFINITY;
+  for (int64_t j = 0; j < vocab; ++j) {
+    p[j] = scaled_logit(base, dtype, r, vocab, j, inv_temp);
+    if (p[j] > m) m = p[j];
+  }
+  if (!isfinite(m)) return 1;
+  double z = 0.0;
+  for (int64_t j = 0; j < vocab; ++j) {
+    p[j] = exp(p[j] - m);
+    z += p[j];
+  }
+  for (int64_t j = 0; j < vocab; ++j) p[j] /= z;
+  return 0;
+}
+
+/* Inverse CDF of the distribution proportional to w >= 0 at u in [0, 1): the smallest k
+ * whose running sum w[0] + ... + w[k] exceeds u * sum(w). *margin receives the distance of
+ * u * sum(w) from the nearer end of k's interval, relative to sum(w). Returns -1 if every
+ * weight is 0. */
+static int64_t inverse_cdf(const double* w, int64_t vocab, double u, double* margin) {
+  double total = 0.0;
+  for (int64_t k = 0; k < vocab; ++k) total += w[k];
+  if (!(total > 0.0)) return -1;
+  const double t = u * total;
+  double cum = 0.0;
+  int64_t last = -1;
+  for (int64_t k = 0; k < vocab; ++k) {
+    if (w[k] > 0.0) last = k;
+    const double prev = cum;
+    cum += w[k];
+    if (cum > t) {
+      const double a = t - prev, b = cum - t;
+      *margin = (a < b ? a : b) / total;
+      return k;
+    }
+  }
+  *margin = 0.0;  /* rounding left t at the end: the last token of positive weight */
+  return last;
+}
+
+/* Stochastic acceptance of every sequence (see the reading above). target: [sum_b W_b,
+ * vocab] logits, the target's rows of each window; draft: [sum_b D_b, vocab], the
+ * drafter's logits at each draft position; draft_tokens [sum_b D_b]; u_accept [sum_b D_b]
+ * and u_sample [B] uniform in [0, 1). Writes accept_len, next_token and, per sequence,
+ * the smallest decision margin: |u q(x) - p(x)| / max(u q(x), p(x)) over the drafts
+ * examined and the inverse-CDF margin of the drawn token (a result decided by floating
+ * point within such a margin may legitimately differ in another precision). */
+int orc_accept_stochastic(int B, int64_t vocab, int dtype, const void* target,
+                          const void* draft, const int32_t* draft_tokens,
+                          const int32_t* draft_len, const float* u_accept,
+                          const float* u_sample, double temperature, int32_t* accept_len,
+                          int32_t* next_token, double* margin) {
+  if (B < 0 || vocab <= 0 || (dtype != 0 && dtype != 2) || !(temperature > 0.0)) return 1;
+  const double inv_temp = 1.0 / temperature;
+  double* p = (double*)malloc(sizeof(double) * (size_t)vocab);
+  double* q = (double*)malloc(sizeof(double) * (size_t)vocab);
+  if (!p || !q) {
+    free(p);
+    free(q);
+    return 1;
+  }
+  int bad = 0;
+  int64_t q_off = 0, d_off = 0;
+  for (int b = 0; b < B && !bad; ++b) {
+    const int D = draft_len[b];
+    if (D < 0) {
+      bad = 1;
+      break;
+    }
+    double mg = INFINITY;
+    int n = D;  /* drafts kept */
+    for (int j = 0; j < D; ++j) {
+      const int32_t x = draft_tokens[d_off + j];
+      if (x < 0 || x >= vocab || softmax_row(target, dtype, q_off + j, vocab, inv_temp, p) ||
+          softmax_row(draft, dtype, d_off + j, vocab, inv_temp, q)) {
+        bad = 1;
+        break;
+      }
+      const double lhs = (double)u_accept[d_off + j] * q[x], rhs = p[x];
+      const double den = lhs > rhs ? lhs : rhs;
+      const double m = den > 0.0 ? fabs(lhs - rhs) / den : 0.0;
+      if (m < mg) mg = m;
+      if (!(lhs < rhs)) {
+        n = j;
+        break;
+      }
+    }
+    if (bad) break;
+    if (n < D) {  /* p and q hold row n: draw from max(0, p - q) */
+      for (int64_t k = 0; k < vocab; ++k) p[k] = p[k] > q[k] ? p[k] - q[k] : 0.0;
+    } else if (softmax_row(target, dtype, q_off + D, vocab, inv_temp, p)) {
+      bad = 1;
+      break;
+    }
+    double m2 = 0.0;
+    const int64_t k = inverse_cdf(p, vocab, (double)u_sample[b], &m2);
+    if (k < 0) {
+      bad = 1;
+      break;
+    }
+    if (m2 < mg) mg = m2;
+    accept_len[b] = n + 1;
+    next_token[b] = (int32_t)k;
+    margin[b] = mg;
+    q_off += 1 + D;
+    d_off += D;
+  }
+  free(p);
+  free(q);
   return bad;
 }
