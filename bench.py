@@ -87,6 +87,8 @@ def parse():
     ap.add_argument("--side-block", type=int, default=16,
                     help="also time the verify call over a paged copy of the cache with "
                          "blocks of this many positions (0: skip)")
+    ap.add_argument("--side-stochastic", type=int, default=1,
+                    help="also time spec_accept_stochastic on the step's shapes (0: skip)")
     return ap.parse_args()
 
 
@@ -507,6 +509,46 @@ def run_ours(args):
     logits_scan["bytes"] = logits_bytes
     logits_scan["note"] = ("each call after L2 is evicted; torch's reductions read the same "
                            "logits; not part of the step")
+
+    # distribution-preserving acceptance on the step's shapes: the step's target logits
+    # plus drafter logits at every draft position (not part of the step)
+    side_stoch = None
+    if args.side_stochastic:
+        xs = synth.stochastic_inputs(w, seed + 7, draft_len=D)
+        dts = torch.bfloat16 if xs["target_logits"].dtype == np.uint16 else torch.float32
+        as_dev = lambda arr: (torch.from_numpy(arr.view(np.int16)).view(torch.bfloat16)
+                              if arr.dtype == np.uint16 else torch.from_numpy(arr)).to(dev)
+        st_in = [as_dev(xs["target_logits"]), as_dev(xs["draft_logits"]),
+                 torch.from_numpy(xs["draft_tokens"]).to(dev),
+                 torch.from_numpy(xs["draft_len"]).to(dev),
+                 torch.from_numpy(xs["u_accept"]).to(dev), torch.from_numpy(xs["u_sample"]).to(dev)]
+        st_out = (torch.empty(w.B, dtype=torch.int32, device=dev),
+                  torch.empty(w.B, dtype=torch.int32, device=dev))
+        ws_st = sv.new_workspace(256, dev)
+        st_call = lambda: sv.spec_accept_stochastic(*st_in, max_draft_len=md, temperature=1.0,
+                                                    accept_len=st_out[0], next_token=st_out[1],
+                                                    workspace=ws_st, stream=stream)
+        st_call()
+        n_st = max(3, min(K3, 20))
+        est = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_st)]
+        for i in range(n_st):
+            sink_l.copy_(flush_l.sum())
+            est[i][0].record(stream)
+            st_call()
+            est[i][1].record(stream)
+        torch.cuda.synchronize()
+        if sv.workspace_status(ws_st) != 0:
+            raise RuntimeError("device-side check failed in the stochastic acceptance")
+        st_ms = float(np.median([a_.elapsed_time(b_) for a_, b_ in est]))
+        st_bytes = sum(t.numel() * t.element_size() for t in st_in[:2])
+        side_stoch = {"ms": round(st_ms, 5), "logits_bytes_allocated": st_bytes,
+                      "mean_accept_len": round(float(st_out[0].float().mean()), 3),
+                      "dtype": str(dts).replace("torch.", ""),
+                      "note": "spec_accept_stochastic (temperature 1) on the step's target "
+                              "logits and drafter logits at every draft position, L2 "
+                              "evicted before each call; one CTA per sequence; rows after "
+                              "the first rejection are not read; not part of the step"}
+        del st_in, xs
     del flush_l
 
     # sliding-window verify attention on the same inputs (not part of the step)
@@ -734,6 +776,7 @@ def run_ours(args):
                               "note": "spec_draft_signals on a logits matrix of the step's "
                                       "shape; not part of the step"},
             "logits_scans": logits_scan,
+            "stochastic_accept": side_stoch,
             "host_lengths": {
                 "ms_per_step": round(ms_step_hl, 5),
                 "value": round(whole_job_rate(world, kv_bytes, ms_step_hl / 1e3) / 1e9, 2),

@@ -234,6 +234,48 @@ SV_API sv_status spec_accept_noalloc(int32_t batch, int32_t max_draft_len, int32
                                      int32_t* accept_len, int32_t* next_token,
                                      int32_t* target_tokens, void* stream);
 
+/* Bytes of workspace spec_accept_stochastic needs (256: the flag word). 0 if invalid. */
+SV_API size_t spec_accept_stochastic_workspace_size(int32_t batch, int32_t max_draft_len,
+                                                   int32_t vocab);
+
+/*
+ * spec_accept_stochastic -- acceptance for sampled decoding that leaves the distribution
+ * of the output that of the target model alone ("GPU and LLM, chapter 5", "Speculative
+ * decoding (2)"; the rule of Leviathan, Kalman and Matias, "Fast Inference from
+ * Transformers via Speculative Decoding", 2023, which that page cites).
+ *
+ * For sequence b, with p_j the softmax of target row j and q_j that of draft row j (logits
+ * divided by `temperature`), and x_j the drafted tokens:
+ *   draft j is kept iff u_accept[j] * q_j(x_j) < p_j(x_j), for j = 0, 1, ... until the
+ *   first that is not; with n drafts kept, accept_len[b] = n + 1 and next_token[b] is drawn
+ *   from the weights max(0, p_n - q_n) if n < D_b (from p_n if every weight is 0), or from
+ *   p_{D_b} if every draft was kept. A draw at u picks the smallest token k whose running
+ *   sum of weights, in token order, exceeds u times their total.
+ * With x_j drawn from q_j and the u uniform, every emitted token follows the target's
+ * distribution. The uniform draws are inputs, so results are reproducible.
+ *
+ *   target_logits  [sum_b (1 + D_b), vocab] (the target's rows of every window, as for
+ *                  spec_accept), bf16 or fp32
+ *   draft_logits   [sum_b D_b, vocab], the drafter's logits at every draft position, the
+ *                  same dtype; may be NULL when max_draft_len is 0
+ *   draft_tokens   int32 [sum_b D_b], each in [0, vocab)
+ *   u_accept       fp32 [sum_b D_b], in [0, 1)
+ *   u_sample       fp32 [B], in [0, 1)
+ *   temperature    > 0 (1: the models' own distributions)
+ *   workspace      >= 256 bytes, 256-byte aligned, flag word zero on first use
+ * Every row must hold at least one finite logit (rows of NaN give unspecified tokens).
+ * A draft length outside [0, max_draft_len] or a draft token outside [0, vocab) sets the
+ * workspace flag (sv_workspace_status: SV_ERR_DEVICE_SHAPE) and leaves the outputs of the
+ * sequences concerned untouched. vocab <= 2^30. One CTA per sequence; asynchronous.
+ */
+SV_API sv_status spec_accept_stochastic(int32_t batch, int32_t max_draft_len, int32_t vocab,
+                                        int32_t logits_dtype, const void* target_logits,
+                                        const void* draft_logits, const int32_t* draft_tokens,
+                                        const int32_t* draft_len, const float* u_accept,
+                                        const float* u_sample, float temperature,
+                                        int32_t* accept_len, int32_t* next_token,
+                                        void* workspace, size_t workspace_bytes, void* stream);
+
 /* Bytes of workspace spec_draft_signals needs on the current CUDA device. 0 if invalid. */
 SV_API size_t spec_draft_signals_workspace_size(int32_t rows, int32_t vocab);
 

@@ -87,7 +87,8 @@ def _load():
             lib.orc_accept.restype = i32
             lib.orc_draft_signals.argtypes = [i64, i64, i32, p, p, p, i32]
             lib.orc_draft_signals.restype = i32
-            lib.orc_accept_stochastic.argtypes = [i32, i64, i32, p, p, p, p, p, p, dbl, p, p, p]
+            lib.orc_accept_stochastic.argtypes = [i32, i64, i32, p, p, p, p, p, p, dbl, p, p, p,
+                                                  p]
             lib.orc_accept_stochastic.restype = i32
             _lib = lib
     return _lib
@@ -269,9 +270,10 @@ def accept_stochastic(target_logits, draft_logits, draft_tokens, draft_len, u_ac
                       u_sample, temperature=1.0):
     """target_logits [sum (1 + D_b), V] and draft_logits [sum D_b, V], fp32 or uint16 bf16
     bits (the same type); draft_tokens int32 [sum D_b]; u_accept float32 [sum D_b] and
-    u_sample float32 [B], uniform in [0, 1). Returns (accept_len, next_token, margin): the
-    acceptance length in [1, 1 + D_b], the emitted token, and the smallest decision
-    margin of each sequence (relative; see oracle.c)."""
+    u_sample float32 [B], uniform in [0, 1). Returns (accept_len, next_token,
+    margin_accept, margin_sample): the acceptance length in [1, 1 + D_b], the emitted
+    token, and per sequence the smallest relative margin of its keep / reject decisions and
+    the relative margin of its draw (see oracle.c)."""
     t = np.ascontiguousarray(target_logits)
     dl = np.ascontiguousarray(draft_logits)
     if t.dtype != dl.dtype or t.dtype not in (np.uint16, np.float32):
@@ -293,11 +295,12 @@ def accept_stochastic(target_logits, draft_logits, draft_tokens, draft_len, u_ac
         u_accept = np.zeros(1, dtype=np.float32)
     al = np.empty(B, dtype=np.int32)
     nt = np.empty(B, dtype=np.int32)
-    mg = np.empty(B, dtype=np.float64)
+    ma = np.empty(B, dtype=np.float64)
+    ms = np.empty(B, dtype=np.float64)
     lib = _load()
     if lib.orc_accept_stochastic(B, V, dt, _ptr(t), _ptr(dl), _ptr(draft_tokens),
                                  _ptr(draft_len), _ptr(u_accept), _ptr(u_sample),
                                  ctypes.c_double(float(temperature)), _ptr(al), _ptr(nt),
-                                 _ptr(mg)):
+                                 _ptr(ma), _ptr(ms)):
         raise ValueError("oracle rejected the arguments")
-    return al, nt, mg
+    return al, nt, ma, ms

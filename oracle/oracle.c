@@ -41,7 +41,8 @@
  *     normalised max(0, p - q); with every draft kept, from the target's last row. The
  *     uniform draws are inputs: draft x_j is kept iff u_j q(x_j) < p(x_j), and a token is
  *     drawn as the smallest index k whose running sum of weights exceeds u times their
- *     total.
+ *     total. If every weight of max(0, p - q) is 0 (p = q, so the rejected draft had
+ *     q(x) = 0), the token is drawn from p.
  *
  * Layouts (packed ragged batch): q and out [sum_b W_b, Hq, d]; k and v
  * [sum_b (T_b + W_b), Hkv, d]; W_b = 1 + D_b; sequences in batch order.
@@ -426,14 +427,15 @@ static int64_t inverse_cdf(const double* w, int64_t vocab, double u, double* mar
  * vocab] logits, the target's rows of each window; draft: [sum_b D_b, vocab], the
  * drafter's logits at each draft position; draft_tokens [sum_b D_b]; u_accept [sum_b D_b]
  * and u_sample [B] uniform in [0, 1). Writes accept_len, next_token and, per sequence,
- * the smallest decision margin: |u q(x) - p(x)| / max(u q(x), p(x)) over the drafts
- * examined and the inverse-CDF margin of the drawn token (a result decided by floating
- * point within such a margin may legitimately differ in another precision). */
+ * two decision margins: margin_accept, the smallest |u q(x) - p(x)| / max(u q(x), p(x))
+ * over the drafts examined (1 without drafts), and margin_sample, the inverse-CDF margin
+ * of the drawn token (a result decided by floating point within such a margin may
+ * legitimately differ in another precision). */
 int orc_accept_stochastic(int B, int64_t vocab, int dtype, const void* target,
                           const void* draft, const int32_t* draft_tokens,
                           const int32_t* draft_len, const float* u_accept,
                           const float* u_sample, double temperature, int32_t* accept_len,
-                          int32_t* next_token, double* margin) {
+                          int32_t* next_token, double* margin_accept, double* margin_sample) {
   if (B < 0 || vocab <= 0 || (dtype != 0 && dtype != 2) || !(temperature > 0.0)) return 1;
   const double inv_temp = 1.0 / temperature;
   double* p = (double*)malloc(sizeof(double) * (size_t)vocab);
@@ -451,7 +453,7 @@ int orc_accept_stochastic(int B, int64_t vocab, int dtype, const void* target,
       bad = 1;
       break;
     }
-    double mg = INFINITY;
+    double mg = 1.0;
     int n = D;  /* drafts kept */
     for (int j = 0; j < D; ++j) {
       const int32_t x = draft_tokens[d_off + j];
@@ -477,15 +479,24 @@ int orc_accept_stochastic(int B, int64_t vocab, int dtype, const void* target,
       break;
     }
     double m2 = 0.0;
-    const int64_t k = inverse_cdf(p, vocab, (double)u_sample[b], &m2);
+    int64_t k = inverse_cdf(p, vocab, (double)u_sample[b], &m2);
+    if (k < 0 && n < D) {
+      /* every residual weight is 0 (p = q; a rejection then needs q(x) = 0): draw from
+       * the target's row instead */
+      if (softmax_row(target, dtype, q_off + n, vocab, inv_temp, p)) {
+        bad = 1;
+        break;
+      }
+      k = inverse_cdf(p, vocab, (double)u_sample[b], &m2);
+    }
     if (k < 0) {
       bad = 1;
       break;
     }
-    if (m2 < mg) mg = m2;
     accept_len[b] = n + 1;
     next_token[b] = (int32_t)k;
-    margin[b] = mg;
+    margin_accept[b] = mg;
+    margin_sample[b] = m2;
     q_off += 1 + D;
     d_off += D;
   }

@@ -10,6 +10,7 @@ include/specverify.h:
 * ``spec_verify_attn_host_lengths`` -- the same with host copies of the lengths (plan on
   the host, no planning kernel).
 * ``spec_accept`` -- greedy acceptance (argmax per window row, first mismatch).
+* ``spec_accept_stochastic`` -- distribution-preserving acceptance for sampled decoding.
 """
 from __future__ import annotations
 
@@ -34,7 +35,8 @@ EXPORTS = ("spec_verify_attn_workspace_size", "spec_verify_attn", "spec_verify_a
            "spec_accept", "spec_draft_signals_workspace_size", "spec_draft_signals",
            "sv_workspace_status", "sv_status_string", "sv_set_attn_kernel", "sv_set_unit_ctas",
            "sv_set_profile_events", "sv_version", "sv_plan_preview",
-           "sv_inject_launch_failure")
+           "sv_inject_launch_failure", "spec_accept_stochastic_workspace_size",
+           "spec_accept_stochastic")
 
 
 class SpecVerifyError(RuntimeError):
@@ -107,6 +109,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.sv_plan_preview.argtypes = [ctypes.POINTER(AttnDesc), i32, vp, vp, i32, i32,
                                         ctypes.POINTER(PlanInfo), vp, vp, vp, i32]
         lib.sv_plan_preview.restype = ctypes.c_int
+        lib.spec_accept_stochastic_workspace_size.argtypes = [i32, i32, i32]
+        lib.spec_accept_stochastic_workspace_size.restype = sz
+        lib.spec_accept_stochastic.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp, vp,
+                                               ctypes.c_float, vp, vp, vp, sz, vp]
+        lib.spec_accept_stochastic.restype = ctypes.c_int
         lib.sv_inject_launch_failure.argtypes = [ctypes.c_int]
         lib.sv_inject_launch_failure.restype = ctypes.c_int
         _lib = lib
@@ -312,6 +319,48 @@ def spec_accept(logits, draft_tokens, draft_len, *, max_draft_len: int, accept_l
         _ptr(next_token), _ptr(target_tokens), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, "spec_accept")
+    return accept_len, next_token
+
+
+def spec_accept_stochastic(target_logits, draft_logits, draft_tokens, draft_len, u_accept,
+                           u_sample, *, max_draft_len: int, temperature: float = 1.0,
+                           accept_len=None, next_token=None, workspace=None, stream=None):
+    """Distribution-preserving acceptance for sampled decoding. target_logits [sum (1 + D_b),
+    V] and draft_logits [sum D_b, V] (bf16 or fp32, the same); draft_tokens int32 [sum
+    D_b]; draft_len int32 [B]; u_accept fp32 [sum D_b] and u_sample fp32 [B], uniform in
+    [0, 1). Returns (accept_len, next_token), int32 [B] each."""
+    _need(target_logits, "target_logits", (torch.bfloat16, torch.float32))
+    _need(draft_logits, "draft_logits", (target_logits.dtype,))
+    _need(draft_tokens, "draft_tokens", (torch.int32,))
+    _need(draft_len, "draft_len", (torch.int32,))
+    _need(u_accept, "u_accept", (torch.float32,))
+    _need(u_sample, "u_sample", (torch.float32,))
+    B = draft_len.shape[0]
+    V = target_logits.shape[-1]
+    if draft_logits.dim() != 2 or draft_logits.shape[1] != V:
+        raise ValueError("draft_logits must be [sum D_b, V] with the target's V")
+    if u_sample.numel() != B:
+        raise ValueError("u_sample must hold one draw per sequence")
+    if accept_len is None:
+        accept_len = torch.empty(B, dtype=torch.int32, device=target_logits.device)
+    if next_token is None:
+        next_token = torch.empty(B, dtype=torch.int32, device=target_logits.device)
+    for t, n in ((accept_len, "accept_len"), (next_token, "next_token")):
+        _need(t, n, (torch.int32,))
+    lib = load_library()
+    if workspace is None:
+        n = lib.spec_accept_stochastic_workspace_size(B, max_draft_len, V)
+        if n == 0:
+            raise SpecVerifyError(2, "spec_accept_stochastic_workspace_size")
+        workspace = new_workspace(n, target_logits.device)
+    dt = SV_BF16 if target_logits.dtype == torch.bfloat16 else SV_FP32
+    none_if_empty = lambda t: t if t.numel() > 0 else None
+    st = lib.spec_accept_stochastic(
+        B, max_draft_len, V, dt, _ptr(target_logits), _ptr(none_if_empty(draft_logits)),
+        _ptr(none_if_empty(draft_tokens)), _ptr(draft_len), _ptr(none_if_empty(u_accept)),
+        _ptr(u_sample), float(temperature), _ptr(accept_len), _ptr(next_token),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "spec_accept_stochastic")
     return accept_len, next_token
 
 

@@ -395,6 +395,43 @@ SV_API sv_status spec_accept(int32_t batch, int32_t max_draft_len, int32_t vocab
   return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
+SV_API size_t spec_accept_stochastic_workspace_size(int32_t batch, int32_t max_draft_len,
+                                                   int32_t vocab) {
+  if (batch < 0 || max_draft_len < 0 || max_draft_len > 255 || vocab <= 0 ||
+      vocab > (1 << 30))
+    return 0;
+  return 256;  // the flag word
+}
+
+SV_API sv_status spec_accept_stochastic(int32_t batch, int32_t max_draft_len, int32_t vocab,
+                                        int32_t logits_dtype, const void* target_logits,
+                                        const void* draft_logits, const int32_t* draft_tokens,
+                                        const int32_t* draft_len, const float* u_accept,
+                                        const float* u_sample, float temperature,
+                                        int32_t* accept_len, int32_t* next_token,
+                                        void* workspace, size_t workspace_bytes, void* stream) {
+  if (batch < 0 || max_draft_len < 0 || max_draft_len > 255 || vocab <= 0 ||
+      vocab > (1 << 30) || !(temperature > 0.f) || isinf(temperature))
+    return SV_ERR_SHAPE;
+  if (logits_dtype != SV_BF16 && logits_dtype != SV_FP32) return SV_ERR_DTYPE;
+  if (batch == 0) return SV_OK;
+  if (!target_logits || !draft_len || !u_sample || !accept_len || !next_token || !workspace)
+    return SV_ERR_NULL;
+  if (max_draft_len > 0 && (!draft_logits || !draft_tokens || !u_accept)) return SV_ERR_NULL;
+  const uintptr_t es = logits_dtype == SV_BF16 ? 2 : 4;
+  if (!aligned(target_logits, es) || (draft_logits && !aligned(draft_logits, es)) ||
+      !aligned(draft_len, 4) || (draft_tokens && !aligned(draft_tokens, 4)) ||
+      (u_accept && !aligned(u_accept, 4)) || !aligned(u_sample, 4) ||
+      !aligned(accept_len, 4) || !aligned(next_token, 4) || !aligned(workspace, 256))
+    return SV_ERR_ALIGN;
+  if (workspace_bytes < 256) return SV_ERR_WORKSPACE;
+  const cudaError_t e = launch_accept_stochastic(
+      batch, max_draft_len, vocab, logits_dtype, target_logits, draft_logits, draft_tokens,
+      draft_len, u_accept, u_sample, 1.f / temperature, accept_len, next_token, workspace,
+      (cudaStream_t)stream);
+  return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
 SV_API size_t spec_draft_signals_workspace_size(int32_t rows, int32_t vocab) {
   if (rows < 0 || vocab <= 0) return 0;
   const int sms = current_sms();

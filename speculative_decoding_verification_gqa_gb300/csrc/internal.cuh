@@ -234,6 +234,14 @@ cudaError_t launch_accept(int B, int max_draft, int vocab, int dtype, const void
                           int32_t* accept_len, int32_t* next_token, int32_t* target_tokens,
                           void* ws, const AcceptWs& lay, cudaStream_t s);
 
+// Stochastic acceptance (workspace: the flag word only).
+cudaError_t launch_accept_stochastic(int B, int max_draft, int vocab, int dtype,
+                                     const void* target, const void* draft,
+                                     const int32_t* draft_tokens, const int32_t* draft_len,
+                                     const float* u_accept, const float* u_sample,
+                                     float inv_temp, int32_t* accept_len, int32_t* next_token,
+                                     void* ws, cudaStream_t s);
+
 // Draft signals.
 struct SigWs {
   size_t ctrl, part, total;

@@ -235,6 +235,42 @@ def accept_inputs(w: Workload, seed: int, draft_len=None, p=None):
                 draft_len=draft_len, p=np.asarray(p))
 
 
+_TAG_DRAFT_LOGITS, _TAG_UNIFORM = 51, 52
+
+
+def stochastic_inputs(w: Workload, seed: int, draft_len=None, noise: float = 0.7):
+    """Inputs of sampled-decoding acceptance: the target's logits of every window row (those
+    of accept_inputs), the drafter's logits at every draft position (the target's row of
+    that position plus N(0, noise^2) per entry, in the logits' dtype: a drafter that mostly
+    agrees), the drafted tokens (the drafter row's argmax with the sequence's match
+    probability p, else a uniform token), and uniform draws u_accept [sum D] and u_sample
+    [B] in [0, 1). Returns dict(target_logits, draft_logits, draft_tokens, draft_len,
+    u_accept, u_sample)."""
+    a = accept_inputs(w, seed, draft_len=draft_len)
+    Dv = a["draft_len"]
+    tgt = a["logits"]
+    rows = [int(o) + j for o, D in zip(np.concatenate([[0], np.cumsum(Dv + 1)[:-1]]), Dv)
+            for j in range(int(D))]
+    nd = len(rows)
+    t32 = (tgt[rows].astype(np.uint32) << np.uint32(16)).view(np.float32) \
+        if tgt.dtype == np.uint16 else tgt[rows]
+    drf = t32 + noise * _normal_f32(nd * w.V, seed, _TAG_DRAFT_LOGITS).reshape(nd, w.V)
+    if tgt.dtype == np.uint16:
+        drf = bf16_bits(drf)
+        greedy = np.argmax((drf.astype(np.uint32) << np.uint32(16)).view(np.float32), axis=1) \
+            if nd else np.zeros(0, np.int64)
+    else:
+        drf = drf.astype(np.float32)
+        greedy = np.argmax(drf, axis=1) if nd else np.zeros(0, np.int64)
+    g = _ss(seed, _TAG_UNIFORM)
+    p = np.repeat(np.asarray(a["p"], dtype=np.float64), Dv)
+    other = g.integers(0, w.V, size=nd)
+    toks = np.where(g.random(nd) < p, greedy, other).astype(np.int32)
+    return dict(target_logits=tgt, draft_logits=drf.reshape(nd, w.V), draft_tokens=toks,
+                draft_len=Dv, u_accept=g.random(nd, dtype=np.float32),
+                u_sample=g.random(len(Dv), dtype=np.float32))
+
+
 def packed_offsets(seq_lens: Sequence[int], draft_len: Sequence[int]):
     """Start rows of each sequence in the packed q/out and k/v arrays (host-side
     bookkeeping for callers that build packed batches)."""

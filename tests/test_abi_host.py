@@ -175,3 +175,36 @@ def test_launch_failure_hook_arms_and_disarms(lib):
     assert lib.sv_inject_launch_failure(0) == 2   # re-armed: the previous arming was pending
     assert lib.sv_inject_launch_failure(-1) == 0  # disarmed
     assert lib.sv_inject_launch_failure(-5) == -1
+
+
+def _stoch(lib, B=2, md=3, V=100, dt=0, temp=1.0, ws_bytes=256, **ptrs):
+    p = dict(t=FAKE, d=FAKE, tok=FAKE, dl=FAKE, ua=FAKE, us=FAKE, al=FAKE, nt=FAKE, ws=FAKE)
+    p.update(ptrs)
+    lib.spec_accept_stochastic.argtypes = [ctypes.c_int32] * 4 + [ctypes.c_void_p] * 6 + [
+        ctypes.c_float] + [ctypes.c_void_p] * 3 + [ctypes.c_size_t, ctypes.c_void_p]
+    return lib.spec_accept_stochastic(B, md, V, dt, p["t"], p["d"], p["tok"], p["dl"], p["ua"],
+                                      p["us"], temp, p["al"], p["nt"], p["ws"], ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(B=-1), 2), (dict(md=256), 2), (dict(V=0), 2), (dict(V=(1 << 30) + 1), 2),
+    (dict(temp=0.0), 2), (dict(temp=-1.0), 2), (dict(temp=float("inf")), 2),
+    (dict(temp=float("nan")), 2), (dict(dt=1), 3),
+    (dict(t=None), 1), (dict(us=None), 1), (dict(d=None), 1), (dict(ua=None), 1),
+    (dict(tok=None), 1), (dict(ws=None), 1),
+    (dict(t=ctypes.c_void_p(0x10001)), 4), (dict(us=ctypes.c_void_p(0x10002)), 4),
+    (dict(ws=ctypes.c_void_p(0x10080)), 4), (dict(ws_bytes=255), 5),
+    (dict(B=0, t=None), 0),
+])
+def test_stochastic_accept_rejects_bad_arguments(lib, kw, status):
+    assert _stoch(lib, **kw) == status
+
+
+def test_stochastic_accept_workspace_size(lib):
+    lib.spec_accept_stochastic_workspace_size.restype = ctypes.c_size_t
+    assert lib.spec_accept_stochastic_workspace_size(4, 0, 100) == 256
+    assert lib.spec_accept_stochastic_workspace_size(4, 256, 100) == 0
+    assert lib.spec_accept_stochastic_workspace_size(-1, 3, 100) == 0
+    # max_draft_len 0: draft logits, tokens and keep draws may be NULL (the next check to
+    # fail is the workspace size, before any launch)
+    assert _stoch(lib, md=0, d=None, tok=None, ua=None, ws_bytes=0) == 5

@@ -35,11 +35,11 @@ def test_emitted_tokens_follow_the_target_distribution(temperature):
     q = [_softmax(drf[j].astype(np.float64) / temperature) for j in range(D)]
     # N sequences with the same rows; the drafter samples its tokens from q
     toks = np.stack([rng.choice(V, size=N, p=q[j]) for j in range(D)], axis=1).astype(np.int32)
-    al, nt, mg = oracle.accept_stochastic(
+    al, nt, ma, ms = oracle.accept_stochastic(
         np.tile(tgt, (N, 1)), np.tile(drf, (N, 1)), toks.reshape(-1), np.full(N, D, np.int32),
         rng.random(N * D, dtype=np.float32), rng.random(N, dtype=np.float32), temperature)
     assert np.all((al >= 1) & (al <= D + 1))
-    assert np.all((mg >= 0) & (mg <= 1))
+    assert np.all((ma >= 0) & (ma <= 1)) and np.all((ms >= 0) & (ms <= 0.5))
     first = np.where(al >= 2, toks[:, 0], nt)
     ok, z = _within(np.bincount(first, minlength=V) / N, p[0], N)
     assert ok, z
@@ -69,7 +69,7 @@ def test_draft_equal_to_target_keeps_every_draft():
     drf = np.concatenate([tgt[b * (D + 1):b * (D + 1) + D] for b in range(B)])
     toks = rng.integers(0, V, size=B * D).astype(np.int32)
     us = rng.random(B, dtype=np.float32)
-    al, nt, _ = oracle.accept_stochastic(tgt, drf, toks, np.full(B, D, np.int32),
+    al, nt, _, _ = oracle.accept_stochastic(tgt, drf, toks, np.full(B, D, np.int32),
                                          rng.random(B * D, dtype=np.float32), us)
     assert np.all(al == D + 1)
     for b in range(B):
@@ -89,7 +89,7 @@ def test_certain_drafter_on_an_impossible_token_is_rejected():
         tgt[2 * b, x[b]] = -np.inf
         drf[b, x[b]] = 0.0
     us = rng.random(B, dtype=np.float32)
-    al, nt, _ = oracle.accept_stochastic(tgt, drf, x, np.ones(B, np.int32),
+    al, nt, _, _ = oracle.accept_stochastic(tgt, drf, x, np.ones(B, np.int32),
                                          rng.random(B, dtype=np.float32), us)
     assert np.all(al == 1)
     for b in range(B):
@@ -103,7 +103,7 @@ def test_no_drafts_draws_from_the_first_row():
     B, V = 30, 1000
     tgt = rng.standard_normal((B, V)).astype(np.float32)
     us = rng.random(B, dtype=np.float32)
-    al, nt, _ = oracle.accept_stochastic(tgt, np.zeros((0, V), np.float32),
+    al, nt, _, _ = oracle.accept_stochastic(tgt, np.zeros((0, V), np.float32),
                                          np.zeros(0, np.int32), np.zeros(B, np.int32),
                                          np.zeros(0, np.float32), us)
     assert np.all(al == 1)
