@@ -5,7 +5,7 @@ import torch
 
 import oracle
 import speculative_decoding_verification_gqa_gb300 as sv
-from speculative_decoding_verification_gqa_gb300 import build, synth
+from speculative_decoding_verification_gqa_gb300 import build
 
 ABS_TOL = 1e-2   # max |gpu - oracle| beyond the bf16 output rounding (see compare)
 REL_TOL = 2e-2   # max |gpu - oracle| / max |oracle| (normwise)

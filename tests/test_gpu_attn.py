@@ -11,7 +11,7 @@ import torch
 import speculative_decoding_verification_gqa_gb300 as sv
 from speculative_decoding_verification_gqa_gb300 import synth
 
-from gpu_util import (assert_close, bf16_to_f64, compare, dev_attn, ensure_built, gpu_attn,
+from gpu_util import (assert_close, bf16_to_f64, dev_attn, ensure_built, gpu_attn,
                       oracle_attn)
 
 pytestmark = pytest.mark.gpu

@@ -4,7 +4,6 @@ their inputs and outputs). Its results must equal spec_accept's, bit for bit, on
 calls in a row with different shapes; shapes beyond its fixed scratch are rejected."""
 import ctypes
 
-import numpy as np
 import pytest
 import torch
 
