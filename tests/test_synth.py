@@ -1,5 +1,6 @@
 """Input generator checks (CPU): rounding, determinism, recipe statistics."""
 import numpy as np
+import pytest
 import torch
 
 from speculative_decoding_verification_gqa_gb300 import synth
@@ -96,3 +97,28 @@ def test_paged_layout_fp8_fill_is_the_e4m3_nan_code():
     kp, tab = pg["k_pages"], pg["block_table"]
     spare = sorted(set(range(kp.shape[0])) - set(tab[tab >= 0].tolist()))
     assert len(spare) == 3 and (kp[spare] == 0x7F).all()
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_stochastic_inputs_recipe(dtype):
+    w = synth.Workload("s", B=6, Hq=1, Hkv=1, d=8, D=5, T=1, V=777, p=0.8, logits_dtype=dtype)
+    Dv = np.array([5, 0, 3, 5, 1, 2], dtype=np.int32)
+    x = synth.stochastic_inputs(w, 9, draft_len=Dv, noise=0.25)
+    y = synth.stochastic_inputs(w, 9, draft_len=Dv, noise=0.25)
+    assert all(np.array_equal(x[k], y[k]) for k in x)
+    nd = int(Dv.sum())
+    assert x["target_logits"].shape == (nd + 6, 777) and x["draft_logits"].shape == (nd, 777)
+    assert x["draft_logits"].dtype == x["target_logits"].dtype
+    assert x["draft_tokens"].shape == (nd,) and x["draft_tokens"].min() >= 0
+    assert x["draft_tokens"].max() < 777
+    for u, n in ((x["u_accept"], nd), (x["u_sample"], 6)):
+        assert u.dtype == np.float32 and u.shape == (n,) and u.min() >= 0 and u.max() < 1
+    # the drafter's row j of sequence b is the target's row j plus N(0, 0.25^2) noise
+    widen = (lambda a: (a.astype(np.uint32) << np.uint32(16)).view(np.float32)) \
+        if dtype == "bf16" else (lambda a: a)
+    rows = [int(np.sum(Dv[:b] + 1)) + j for b in range(6) for j in range(int(Dv[b]))]
+    diff = widen(x["draft_logits"]) - widen(x["target_logits"][rows])
+    assert abs(float(diff.std()) - 0.25) < 0.02 and abs(float(diff.mean())) < 0.01
+    # the accept-step logits are the same as spec_accept's inputs of that seed
+    a = synth.accept_inputs(w, 9, draft_len=Dv)
+    assert np.array_equal(a["logits"], x["target_logits"])
