@@ -153,8 +153,8 @@ def test_policies_chosen_on_the_measured_workloads():
 @pytest.mark.parametrize("seed", range(12))
 def test_ragged_batches(seed):
     """Ragged lengths (the adaptive-draft-length mix: T ~ U[0, 65536], D ~ U{0 .. Dmax}),
-    G in {1, 4, 8, 16}, with and without a sliding window, on both kernels and on grids
-    smaller than the batch's units."""
+    G in {1, 4, 8, 16}, with and without a sliding window, packed or paged, on both
+    kernels and on grids smaller than the batch's units."""
     rng = np.random.default_rng(100 + seed)
     G = int(rng.choice([1, 4, 8, 16]))
     Hkv = int(rng.choice([1, 2, 8]))
@@ -168,8 +168,11 @@ def test_ragged_batches(seed):
     W = int(rng.choice([0, 1, 100, 4096, 70000]))
     sms = int(rng.choice([152, 20, 3]))
     kernel = int(rng.choice([1, 2]))
+    block_size = int(rng.choice([0, 16, 128, 1024]))  # 0: packed cache
     desc = _desc(B, G * Hkv, Hkv, 128, Dmax, 65536, W=W)
-    plan = _plan(desc, Tv, Dv, sms=sms, kernel=kernel)
+    plan = _plan(desc, Tv, Dv, sms=sms, kernel=kernel, block_size=block_size)
+    if block_size and block_size < plan["tile_keys"]:
+        assert plan["unit_ctas"] == 0  # small blocks: always the split line
     # a window covering every position of the longest sequence is no window
     W_eff = 0 if W > 65536 + Dmax else W
     check_plan(plan, Tv, Dv, G, Hkv, W_eff)
