@@ -208,3 +208,47 @@ def test_stochastic_accept_workspace_size(lib):
     # max_draft_len 0: draft logits, tokens and keep draws may be NULL (the next check to
     # fail is the workspace size, before any launch)
     assert _stoch(lib, md=0, d=None, tok=None, ua=None, ws_bytes=0) == 5
+
+
+def _header_signatures():
+    """{name: (return type, [parameter types])} of every SV_API declaration."""
+    txt = open(HEADER).read()
+    txt = re.sub(r"/\*.*?\*/", " ", txt, flags=re.S)
+    out = {}
+    for m in re.finditer(r"SV_API\s+([\w\s\*]+?)\b(\w+)\s*\(([^)]*)\)\s*;", txt):
+        ret, name, params = m.group(1).strip(), m.group(2), m.group(3).strip()
+        types = []
+        if params and params != "void":
+            for p in params.split(","):
+                p = " ".join(p.split())
+                types.append("ptr" if "*" in p else p.rsplit(" ", 1)[0].replace("const ", ""))
+        out[name] = ("ptr" if "*" in ret else ret.replace("const ", "").strip(), types)
+    return out
+
+
+_CTYPES = {"int32_t": ctypes.c_int32, "int": ctypes.c_int, "int64_t": ctypes.c_int64,
+           "size_t": ctypes.c_size_t, "float": ctypes.c_float, "sv_status": ctypes.c_int,
+           "void": None}
+
+
+def test_binding_signatures_match_the_header(lib):
+    """Every function the Python binding declares to ctypes has the header's parameter
+    count and types (pointers as pointers, each scalar with its exact width)."""
+    sigs = _header_signatures()
+    checked = 0
+    for name, (ret, params) in sigs.items():
+        fn = getattr(lib, name)
+        if fn.argtypes is None:
+            continue
+        assert len(fn.argtypes) == len(params), name
+        for got, want in zip(fn.argtypes, params):
+            if want == "ptr":
+                assert got is ctypes.c_void_p or hasattr(got, "_type_") and \
+                    issubclass(got, ctypes._Pointer), (name, got)
+            else:
+                assert ctypes.sizeof(got) == ctypes.sizeof(_CTYPES[want]), (name, got, want)
+                assert (got in (ctypes.c_float, ctypes.c_double)) == (want == "float"), name
+        if ret != "ptr" and _CTYPES.get(ret) is not None:
+            assert ctypes.sizeof(fn.restype) == ctypes.sizeof(_CTYPES[ret]), name
+        checked += 1
+    assert checked >= 15
