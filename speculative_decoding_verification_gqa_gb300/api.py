@@ -130,6 +130,12 @@ def _stream(stream) -> ctypes.c_void_p:
     return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
 
 
+def _or_placeholder(t: torch.Tensor) -> torch.Tensor:
+    """t, or a small allocation of its dtype on its device when t is empty (a batch without
+    drafts: the library requires the pointer when max_draft_len > 0 but never reads it)."""
+    return t if t.numel() > 0 else torch.empty(16, dtype=t.dtype, device=t.device)
+
+
 def _check(st: int, where: str):
     if st != 0:
         raise SpecVerifyError(st, where)
@@ -313,7 +319,7 @@ def spec_accept(logits, draft_tokens, draft_len, *, max_draft_len: int, accept_l
     if workspace is None:
         workspace = new_workspace(accept_workspace_bytes(B, max_draft_len, V), logits.device)
     dt = SV_BF16 if logits.dtype == torch.bfloat16 else SV_FP32
-    dtok = draft_tokens if draft_tokens.numel() > 0 else None
+    dtok = _or_placeholder(draft_tokens)
     st = load_library().spec_accept(
         B, max_draft_len, V, dt, _ptr(logits), _ptr(dtok), _ptr(draft_len), _ptr(accept_len),
         _ptr(next_token), _ptr(target_tokens), _ptr(workspace),
@@ -354,10 +360,10 @@ def spec_accept_stochastic(target_logits, draft_logits, draft_tokens, draft_len,
             raise SpecVerifyError(2, "spec_accept_stochastic_workspace_size")
         workspace = new_workspace(n, target_logits.device)
     dt = SV_BF16 if target_logits.dtype == torch.bfloat16 else SV_FP32
-    none_if_empty = lambda t: t if t.numel() > 0 else None
+    dlg, dtk, ua = (_or_placeholder(t) for t in (draft_logits, draft_tokens, u_accept))
     st = lib.spec_accept_stochastic(
-        B, max_draft_len, V, dt, _ptr(target_logits), _ptr(none_if_empty(draft_logits)),
-        _ptr(none_if_empty(draft_tokens)), _ptr(draft_len), _ptr(none_if_empty(u_accept)),
+        B, max_draft_len, V, dt, _ptr(target_logits), _ptr(dlg), _ptr(dtk), _ptr(draft_len),
+        _ptr(ua),
         _ptr(u_sample), float(temperature), _ptr(accept_len), _ptr(next_token),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, "spec_accept_stochastic")

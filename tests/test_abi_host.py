@@ -252,3 +252,16 @@ def test_binding_signatures_match_the_header(lib):
             assert ctypes.sizeof(fn.restype) == ctypes.sizeof(_CTYPES[ret]), name
         checked += 1
     assert checked >= 15
+
+
+def test_empty_draft_arrays_get_a_placeholder_pointer():
+    """A batch without drafts passes empty draft arrays; the library still wants a pointer
+    when max_draft_len > 0, so the binding passes a small allocation of the same dtype
+    (never read). Non-empty arrays pass through unchanged."""
+    import torch
+    for dt in (torch.int32, torch.float32, torch.bfloat16):
+        e = torch.empty(0, dtype=dt)
+        p = api._or_placeholder(e)
+        assert p.numel() > 0 and p.dtype == dt and p.device == e.device
+        full = torch.ones(3, dtype=dt)
+        assert api._or_placeholder(full) is full
