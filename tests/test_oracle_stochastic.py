@@ -137,3 +137,33 @@ def test_bf16_logits_decode_like_fp32():
     a = oracle.accept_stochastic(tgt, drf, toks, Dv, ua, us)
     b = oracle.accept_stochastic(widen(tgt), widen(drf), toks, Dv, ua, us)
     assert all(np.array_equal(x, y) for x, y in zip(a, b))
+
+
+def test_mean_acceptance_length_matches_the_printed_values():
+    """With two-token distributions p = (a, 1 - a) and q = (b, 1 - b) at every draft
+    position, a draft drawn from q is kept with probability alpha = 1 - |a - b|,
+    independently of the other positions. So the mean acceptance length of k = 4 drafts is
+    (1 - alpha^5) / (1 - alpha), the expected value the pages print for alpha = 0.5, 0.7
+    and 0.9 (tests/golden/expected_al_k4.txt; alpha = 1 gives k + 1)."""
+    import os
+    golden = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden",
+                          "expected_al_k4.txt")
+    rows = [l.split() for l in open(golden) if l.strip() and not l.startswith("#")]
+    rng = np.random.default_rng(12)
+    N = 30000
+    for alpha_s, k_s, printed_s, decimals_s in rows:
+        alpha, k, printed = float(alpha_s), int(k_s), float(printed_s)
+        a = 0.9
+        b = a - (1.0 - alpha)  # |a - b| = 1 - alpha
+        lt = np.log(np.array([a, 1 - a]))
+        ld = np.log(np.array([max(b, 1e-300), 1 - b]))
+        tgt = np.tile(lt, (N * (k + 1), 1)).astype(np.float32)
+        drf = np.tile(ld, (N * k, 1)).astype(np.float32)
+        toks = (rng.random(N * k) >= b).astype(np.int32)  # token 0 with probability b
+        al, _, _, _ = oracle.accept_stochastic(tgt, drf, toks, np.full(N, k, np.int32),
+                                               rng.random(N * k, dtype=np.float32),
+                                               rng.random(N, dtype=np.float32))
+        exact = (1 - alpha ** (k + 1)) / (1 - alpha) if alpha < 1 else k + 1.0
+        assert round(exact, int(decimals_s)) == printed
+        sigma = al.std() / np.sqrt(N) + 1e-12
+        assert abs(al.mean() - exact) <= 4.5 * sigma + 1e-9, (alpha, al.mean(), exact)
