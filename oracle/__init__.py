@@ -32,6 +32,9 @@ Functions and the passages they follow (page title, then section):
   the large model alone); the rule of the paper that page cites (Leviathan et al., 2023):
   keep draft x with probability min(1, p(x)/q(x)), at the first rejection draw from the
   normalised max(0, p - q), with every draft kept draw from the target's last row.
+* ``stochastic_decisions`` -- every keep / reject decision of that rule as a signed
+  relative margin (positive: kept), also at positions after the first rejection, so a
+  test can check another implementation's path decision by decision.
 * ``bf16_to_f64`` / ``e4m3_to_f64`` -- decoders written from the binary32 and OCP E4M3
   format definitions.
 """
@@ -90,6 +93,8 @@ def _load():
             lib.orc_accept_stochastic.argtypes = [i32, i64, i32, p, p, p, p, p, p, dbl, p, p, p,
                                                   p]
             lib.orc_accept_stochastic.restype = i32
+            lib.orc_stochastic_decisions.argtypes = [i32, i64, i32, p, p, p, p, p, dbl, p]
+            lib.orc_stochastic_decisions.restype = i32
             _lib = lib
     return _lib
 
@@ -304,3 +309,34 @@ def accept_stochastic(target_logits, draft_logits, draft_tokens, draft_len, u_ac
                                  _ptr(ma), _ptr(ms)):
         raise ValueError("oracle rejected the arguments")
     return al, nt, ma, ms
+
+
+def stochastic_decisions(target_logits, draft_logits, draft_tokens, draft_len, u_accept,
+                         temperature=1.0):
+    """Signed relative margin of every draft position's keep / reject decision
+    (float64 [sum D_b]): (p(x) - u q(x)) / max(u q(x), p(x)), 0 when both are 0. Positive
+    means kept; the acceptance length of ``accept_stochastic`` is 1 + the number of
+    leading positive values of the sequence. Same arguments as ``accept_stochastic``
+    without ``u_sample``."""
+    t = np.ascontiguousarray(target_logits)
+    dl = np.ascontiguousarray(draft_logits)
+    if t.dtype != dl.dtype or t.dtype not in (np.uint16, np.float32):
+        raise TypeError("logits must both be float32 or both uint16 (bf16 bits)")
+    dt = 0 if t.dtype == np.uint16 else 2
+    draft_len = np.ascontiguousarray(draft_len, dtype=np.int32)
+    draft_tokens = np.ascontiguousarray(draft_tokens, dtype=np.int32)
+    u_accept = np.ascontiguousarray(u_accept, dtype=np.float32)
+    B = draft_len.shape[0]
+    nd = int(np.sum(draft_len.astype(np.int64)))
+    V = t.shape[1]
+    if t.shape[0] != nd + B or (nd and dl.shape != (nd, V)) or draft_tokens.shape[0] != nd \
+            or u_accept.shape[0] != nd:
+        raise ValueError("inconsistent shapes")
+    out = np.empty(max(nd, 1), dtype=np.float64)
+    if nd == 0:
+        return out[:0]
+    if _load().orc_stochastic_decisions(B, V, dt, _ptr(t), _ptr(dl), _ptr(draft_tokens),
+                                        _ptr(draft_len), _ptr(u_accept),
+                                        ctypes.c_double(float(temperature)), _ptr(out)):
+        raise ValueError("oracle rejected the arguments")
+    return out

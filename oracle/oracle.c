@@ -504,3 +504,52 @@ int orc_accept_stochastic(int B, int64_t vocab, int dtype, const void* target,
   free(q);
   return bad;
 }
+
+/* Every keep / reject decision of stochastic acceptance, whether or not the sequence's
+ * acceptance reaches it: for draft position j of sequence b (row d_off + j of the
+ * drafter's logits, d_off = D_0 + ... + D_(b-1); row q_off + j of the target's, q_off =
+ * d_off + b), with x = draft_tokens[d_off + j], lhs = u_accept[d_off + j] q(x) and rhs =
+ * p(x), decision[d_off + j] = (rhs - lhs) / max(lhs, rhs), or 0 when both are 0. The draft
+ * is kept iff the value is positive (u q(x) < p(x), the rule of orc_accept_stochastic), and
+ * its magnitude is the decision's relative margin: a value within a small margin of 0 may
+ * come out either way in another precision. [P3] "Speculative decoding (2)"; the rule of
+ * Leviathan et al. (2023) as above. */
+int orc_stochastic_decisions(int B, int64_t vocab, int dtype, const void* target,
+                             const void* draft, const int32_t* draft_tokens,
+                             const int32_t* draft_len, const float* u_accept,
+                             double temperature, double* decision) {
+  if (B < 0 || vocab <= 0 || (dtype != 0 && dtype != 2) || !(temperature > 0.0)) return 1;
+  const double inv_temp = 1.0 / temperature;
+  double* p = (double*)malloc(sizeof(double) * (size_t)vocab);
+  double* q = (double*)malloc(sizeof(double) * (size_t)vocab);
+  if (!p || !q) {
+    free(p);
+    free(q);
+    return 1;
+  }
+  int bad = 0;
+  int64_t d_off = 0;
+  for (int b = 0; b < B && !bad; ++b) {
+    const int D = draft_len[b];
+    if (D < 0) {
+      bad = 1;
+      break;
+    }
+    const int64_t q_off = d_off + b;
+    for (int j = 0; j < D; ++j) {
+      const int32_t x = draft_tokens[d_off + j];
+      if (x < 0 || x >= vocab || softmax_row(target, dtype, q_off + j, vocab, inv_temp, p) ||
+          softmax_row(draft, dtype, d_off + j, vocab, inv_temp, q)) {
+        bad = 1;
+        break;
+      }
+      const double lhs = (double)u_accept[d_off + j] * q[x], rhs = p[x];
+      const double den = lhs > rhs ? lhs : rhs;
+      decision[d_off + j] = den > 0.0 ? (rhs - lhs) / den : 0.0;
+    }
+    d_off += D;
+  }
+  free(p);
+  free(q);
+  return bad;
+}

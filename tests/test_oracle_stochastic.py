@@ -167,3 +167,110 @@ def test_mean_acceptance_length_matches_the_printed_values():
         assert round(exact, int(decimals_s)) == printed
         sigma = al.std() / np.sqrt(N) + 1e-12
         assert abs(al.mean() - exact) <= 4.5 * sigma + 1e-9, (alpha, al.mean(), exact)
+
+
+def test_all_zero_residual_draws_from_the_target():
+    """p = q at the draft position and the drafted token has probability 0 under both
+    (logit -inf in both rows): u q(x) < p(x) reads 0 < 0, so the draft is rejected, and
+    every weight of max(0, p - q) is 0. The emitted token then follows p (the output must
+    keep the target's distribution): exactly numpy's inverse CDF of p at u_sample for every
+    sequence, and over 40,000 sequences each token's frequency within 4.5 sigma of p."""
+    rng = np.random.default_rng(21)
+    V, N = 7, 40000
+    row = (rng.standard_normal(V) * 1.3).astype(np.float32)
+    x = 3
+    row[x] = -np.inf
+    p = _softmax(row.astype(np.float64))
+    assert p[x] == 0.0
+    tgt = np.tile(row, (2 * N, 1))            # rows 0 and 1 of every sequence
+    drf = np.tile(row, (N, 1))                # q = p at the draft position
+    us = rng.random(N, dtype=np.float32)
+    al, nt, ma, _ = oracle.accept_stochastic(tgt, drf, np.full(N, x, np.int32),
+                                             np.ones(N, np.int32),
+                                             rng.random(N, dtype=np.float32), us)
+    assert np.all(al == 1) and np.all(ma == 0.0)
+    assert all(nt[b] == _inverse_cdf(p, float(us[b])) for b in range(0, N, 97))
+    assert np.all(nt != x)
+    ok, z = _within(np.bincount(nt, minlength=V) / N, p, N)
+    assert ok, z
+
+
+def test_all_zero_residual_after_kept_drafts():
+    """The same degenerate rejection at the third draft position, after two drafts that
+    q = p keeps whenever u < 1: the token is drawn from the target's row of that position,
+    not from the first row or the bonus row."""
+    rng = np.random.default_rng(22)
+    V, B, D = 11, 60, 4
+    tgt = rng.standard_normal((B * (D + 1), V)).astype(np.float32)
+    drf = np.empty((B * D, V), dtype=np.float32)
+    toks = np.empty(B * D, dtype=np.int32)
+    for b in range(B):
+        for j in range(D):
+            r = tgt[b * (D + 1) + j]
+            if j == 2:
+                r[j] = -np.inf               # token j: probability 0 in both rows
+            drf[b * D + j] = r
+            toks[b * D + j] = j if j == 2 else int(np.argmax(r))
+    ua = rng.random(B * D, dtype=np.float32) * np.float32(0.99)
+    us = rng.random(B, dtype=np.float32)
+    al, nt, _, _ = oracle.accept_stochastic(tgt, drf, toks, np.full(B, D, np.int32), ua, us)
+    assert np.all(al == 3)
+    for b in range(B):
+        p2 = _softmax(tgt[b * (D + 1) + 2].astype(np.float64))
+        assert nt[b] == _inverse_cdf(p2, float(us[b])) and nt[b] != 2
+
+
+def test_decision_margins_closed_forms():
+    """Signed decision margins, (p(x) - u q(x)) / max(p(x), u q(x)):
+    * q = p: 1 - u at every position (kept unless u = 1);
+    * a drafter certain of x where p(x) = 0: -1 (rejected), or 0 when u = 0;
+    * two-token rows p = (a, 1 - a), q = (b, 1 - b), x = 0: (a - u b) / max(a, u b).
+    And the acceptance length is 1 + the number of leading positive decisions."""
+    rng = np.random.default_rng(23)
+    B, D, V = 20, 5, 40
+    tgt = rng.standard_normal((B * (D + 1), V)).astype(np.float32)
+    drf = np.concatenate([tgt[b * (D + 1):b * (D + 1) + D] for b in range(B)])
+    toks = rng.integers(0, V, size=B * D).astype(np.int32)
+    ua = rng.random(B * D, dtype=np.float32)
+    dm = oracle.stochastic_decisions(tgt, drf, toks, np.full(B, D, np.int32), ua)
+    assert np.allclose(dm, 1.0 - ua.astype(np.float64), rtol=0, atol=1e-12)
+
+    tg = rng.standard_normal((2 * 8, V)).astype(np.float32)
+    dr = np.full((8, V), -1e30, dtype=np.float32)
+    x = rng.integers(0, V, size=8).astype(np.int32)
+    for b in range(8):
+        tg[2 * b, x[b]] = -np.inf
+        dr[b, x[b]] = 0.0
+    u = rng.random(8, dtype=np.float32)
+    u[0] = 0.0
+    dm = oracle.stochastic_decisions(tg, dr, x, np.ones(8, np.int32), u)
+    assert dm[0] == 0.0 and np.all(dm[1:] == -1.0)
+
+    a = rng.uniform(0.05, 0.95, size=30)
+    b = rng.uniform(0.05, 0.95, size=30)
+    u = rng.random(30, dtype=np.float32)
+    lt = np.log(np.stack([a, 1 - a], axis=1))
+    ld = np.log(np.stack([b, 1 - b], axis=1))
+    tgt2 = np.repeat(lt, 2, axis=0).astype(np.float32)   # rows 0 and 1 of each sequence
+    drf2 = ld.astype(np.float32)
+    dm = oracle.stochastic_decisions(tgt2, drf2, np.zeros(30, np.int32), np.ones(30, np.int32), u)
+    pa = _softmax_rows(lt.astype(np.float32).astype(np.float64))[:, 0]
+    qb = _softmax_rows(ld.astype(np.float32).astype(np.float64))[:, 0]
+    lhs, rhs = u.astype(np.float64) * qb, pa
+    assert np.allclose(dm, (rhs - lhs) / np.maximum(lhs, rhs), rtol=1e-12, atol=1e-15)
+
+    # the acceptance path follows the signs
+    drf3 = (tgt[[b * (D + 1) + j for b in range(B) for j in range(D)]]
+            + rng.standard_normal((B * D, V)).astype(np.float32) * 0.5)
+    toks3 = np.array([int(np.argmax(r)) for r in drf3], dtype=np.int32)
+    al, _, _, _ = oracle.accept_stochastic(tgt, drf3, toks3, np.full(B, D, np.int32), ua,
+                                           rng.random(B, dtype=np.float32))
+    dm = oracle.stochastic_decisions(tgt, drf3, toks3, np.full(B, D, np.int32), ua).reshape(B, D)
+    lead = np.array([int(np.argmin(np.append(r > 0, False))) for r in dm])
+    assert np.array_equal(al, lead + 1)
+    assert 0 < (al - 1).mean() < D
+
+
+def _softmax_rows(x):
+    z = np.exp(x - x.max(axis=1, keepdims=True))
+    return z / z.sum(axis=1, keepdims=True)
