@@ -58,10 +58,11 @@ def bf16_half_ulp(x):
     return np.where(ax > 0, np.exp2(e - 8), 0.0)
 
 
-def compare(gpu_bits, ref, rows_mask=None):
+def compare(gpu_bits, ref, rows_mask=None, raw=False):
     """Returns (max_abs, normwise_rel) over the outputs where ref is finite. max_abs is the
     error beyond the bf16 output format's own rounding: max(|g - r| - half_ulp(max(|g|,
-    |r|)), 0); normwise_rel = max |g - r| / max |r|."""
+    |r|)), 0); normwise_rel = max |g - r| / max |r|. With raw=True a third value is the
+    plain max |g - r|."""
     g = bf16_to_f64(gpu_bits)
     sel = np.isfinite(ref)
     if rows_mask is not None:
@@ -70,12 +71,20 @@ def compare(gpu_bits, ref, rows_mask=None):
     assert np.isfinite(g[sel]).all(), "non-finite GPU output"
     err = np.abs(g[sel] - ref[sel])
     excess = np.maximum(err - bf16_half_ulp(np.maximum(np.abs(g[sel]), np.abs(ref[sel]))), 0.0)
-    return float(excess.max()), float(err.max() / np.abs(ref[sel]).max())
+    res = (float(excess.max()), float(err.max() / np.abs(ref[sel]).max()))
+    return res + (float(err.max()),) if raw else res
 
 
 def assert_close(gpu_bits, ref):
-    ma, mr = compare(gpu_bits, ref)
-    assert ma <= ABS_TOL and mr <= REL_TOL, (ma, mr)
+    """The parity bound: error beyond the output format's rounding <= ABS_TOL and normwise
+    relative error <= REL_TOL. The plain max |gpu - oracle| and max |oracle| are reported
+    beside them (printed, and in the assertion message)."""
+    ma, mr, raw = compare(gpu_bits, ref, raw=True)
+    peak = float(np.abs(ref[np.isfinite(ref)]).max())
+    msg = ("max|gpu-oracle| beyond bf16 half-ulp %.3g (bound %g), plain max|gpu-oracle| %.3g, "
+           "max|oracle| %.3g, normwise rel %.3g (bound %g)" % (ma, ABS_TOL, raw, peak, mr, REL_TOL))
+    print(msg)
+    assert ma <= ABS_TOL and mr <= REL_TOL, msg
     return ma, mr
 
 

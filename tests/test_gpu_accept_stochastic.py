@@ -9,11 +9,14 @@ Where floating point decides an integer here, fp32 and fp64 may legitimately dif
   segment sums) are within CDF_TOL of the total, so near an interval's end a neighbour
   may be drawn. For a flat softmax over a large vocabulary the intervals are themselves
   about 1e-5 of the total.
-So the acceptance length must equal the oracle's wherever every decision of the sequence
-has a margin of at least ACC_MARGIN, the token must equal the oracle's where the draw's
-margin is at least CDF_TOL, and elsewhere it must be a valid draw: a token of positive
-weight whose fp64 interval lies within CDF_TOL of u times the total. Nothing else
-differs."""
+So every keep / reject decision on the GPU's path must agree with the oracle's wherever
+the oracle's margin for that decision is at least ACC_MARGIN: the GPU may leave the
+oracle's path only at a position whose own margin is below it (every decision is checked,
+also on sequences with a low-margin decision elsewhere). Where the two paths agree, the
+token must equal the oracle's where the draw's margin is at least CDF_TOL; elsewhere, and
+on a path that left the oracle's at a low-margin position, it must be a valid draw from
+the GPU path's weights: a token of positive weight whose fp64 interval lies within CDF_TOL
+of u times the total. Nothing else differs."""
 import numpy as np
 import pytest
 import torch
@@ -71,26 +74,44 @@ def _draw_weights(x, b, n, temperature):
     return p
 
 
+def _valid_draw(x, b, n, temperature, tok):
+    w = _draw_weights(x, b, n, temperature)
+    c = np.cumsum(w)
+    t = float(x["u_sample"][b]) * c[-1]
+    lo = c[tok - 1] if tok > 0 else 0.0
+    return w[tok] > 0 and lo - CDF_TOL * c[-1] <= t <= c[tok] + CDF_TOL * c[-1]
+
+
 def check(x, temperature, min_decided=0.5):
     al, nt = gpu_stochastic(x, temperature)
     ral, rnt, ma, ms = oracle.accept_stochastic(
         x["target_logits"], x["draft_logits"], x["draft_tokens"], x["draft_len"],
         x["u_accept"], x["u_sample"], temperature)
+    dm = oracle.stochastic_decisions(x["target_logits"], x["draft_logits"], x["draft_tokens"],
+                                     x["draft_len"], x["u_accept"], temperature)
     D = x["draft_len"]
+    d_off = np.concatenate([[0], np.cumsum(D.astype(np.int64))])
     assert np.all((al >= 1) & (al <= D + 1))
+    raw_diff = 0
+    for b in range(len(D)):
+        n = int(al[b]) - 1            # drafts the GPU kept
+        sb = dm[d_off[b]:d_off[b + 1]]
+        firm = np.abs(sb) >= ACC_MARGIN
+        # kept on the GPU: positions 0..n-1; rejected: position n (if n < D)
+        assert not np.any(firm[:n] & (sb[:n] <= 0)), (b, n, sb[:n + 1])
+        if n < D[b]:
+            assert not (firm[n] and sb[n] > 0), (b, n, sb[n])
+        raw_diff += int(al[b] != ral[b])
     decided = ma >= ACC_MARGIN
     assert np.array_equal(al[decided], ral[decided]), (al, ral, ma)
     assert decided.mean() >= min_decided
-    for b in np.nonzero(al == ral)[0]:
-        if ms[b] >= CDF_TOL:
+    for b in range(len(D)):
+        if al[b] == ral[b] and ms[b] >= CDF_TOL:
             assert nt[b] == rnt[b], (b, nt[b], rnt[b], ms[b])
         else:
-            w = _draw_weights(x, b, int(al[b]) - 1, temperature)
-            c = np.cumsum(w)
-            t = float(x["u_sample"][b]) * c[-1]
-            k = int(nt[b])
-            lo = c[k - 1] if k > 0 else 0.0
-            assert w[k] > 0 and lo - CDF_TOL * c[-1] <= t <= c[k] + CDF_TOL * c[-1], (b, k)
+            assert _valid_draw(x, b, int(al[b]) - 1, temperature, int(nt[b])), (b, nt[b])
+    print("sequences %d, acceptance lengths differing at a low-margin decision: %d"
+          % (len(D), raw_diff))
     return al, nt
 
 
@@ -162,3 +183,34 @@ def test_repeatable_and_device_checks():
     assert sv.workspace_status(ws, clear=True) == 8
     assert int(outs[0][0]) == -7 and int(outs[1][0]) == -7
     assert bool((outs[0][1:] != -7).all()) and bool((outs[1][1:] != -7).all())
+
+
+def test_all_zero_residual_draws_from_the_target():
+    """p = q at a draft position and the drafted token impossible under both (logit -inf in
+    both rows): the draft is rejected (0 < 0 fails) and every weight of max(0, p - q) is 0,
+    so the token is drawn from the target's row of that position."""
+    V = 5000
+    w = synth.Workload("z", B=6, Hq=1, Hkv=1, d=8, D=3, T=1, V=V, p=0.5, logits_dtype="fp32")
+    x = synth.stochastic_inputs(w, 8, noise=0.2)
+    D = x["draft_len"]
+    rng = np.random.default_rng(9)
+    d_off = 0
+    for b in range(len(D)):
+        q_off = d_off + b
+        if D[b] >= 1:
+            j = int(rng.integers(D[b]))
+            tok = int(rng.integers(V))
+            row = x["target_logits"][q_off + j].copy()
+            row[tok] = -np.inf
+            x["target_logits"][q_off + j] = row
+            x["draft_logits"][d_off + j] = row
+            x["draft_tokens"][d_off + j] = tok
+            # the drafts before it are the drafter's copies of the target (kept for u < 1)
+            for jj in range(j):
+                x["draft_logits"][d_off + jj] = x["target_logits"][q_off + jj]
+        d_off += int(D[b])
+    al, nt = check(x, 1.0, min_decided=0.0)
+    ral, _, _, _ = oracle.accept_stochastic(
+        x["target_logits"], x["draft_logits"], x["draft_tokens"], x["draft_len"],
+        x["u_accept"], x["u_sample"], 1.0)
+    assert np.array_equal(al, ral)

@@ -50,6 +50,7 @@ SMALL = {
     "empty_prefix": dict(B=2, Hq=8, Hkv=2, d=64, T=(0, 1), D=(4, 0)),
     "tile_edges": dict(B=4, Hq=8, Hkv=2, d=128, T=(63, 64, 127, 128), D=(0, 1, 0, 1)),
     "rows_136": dict(B=2, Hq=32, Hkv=4, d=128, T=(500, 260), D=(16, 16)),
+    "rows_192": dict(B=2, Hq=32, Hkv=4, d=128, T=(700, 129), D=(23, 23)),
     "rows_256": dict(B=1, Hq=32, Hkv=4, d=128, T=(400,), D=(31,)),
     "llama3_8b_shape": dict(B=2, Hq=32, Hkv=8, d=128, T=(1500, 333), D=(31, 31)),
     "d64_ragged": dict(B=3, Hq=16, Hkv=2, d=64, T=(513, 5, 2049), D=(8, 2, 1)),
@@ -162,8 +163,8 @@ def _sample_units(w, x, n, seed):
     return sorted(picks)
 
 
-@pytest.mark.parametrize("cfg,D", [("c1", None), ("c2", None), ("c3", None), ("c4", 0),
-                                   ("c4", 15), ("c4", 16), ("c4", 31), ("c5", None)])
+@pytest.mark.parametrize("cfg,D", [("c1", None), ("c2", None), ("c3", None)]
+                         + [("c4", Dc) for Dc in synth.C4_SWEEP_D] + [("c5", None)])
 def test_full_size_sampled_units(kernel, cfg, D):
     w, x = _full(cfg, D)
     got = gpu_attn(x)
