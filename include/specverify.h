@@ -217,8 +217,9 @@ SV_API sv_status spec_accept(int32_t batch, int32_t max_draft_len, int32_t vocab
  *   - a shape whose spec_accept_workspace_size() exceeds it is rejected with
  *     SV_ERR_WORKSPACE and nothing is launched (512 KiB covers 43,000 window rows);
  *   - the first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call before any
- *     stream capture;
+ *     (cudaGetSymbolAddress) with that device current, and caches it with the id of the
+ *     device's current context; a call in a new context (after cudaDeviceReset, say)
+ *     looks it up again. Make the first call in each context before any stream capture;
  *   - all calls share the array and it keeps the last call's contents: two calls that can
  *     run at the same time on the GPU (different streams or host threads) race and may
  *     return wrong tokens;
@@ -387,6 +388,18 @@ SV_API void sv_set_profile_events(void* start_event, void* stop_event);
  * failure per arming; after < 0 disarms. Returns the launches that were still to go
  * before a pending failure, or -1 if none was pending. Process-wide. */
 SV_API int sv_inject_launch_failure(int after);
+
+/* Fault injection for tests, on the device side of the tcgen05 attention kernel's bounded
+ * waits: the next verify-attention launch of that kernel gives every barrier wait
+ * `limit_cycles` clock cycles instead of about 2 s, and each of its CTAs withholds the K
+ * and V loads of the first tile of its range, so the waits for that tile run out. The kernel
+ * then sets SV_ERR_TIMEOUT in the workspace (read it with sv_workspace_status); every role
+ * of every CTA leaves its loop, the copies and MMAs still in flight are waited for, TMEM
+ * is freed, and the kernel returns. The call itself returns SV_OK and its outputs are
+ * unspecified; the workspace serves the next call once its flags are cleared. Calls that
+ * run the mma.sync kernel leave the arming pending. limit_cycles <= 0 disarms. Returns 1
+ * if an arming was pending, else 0. Process-wide. */
+SV_API int sv_inject_wait_timeout(int64_t limit_cycles);
 
 /* Library version: major * 10000 + minor * 100 + patch. */
 SV_API int sv_version(void);

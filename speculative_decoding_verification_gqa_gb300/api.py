@@ -35,7 +35,8 @@ EXPORTS = ("spec_verify_attn_workspace_size", "spec_verify_attn", "spec_verify_a
            "spec_accept", "spec_draft_signals_workspace_size", "spec_draft_signals",
            "sv_workspace_status", "sv_status_string", "sv_set_attn_kernel", "sv_set_unit_ctas",
            "sv_set_profile_events", "sv_version", "sv_plan_preview",
-           "sv_inject_launch_failure", "spec_accept_stochastic_workspace_size",
+           "sv_inject_launch_failure", "sv_inject_wait_timeout",
+           "spec_accept_stochastic_workspace_size",
            "spec_accept_stochastic")
 
 
@@ -116,6 +117,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.spec_accept_stochastic.restype = ctypes.c_int
         lib.sv_inject_launch_failure.argtypes = [ctypes.c_int]
         lib.sv_inject_launch_failure.restype = ctypes.c_int
+        lib.sv_inject_wait_timeout.argtypes = [ctypes.c_int64]
+        lib.sv_inject_wait_timeout.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -420,6 +423,15 @@ def inject_launch_failure(after: int) -> int:
     negative ``after`` disarms. Returns the launches that were still to go before a
     pending failure, or -1."""
     return load_library().sv_inject_launch_failure(int(after))
+
+
+def inject_wait_timeout(limit_cycles: int) -> int:
+    """Test hook: the next launch of the tcgen05 attention kernel waits at most
+    ``limit_cycles`` clock cycles per barrier and each CTA withholds its first tile's
+    loads, so the kernel gives up, sets SV_ERR_TIMEOUT in the workspace and returns. 0
+    disarms.
+    Returns 1 if an arming was pending, else 0."""
+    return load_library().sv_inject_wait_timeout(int(limit_cycles))
 
 
 def set_profile_events(start=None, stop=None):

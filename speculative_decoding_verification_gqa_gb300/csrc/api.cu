@@ -41,6 +41,8 @@ constexpr int64_t MAX_KV_ROWS = 0x7fffffff - 1024;
 
 // Launches until the armed failure, plus one (0: nothing armed). Tests only.
 std::atomic<int> g_fail_countdown{0};
+// Wait limit of the next tcgen05 attention launch that withholds a tile (0: none). Tests.
+std::atomic<long long> g_stall_limit{0};
 int g_attn_kernel = 0;  // 0 automatic, 1 mma.sync, 2 tcgen05
 int g_unit_ctas = SV_UNIT_CTAS;  // -1 cost model, 0 split tile line, k > 0 k CTAs per unit
 cudaEvent_t g_ev_start = nullptr;
@@ -100,7 +102,11 @@ SV_API int sv_inject_launch_failure(int after) {
   return prev - 1;
 }
 
-SV_API int sv_version(void) { return 300; }  // 0.3.0: plan preview
+SV_API int sv_inject_wait_timeout(int64_t limit_cycles) {
+  return g_stall_limit.exchange(limit_cycles > 0 ? (long long)limit_cycles : 0) > 0 ? 1 : 0;
+}
+
+SV_API int sv_version(void) { return 400; }  // 0.4.0: wait-timeout injection
 
 SV_API const char* sv_status_string(sv_status s) {
   switch (s) {
@@ -237,6 +243,13 @@ sv_status verify_impl(const sv_attn_desc* desc, const void* q, const void* k_cac
   const int which = pick_kernel(desc);
   const int kt = which == 2 ? attn_tc_kt() : attn_mma_kt();
   AttnParams p = shape_params(desc, pg, which, sms);
+  if (which == 2) {  // a pending wait-timeout injection applies to this launch
+    const long long lim = g_stall_limit.exchange(0);
+    if (lim > 0) {
+      p.wait_limit = lim;
+      p.stall_first_tile = 1;
+    }
+  }
   uint8_t* ws = (uint8_t*)workspace;
   p.q = q;
   p.k = k_cache;

@@ -101,26 +101,32 @@ __device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// What a bounded wait needs: the CTA's abort flag (shared memory), the workspace flag word
+// and the limit in clock cycles (a kernel parameter).
+struct Waiter {
+  volatile int* abort;
+  uint32_t* flags;
+  long long limit;
+};
+
 // Bounded wait for the phase with the given parity. Returns false (and raises the CTA's
 // abort flag and the workspace timeout flag) if it gives up or another role already did.
-__device__ __noinline__ bool mbar_wait_slow(uint64_t* b, uint32_t parity, volatile int* abort,
-                                            uint32_t* flags) {
+__device__ __noinline__ bool mbar_wait_slow(uint64_t* b, uint32_t parity, const Waiter w) {
   const long long t0 = clock64();
   while (true) {
     if (mbar_try(b, parity)) return true;
-    if (*abort) return false;
-    if (clock64() - t0 > TIMEOUT_CYCLES) {
-      *abort = 1;
-      atomicOr(flags, FLAG_TIMEOUT);
+    if (*w.abort) return false;
+    if (clock64() - t0 > w.limit) {
+      *w.abort = 1;
+      atomicOr(w.flags, FLAG_TIMEOUT);
       return false;
     }
   }
 }
 
 // The common case (phase already complete) costs one try_wait and no call.
-__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, volatile int* abort,
-                                          uint32_t* flags) {
-  return mbar_try(b, parity) || mbar_wait_slow(b, parity, abort, flags);
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, const Waiter& w) {
+  return mbar_try(b, parity) || mbar_wait_slow(b, parity, w);
 }
 
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint64_t* bar,
@@ -408,6 +414,7 @@ __device__ __forceinline__ void attn_tc_body(const AttnParams& p, const CUtensor
   extern __shared__ __align__(1024) uint8_t smem[];  // 128-byte swizzled tiles: 1 KiB aligned
   Bars* bars = (Bars*)(smem + L::BARS);
   volatile int* abort = &bars->abort;
+  const Waiter wt{abort, p.flags, p.wait_limit > 0 ? p.wait_limit : TIMEOUT_CYCLES};
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   pdl_trigger();
   pdl_wait();  // the plan of this call is complete
@@ -477,6 +484,9 @@ __device__ __forceinline__ void attn_tc_body(const AttnParams& p, const CUtensor
     bool ok = true;
     const int box = p.block_size > 0 ? min(p.block_size, KT) : KT;
     const int nbox = KT / box;  // boxes per tile, one per lane
+    // test hook: the first tile of the CTA's range is never loaded (its barriers are never
+    // armed), so every wait for it runs out; stage 0 then holds no copy to wait for
+    const bool withhold = p.stall_first_tile != 0;
     auto load_k = [&](uint32_t st, int n, int g, int grow) {
       const uint32_t roff = (uint32_t)(n * box * 128);
       if constexpr (F8) {
@@ -524,11 +534,12 @@ __device__ __forceinline__ void attn_tc_body(const AttnParams& p, const CUtensor
         const int grow = p.block_size == 0 ? row0 + j * KT : (mine ? paged_row(j, lane) : 0);
         bool w = true;
         if (it >= L::NR && lane == 0)
-          w = mbar_wait(&bars->kv_empty[st], ((it / L::NR) - 1) & 1, abort, p.flags);
+          w = mbar_wait(&bars->kv_empty[st], ((it / L::NR) - 1) & 1, wt);
         if (!__shfl_sync(0xffffffffu, w, 0)) {
           ok = false;
           break;
         }
+        if (withhold && it == 0) continue;
         // the boxes of a tile add up to one full tile per tensor
         if (lane == 0) mbar_expect_tx(&bars->k_full[st], F8 ? L::RAW : L::TILE);
         __syncwarp();
@@ -538,9 +549,11 @@ __device__ __forceinline__ void attn_tc_body(const AttnParams& p, const CUtensor
         if (mine) load_v(st, lane, s.g, grow);
       }
     }
-    if (lane == 0 && (!ok || *abort)) {
-      // leave no copy in flight: wait (bounded) for the last fill of every stage
-      for (uint32_t st = 0; st < L::NR && st < it; ++st) {
+    if (lane == 0) {
+      // leave no copy in flight: wait (bounded) for the last fill of every stage. Normally
+      // its readers have waited for it too; after another role gave up they may not have,
+      // and the copy must land before the CTA's shared memory is released.
+      for (uint32_t st = withhold ? 1 : 0; st < L::NR && st < it; ++st) {
         const uint32_t fills = (it - 1 - st) / L::NR + 1;
         const uint32_t par = (fills - 1) & 1;
         const long long t0 = clock64();
@@ -562,12 +575,12 @@ __device__ __forceinline__ void attn_tc_body(const AttnParams& p, const CUtensor
       uint32_t it = 0, seg_i = 0;
       bool ok = true;
       while (ok && seg_next<WIN>(pl, num_units, t, t_end, u, s)) {
-        if (!mbar_wait(&bars->q_full, seg_i & 1, abort, p.flags)) break;
+        if (!mbar_wait(&bars->q_full, seg_i & 1, wt)) break;
         fence_after();
         for (int j = s.j0; j < s.j1; ++j, ++it) {
           const uint32_t st = it % L::NR;
-          if (!mbar_wait(&bars->k_full[st], (it / L::NR) & 1, abort, p.flags) ||
-              (it >= 1 && !mbar_wait(&bars->s_free, (it - 1) & 1, abort, p.flags))) {
+          if (!mbar_wait(&bars->k_full[st], (it / L::NR) & 1, wt) ||
+              (it >= 1 && !mbar_wait(&bars->s_free, (it - 1) & 1, wt))) {
             ok = false;
             break;
           }
@@ -615,13 +628,13 @@ __device__ __forceinline__ void attn_tc_body(const AttnParams& p, const CUtensor
           const uint32_t st = F8 ? it % NCV : it % L::NR;
           uint64_t* vready = F8 ? &bars->vc_full[st] : &bars->v_full[st];
           const uint32_t vpar = F8 ? (it / NCV) & 1 : (it / L::NR) & 1;
-          if (!mbar_wait(vready, vpar, abort, p.flags)) {
+          if (!mbar_wait(vready, vpar, wt)) {
             ok = false;
             break;
           }
           const uint64_t vd = vdesc0 + ((st * (F8 ? L::TILE : L::STAGE)) >> 4);
           for (int w = 0; w < 2 && ok; ++w) {
-            if (!mbar_wait(&bars->p_full[w], it & 1, abort, p.flags)) {
+            if (!mbar_wait(&bars->p_full[w], it & 1, wt)) {
               ok = false;
               break;
             }
@@ -652,7 +665,7 @@ __device__ __forceinline__ void attn_tc_body(const AttnParams& p, const CUtensor
     const uint32_t colS = COL_S + wg * HK;
     constexpr int OC = HD / 2;             // output columns per warpgroup in the epilogue
     auto wwait = [&](uint64_t* bar, uint32_t par) -> bool {
-      return __all_sync(0xffffffffu, mbar_wait(bar, par, abort, p.flags));
+      return __all_sync(0xffffffffu, mbar_wait(bar, par, wt));
     };
     int64_t t = t_begin;
     int u = u_first;
@@ -947,8 +960,8 @@ __device__ __forceinline__ void attn_tc_body(const AttnParams& p, const CUtensor
         const int kvis = WIN ? T + 1 - window : -1;
         for (int j = s.j0; j < s.j1; ++j, ++it) {
           const uint32_t rs = it % L::NR, cs = it % NCV;
-          if (!mbar_wait(&bars->v_full[rs], (it / L::NR) & 1, abort, p.flags) ||
-              (it >= NCV && !mbar_wait(&bars->vc_empty[cs], ((it / NCV) - 1) & 1, abort, p.flags))) {
+          if (!mbar_wait(&bars->v_full[rs], (it / L::NR) & 1, wt) ||
+              (it >= NCV && !mbar_wait(&bars->vc_empty[cs], ((it / NCV) - 1) & 1, wt))) {
             ok = false;
             break;
           }

@@ -129,6 +129,10 @@ struct AttnParams {
   int window;                 // sliding window in positions (0: every earlier key); set to 0
                               // when it covers max_seq + max_draft + 1 positions
   float scale_log2;           // softmax_scale * log2(e)
+  long long wait_limit;       // tcgen05 kernel: clock cycles a barrier wait may take before
+                              // it gives up (0: the default, about 2 s)
+  int stall_first_tile;       // test hook: every CTA's producer withholds the K and V loads
+                              // of the first tile of its range, so the waits for it run out
 };
 
 // First key tile of row tile mt of a sequence with T cached keys. Window row i sees keys

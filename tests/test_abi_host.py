@@ -265,3 +265,12 @@ def test_empty_draft_arrays_get_a_placeholder_pointer():
         assert p.numel() > 0 and p.dtype == dt and p.device == e.device
         full = torch.ones(3, dtype=dt)
         assert api._or_placeholder(full) is full
+
+
+def test_wait_timeout_hook_arms_and_disarms(lib):
+    lib.sv_inject_wait_timeout.argtypes = [ctypes.c_int64]
+    assert lib.sv_inject_wait_timeout(0) == 0       # nothing pending
+    assert lib.sv_inject_wait_timeout(100000) == 0
+    assert lib.sv_inject_wait_timeout(5000) == 1    # re-armed: the previous arming was pending
+    assert lib.sv_inject_wait_timeout(-3) == 1      # disarmed
+    assert lib.sv_inject_wait_timeout(0) == 0

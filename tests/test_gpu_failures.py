@@ -159,3 +159,61 @@ def test_accept_and_signals_write_nothing_outside_their_outputs():
     ral, rnt, ramax = oracle.spec_accept(a["logits"], a["draft_tokens"], a["draft_len"])
     assert np.array_equal(al.cpu().numpy(), ral) and np.array_equal(nt.cpu().numpy(), rnt)
     assert np.array_equal(tg.cpu().numpy(), ramax)
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8_e4m3"])
+@pytest.mark.parametrize("entry", ["packed", "host_lengths"])
+def test_bounded_wait_runs_out_and_the_kernel_returns(kv, entry):
+    """The tcgen05 kernel's barrier waits are bounded. With a short limit (1e5 cycles, about
+    50 us) and the first tile of every CTA's range withheld (sv_inject_wait_timeout), the
+    waits for that tile run out: the call returns, the workspace reports SV_ERR_TIMEOUT,
+    the kernel ends well before the default limit (about 2 s), and the next calls, on the
+    same workspace once its flags are cleared and on a fresh one, match the oracle."""
+    import time
+    try:
+        prev = sv.set_attn_kernel(2)
+    except ValueError:
+        pytest.skip("tcgen05 kernel not built")
+    try:
+        w = synth.Workload("t", B=3, Hq=16, Hkv=4, d=128, D=0, T=0, V=8, p=0.5, kv_dtype=kv,
+                           outlier_prob=0.001 if kv != "bf16" else 0.0)
+        x = synth.attn_inputs(w, 23, seq_lens=np.array([900, 5, 300]),
+                              draft_len=np.array([7, 0, 3]))
+        q, k, v, sc, T, D = dev_attn(x)
+        Th = torch.from_numpy(x["seq_lens"].astype(np.int32))
+        Dh = torch.from_numpy(x["draft_len"].astype(np.int32))
+        ws = sv.new_workspace(sv.verify_workspace_bytes(sv.api.attn_desc(q, k, 3, 7, 900)))
+        out = torch.empty_like(q)
+
+        def call(wsp):
+            if entry == "packed":
+                return sv.spec_verify_attn(q, k, v, T, D, max_draft_len=7, max_seq_len=900,
+                                           kv_scale=sc, out=out, workspace=wsp)
+            return sv.spec_verify_attn_host_lengths(q, k, v, T, D, Th, Dh, max_draft_len=7,
+                                                    max_seq_len=900, kv_scale=sc, out=out,
+                                                    workspace=wsp)
+
+        call(ws)  # warm: module load, first launch
+        torch.cuda.synchronize()
+        assert sv.workspace_status(ws) == 0
+        ref = oracle_attn(w, x)
+        assert sv.api.inject_wait_timeout(100000) == 0
+        t0 = time.perf_counter()
+        call(ws)
+        torch.cuda.synchronize()
+        elapsed = time.perf_counter() - t0
+        assert sv.workspace_status(ws, clear=True) == 7   # SV_ERR_TIMEOUT
+        assert elapsed < 0.5, elapsed
+        assert sv.api.inject_wait_timeout(0) == 0          # the arming was used once
+        call(ws)
+        torch.cuda.synchronize()
+        assert sv.workspace_status(ws) == 0
+        assert_close(_bits(out), ref)
+        ws2 = sv.new_workspace(sv.verify_workspace_bytes(sv.api.attn_desc(q, k, 3, 7, 900)))
+        call(ws2)
+        torch.cuda.synchronize()
+        assert sv.workspace_status(ws2) == 0
+        assert_close(_bits(out), ref)
+    finally:
+        sv.api.inject_wait_timeout(0)
+        sv.set_attn_kernel(prev)
