@@ -10,6 +10,8 @@
 // Cost and limits: every GPU that loads the library holds kNoallocScratchBytes of device
 // memory until the process exits; shapes that need more scratch are rejected. All calls
 // share the one array per device, so calls that can overlap on the GPU race.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "internal.cuh"
@@ -21,22 +23,59 @@ constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) uint8_t g_accept_scratch[kNoallocScratchBytes];
 
-std::mutex g_scratch_mu;
-void* g_scratch_addr[kMaxDevices];  // device address of g_accept_scratch, per device
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
 
-// Device address of the scratch array on the current device. In host code the array's
-// name is only a host-side stand-in, so the address is looked up once per device (with
-// that device current) and cached.
+// Driver entry points, fetched through the runtime (the library links no libcuda).
+template <class Fn>
+Fn driver_fn(const char* name) {
+  void* f = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  return (Fn)f;
+}
+
+// Unique id of the calling thread's current context (0 if there is none yet).
+bool current_ctx_id(unsigned long long* id) {
+  static CtxGetCurrentFn get_cur = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+  static CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+  if (!get_cur || !get_id) return false;
+  CUcontext c = nullptr;
+  if (get_cur(&c) != CUDA_SUCCESS) return false;
+  if (!c) {
+    *id = 0;
+    return true;
+  }
+  return get_id(c, id) == CUDA_SUCCESS;
+}
+
+struct ScratchEntry {
+  unsigned long long ctx;  // context the address belongs to
+  void* addr;              // device address of g_accept_scratch in it
+};
+std::mutex g_scratch_mu;
+ScratchEntry g_scratch[kMaxDevices];
+
+// Device address of the scratch array in the current device's current context. In host
+// code the array's name is only a host-side stand-in, so the address is looked up with
+// cudaGetSymbolAddress and cached per device, together with the id of the context it
+// belongs to: after cudaDeviceReset (or any new primary context) the id changes and the
+// address is looked up again in the new context, whose copy of the array starts at zero.
 sv_status scratch_on_current_device(void** addr) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SV_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
+  unsigned long long ctx = 0;
+  if (!current_ctx_id(&ctx)) return SV_ERR_CUDA;
+  if (ctx == 0 || g_scratch[dev].ctx != ctx || !g_scratch[dev].addr) {
+    void* p = nullptr;  // (makes the device's primary context current if there was none)
     if (cudaGetSymbolAddress(&p, g_accept_scratch) != cudaSuccess || !p) return SV_ERR_CUDA;
-    g_scratch_addr[dev] = p;
+    if (!current_ctx_id(&ctx) || ctx == 0) return SV_ERR_CUDA;
+    g_scratch[dev] = ScratchEntry{ctx, p};
   }
-  *addr = g_scratch_addr[dev];
+  *addr = g_scratch[dev].addr;
   return SV_OK;
 }
 
