@@ -89,6 +89,12 @@ def parse():
                          "blocks of this many positions (0: skip)")
     ap.add_argument("--side-stochastic", type=int, default=1,
                     help="also time spec_accept_stochastic on the step's shapes (0: skip)")
+    ap.add_argument("--per-config", default="c3,c4:15,c4:16,c4:31,c5",
+                    help="other workloads measured into the line's per_config object, as "
+                         "config[:D] items ('none': skip; only with the default --config)")
+    ap.add_argument("--per-config-steps", type=int, default=100)
+    ap.add_argument("--only-step", action="store_true",
+                    help="run W + K steps of the workload and exit (for profilers)")
     return ap.parse_args()
 
 
@@ -139,6 +145,70 @@ def flops(w, T, D):
     # QK and PV over the visible keys of every row (window-causal): 4 * d per (row, key)
     keys = np.sum(W * T + W * (W + 1) // 2)
     return int(4 * w.Hq * w.d * keys)
+
+
+# Nominal dense tensor rates of the part (PFLOP/s): e4m3 4.5, bf16/f16 2.25. Only bf16 is
+# measured, so an e4m3 contraction's peak is the measured bf16 peak times their ratio.
+E4M3_OVER_BF16 = 4.5 / 2.25
+
+
+def tensor_seconds(fl, kv_dtype, attn_kernel, bf16_tflops):
+    """Tensor-core time of the attention's algorithmic FLOPs at the peak of the type each
+    contraction runs in. Q K^T and P V are half of the FLOPs each. bf16 K/V: both on the
+    16-bit path. FP8 K/V on the tcgen05 kernel: Q K^T on the 8-bit path (E4M3 K, Q as E4M3
+    terms) at the e4m3 peak, P V on the 16-bit path; on the mma.sync kernel both run in f16
+    (K and V decoded)."""
+    p16 = bf16_tflops * 1e12
+    if kv_dtype == "fp8_e4m3" and attn_kernel == "tcgen05":
+        return fl / 2.0 / (p16 * E4M3_OVER_BF16) + fl / 2.0 / p16
+    return fl / p16
+
+
+def roofline_record(kv_bytes, qo_bytes, fl, attn_s, hbm_gbs, bf16_tflops, kv_dtype,
+                    attn_kernel, traffic=None):
+    """The attention kernel against its roofline: the bound is the slower of its
+    algorithmic bytes at the HBM peak and its algorithmic FLOPs at the tensor peak of their
+    types; achieved and peak are in that bound's unit, frac = achieved / peak (the bound's
+    time over the kernel's)."""
+    nbytes = kv_bytes + qo_bytes
+    t_hbm = nbytes / (hbm_gbs * 1e9)
+    t_tc = tensor_seconds(fl, kv_dtype, attn_kernel, bf16_tflops)
+    if t_hbm >= t_tc:
+        bound, unit = "hbm", "GB/s"
+        achieved, peak = nbytes / attn_s / 1e9, hbm_gbs
+    else:
+        bound, unit = "tensor", "TFLOP/s"
+        achieved, peak = fl / attn_s / 1e12, fl / t_tc / 1e12
+    return {"bound": bound, "achieved": round(achieved, 1), "peak": round(peak, 1),
+            "unit": unit, "frac": round(achieved / peak, 4), "traffic": traffic,
+            "algorithmic_bytes": nbytes, "algorithmic_flops": int(fl),
+            "t_hbm_us": round(t_hbm * 1e6, 2), "t_tensor_us": round(t_tc * 1e6, 2)}
+
+
+def kernel_source_hash():
+    """First 16 hex digits of the sha256 of the library's CUDA sources and header: names
+    the kernel version an ncu capture was taken of."""
+    import glob
+    import hashlib
+    pkg = os.path.join(ROOT, "speculative_decoding_verification_gqa_gb300", "csrc")
+    files = sorted(glob.glob(os.path.join(pkg, "*.cu")) + glob.glob(os.path.join(pkg, "*.cuh")))
+    files.append(os.path.join(ROOT, "include", "specverify.h"))
+    h = hashlib.sha256()
+    for f in files:
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(config, D, attn_kernel, src_hash=None):
+    """DRAM bytes (read + written) per launch of the attention kernel from the ncu capture
+    of this workload, or None when there is none for the current sources."""
+    e = NCU_TRAFFIC.get((config, D, attn_kernel))
+    if e is None:
+        return None
+    h, nbytes = e
+    return nbytes if h == (src_hash or kernel_source_hash()) else None
 
 
 class ClockSampler:
@@ -307,10 +377,139 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-# DRAM bytes (read + written) per launch of the attention kernel, from one ncu capture of
-# the current kernel on that workload (dram__bytes_read.sum + dram__bytes_write.sum). Only
-# valid for the kernel version that was captured: drop an entry when the kernel changes.
-NCU_TRAFFIC = {("c2", "tcgen05"): 549_326_080, ("c3", "tcgen05"): 546_970_368}
+# DRAM bytes (read + written) per launch of the attention kernel, from one ncu capture per
+# workload (dram__bytes_read.sum + dram__bytes_write.sum), keyed by (config, D override,
+# kernel) with the kernel_source_hash() of the sources captured: an entry whose hash is not
+# the current one reads as None.
+NCU_TRAFFIC = {}
+
+
+class Rig:
+    """One workload's inputs on the device (and in pinned host memory for the end-to-end
+    figures), its outputs and workspaces, and the step: spec_verify_attn + spec_accept."""
+
+
+def build_rig(sv, synth, w, T, D, p, seed, dev, pinned=True):
+    import torch
+    r = Rig()
+    r.x = x = synth.attn_inputs(w, seed, seq_lens=T, draft_len=D)
+    r.a = a = synth.accept_inputs(w, seed, draft_len=D, p=p)
+
+    def host_tensor(arr, dtype):
+        t = torch.from_numpy(arr.view(np.int16) if dtype == torch.bfloat16 else arr)
+        if dtype == torch.bfloat16:
+            t = t.view(torch.bfloat16)
+        return t.pin_memory() if pinned else t
+
+    r.kvdt = kvdt = torch.uint8 if w.kv_dtype == "fp8_e4m3" else torch.bfloat16
+    lgdt = torch.bfloat16 if w.logits_dtype == "bf16" else torch.float32
+    h = {"q": host_tensor(x["q"], torch.bfloat16), "k": host_tensor(x["k"], kvdt),
+         "v": host_tensor(x["v"], kvdt), "T": host_tensor(x["seq_lens"], torch.int32),
+         "D": host_tensor(x["draft_len"], torch.int32),
+         "logits": host_tensor(a["logits"], lgdt),
+         "draft": host_tensor(a["draft_tokens"], torch.int32)}
+    if x["kv_scale"] is not None:
+        h["sc"] = host_tensor(x["kv_scale"], torch.float32)
+    r.h = h
+    r.d = d = {k: t.to(dev) for k, t in h.items()}
+    r.out = torch.empty_like(d["q"])
+    r.al = torch.empty(w.B, dtype=torch.int32, device=dev)
+    r.nt = torch.empty(w.B, dtype=torch.int32, device=dev)
+    r.md, r.ms = int(D.max()), int(T.max())
+    r.desc = sv.api.attn_desc(d["q"], d["k"], w.B, r.md, r.ms)
+    r.ws_attn = sv.new_workspace(sv.verify_workspace_bytes(r.desc), dev)
+    r.ws_acc = sv.new_workspace(sv.accept_workspace_bytes(w.B, r.md, w.V), dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        sv.spec_verify_attn(d["q"], d["k"], d["v"], d["T"], d["D"], max_draft_len=r.md,
+                            max_seq_len=r.ms, kv_scale=d.get("sc"), out=r.out,
+                            workspace=r.ws_attn, stream=stream)
+        sv.spec_accept(d["logits"], d["draft"], d["D"], max_draft_len=r.md, accept_len=r.al,
+                       next_token=r.nt, workspace=r.ws_acc, stream=stream)
+
+    r.step = step
+    return r
+
+
+def warm_up(step, n_min, seconds=0.3):
+    """At least n_min steps and `seconds` of them. Returns the number run."""
+    import torch
+    n = 0
+    t0 = time.perf_counter()
+    while n < n_min or time.perf_counter() - t0 < seconds:
+        step()
+        n += 1
+        if n % 16 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    return n
+
+
+def timed_steps(step, stream, K):
+    """ms per step over exactly K steps: CUDA events on the launching stream around the
+    loop, synchronised on both sides."""
+    import torch
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for _ in range(K):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1) / K
+
+
+def timed_attention(sv, step, stream, K):
+    """Mean duration (ms) of the attention kernel over K more steps, from events the library
+    records just before and after it on the call's stream."""
+    import torch
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    for a_, b_ in ev:  # create the events the library records into
+        a_.record(stream)
+        b_.record(stream)
+    torch.cuda.synchronize()
+    for a_, b_ in ev:
+        sv.set_profile_events(a_, b_)
+        step()
+    torch.cuda.synchronize()
+    sv.set_profile_events(None, None)
+    return float(np.mean([a_.elapsed_time(b_) for a_, b_ in ev]))
+
+
+def measure_config(sv, synth, cfg, Dv, seed, dev, K, W, attn_kernel, src_hash):
+    """The step of another workload: attention and step time, K/V GB/s, verified query
+    tokens/s, accepted tokens/s and the attention kernel's roofline."""
+    import torch
+    w = synth.CONFIGS[cfg]
+    T, D, p = synth.lengths(w, seed, D=Dv)
+    rig = build_rig(sv, synth, w, T, D, p, seed, dev, pinned=False)
+    stream = torch.cuda.current_stream()
+    warm_up(rig.step, W)
+    if sv.workspace_status(rig.ws_attn) != 0 or sv.workspace_status(rig.ws_acc) != 0:
+        raise RuntimeError("device-side check failed on %s" % cfg)
+    accepted = int(rig.al.sum().item())
+    ms_step = timed_steps(rig.step, stream, K)
+    attn_ms = timed_attention(sv, rig.step, stream, K)
+    kv, qo = algorithmic_bytes(w, T, D)
+    fl = flops(w, T, D)
+    hbm, tf, _ = peaks()
+    W_rows = int(np.sum(D.astype(np.int64) + 1))
+    rec = {"workload": describe(w, T, D), "steps": K, "attn_us": round(attn_ms * 1e3, 2),
+           "step_us": round(ms_step * 1e3, 2),
+           "attn_kv_GB_per_s": round(kv / (attn_ms / 1e3) / 1e9, 1),
+           "step_kv_GB_per_s": round(kv / (ms_step / 1e3) / 1e9, 1),
+           "verified_query_tokens_per_s": round(W_rows / (ms_step / 1e3), 1),
+           "accepted_tokens_per_s": round(accepted / (ms_step / 1e3), 1),
+           "mean_accept_len": round(accepted / w.B, 3),
+           "attn_tflops": round(fl / (attn_ms / 1e3) / 1e12, 1),
+           "roofline": roofline_record(kv, qo, fl, attn_ms / 1e3, hbm, tf, w.kv_dtype,
+                                       attn_kernel, ncu_traffic(cfg, Dv, attn_kernel, src_hash))}
+    del rig
+    torch.cuda.empty_cache()
+    return rec
 
 
 def run_ours(args):
@@ -338,46 +537,31 @@ def run_ours(args):
 
     w, T, D, p = workload(args)
     seed = replica_seed(args.seed, rank)  # each rank verifies its own batch (replicas)
-    x = synth.attn_inputs(w, seed, seq_lens=T, draft_len=D)
-    a = synth.accept_inputs(w, seed, draft_len=D, p=p)
+    rig = build_rig(sv, synth, w, T, D, p, seed, dev, pinned=True)
+    x, a, h, d = rig.x, rig.a, rig.h, rig.d
+    out, al, nt, ws_attn, ws_acc = rig.out, rig.al, rig.nt, rig.ws_attn, rig.ws_acc
+    md, ms, desc, step = rig.md, rig.ms, rig.desc, rig.step
+    kvdt = rig.kvdt
     kv_bytes, qo_bytes = algorithmic_bytes(w, T, D)
     fl = flops(w, T, D)
-    md, ms = int(D.max()), int(T.max())
-
-    def host_tensor(arr, dtype):
-        t = torch.from_numpy(arr.view(np.int16) if dtype == torch.bfloat16 else arr)
-        if dtype == torch.bfloat16:
-            t = t.view(torch.bfloat16)
-        return t.pin_memory()
-
-    kvdt = torch.uint8 if w.kv_dtype == "fp8_e4m3" else torch.bfloat16
-    lgdt = torch.bfloat16 if w.logits_dtype == "bf16" else torch.float32
-    h = {"q": host_tensor(x["q"], torch.bfloat16), "k": host_tensor(x["k"], kvdt),
-         "v": host_tensor(x["v"], kvdt), "T": host_tensor(x["seq_lens"], torch.int32),
-         "D": host_tensor(x["draft_len"], torch.int32),
-         "logits": host_tensor(a["logits"], lgdt),
-         "draft": host_tensor(a["draft_tokens"], torch.int32)}
-    if x["kv_scale"] is not None:
-        h["sc"] = host_tensor(x["kv_scale"], torch.float32)
-    d = {k: t.to(dev) for k, t in h.items()}
-    out = torch.empty_like(d["q"])
-    al = torch.empty(w.B, dtype=torch.int32, device=dev)
-    nt = torch.empty(w.B, dtype=torch.int32, device=dev)
-    desc = sv.api.attn_desc(d["q"], d["k"], w.B, md, ms)
-    ws_attn = sv.new_workspace(sv.verify_workspace_bytes(desc), dev)
-    ws_acc = sv.new_workspace(sv.accept_workspace_bytes(w.B, md, w.V), dev)
     stream = torch.cuda.current_stream()
+    if args.only_step:  # W + K plain steps, nothing else (what a profiler captures)
+        for _ in range(args.warmup + args.steps):
+            step()
+        torch.cuda.synchronize()
+        st = (sv.workspace_status(ws_attn), sv.workspace_status(ws_acc))
+        if rank == 0:
+            print(json.dumps({"only_step": True, "workload": describe(w, T, D),
+                              "steps": args.warmup + args.steps, "status": st}), flush=True)
+        if st != (0, 0):
+            raise RuntimeError("device-side check failed")
+        return
 
-    def step():
-        sv.spec_verify_attn(d["q"], d["k"], d["v"], d["T"], d["D"], max_draft_len=md,
-                            max_seq_len=ms, kv_scale=d.get("sc"), out=out, workspace=ws_attn,
-                            stream=stream)
-        sv.spec_accept(d["logits"], d["draft"], d["D"], max_draft_len=md, accept_len=al,
-                       next_token=nt, workspace=ws_acc, stream=stream)
-
-    for _ in range(max(3, args.warmup)):
-        step()
-    torch.cuda.synchronize()
+    # warm-up: at least W steps and 0.3 s, so the clocks are up before the timed region
+    clocks = ClockSampler(dev.index)
+    if rank == 0:
+        clocks.start()
+    n_warm = warm_up(step, max(3, args.warmup))
     if sv.workspace_status(ws_attn) != 0 or sv.workspace_status(ws_acc) != 0:
         raise RuntimeError("device-side check failed during warm-up")
     accepted_per_step = int(al.sum().item())
@@ -388,33 +572,13 @@ def run_ours(args):
     # attention kernel, for its duration (the roofline); those events cost the step its
     # launch overlap, so region 2 is not the step time.
     K = args.steps
-    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    for e in ev_a + ev_b:
-        e.record(stream)
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_stop = torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(dev.index)
-    if rank == 0:
-        clocks.start()
     if world > 1:
         dist.barrier()
-    torch.cuda.synchronize()
-    t_start.record(stream)
-    for i in range(K):
-        step()
-    t_stop.record(stream)
-    torch.cuda.synchronize()
-    for i in range(K):
-        sv.set_profile_events(ev_a[i], ev_b[i])
-        step()
-    torch.cuda.synchronize()
-    sv.set_profile_events(None, None)
+    ms_step = timed_steps(step, stream, K)
+    attn_ms = timed_attention(sv, step, stream, K)
     if world > 1:
         dist.barrier()
     clk = clocks.stop() if rank == 0 else None
-    ms_step = t_start.elapsed_time(t_stop) / K
-    attn_ms = float(np.mean([a_.elapsed_time(b_) for a_, b_ in zip(ev_a, ev_b)]))
 
     # The same step through spec_verify_attn_host_lengths (lengths also in host memory, as
     # an engine's scheduler holds them: the work plan travels with the attention launch and
@@ -717,6 +881,19 @@ def run_ours(args):
         e2e["ms_resident"] = e0.elapsed_time(e1) / K2
         e2e["h2d_resident"] = h2d_r
 
+    # the other workloads, each through the same step (not part of the headline)
+    per_config = None
+    src_hash = kernel_source_hash()
+    if args.per_config != "none" and args.config == "c2" and args.D is None:
+        per_config = {}
+        for item in args.per_config.split(","):
+            cfg, _, dv = item.partition(":")
+            Dv = int(dv) if dv else None
+            key = cfg + ("_D%d" % Dv if Dv is not None else "")
+            per_config[key] = measure_config(sv, synth, cfg, Dv, seed, dev,
+                                             args.per_config_steps, max(3, args.warmup),
+                                             attn_kernel, src_hash)
+
     # max over ranks
     ms_step, attn_ms, e2e_ms, e2e_res_ms, ms_step_hl = max_over_ranks(
         [ms_step, attn_ms, e2e["ms"] if e2e else 0.0, e2e["ms_resident"] if e2e else 0.0,
@@ -726,7 +903,6 @@ def run_ours(args):
         hbm, tf, src = peaks()
         sec = ms_step / 1e3
         value = whole_job_rate(world, kv_bytes, sec) / 1e9
-        achieved = (kv_bytes + qo_bytes) / (attn_ms / 1e3) / 1e9
         cpu = None
         if not args.no_cpu_baseline:
             r = cpu_oracle_sample(w, x, a, args.cpu_seconds, args.seed)
@@ -750,7 +926,7 @@ def run_ours(args):
             attn_plan = None
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
-            "steps": K, "warmup": max(3, args.warmup), "ms_per_step": round(ms_step, 5),
+            "steps": K, "warmup": n_warm, "ms_per_step": round(ms_step, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": ("fp8_e4m3 (QK^T: e4m3 x e4m3, Q as two e4m3 terms; PV: f16), fp32 accum"
                       if attn_kernel == "tcgen05" else "fp8_e4m3->f16 mma, fp32 accum")
@@ -759,7 +935,7 @@ def run_ours(args):
             "data": "synthetic",
             "config": {"workload": describe(w, T, D),
                        "l2": "inputs larger than L2 (%.0f MB K/V + %.0f MB logits vs 129 MB L2)"
-                             % (kv_bytes / 1e6, a["logits"].nbytes / 1e6)
+                             % (kv_bytes / 1e6, logits_bytes / 1e6)
                              if kv_bytes > L2_BYTES else "inputs smaller than L2",
                        "parallelism": "replicas" if world > 1 else "1 GPU"},
             "accepted_tokens_per_s": round(whole_job_rate(world, accepted_per_step, sec), 1),
@@ -787,18 +963,21 @@ def run_ours(args):
             "sliding_window": side_win,
             "paged": side_paged,
             "attn_tflops": round(fl / (attn_ms / 1e3) / 1e12, 2),
-            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
-                         "unit": "GB/s", "frac": round(achieved / hbm, 4),
-                         "traffic": (NCU_TRAFFIC.get((args.config, attn_kernel))
-                                     if args.D is None else None),
-                         "traffic_unit": "bytes per launch (ncu)",
-                         "algorithmic_bytes": kv_bytes + qo_bytes,
-                         "peak_source": src + " (STREAM-style copy)",
-                         "kernel": "verify attention (%s)" % attn_kernel,
-                         "timing": "CUDA events recorded just before and after the attention "
-                                   "kernel on its stream, averaged over a second pass of "
-                                   "the K steps (the step time comes from a pass without "
-                                   "them)"},
+            "roofline": dict(roofline_record(kv_bytes, qo_bytes, fl, attn_ms / 1e3, hbm, tf,
+                                             w.kv_dtype, attn_kernel,
+                                             ncu_traffic(args.config, args.D, attn_kernel,
+                                                         src_hash)),
+                             traffic_unit="bytes per launch (ncu), null unless captured "
+                                          "from the current kernel sources",
+                             kernel_source_hash=src_hash,
+                             peak_source=src + " (HBM: STREAM-style copy; tensor: cuBLAS "
+                                               "bf16 burst, e4m3 = bf16 x 2 nominal)",
+                             kernel="verify attention (%s)" % attn_kernel,
+                             timing="CUDA events recorded just before and after the "
+                                    "attention kernel on its stream, averaged over a "
+                                    "second pass of the K steps (the step time comes "
+                                    "from a pass without them)"),
+            "per_config": per_config,
             "cpu_baseline": cpu,
             "e2e": None if e2e is None else {
                 "value": round(whole_job_rate(world, kv_bytes, e2e_ms / 1e3) / 1e9, 2),

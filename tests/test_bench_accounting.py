@@ -78,3 +78,52 @@ def test_window_bytes_on_the_side_figure():
     T, D, _ = synth.lengths(w, 0)
     kv_b, _ = bench.algorithmic_bytes(w, T, D, window=4096)
     assert kv_b == 2 * 8 * 128 * 2 * 16 * 4127 == 270_467_072
+
+
+def test_roofline_bound_is_the_slower_of_hbm_and_tensor_time():
+    """The bound is whichever of (bytes / HBM peak) and (FLOPs / tensor peak of their types)
+    is larger, and frac = that time / the kernel's time. c2 (bf16, G(1+D) = 128): HBM, 80.8
+    us of bytes against 35.3 us of FLOPs at 6780 GB/s and 1948 TFLOP/s. A contraction of 64
+    rows per key at d = 128 over 1 GB is tensor-bound."""
+    w = synth.CONFIGS["c2"]
+    T, D, _ = synth.lengths(w, 0)
+    kv_b, qo_b = bench.algorithmic_bytes(w, T, D)
+    fl = bench.flops(w, T, D)
+    r = bench.roofline_record(kv_b, qo_b, fl, 100e-6, 6780.0, 1948.2, "bf16", "tcgen05")
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["peak"] == 6780.0
+    assert abs(r["t_hbm_us"] - (kv_b + qo_b) / 6780e9 * 1e6) < 0.01
+    assert abs(r["t_tensor_us"] - fl / 1948.2e12 * 1e6) < 0.01
+    assert abs(r["frac"] - r["t_hbm_us"] / 100.0) < 1e-4
+    assert abs(r["achieved"] - (kv_b + qo_b) / 100e-6 / 1e9) < 0.1
+    # tensor-bound: FLOPs far above the bytes' worth
+    r = bench.roofline_record(1e9, 0, 4e15, 3e-3, 6780.0, 1948.2, "bf16", "tcgen05")
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
+    assert abs(r["peak"] - 1948.2) < 0.1 and abs(r["achieved"] - 4e15 / 3e-3 / 1e12) < 0.1
+    assert abs(r["frac"] - (4e15 / 1948.2e12) / 3e-3) < 1e-4
+
+
+def test_fp8_tensor_time_uses_the_e4m3_rate_for_qk_only():
+    """FP8 K/V on the tcgen05 kernel: Q K^T (half the FLOPs) at twice the bf16 rate, P V
+    (the other half) at the bf16 rate; 0.75 of the bf16 time. The mma.sync kernel decodes
+    to f16: the full bf16 time. c3 stays HBM-bound (79.8 us of bytes vs 52.9 us)."""
+    fl = 1e12
+    t16 = bench.tensor_seconds(fl, "bf16", "tcgen05", 1000.0)
+    assert abs(t16 - 1e-3) < 1e-12
+    assert abs(bench.tensor_seconds(fl, "fp8_e4m3", "tcgen05", 1000.0) - 0.75e-3) < 1e-12
+    assert abs(bench.tensor_seconds(fl, "fp8_e4m3", "mma.sync", 1000.0) - 1e-3) < 1e-12
+    w = synth.CONFIGS["c3"]
+    T, D, _ = synth.lengths(w, 0)
+    kv_b, qo_b = bench.algorithmic_bytes(w, T, D)
+    r = bench.roofline_record(kv_b, qo_b, bench.flops(w, T, D), 120e-6, 6780.0, 1948.2,
+                              "fp8_e4m3", "tcgen05")
+    assert r["bound"] == "hbm" and 52 < r["t_tensor_us"] < 54 and 79 < r["t_hbm_us"] < 81
+
+
+def test_ncu_traffic_is_dropped_when_the_sources_change(monkeypatch):
+    h = bench.kernel_source_hash()
+    assert len(h) == 16 and h == bench.kernel_source_hash()
+    monkeypatch.setitem(bench.NCU_TRAFFIC, ("c2", None, "tcgen05"), (h, 12345))
+    monkeypatch.setitem(bench.NCU_TRAFFIC, ("c3", None, "tcgen05"), ("0" * 16, 999))
+    assert bench.ncu_traffic("c2", None, "tcgen05") == 12345
+    assert bench.ncu_traffic("c3", None, "tcgen05") is None      # another kernel version
+    assert bench.ncu_traffic("c4", 15, "tcgen05") is None        # never captured
