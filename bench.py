@@ -705,13 +705,23 @@ def run_ours(args):
             raise RuntimeError("device-side check failed in the stochastic acceptance")
         st_ms = float(np.median([a_.elapsed_time(b_) for a_, b_ in est]))
         st_bytes = sum(t.numel() * t.element_size() for t in st_in[:2])
+        # rows read: per sequence the (target, drafter) pairs examined (min(AL, D) of
+        # them) and, when every draft was kept, the target's last row
+        alh = st_out[0].cpu().numpy().astype(np.int64)
+        Dn = D.astype(np.int64)
+        row_b = V_l * (2 if dts == torch.bfloat16 else 4)
+        st_read = int(np.sum(2 * np.minimum(alh, Dn) + (alh == Dn + 1)) * row_b)
         side_stoch = {"ms": round(st_ms, 5), "logits_bytes_allocated": st_bytes,
+                      "bytes_examined": st_read,
+                      "GB_per_s_examined": round(st_read / (st_ms / 1e3) / 1e9, 1),
                       "mean_accept_len": round(float(st_out[0].float().mean()), 3),
+                      "max_accept_len": int(alh.max()),
                       "dtype": str(dts).replace("torch.", ""),
                       "note": "spec_accept_stochastic (temperature 1) on the step's target "
                               "logits and drafter logits at every draft position, L2 "
-                              "evicted before each call; one CTA per sequence; rows after "
-                              "the first rejection are not read; not part of the step"}
+                              "evicted before each call; one cluster of 8 CTAs per "
+                              "sequence; rows after the first rejection are not read; "
+                              "not part of the step"}
         del st_in, xs
     del flush_l
 

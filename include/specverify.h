@@ -267,7 +267,9 @@ SV_API size_t spec_accept_stochastic_workspace_size(int32_t batch, int32_t max_d
  * Every row must hold at least one finite logit (rows of NaN give unspecified tokens).
  * A draft length outside [0, max_draft_len] or a draft token outside [0, vocab) sets the
  * workspace flag (sv_workspace_status: SV_ERR_DEVICE_SHAPE) and leaves the outputs of the
- * sequences concerned untouched. vocab <= 2^30. One CTA per sequence; asynchronous.
+ * sequences concerned untouched. vocab <= 2^30. One cluster of 8 CTAs per sequence, each
+ * CTA streaming an eighth of every row it reads; rows after the first rejection are not
+ * read. Asynchronous.
  */
 SV_API sv_status spec_accept_stochastic(int32_t batch, int32_t max_draft_len, int32_t vocab,
                                         int32_t logits_dtype, const void* target_logits,

@@ -9,22 +9,35 @@
 // draft kept, it is drawn from the target's row D_b. A token is drawn as the smallest index
 // whose running sum of weights exceeds u_sample times their total.
 //
-// One CTA per sequence walks its draft positions in order. For each position, one pass
-// over the target's and the drafter's rows gives both softmax normalisers (a running max
-// and sum per thread, merged across the CTA); the decision needs p and q at x_j only, and
-// every thread computes it alike. The draw reads its row once more: each thread sums the
-// weights of a contiguous segment, a CTA-wide exclusive scan of the segment sums finds the
-// first segment whose end passes u times the total, and that segment's thread walks it.
-// Every loop is bounded by the row length; there are no waits.
+// One thread-block cluster of CL CTAs per sequence; CTA c of the cluster owns the vocabulary
+// slice [c S, (c + 1) S). The cluster walks the sequence's draft positions in order:
+//   * each CTA streams its slice of the target's and the drafter's row with 16-byte loads
+//     (L2 prefetch of the next position's slices is issued at once) and reduces a running
+//     max and sum of 2^t per row (t = logit / temperature in log2 units);
+//   * the CTAs exchange their (max, sum) pairs through distributed shared memory at a
+//     cluster barrier, and every CTA merges them in the same order, so every CTA holds the
+//     same normalisers and takes the same keep / reject decision from p(x) and q(x);
+//   * rows after the first rejection are never read.
+// The draw: each thread sums the weights of a contiguous segment of its CTA's slice; the
+// segment sums are scanned within the CTA and the CTA totals across the cluster; the CTA
+// whose interval holds u times the total finds the thread, and that thread walks its
+// segment. Every loop is bounded by the row length. There are no spin waits: the CTAs of a
+// cluster meet only at hardware cluster barriers, which every CTA of the cluster reaches
+// the same number of times because every branch between them is taken on values that all
+// of them hold identically.
 #include <cuda_bf16.h>
 
 #include "internal.cuh"
+#include "logits_vec.cuh"
 
 namespace sv {
 namespace {
 
-constexpr int ST_THREADS = 512;
-constexpr int ST_WARPS = ST_THREADS / 32;
+constexpr int CL = 8;             // CTAs per cluster (one cluster per sequence)
+constexpr int NT = 256;           // threads per CTA
+constexpr int NW = NT / 32;
+constexpr int UB = 8;             // 16-byte loads per row and thread in flight
+constexpr float LOG2E = 1.4426950408889634f;
 
 struct StArgs {
   const void* target;  // [sum_b (1 + D_b), V]
@@ -36,9 +49,66 @@ struct StArgs {
   int32_t* accept_len;
   int32_t* next_token;
   uint32_t* flags;
-  float inv_temp;
+  float c2;    // log2(e) / temperature: logit -> t in log2 units
   int B, max_draft, vocab;
+  int slice;   // vocabulary elements per CTA (a multiple of the vector width)
+  int vec;     // 1: every row starts on a 16-byte boundary (vector loads)
 };
+
+template <bool BF16>
+struct Vec {
+  static constexpr int N = BF16 ? 8 : 4;  // elements per 16-byte vector
+};
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// 2^(a - m) for a <= m, exactly 1 when a == m (the approximation of 2^0 is not exactly 1)
+__device__ __forceinline__ float rescale(float a, float m) { return a == m ? 1.f : ex2(a - m); }
+
+__device__ __forceinline__ uint32_t saddr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_size() {
+  uint32_t r;
+  asm("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of every CTA of the cluster; writes to shared memory before it are visible
+// to the other CTAs' distributed-shared-memory reads after it.
+__device__ __forceinline__ void cluster_sync() {
+  __syncwarp();  // the .aligned forms are executed by whole, converged warps
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+               ::: "memory");
+}
+__device__ __forceinline__ float4 ld_remote(const float4* local, uint32_t rank) {
+  uint32_t ra;
+  asm("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(saddr(local)), "r"(rank));
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(ra)
+               : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
 
 template <bool BF16>
 __device__ __forceinline__ float logit(const void* base, int64_t row, int vocab, int k) {
@@ -48,202 +118,374 @@ __device__ __forceinline__ float logit(const void* base, int64_t row, int vocab,
   else
     return ((const float*)base)[i];
 }
+// Element e of a 16-byte vector.
+template <bool BF16>
+__device__ __forceinline__ float velem(const uint4& v, int e) {
+  const uint32_t w = e / (BF16 ? 2 : 1) == 0 ? v.x
+                     : e / (BF16 ? 2 : 1) == 1 ? v.y
+                     : e / (BF16 ? 2 : 1) == 2 ? v.z : v.w;
+  if constexpr (BF16) return bf16_at(w, e & 1);
+  else return __uint_as_float(w);
+}
+template <bool BF16>
+__device__ __forceinline__ float vmax(const uint4& v) {
+  if constexpr (BF16) return vmax_bf16x8(v);
+  else return fmaxf(fmaxf(__uint_as_float(v.x), __uint_as_float(v.y)),
+                    fmaxf(__uint_as_float(v.z), __uint_as_float(v.w)));
+}
 
-// Running max m and sum s of exp(x - m) (x = logit / temperature); -inf adds nothing.
+// Running max m (log2 units) and sum s of 2^(t - m); empty: (-inf, 0).
 struct MS {
   float m, s;
 };
-__device__ __forceinline__ void ms_add(MS& a, float x) {
-  if (x == -INFINITY) return;
-  if (x > a.m) {
-    a.s = a.s * expf(a.m - x) + 1.f;  // a.m = -inf: a.s is 0 and stays 0 before the + 1
-    a.m = x;
-  } else {
-    a.s += expf(x - a.m);
-  }
-}
+// The arithmetic of these reductions is spelled out with explicitly rounded operations, so
+// no instance can be contracted into a fused multiply-add differently from another: merges
+// are then exactly commutative (a + b == b + a in IEEE arithmetic), and two identical rows
+// give bitwise identical normalisers wherever they are reduced.
 __device__ __forceinline__ MS ms_merge(MS a, MS b) {
-  if (b.m == -INFINITY) return a;
-  if (a.m == -INFINITY) return b;
   const float m = fmaxf(a.m, b.m);
-  return MS{m, a.s * expf(a.m - m) + b.s * expf(b.m - m)};
+  const float fa = a.s > 0.f ? rescale(a.m, m) : 0.f;
+  const float fb = b.s > 0.f ? rescale(b.m, m) : 0.f;
+  return MS{m, __fadd_rn(__fmul_rn(a.s, fa), __fmul_rn(b.s, fb))};
 }
 __device__ __forceinline__ MS ms_shfl(MS a, int o) {
   return MS{__shfl_xor_sync(0xffffffffu, a.m, o), __shfl_xor_sync(0xffffffffu, a.s, o)};
 }
+// Adds values t_i (log2 units; -inf adds nothing) whose max is bm to (m, s).
+__device__ __forceinline__ void ms_raise(MS& a, float bm) {
+  if (bm > a.m) {
+    a.s = a.s > 0.f ? __fmul_rn(a.s, ex2(__fsub_rn(a.m, bm))) : 0.f;
+    a.m = bm;
+  }
+}
 
-// Merges (a, c) over the CTA; every thread returns with the same two results (the warps'
-// parts are folded in the same order by every thread).
-__device__ void block_ms2(MS& a, MS& c, MS* sh) {
+// This CTA's (max, sum) of one or two rows (target row tr; draft row dr when `two`) over
+// the slice [k0, k1), reduced over the CTA; every thread returns the same values.
+template <bool BF16>
+__device__ __forceinline__ void slice_norms(const StArgs& a, int64_t tr, int64_t dr, bool two,
+                                            int k0, int k1, MS& P, MS& Q, MS* sh) {
+  constexpr int VN = Vec<BF16>::N;
+  const int V = a.vocab, tid = threadIdx.x;
+  const float c2 = a.c2;
+  P = MS{-INFINITY, 0.f};
+  Q = MS{-INFINITY, 0.f};
+  if (a.vec) {
+    const uint4* tp = reinterpret_cast<const uint4*>((const char*)a.target +
+                                                     (tr * V + k0) * (BF16 ? 2 : 4));
+    const uint4* dp = two ? reinterpret_cast<const uint4*>((const char*)a.draft +
+                                                           (dr * V + k0) * (BF16 ? 2 : 4))
+                          : tp;
+    const int nv = (k1 - k0) / VN;
+    for (int v0 = 0; v0 < nv; v0 += NT * UB) {
+      uint4 tv[UB], dv[UB];
+#pragma unroll
+      for (int i = 0; i < UB; ++i) {
+        const int v = v0 + i * NT + tid;
+        if (v < nv) {
+          tv[i] = ld_stream(tp + v);
+          if (two) dv[i] = ld_stream(dp + v);
+        }
+      }
+      float bt = -INFINITY, bd = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < UB; ++i)
+        if (v0 + i * NT + tid < nv) {
+          bt = fmaxf(bt, vmax<BF16>(tv[i]));
+          if (two) bd = fmaxf(bd, vmax<BF16>(dv[i]));
+        }
+      ms_raise(P, __fmul_rn(bt, c2));
+      if (two) ms_raise(Q, __fmul_rn(bd, c2));
+      const float nmp = P.m == -INFINITY ? 0.f : -P.m, nmq = Q.m == -INFINITY ? 0.f : -Q.m;
+#pragma unroll
+      for (int i = 0; i < UB; ++i)
+        if (v0 + i * NT + tid < nv) {
+#pragma unroll
+          for (int e = 0; e < VN; ++e) {
+            P.s = __fadd_rn(P.s, ex2(__fmaf_rn(velem<BF16>(tv[i], e), c2, nmp)));
+            if (two) Q.s = __fadd_rn(Q.s, ex2(__fmaf_rn(velem<BF16>(dv[i], e), c2, nmq)));
+          }
+        }
+    }
+  } else {
+    for (int k = k0 + tid; k < k1; k += NT) {
+      const float t = __fmul_rn(logit<BF16>(a.target, tr, V, k), c2);
+      ms_raise(P, t);
+      if (P.m != -INFINITY) P.s = __fadd_rn(P.s, ex2(__fsub_rn(t, P.m)));
+      if (two) {
+        const float d = __fmul_rn(logit<BF16>(a.draft, dr, V, k), c2);
+        ms_raise(Q, d);
+        if (Q.m != -INFINITY) Q.s = __fadd_rn(Q.s, ex2(__fsub_rn(d, Q.m)));
+      }
+    }
+  }
+  // A row of -inf alone keeps (-inf, 0); a -inf element adds 2^-inf = 0.
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
-    a = ms_merge(a, ms_shfl(a, o));
-    c = ms_merge(c, ms_shfl(c, o));
+    P = ms_merge(P, ms_shfl(P, o));
+    Q = ms_merge(Q, ms_shfl(Q, o));
   }
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int lane = tid & 31, w = tid >> 5;
   if (lane == 0) {
-    sh[wid] = a;
-    sh[ST_WARPS + wid] = c;
+    sh[w] = P;
+    sh[NW + w] = Q;
   }
   __syncthreads();
-  a = sh[0];
-  c = sh[ST_WARPS];
-  for (int w = 1; w < ST_WARPS; ++w) {
-    a = ms_merge(a, sh[w]);
-    c = ms_merge(c, sh[ST_WARPS + w]);
+  P = sh[0];
+  Q = sh[NW];
+  for (int i = 1; i < NW; ++i) {
+    P = ms_merge(P, sh[i]);
+    Q = ms_merge(Q, sh[NW + i]);
   }
   __syncthreads();  // sh is reused by the next call
 }
 
-// Sum of int64 values over the CTA (every thread gets it).
-__device__ int64_t block_sum64(int64_t v, int64_t* sh) {
+// Exchange of one float4 per CTA through distributed shared memory: each CTA publishes
+// `mine`, and every CTA returns all CL values in rank order (the same in every CTA).
+// `slots` has two buffers of CL entries, used alternately (`round` parity), so a fast CTA
+// never overwrites values a slower one has yet to read: it can only start round r + 2 after
+// every CTA has reached the barrier of round r + 1, i.e. finished reading round r.
+__device__ __forceinline__ void exchange(float4 mine, float4 (*slots)[CL], uint32_t& round, float4* all) {
+  const uint32_t rank = cluster_rank();
+  float4* buf = slots[round & 1];
+  if (threadIdx.x == 0) buf[rank] = mine;
+  cluster_sync();
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = v;
-  __syncthreads();
-  int64_t t = 0;
-  for (int w = 0; w < ST_WARPS; ++w) t += sh[w];
-  __syncthreads();
-  return t;
+  for (int c = 0; c < CL; ++c) all[c] = ld_remote(&buf[c], (uint32_t)c);  // CTA c's own slot
+  ++round;
 }
 
-// Draws from the weights weight(k) >= 0 of a row at u (see the file comment). Returns the
-// token on every thread, or -1 if every weight is 0.
-template <class Weight>
-__device__ int draw(int vocab, float u, const Weight& weight, float* shf, int* shi) {
-  const int seg = (vocab + ST_THREADS - 1) / ST_THREADS;
-  const int k0 = min(vocab, (int)threadIdx.x * seg), k1 = min(vocab, k0 + seg);
+// The weight of token k: max(0, p_k - q_k) (residual) or p_k up to a constant factor.
+template <bool BF16>
+struct Weight {
+  const void* target;
+  const void* draft;
+  int vocab;
+  float c2;
+  int64_t tr, dr;
+  float pm, pinv, qm, qinv;
+  bool residual;
+  // (p and q by the same explicitly rounded steps: identical rows give p_k - q_k = 0)
+  __device__ __forceinline__ float operator()(int k) const {
+    const float p = __fmul_rn(ex2(__fmaf_rn(logit<BF16>(target, tr, vocab, k), c2, -pm)), pinv);
+    if (!residual) return p;
+    const float q = __fmul_rn(ex2(__fmaf_rn(logit<BF16>(draft, dr, vocab, k), c2, -qm)), qinv);
+    return fmaxf(__fsub_rn(p, q), 0.f);
+  }
+};
+
+// Draws from the weights over the whole row (all CTAs of the cluster take part). Returns
+// -1 on every CTA if every weight is 0; otherwise the drawing CTA writes the token to
+// *out and the function returns 0.
+template <bool BF16>
+__device__ __forceinline__ int cluster_draw(const Weight<BF16>& wt, float u, int k0, int k1, float4 (*slots)[CL],
+                            uint32_t& round, float* shf, int* shi, int32_t* out) {
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int n = max(k1 - k0, 0);
+  const int seg = (n + NT - 1) / NT;
+  const int s0 = min(k0 + tid * seg, k1), s1 = min(s0 + seg, k1);
   float sum = 0.f;
-  int last = -1;  // last index of positive weight in the segment
-  for (int k = k0; k < k1; ++k) {
-    const float w = weight(k);
+  int last = -1;
+#pragma unroll 8
+  for (int k = s0; k < s1; ++k) {
+    const float w = wt(k);
     sum += w;
     if (w > 0.f) last = k;
   }
   // exclusive scan of the segment sums in thread order
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   float incl = sum;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const float y = __shfl_up_sync(0xffffffffu, incl, o);
     if (lane >= o) incl += y;
   }
+  int lmax = last;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) lmax = max(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
   if (lane == 31) shf[wid] = incl;
-  if (threadIdx.x == 0) {
-    shi[0] = 0x7fffffff;  // first thread whose segment end passes the target
-    shi[1] = -1;          // last index of positive weight in the row
-    shi[2] = -1;          // the drawn token
-  }
+  if (lane == 0) shi[wid] = lmax;
   __syncthreads();
-  float before = 0.f, total = 0.f;
-  for (int w = 0; w < ST_WARPS; ++w) {
+  float before = 0.f, ctot = 0.f;
+  int clast = -1;
+  for (int w = 0; w < NW; ++w) {
     if (w < wid) before += shf[w];
-    total += shf[w];
+    ctot += shf[w];
+    clast = max(clast, shi[w]);
   }
   const float ex = before + incl - sum;
-  const float target = u * total;
-  if (sum > 0.f && target < ex + sum) atomicMin(&shi[0], (int)threadIdx.x);
-  if (last >= 0) atomicMax(&shi[1], last);
   __syncthreads();
-  if ((int)threadIdx.x == shi[0]) {
+  float4 all[CL];
+  exchange(make_float4(ctot, __int_as_float(clast), 0.f, 0.f), slots, round, all);
+  float pre = 0.f, total = 0.f;
+  int glast = -1;
+  for (int c = 0; c < CL; ++c) {
+    total += all[c].x;
+    glast = max(glast, __float_as_int(all[c].y));
+  }
+  if (!(total > 0.f)) return -1;  // the same on every CTA
+  const float target = u * total;
+  int cstar = -1;
+  for (int c = 0; c < CL; ++c) {
+    if (cstar < 0 && all[c].x > 0.f && target < pre + all[c].x) cstar = c;
+    if (cstar < 0) pre += all[c].x;
+  }
+  const uint32_t rank = cluster_rank();
+  if (cstar < 0) {  // rounding left the target at the end: the last token of positive weight
+    if (rank == 0 && tid == 0) *out = glast;
+    return 0;
+  }
+  if ((int)rank != cstar) return 0;
+  const float tl = target - pre;
+  if (tid == 0) shi[NW] = 0x7fffffff;
+  __syncthreads();
+  if (sum > 0.f && tl < ex + sum) atomicMin(&shi[NW], tid);
+  __syncthreads();
+  const int who = shi[NW];
+  if (who == 0x7fffffff) {
+    if (tid == 0) *out = clast;
+  } else if (tid == who) {
     float c = ex;
     int pick = last;
-    for (int k = k0; k < k1; ++k) {
-      const float w = weight(k);
+    for (int k = s0; k < s1; ++k) {
+      const float w = wt(k);
       c += w;
-      if (w > 0.f && c > target) {
+      if (w > 0.f && c > tl) {
         pick = k;
         break;
       }
     }
-    shi[2] = pick;
+    *out = pick;
   }
-  __syncthreads();
-  const int tok = shi[0] == 0x7fffffff ? shi[1] : shi[2];
-  __syncthreads();  // shf and shi are reused by the next draw
-  return tok;
+  return 0;
 }
 
 template <bool BF16>
-__global__ void __launch_bounds__(ST_THREADS) accept_stochastic_kernel(StArgs a) {
-  __shared__ MS sh_ms[2 * ST_WARPS];
-  __shared__ int64_t sh64[ST_WARPS];
-  __shared__ float shf[ST_WARPS];
-  __shared__ int shi[4];
+__global__ void __launch_bounds__(NT) accept_stochastic_kernel(StArgs a) {
+  __shared__ MS sh_ms[2 * NW];
+  __shared__ float4 slots[2][CL];
+  __shared__ float shf[NW];
+  __shared__ int shi[NW + 1];
+  __shared__ int64_t sh64[NW];
   pdl_trigger();
   pdl_wait();
-  const int b = blockIdx.x, V = a.vocab;
-  // this sequence's rows: q_off = sum over earlier sequences of (1 + D), d_off of D; every
-  // length up to this one must be in range for the offsets to mean anything
+  const int tid = threadIdx.x;
+  const int b = blockIdx.x / CL;
+  const uint32_t rank = cluster_rank();
+  const int V = a.vocab;
+  if (cluster_size() != CL || rank != blockIdx.x % CL) {  // launched without its cluster shape
+    if (tid == 0) atomicOr(a.flags, FLAG_ACCEPT_SHAPE);
+    return;  // (before any cluster barrier or remote access)
+  }
+
+  // this sequence's rows: d_off = sum of D over earlier sequences, q_off = d_off + b. Every
+  // length up to this one must be in range for the offsets to mean anything. Every CTA of
+  // the cluster computes the same sums, so all of them return here together or none does.
+  auto block_sum = [&](int64_t v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if ((tid & 31) == 0) sh64[tid >> 5] = v;
+    __syncthreads();
+    int64_t t = 0;
+    for (int w = 0; w < NW; ++w) t += sh64[w];
+    __syncthreads();
+    return t;
+  };
   int64_t dsum = 0, nbad = 0;
-  for (int bb = threadIdx.x; bb <= b; bb += ST_THREADS) {
+  for (int bb = tid; bb <= b; bb += NT) {
     const int D = a.draft_len[bb];
     if (D < 0 || D > a.max_draft) ++nbad;
     if (bb < b) dsum += D;
   }
-  nbad = block_sum64(nbad, sh64);
-  const int64_t d_off = block_sum64(dsum, sh64);
+  nbad = block_sum(nbad);
+  const int64_t d_off = block_sum(dsum);
   const int D = a.draft_len[b];
   if (nbad == 0) {
-    for (int j = threadIdx.x; j < D; j += ST_THREADS) {
+    for (int j = tid; j < D; j += NT) {
       const int x = a.draft_tokens[d_off + j];
       if (x < 0 || x >= V) ++nbad;
     }
-    nbad = block_sum64(nbad, sh64);
+    nbad = block_sum(nbad);
   }
   if (nbad != 0) {  // leave this sequence's outputs untouched
-    if (threadIdx.x == 0) atomicOr(a.flags, FLAG_ACCEPT_SHAPE);
+    if (rank == 0 && tid == 0) atomicOr(a.flags, FLAG_ACCEPT_SHAPE);
     return;
   }
   const int64_t q_off = d_off + b;
-  const float it = a.inv_temp;
+  const int k0 = min((int)rank * a.slice, V), k1 = min(k0 + a.slice, V);
+  const uint32_t esz = BF16 ? 2 : 4;
+  auto prefetch_rows = [&](int64_t tr, int64_t dr, bool two) {
+    if (a.vec && tid == 0 && k1 > k0) {
+      const uint32_t bytes = (uint32_t)(k1 - k0) * esz;
+      prefetch_l2((const char*)a.target + (tr * V + k0) * esz, bytes);
+      if (two) prefetch_l2((const char*)a.draft + (dr * V + k0) * esz, bytes);
+    }
+  };
+  uint32_t round = 0;
+  float4 all[CL];
+  auto cluster_norms = [&](MS& P, MS& Q) {  // merge every CTA's parts in rank order
+    exchange(make_float4(P.m, P.s, Q.m, Q.s), slots, round, all);
+    P = MS{all[0].x, all[0].y};
+    Q = MS{all[0].z, all[0].w};
+    for (int c = 1; c < CL; ++c) {
+      P = ms_merge(P, MS{all[c].x, all[c].y});
+      Q = ms_merge(Q, MS{all[c].z, all[c].w});
+    }
+  };
+
   int n = D;  // drafts kept
-  MS sp{-INFINITY, 0.f}, sq{-INFINITY, 0.f};
+  MS P, Q;
+  prefetch_rows(q_off, d_off, D > 0);
   for (int j = 0; j < D; ++j) {
     const int64_t tr = q_off + j, dr = d_off + j;
-    sp = MS{-INFINITY, 0.f};
-    sq = MS{-INFINITY, 0.f};
-    for (int k = threadIdx.x; k < V; k += ST_THREADS) {
-      ms_add(sp, logit<BF16>(a.target, tr, V, k) * it);
-      ms_add(sq, logit<BF16>(a.draft, dr, V, k) * it);
-    }
-    block_ms2(sp, sq, sh_ms);
+    slice_norms<BF16>(a, tr, dr, true, k0, k1, P, Q, sh_ms);
+    prefetch_rows(tr + 1, dr + 1, j + 1 < D);  // the next position's rows (the bonus row last)
+    cluster_norms(P, Q);
     const int x = a.draft_tokens[dr];
-    const float px = expf(logit<BF16>(a.target, tr, V, x) * it - sp.m) / sp.s;
-    const float qx = expf(logit<BF16>(a.draft, dr, V, x) * it - sq.m) / sq.s;
-    if (!(a.u_accept[dr] * qx < px)) {  // the same decision on every thread
+    const float px = __fdiv_rn(ex2(__fmaf_rn(logit<BF16>(a.target, tr, V, x), a.c2, -P.m)), P.s);
+    const float qx = __fdiv_rn(ex2(__fmaf_rn(logit<BF16>(a.draft, dr, V, x), a.c2, -Q.m)), Q.s);
+    if (!(__fmul_rn(a.u_accept[dr], qx) < px)) {  // the same decision on every thread
       n = j;
       break;
     }
   }
   const float us = a.u_sample[b];
-  int tok = -1;
-  if (n < D) {  // sp, sq hold row n's normalisers: draw from max(0, p - q)
-    const int64_t tr = q_off + n, dr = d_off + n;
-    const MS P = sp, Q = sq;
-    auto resid = [&](int k) {
-      const float pk = expf(logit<BF16>(a.target, tr, V, k) * it - P.m) / P.s;
-      const float qk = expf(logit<BF16>(a.draft, dr, V, k) * it - Q.m) / Q.s;
-      return fmaxf(pk - qk, 0.f);
-    };
-    tok = draw(V, us, resid, shf, shi);
+  int status = -1;
+  if (n < D) {  // P, Q hold row n's normalisers: draw from max(0, p - q)
+    const Weight<BF16> w{a.target, a.draft, V, a.c2, q_off + n, d_off + n,
+                         P.m, __frcp_rn(P.s), Q.m, __frcp_rn(Q.s), true};
+    status = cluster_draw<BF16>(w, us, k0, k1, slots, round, shf, shi, a.next_token + b);
   }
-  if (tok < 0) {  // every draft kept (row D), or an all-zero residual (row n)
-    const int64_t tr = q_off + (n < D ? n : D);
+  if (status < 0) {  // every draft kept (row D), or an all-zero residual (row n)
+    const int64_t tr = q_off + n;
     if (n == D) {
-      sp = MS{-INFINITY, 0.f};
-      MS unused{-INFINITY, 0.f};
-      for (int k = threadIdx.x; k < V; k += ST_THREADS) ms_add(sp, logit<BF16>(a.target, tr, V, k) * it);
-      block_ms2(sp, unused, sh_ms);
+      MS unused;
+      slice_norms<BF16>(a, tr, 0, false, k0, k1, P, unused, sh_ms);
+      cluster_norms(P, unused);
     }
-    const MS P = sp;
-    auto prob = [&](int k) { return expf(logit<BF16>(a.target, tr, V, k) * it - P.m) / P.s; };
-    tok = draw(V, us, prob, shf, shi);
+    const Weight<BF16> w{a.target, a.draft, V, a.c2, tr, 0, P.m, 1.f, 0.f, 0.f, false};
+    cluster_draw<BF16>(w, us, k0, k1, slots, round, shf, shi, a.next_token + b);
   }
-  if (threadIdx.x == 0) {
-    a.accept_len[b] = n + 1;
-    a.next_token[b] = tok;
-  }
+  if (rank == 0 && tid == 0) a.accept_len[b] = n + 1;
+  cluster_sync();  // no CTA leaves while another may still read its shared memory
+}
+
+template <bool BF16>
+cudaError_t launch_st(const StArgs& a, cudaStream_t s) {
+  if (take_injected_launch_failure()) return cudaErrorLaunchFailure;  // nothing launched
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)a.B * CL);
+  cfg.blockDim = dim3(NT);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = CL;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, accept_stochastic_kernel<BF16>, a);
 }
 
 }  // namespace
@@ -264,13 +506,18 @@ cudaError_t launch_accept_stochastic(int B, int max_draft, int vocab, int dtype,
   a.accept_len = accept_len;
   a.next_token = next_token;
   a.flags = (uint32_t*)ws;
-  a.inv_temp = inv_temp;
+  a.c2 = inv_temp * LOG2E;
   a.B = B;
   a.max_draft = max_draft;
   a.vocab = vocab;
-  return dtype == SV_BF16
-             ? launch_pdl(accept_stochastic_kernel<true>, dim3(B), dim3(ST_THREADS), 0, s, a)
-             : launch_pdl(accept_stochastic_kernel<false>, dim3(B), dim3(ST_THREADS), 0, s, a);
+  const bool bf16 = dtype == SV_BF16;
+  const int vn = bf16 ? 8 : 4;
+  const uintptr_t al = 16;
+  a.vec = vocab % vn == 0 && ((uintptr_t)target % al) == 0 &&
+          (draft == nullptr || ((uintptr_t)draft % al) == 0);
+  // slices of whole vectors: every slice of an aligned row starts on a 16-byte boundary
+  a.slice = ((vocab + CL - 1) / CL + vn - 1) / vn * vn;
+  return bf16 ? launch_st<true>(a, s) : launch_st<false>(a, s);
 }
 
 }  // namespace sv

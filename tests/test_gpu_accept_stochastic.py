@@ -5,9 +5,9 @@ Where floating point decides an integer here, fp32 and fp64 may legitimately dif
   (relative) may go either way: p(x) and q(x) carry relative errors of about 1e-6 in
   fp32;
 * a draw picks the token whose interval of the running sum holds u times the total; the
-  fp32 running sums over up to 128K weights (per-thread segments, then a scan of 512
-  segment sums) are within CDF_TOL of the total, so near an interval's end a neighbour
-  may be drawn. For a flat softmax over a large vocabulary the intervals are themselves
+  fp32 running sums over up to 128K weights (per-thread segments, a scan of 256 segment
+  sums in each of the 8 CTAs that share the row, then the 8 CTA totals) are within
+  CDF_TOL of the total, so near an interval's end a neighbour may be drawn. For a flat softmax over a large vocabulary the intervals are themselves
   about 1e-5 of the total.
 So every keep / reject decision on the GPU's path must agree with the oracle's wherever
 the oracle's margin for that decision is at least ACC_MARGIN: the GPU may leave the
