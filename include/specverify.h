@@ -374,6 +374,26 @@ SV_API int sv_set_attn_kernel(int which);
  * [-1, 1024]. Process-wide. */
 SV_API int sv_set_unit_ctas(int mode);
 
+/* Row pairs, for measurement and tests. When a KV head serves more than one 128-row tile
+ * but at most two (128 < G * (1 + max_draft_len) <= 256), with bf16 K/V, head_dim 128, a
+ * packed cache, no sliding window, and batch * num_kv_heads at most the number of SMs,
+ * spec_verify_attn (and the host-lengths call) can run one CTA per (sequence, KV head) that
+ * holds both row tiles and reads each K/V tile once for both, instead of the unit plan
+ * (whose row tiles each stream the keys, the second mostly from L2). 0 = never (default),
+ * 1 = whenever it applies. It is one kernel launch: no planning and no combining kernel.
+ * It is off by default because it measures slower than the unit plan: with the whole of
+ * TMEM taken by two accumulators and two score tiles, Q comes from shared memory and P
+ * shares its score tile's columns, so each row tile's score MMA waits for its previous P V.
+ * Returns the previous value, or -2 if mode is not 0 or 1. Process-wide. */
+SV_API int sv_set_row_pairs(int mode);
+
+/* 1 if spec_verify_attn with this descriptor, cache layout (block_size 0: packed), SM count
+ * and kernel (1 = mma.sync, 2 = tcgen05) runs the row-pair kernel under the current
+ * setting, 0 if it runs the unit plan that sv_plan_preview describes, -1 if the arguments
+ * are invalid. Needs no device. */
+SV_API int sv_row_pair_mode(const sv_attn_desc* desc, int32_t block_size, int32_t num_sms,
+                            int32_t attn_kernel);
+
 /* Profiling hook: when both are non-NULL, every later spec_verify_attn records `start`
  * just before and `stop` just after its main attention kernel, on the call's stream
  * (cudaEvent_t handles owned by the caller). Pass NULLs to turn it off. Process-wide.

@@ -35,7 +35,8 @@ EXPORTS = ("spec_verify_attn_workspace_size", "spec_verify_attn", "spec_verify_a
            "spec_accept", "spec_draft_signals_workspace_size", "spec_draft_signals",
            "sv_workspace_status", "sv_status_string", "sv_set_attn_kernel", "sv_set_unit_ctas",
            "sv_set_profile_events", "sv_version", "sv_plan_preview",
-           "sv_inject_launch_failure", "sv_inject_wait_timeout",
+           "sv_inject_launch_failure", "sv_inject_wait_timeout", "sv_set_row_pairs",
+           "sv_row_pair_mode",
            "spec_accept_stochastic_workspace_size",
            "spec_accept_stochastic")
 
@@ -119,6 +120,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.sv_inject_launch_failure.restype = ctypes.c_int
         lib.sv_inject_wait_timeout.argtypes = [ctypes.c_int64]
         lib.sv_inject_wait_timeout.restype = ctypes.c_int
+        lib.sv_set_row_pairs.argtypes = [ctypes.c_int]
+        lib.sv_set_row_pairs.restype = ctypes.c_int
+        lib.sv_row_pair_mode.argtypes = [ctypes.POINTER(AttnDesc), i32, i32, i32]
+        lib.sv_row_pair_mode.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -423,6 +428,24 @@ def inject_launch_failure(after: int) -> int:
     negative ``after`` disarms. Returns the launches that were still to go before a
     pending failure, or -1."""
     return load_library().sv_inject_launch_failure(int(after))
+
+
+def set_row_pairs(mode: int) -> int:
+    """0 never (default), 1 whenever the row-pair kernel applies (128 < G(1 + max_draft) <=
+    256, bf16, d = 128, packed, no window, B * Hkv <= SMs). Returns the previous mode."""
+    prev = load_library().sv_set_row_pairs(int(mode))
+    if prev < 0:
+        raise ValueError("row-pair mode must be 0 or 1")
+    return prev
+
+
+def row_pair_mode(desc, num_sms: int, attn_kernel: int = 2, block_size: int = 0) -> int:
+    """1 if a call with this descriptor runs the row-pair kernel, else 0."""
+    r = load_library().sv_row_pair_mode(ctypes.byref(desc), int(block_size), int(num_sms),
+                                        int(attn_kernel))
+    if r < 0:
+        raise SpecVerifyError(2, "sv_row_pair_mode")
+    return r
 
 
 def inject_wait_timeout(limit_cycles: int) -> int:

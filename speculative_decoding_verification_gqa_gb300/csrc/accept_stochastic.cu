@@ -264,33 +264,81 @@ struct Weight {
   int64_t tr, dr;
   float pm, pinv, qm, qinv;
   bool residual;
-  // (p and q by the same explicitly rounded steps: identical rows give p_k - q_k = 0)
-  __device__ __forceinline__ float operator()(int k) const {
-    const float p = __fmul_rn(ex2(__fmaf_rn(logit<BF16>(target, tr, vocab, k), c2, -pm)), pinv);
+  // from the two logits (p and q by the same explicitly rounded steps: identical rows give
+  // p_k - q_k = 0)
+  __device__ __forceinline__ float eval(float lt, float ld) const {
+    const float p = __fmul_rn(ex2(__fmaf_rn(lt, c2, -pm)), pinv);
     if (!residual) return p;
-    const float q = __fmul_rn(ex2(__fmaf_rn(logit<BF16>(draft, dr, vocab, k), c2, -qm)), qinv);
+    const float q = __fmul_rn(ex2(__fmaf_rn(ld, c2, -qm)), qinv);
     return fmaxf(__fsub_rn(p, q), 0.f);
   }
+  __device__ __forceinline__ float operator()(int k) const {
+    return eval(logit<BF16>(target, tr, vocab, k),
+                residual ? logit<BF16>(draft, dr, vocab, k) : 0.f);
+  }
 };
+
+constexpr int DV = 8;  // vectors per row loaded at once by a drawing thread
+
+// Visits the weights of tokens [s0, s1) in token order: f(k, w) returns true to stop.
+// With 16-byte rows (vec) s0 is a multiple of the vector width and the segment is read
+// DV vectors per row at a time, every load of a chunk issued before the first is used.
+template <bool BF16, class F>
+__device__ __forceinline__ void visit(const Weight<BF16>& wt, bool vec, int s0, int s1, F&& f) {
+  constexpr int VN = Vec<BF16>::N;
+  if (vec) {
+    const uint4* tp = reinterpret_cast<const uint4*>(
+        (const char*)wt.target + (wt.tr * wt.vocab + s0) * (BF16 ? 2 : 4));
+    const uint4* dp = reinterpret_cast<const uint4*>(
+        (const char*)wt.draft + (wt.dr * wt.vocab + s0) * (BF16 ? 2 : 4));
+    const int nv = (s1 - s0 + VN - 1) / VN;  // the last vector may end past s1 (not past V)
+    for (int i0 = 0; i0 < nv; i0 += DV) {
+      uint4 tv[DV], dv[DV];
+#pragma unroll
+      for (int i = 0; i < DV; ++i)
+        if (i0 + i < nv) {
+          tv[i] = tp[i0 + i];
+          if (wt.residual) dv[i] = dp[i0 + i];
+        }
+#pragma unroll
+      for (int i = 0; i < DV; ++i)
+        if (i0 + i < nv) {
+#pragma unroll
+          for (int e = 0; e < VN; ++e) {
+            const int k = s0 + (i0 + i) * VN + e;
+            if (k < s1 && f(k, wt.eval(velem<BF16>(tv[i], e),
+                                       wt.residual ? velem<BF16>(dv[i], e) : 0.f)))
+              return;
+          }
+        }
+    }
+  } else {
+#pragma unroll 8
+    for (int k = s0; k < s1; ++k)
+      if (f(k, wt(k))) return;
+  }
+}
 
 // Draws from the weights over the whole row (all CTAs of the cluster take part). Returns
 // -1 on every CTA if every weight is 0; otherwise the drawing CTA writes the token to
 // *out and the function returns 0.
 template <bool BF16>
-__device__ __forceinline__ int cluster_draw(const Weight<BF16>& wt, float u, int k0, int k1, float4 (*slots)[CL],
-                            uint32_t& round, float* shf, int* shi, int32_t* out) {
+__device__ __forceinline__ int cluster_draw(const Weight<BF16>& wt, bool vec, float u, int k0,
+                                            int k1, float4 (*slots)[CL], uint32_t& round,
+                                            float* shf, int* shi, int32_t* out) {
+  constexpr int VN = Vec<BF16>::N;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int n = max(k1 - k0, 0);
-  const int seg = (n + NT - 1) / NT;
+  int seg = (n + NT - 1) / NT;
+  if (vec) seg = (seg + VN - 1) / VN * VN;  // segments of whole vectors
   const int s0 = min(k0 + tid * seg, k1), s1 = min(s0 + seg, k1);
   float sum = 0.f;
   int last = -1;
-#pragma unroll 8
-  for (int k = s0; k < s1; ++k) {
-    const float w = wt(k);
-    sum += w;
+  visit<BF16>(wt, vec, s0, s1, [&](int k, float w) {
+    sum = __fadd_rn(sum, w);
     if (w > 0.f) last = k;
-  }
+    return false;
+  });
   // exclusive scan of the segment sums in thread order
   float incl = sum;
 #pragma unroll
@@ -345,14 +393,14 @@ __device__ __forceinline__ int cluster_draw(const Weight<BF16>& wt, float u, int
   } else if (tid == who) {
     float c = ex;
     int pick = last;
-    for (int k = s0; k < s1; ++k) {
-      const float w = wt(k);
-      c += w;
+    visit<BF16>(wt, vec, s0, s1, [&](int k, float w) {
+      c = __fadd_rn(c, w);
       if (w > 0.f && c > tl) {
         pick = k;
-        break;
+        return true;
       }
-    }
+      return false;
+    });
     *out = pick;
   }
   return 0;
@@ -436,13 +484,16 @@ __global__ void __launch_bounds__(NT) accept_stochastic_kernel(StArgs a) {
   prefetch_rows(q_off, d_off, D > 0);
   for (int j = 0; j < D; ++j) {
     const int64_t tr = q_off + j, dr = d_off + j;
+    // what the decision needs besides the normalisers, loaded before the rows stream
+    const int x = a.draft_tokens[dr];
+    const float lx = logit<BF16>(a.target, tr, V, x), dx = logit<BF16>(a.draft, dr, V, x);
+    const float ua = a.u_accept[dr];
     slice_norms<BF16>(a, tr, dr, true, k0, k1, P, Q, sh_ms);
     prefetch_rows(tr + 1, dr + 1, j + 1 < D);  // the next position's rows (the bonus row last)
     cluster_norms(P, Q);
-    const int x = a.draft_tokens[dr];
-    const float px = __fdiv_rn(ex2(__fmaf_rn(logit<BF16>(a.target, tr, V, x), a.c2, -P.m)), P.s);
-    const float qx = __fdiv_rn(ex2(__fmaf_rn(logit<BF16>(a.draft, dr, V, x), a.c2, -Q.m)), Q.s);
-    if (!(__fmul_rn(a.u_accept[dr], qx) < px)) {  // the same decision on every thread
+    const float px = __fdiv_rn(ex2(__fmaf_rn(lx, a.c2, -P.m)), P.s);
+    const float qx = __fdiv_rn(ex2(__fmaf_rn(dx, a.c2, -Q.m)), Q.s);
+    if (!(__fmul_rn(ua, qx) < px)) {  // the same decision on every thread of the cluster
       n = j;
       break;
     }
@@ -452,7 +503,7 @@ __global__ void __launch_bounds__(NT) accept_stochastic_kernel(StArgs a) {
   if (n < D) {  // P, Q hold row n's normalisers: draw from max(0, p - q)
     const Weight<BF16> w{a.target, a.draft, V, a.c2, q_off + n, d_off + n,
                          P.m, __frcp_rn(P.s), Q.m, __frcp_rn(Q.s), true};
-    status = cluster_draw<BF16>(w, us, k0, k1, slots, round, shf, shi, a.next_token + b);
+    status = cluster_draw<BF16>(w, a.vec, us, k0, k1, slots, round, shf, shi, a.next_token + b);
   }
   if (status < 0) {  // every draft kept (row D), or an all-zero residual (row n)
     const int64_t tr = q_off + n;
@@ -462,7 +513,7 @@ __global__ void __launch_bounds__(NT) accept_stochastic_kernel(StArgs a) {
       cluster_norms(P, unused);
     }
     const Weight<BF16> w{a.target, a.draft, V, a.c2, tr, 0, P.m, 1.f, 0.f, 0.f, false};
-    cluster_draw<BF16>(w, us, k0, k1, slots, round, shf, shi, a.next_token + b);
+    cluster_draw<BF16>(w, a.vec, us, k0, k1, slots, round, shf, shi, a.next_token + b);
   }
   if (rank == 0 && tid == 0) a.accept_len[b] = n + 1;
   cluster_sync();  // no CTA leaves while another may still read its shared memory

@@ -45,6 +45,7 @@ std::atomic<int> g_fail_countdown{0};
 std::atomic<long long> g_stall_limit{0};
 int g_attn_kernel = 0;  // 0 automatic, 1 mma.sync, 2 tcgen05
 int g_unit_ctas = SV_UNIT_CTAS;  // -1 cost model, 0 split tile line, k > 0 k CTAs per unit
+int g_row_pairs = 0;  // 1: the row-pair kernel whenever it applies; 0: never (default)
 cudaEvent_t g_ev_start = nullptr;
 cudaEvent_t g_ev_stop = nullptr;
 
@@ -138,6 +139,13 @@ SV_API int sv_set_unit_ctas(int mode) {
   return prev;
 }
 
+SV_API int sv_set_row_pairs(int mode) {
+  if (mode < 0 || mode > 1) return -2;
+  const int prev = g_row_pairs;
+  g_row_pairs = mode;
+  return prev;
+}
+
 SV_API void sv_set_profile_events(void* start_event, void* stop_event) {
   if (start_event && stop_event) {
     g_ev_start = (cudaEvent_t)start_event;
@@ -210,6 +218,13 @@ AttnParams shape_params(const sv_attn_desc* desc, const PagedArgs& pg, int which
   return p;
 }
 
+// Whether a call of kernel `which` with these parameters runs the row-pair kernel: it is
+// switched on and applies (see attn_pair_applies). Off by default: on every workload
+// measured, the unit plan (each row tile streaming the keys, the second from L2) is faster.
+bool use_row_pairs(const AttnParams& p, bool fp8, int which, int sms) {
+  return which == 2 && g_row_pairs == 1 && attn_pair_applies(p, fp8, sms);
+}
+
 sv_status verify_impl(const sv_attn_desc* desc, const void* q, const void* k_cache,
                       const void* v_cache, const PagedArgs& pg, const int32_t* seq_lens,
                       const int32_t* draft_len, const float* kv_scale, void* out,
@@ -270,6 +285,12 @@ sv_status verify_impl(const sv_attn_desc* desc, const void* q, const void* k_cac
   p.block_table = pg.table;
 
   cudaStream_t s = (cudaStream_t)stream;
+  if (use_row_pairs(p, fp8, which, sms)) {  // one launch: no plan, nothing to combine
+    if (g_ev_start && cudaEventRecord(g_ev_start, s) != cudaSuccess) return SV_ERR_CUDA;
+    if (launch_attn_pair(p, s) != cudaSuccess) return SV_ERR_CUDA;
+    if (g_ev_stop && cudaEventRecord(g_ev_stop, s) != cudaSuccess) return SV_ERR_CUDA;
+    return SV_OK;
+  }
   // Host lengths: plan on the host and pass the plan with the attention launch (tcgen05
   // kernel, packed cache), unless it does not fit a HostPlan.
   static thread_local HostPlan hp;
@@ -374,6 +395,17 @@ SV_API sv_status sv_plan_preview(const sv_attn_desc* desc, int32_t block_size,
     cta_begin[2 * c + 1] = hp.cta_tab[c].y;
   }
   return SV_OK;
+}
+
+SV_API int sv_row_pair_mode(const sv_attn_desc* desc, int32_t block_size, int32_t num_sms,
+                           int32_t attn_kernel) {
+  if (check_desc(desc) != SV_OK || num_sms < 1 || (attn_kernel != 1 && attn_kernel != 2) ||
+      block_size < 0)
+    return -1;
+  const PagedArgs pg = {nullptr, 1 << 30, block_size,
+                        block_size > 0 ? MAX_KV_ROWS / block_size : 0};
+  const AttnParams p = shape_params(desc, pg, attn_kernel, num_sms);
+  return use_row_pairs(p, desc->kv_dtype == SV_FP8_E4M3, attn_kernel, num_sms) ? 1 : 0;
 }
 
 SV_API size_t spec_accept_workspace_size(int32_t batch, int32_t max_draft_len, int32_t vocab) {

@@ -226,6 +226,11 @@ bool attn_tc_supports(int head_dim, bool fp8);
 int attn_tc_kt();
 cudaError_t launch_attn_tc(const AttnParams& p, bool fp8, cudaStream_t s);
 cudaError_t launch_attn_tc_hp(const AttnParams& p, bool fp8, const HostPlan& hp, cudaStream_t s);
+// Row pairs (attn_pair.cu): one CTA per (sequence, KV head) holding both 128-row tiles when
+// 128 < G (1 + max_draft) <= 256; bf16 K/V, d = 128, packed cache, no sliding window, and
+// at most one CTA per SM. The CTAs check the lengths and work out the offsets themselves.
+bool attn_pair_applies(const AttnParams& p, bool fp8, int sms);
+cudaError_t launch_attn_pair(const AttnParams& p, cudaStream_t s);
 
 // Acceptance.
 struct AcceptWs {

@@ -161,7 +161,7 @@ def test_accept_and_signals_write_nothing_outside_their_outputs():
     assert np.array_equal(tg.cpu().numpy(), ramax)
 
 
-@pytest.mark.parametrize("kv", ["bf16", "fp8_e4m3"])
+@pytest.mark.parametrize("kv", ["bf16", "fp8_e4m3", "bf16_row_pairs"])
 @pytest.mark.parametrize("entry", ["packed", "host_lengths"])
 def test_bounded_wait_runs_out_and_the_kernel_returns(kv, entry):
     """The tcgen05 kernel's barrier waits are bounded. With a short limit (1e5 cycles, about
@@ -174,22 +174,26 @@ def test_bounded_wait_runs_out_and_the_kernel_returns(kv, entry):
         prev = sv.set_attn_kernel(2)
     except ValueError:
         pytest.skip("tcgen05 kernel not built")
+    pairs = kv == "bf16_row_pairs"  # G (1 + D) = 256 rows: the row-pair kernel
+    prev_pairs = sv.api.set_row_pairs(1 if pairs else 0)
     try:
-        w = synth.Workload("t", B=3, Hq=16, Hkv=4, d=128, D=0, T=0, V=8, p=0.5, kv_dtype=kv,
-                           outlier_prob=0.001 if kv != "bf16" else 0.0)
+        kvd = "bf16" if pairs else kv
+        w = synth.Workload("t", B=3, Hq=32 if pairs else 16, Hkv=4, d=128, D=0, T=0, V=8,
+                           p=0.5, kv_dtype=kvd, outlier_prob=0.001 if kvd != "bf16" else 0.0)
         x = synth.attn_inputs(w, 23, seq_lens=np.array([900, 5, 300]),
-                              draft_len=np.array([7, 0, 3]))
+                              draft_len=np.array([7, 0, 3]) + (24 if pairs else 0))
         q, k, v, sc, T, D = dev_attn(x)
         Th = torch.from_numpy(x["seq_lens"].astype(np.int32))
         Dh = torch.from_numpy(x["draft_len"].astype(np.int32))
-        ws = sv.new_workspace(sv.verify_workspace_bytes(sv.api.attn_desc(q, k, 3, 7, 900)))
+        md = int(x["draft_len"].max())
+        ws = sv.new_workspace(sv.verify_workspace_bytes(sv.api.attn_desc(q, k, 3, md, 900)))
         out = torch.empty_like(q)
 
         def call(wsp):
             if entry == "packed":
-                return sv.spec_verify_attn(q, k, v, T, D, max_draft_len=7, max_seq_len=900,
+                return sv.spec_verify_attn(q, k, v, T, D, max_draft_len=md, max_seq_len=900,
                                            kv_scale=sc, out=out, workspace=wsp)
-            return sv.spec_verify_attn_host_lengths(q, k, v, T, D, Th, Dh, max_draft_len=7,
+            return sv.spec_verify_attn_host_lengths(q, k, v, T, D, Th, Dh, max_draft_len=md,
                                                     max_seq_len=900, kv_scale=sc, out=out,
                                                     workspace=wsp)
 
@@ -209,7 +213,7 @@ def test_bounded_wait_runs_out_and_the_kernel_returns(kv, entry):
         torch.cuda.synchronize()
         assert sv.workspace_status(ws) == 0
         assert_close(_bits(out), ref)
-        ws2 = sv.new_workspace(sv.verify_workspace_bytes(sv.api.attn_desc(q, k, 3, 7, 900)))
+        ws2 = sv.new_workspace(sv.verify_workspace_bytes(sv.api.attn_desc(q, k, 3, md, 900)))
         call(ws2)
         torch.cuda.synchronize()
         assert sv.workspace_status(ws2) == 0
@@ -217,3 +221,4 @@ def test_bounded_wait_runs_out_and_the_kernel_returns(kv, entry):
     finally:
         sv.api.inject_wait_timeout(0)
         sv.set_attn_kernel(prev)
+        sv.api.set_row_pairs(prev_pairs)

@@ -246,3 +246,30 @@ def test_every_small_shape_exhaustively():
                 for G, W in ((4, 0), (8, 130)):
                     plan = _plan(_desc(n, G * 2, 2, 128, 31, 300, W=W), Ts, Ds, sms=7)
                     check_plan(plan, Ts, Ds, G, 2, W)
+
+
+def test_row_pair_mode_query(lib):
+    """Which calls run the row-pair kernel (sv_row_pair_mode, no device): only when switched
+    on, and then when 128 < G (1 + D) <= 256 rows per KV head, bf16, d = 128, packed cache,
+    no sliding window, tcgen05, and at most one CTA per (sequence, KV head) per SM."""
+    prev = lib.sv_set_row_pairs(0)
+    try:
+        c4 = lambda D, **kw: _desc(32, 32, 4, 128, D, 16384, **kw)
+        assert api.row_pair_mode(c4(31), 152) == 0          # off by default
+        assert lib.sv_set_row_pairs(1) == 0
+        assert api.row_pair_mode(c4(15), 152) == 0          # 128 rows: one tile
+        for D in (16, 23, 31):
+            assert api.row_pair_mode(c4(D), 152) == 1       # 136 .. 256 rows
+        assert api.row_pair_mode(_desc(32, 64, 4, 128, 31, 16384), 152) == 0  # 512 rows
+        assert api.row_pair_mode(c4(16, fp8=True), 152) == 0
+        assert api.row_pair_mode(c4(16, W=4096), 152) == 0
+        assert api.row_pair_mode(c4(16), 152, block_size=16) == 0
+        assert api.row_pair_mode(c4(16), 152, attn_kernel=1) == 0
+        assert api.row_pair_mode(_desc(32, 32, 4, 64, 16, 16384), 152) == 0   # d = 64
+        assert api.row_pair_mode(c4(16), 127) == 0          # 128 CTAs > 127 SMs
+        assert api.row_pair_mode(_desc(4, 32, 4, 128, 31, 1000), 152) == 1   # 16 CTAs
+        assert lib.sv_set_row_pairs(0) == 1
+        assert api.row_pair_mode(c4(31), 152) == 0
+        assert lib.sv_set_row_pairs(2) == -2 and lib.sv_set_row_pairs(-1) == -2
+    finally:
+        lib.sv_set_row_pairs(prev)
