@@ -185,13 +185,16 @@ def roofline_record(kv_bytes, qo_bytes, fl, attn_s, hbm_gbs, bf16_tflops, kv_dty
             "t_hbm_us": round(t_hbm * 1e6, 2), "t_tensor_us": round(t_tc * 1e6, 2)}
 
 
+# The sources that define the verify-attention kernel's code and its work plan.
+ATTN_SOURCES = ("attn_tc.cu", "tc_util.cuh", "internal.cuh", "plan_combine.cu", "api.cu")
+
+
 def kernel_source_hash():
-    """First 16 hex digits of the sha256 of the library's CUDA sources and header: names
-    the kernel version an ncu capture was taken of."""
-    import glob
+    """First 16 hex digits of the sha256 of the verify-attention kernel's sources and the
+    library header: names the kernel version an ncu capture was taken of."""
     import hashlib
     pkg = os.path.join(ROOT, "speculative_decoding_verification_gqa_gb300", "csrc")
-    files = sorted(glob.glob(os.path.join(pkg, "*.cu")) + glob.glob(os.path.join(pkg, "*.cuh")))
+    files = [os.path.join(pkg, f) for f in ATTN_SOURCES]
     files.append(os.path.join(ROOT, "include", "specverify.h"))
     h = hashlib.sha256()
     for f in files:
@@ -644,9 +647,11 @@ def run_ours(args):
     logits_bytes = d["logits"].numel() * d["logits"].element_size()
 
     # The two logits scans beside torch's own row reductions over the same logits, each
-    # call after L2 is evicted (a buffer twice L2's size read), as a yardstick for a
+    # call after L2 is evicted (a buffer four times L2's size read), as a yardstick for a
     # one-shot read of this size (not part of the step)
-    flush_l = torch.ones(int(2 * L2_BYTES) // 4, dtype=torch.float32, device=dev)
+    # four times L2: reading it also keeps the GPU busy for longer than the host needs to
+    # enqueue the timed call, so the events time the call, not the host
+    flush_l = torch.ones(int(4 * L2_BYTES) // 4, dtype=torch.float32, device=dev)
     sink_l = torch.empty((), dtype=torch.float32, device=dev)
     scans = {
         "spec_accept": lambda: sv.spec_accept(d["logits"], d["draft"], d["D"], max_draft_len=md,
@@ -671,8 +676,8 @@ def run_ours(args):
         logits_scan[name + "_us"] = round(
             1e3 * float(np.median([a_.elapsed_time(b_) for a_, b_ in ec])), 2)
     logits_scan["bytes"] = logits_bytes
-    logits_scan["note"] = ("each call after L2 is evicted; torch's reductions read the same "
-                           "logits; not part of the step")
+    logits_scan["note"] = ("each call after L2 is evicted (a read of 4x L2's size); torch's "
+                           "reductions read the same logits; not part of the step")
 
     # distribution-preserving acceptance on the step's shapes: the step's target logits
     # plus drafter logits at every draft position (not part of the step)

@@ -10,14 +10,17 @@
 // whose running sum of weights exceeds u_sample times their total.
 //
 // One thread-block cluster of CL CTAs per sequence; CTA c of the cluster owns the vocabulary
-// slice [c S, (c + 1) S). The cluster walks the sequence's draft positions in order:
-//   * each CTA streams its slice of the target's and the drafter's row with 16-byte loads
-//     (L2 prefetch of the next position's slices is issued at once) and reduces a running
-//     max and sum of 2^t per row (t = logit / temperature in log2 units);
-//   * the CTAs exchange their (max, sum) pairs through distributed shared memory at a
-//     cluster barrier, and every CTA merges them in the same order, so every CTA holds the
-//     same normalisers and takes the same keep / reject decision from p(x) and q(x);
-//   * rows after the first rejection are never read.
+// slice [c S, (c + 1) S). The cluster walks the sequence's draft positions in rounds of R:
+//   * each CTA streams its slice of the target's and the drafter's rows of the round's
+//     positions with 16-byte loads, all rows' loads in flight together (the slices of the
+//     positions ahead are prefetched into L2), and reduces a running max and sum of 2^t
+//     per row (t = logit / temperature in log2 units);
+//   * the CTAs exchange their (max, sum) pairs through distributed shared memory at one
+//     cluster barrier per round, and every CTA merges them in the same order, so every CTA
+//     holds the same normalisers and takes the same keep / reject decisions from p(x) and
+//     q(x), in order, up to the first rejection;
+//   * rows of positions after the first rejection are read at most by the round that
+//     holds it and the prefetch window.
 // The draw: each thread sums the weights of a contiguous segment of its CTA's slice; the
 // segment sums are scanned within the CTA and the CTA totals across the cluster; the CTA
 // whose interval holds u times the total finds the thread, and that thread walks its
@@ -36,7 +39,9 @@ namespace {
 constexpr int CL = 8;             // CTAs per cluster (one cluster per sequence)
 constexpr int NT = 256;           // threads per CTA
 constexpr int NW = NT / 32;
-constexpr int UB = 8;             // 16-byte loads per row and thread in flight
+constexpr int R = 1;              // draft positions reduced per round
+constexpr int UBR = 8;            // 16-byte loads per row and thread in flight (2 R rows)
+constexpr int PF = 4;             // draft positions whose rows are prefetched ahead
 constexpr float LOG2E = 1.4426950408889634f;
 
 struct StArgs {
@@ -83,10 +88,15 @@ __device__ __forceinline__ uint32_t cluster_size() {
 }
 // Every thread of every CTA of the cluster; writes to shared memory before it are visible
 // to the other CTAs' distributed-shared-memory reads after it.
+// Only thread 0 of a CTA writes shared memory that other CTAs read (the exchange slots), so
+// only warp 0 arrives with release semantics.
 __device__ __forceinline__ void cluster_sync() {
   __syncwarp();  // the .aligned forms are executed by whole, converged warps
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
-               ::: "memory");
+  if ((threadIdx.x >> 5) == 0)
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  else
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 __device__ __forceinline__ float4 ld_remote(const float4* local, uint32_t rank) {
   uint32_t ra;
@@ -159,98 +169,171 @@ __device__ __forceinline__ void ms_raise(MS& a, float bm) {
   }
 }
 
-// This CTA's (max, sum) of one or two rows (target row tr; draft row dr when `two`) over
-// the slice [k0, k1), reduced over the CTA; every thread returns the same values.
+template <int N>
+__device__ __forceinline__ void cta_merge(MS (&acc)[N], MS* sh);
+
+// This CTA's (max, sum) over the slice [k0, k1) of NR = 2 R rows at once (the target's and
+// the drafter's row of R draft positions; row r is read only where use[r]), reduced over
+// the CTA; every thread returns the same values. The rows' loads are issued together, UBR
+// vectors per row and thread, so their latencies overlap.
 template <bool BF16>
-__device__ __forceinline__ void slice_norms(const StArgs& a, int64_t tr, int64_t dr, bool two,
-                                            int k0, int k1, MS& P, MS& Q, MS* sh) {
-  constexpr int VN = Vec<BF16>::N;
+__device__ __forceinline__ void round_norms(const StArgs& a, const int64_t (&row)[2 * R],
+                                            const bool (&use)[2 * R], int k0, int k1,
+                                            MS (&acc)[2 * R], MS* sh) {
+  constexpr int VN = Vec<BF16>::N, NR = 2 * R;
   const int V = a.vocab, tid = threadIdx.x;
   const float c2 = a.c2;
-  P = MS{-INFINITY, 0.f};
-  Q = MS{-INFINITY, 0.f};
+#pragma unroll
+  for (int r = 0; r < NR; ++r) acc[r] = MS{-INFINITY, 0.f};
   if (a.vec) {
-    const uint4* tp = reinterpret_cast<const uint4*>((const char*)a.target +
-                                                     (tr * V + k0) * (BF16 ? 2 : 4));
-    const uint4* dp = two ? reinterpret_cast<const uint4*>((const char*)a.draft +
-                                                           (dr * V + k0) * (BF16 ? 2 : 4))
-                          : tp;
+    const uint4* base[NR];
+#pragma unroll
+    for (int r = 0; r < NR; ++r)
+      base[r] = reinterpret_cast<const uint4*>((const char*)((r & 1) ? a.draft : a.target) +
+                                               (row[r] * V + k0) * (BF16 ? 2 : 4));
     const int nv = (k1 - k0) / VN;
-    for (int v0 = 0; v0 < nv; v0 += NT * UB) {
-      uint4 tv[UB], dv[UB];
+    for (int v0 = 0; v0 < nv; v0 += NT * UBR) {
+      uint4 w[NR][UBR];
 #pragma unroll
-      for (int i = 0; i < UB; ++i) {
-        const int v = v0 + i * NT + tid;
-        if (v < nv) {
-          tv[i] = ld_stream(tp + v);
-          if (two) dv[i] = ld_stream(dp + v);
+      for (int r = 0; r < NR; ++r)
+#pragma unroll
+        for (int i = 0; i < UBR; ++i) {
+          const int v = v0 + i * NT + tid;
+          if (use[r] && v < nv) w[r][i] = ld_stream(base[r] + v);
         }
-      }
-      float bt = -INFINITY, bd = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < UB; ++i)
-        if (v0 + i * NT + tid < nv) {
-          bt = fmaxf(bt, vmax<BF16>(tv[i]));
-          if (two) bd = fmaxf(bd, vmax<BF16>(dv[i]));
-        }
-      ms_raise(P, __fmul_rn(bt, c2));
-      if (two) ms_raise(Q, __fmul_rn(bd, c2));
-      const float nmp = P.m == -INFINITY ? 0.f : -P.m, nmq = Q.m == -INFINITY ? 0.f : -Q.m;
+      for (int r = 0; r < NR; ++r) {
+        if (!use[r]) continue;
+        float bm = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < UB; ++i)
-        if (v0 + i * NT + tid < nv) {
+        for (int i = 0; i < UBR; ++i)
+          if (v0 + i * NT + tid < nv) bm = fmaxf(bm, vmax<BF16>(w[r][i]));
+        ms_raise(acc[r], __fmul_rn(bm, c2));
+        const float nm = acc[r].m == -INFINITY ? 0.f : -acc[r].m;
 #pragma unroll
-          for (int e = 0; e < VN; ++e) {
-            P.s = __fadd_rn(P.s, ex2(__fmaf_rn(velem<BF16>(tv[i], e), c2, nmp)));
-            if (two) Q.s = __fadd_rn(Q.s, ex2(__fmaf_rn(velem<BF16>(dv[i], e), c2, nmq)));
+        for (int i = 0; i < UBR; ++i)
+          if (v0 + i * NT + tid < nv) {  // a vector's terms summed as a tree (depth 3)
+            float t[VN];
+#pragma unroll
+            for (int e = 0; e < VN; ++e) t[e] = ex2(__fmaf_rn(velem<BF16>(w[r][i], e), c2, nm));
+#pragma unroll
+            for (int h = VN / 2; h > 0; h >>= 1)
+#pragma unroll
+              for (int e = 0; e < h; ++e) t[e] = __fadd_rn(t[e], t[e + h]);
+            acc[r].s = __fadd_rn(acc[r].s, t[0]);
           }
-        }
+      }
     }
   } else {
     for (int k = k0 + tid; k < k1; k += NT) {
-      const float t = __fmul_rn(logit<BF16>(a.target, tr, V, k), c2);
-      ms_raise(P, t);
-      if (P.m != -INFINITY) P.s = __fadd_rn(P.s, ex2(__fsub_rn(t, P.m)));
-      if (two) {
-        const float d = __fmul_rn(logit<BF16>(a.draft, dr, V, k), c2);
-        ms_raise(Q, d);
-        if (Q.m != -INFINITY) Q.s = __fadd_rn(Q.s, ex2(__fsub_rn(d, Q.m)));
+#pragma unroll
+      for (int r = 0; r < NR; ++r) {
+        if (!use[r]) continue;
+        const float t = __fmul_rn(logit<BF16>((r & 1) ? a.draft : a.target, row[r], V, k), c2);
+        ms_raise(acc[r], t);
+        if (acc[r].m != -INFINITY) acc[r].s = __fadd_rn(acc[r].s, ex2(__fsub_rn(t, acc[r].m)));
       }
     }
   }
+  cta_merge<NR>(acc, sh);
+}
+
+// Threads' parts (acc, the same count N on every thread) merged over the CTA; every thread
+// returns the same values.
+template <int N>
+__device__ __forceinline__ void cta_merge(MS (&acc)[N], MS* sh) {
+  const int tid = threadIdx.x;
   // A row of -inf alone keeps (-inf, 0); a -inf element adds 2^-inf = 0.
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    P = ms_merge(P, ms_shfl(P, o));
-    Q = ms_merge(Q, ms_shfl(Q, o));
-  }
-  const int lane = tid & 31, w = tid >> 5;
-  if (lane == 0) {
-    sh[w] = P;
-    sh[NW + w] = Q;
-  }
+  for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+    for (int r = 0; r < N; ++r) acc[r] = ms_merge(acc[r], ms_shfl(acc[r], o));
+  const int lane = tid & 31, wid = tid >> 5;
+  if (lane == 0)
+#pragma unroll
+    for (int r = 0; r < N; ++r) sh[r * NW + wid] = acc[r];
   __syncthreads();
-  P = sh[0];
-  Q = sh[NW];
-  for (int i = 1; i < NW; ++i) {
-    P = ms_merge(P, sh[i]);
-    Q = ms_merge(Q, sh[NW + i]);
+  // the NW warp parts merged as a tree over lanes 0 .. NW - 1 of every warp: the same
+  // operations in the same order in every warp, so every thread holds the same result
+#pragma unroll
+  for (int r = 0; r < N; ++r) {
+    MS v = lane < NW ? sh[r * NW + lane] : MS{-INFINITY, 0.f};
+#pragma unroll
+    for (int o = NW / 2; o > 0; o >>= 1) v = ms_merge(v, ms_shfl(v, o));
+    acc[r] = MS{__shfl_sync(0xffffffffu, v.m, 0), __shfl_sync(0xffffffffu, v.s, 0)};
   }
   __syncthreads();  // sh is reused by the next call
 }
 
-// Exchange of one float4 per CTA through distributed shared memory: each CTA publishes
-// `mine`, and every CTA returns all CL values in rank order (the same in every CTA).
-// `slots` has two buffers of CL entries, used alternately (`round` parity), so a fast CTA
-// never overwrites values a slower one has yet to read: it can only start round r + 2 after
+// One position's row slices, one batch (every vector of the thread at once): the loads of
+// the target's row tr and, when `two`, the drafter's row dr.
+template <bool BF16>
+__device__ __forceinline__ void issue_rows(const StArgs& a, int64_t tr, int64_t dr, bool two,
+                                           int k0, int nv, uint4 (&tv)[UBR], uint4 (&dv)[UBR]) {
+  const int V = a.vocab, tid = threadIdx.x;
+  const uint4* tp = reinterpret_cast<const uint4*>((const char*)a.target + (tr * V + k0) * (BF16 ? 2 : 4));
+  const uint4* dp = reinterpret_cast<const uint4*>((const char*)a.draft + (dr * V + k0) * (BF16 ? 2 : 4));
+#pragma unroll
+  for (int i = 0; i < UBR; ++i) {
+    const int v = i * NT + tid;
+    if (v < nv) {
+      tv[i] = ld_stream(tp + v);
+      if (two) dv[i] = ld_stream(dp + v);
+    }
+  }
+}
+
+// The thread's (max, sum) parts of the vectors loaded by issue_rows.
+template <bool BF16>
+__device__ __forceinline__ void thread_parts(const uint4 (&tv)[UBR], const uint4 (&dv)[UBR],
+                                             bool two, int nv, float c2, MS (&acc)[2]) {
+  constexpr int VN = Vec<BF16>::N;
+  const int tid = threadIdx.x;
+  acc[0] = MS{-INFINITY, 0.f};
+  acc[1] = MS{-INFINITY, 0.f};
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    if (r == 1 && !two) continue;
+    const uint4(&w)[UBR] = r ? dv : tv;
+    float bm = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < UBR; ++i)
+      if (i * NT + tid < nv) bm = fmaxf(bm, vmax<BF16>(w[i]));
+    ms_raise(acc[r], __fmul_rn(bm, c2));
+    const float nm = acc[r].m == -INFINITY ? 0.f : -acc[r].m;
+#pragma unroll
+    for (int i = 0; i < UBR; ++i)
+      if (i * NT + tid < nv) {  // a vector's terms summed as a tree (depth 3)
+        float t[VN];
+#pragma unroll
+        for (int e = 0; e < VN; ++e) t[e] = ex2(__fmaf_rn(velem<BF16>(w[i], e), c2, nm));
+#pragma unroll
+        for (int h = VN / 2; h > 0; h >>= 1)
+#pragma unroll
+          for (int e = 0; e < h; ++e) t[e] = __fadd_rn(t[e], t[e + h]);
+        acc[r].s = __fadd_rn(acc[r].s, t[0]);
+      }
+  }
+}
+
+// Exchange of N float4 per CTA through distributed shared memory: each CTA publishes
+// `mine`, and every CTA returns all CL x N values in rank order (the same in every CTA).
+// `slots` has two buffers, used alternately (`round` parity), so a fast CTA never
+// overwrites values a slower one has yet to read: it can only start round r + 2 after
 // every CTA has reached the barrier of round r + 1, i.e. finished reading round r.
-__device__ __forceinline__ void exchange(float4 mine, float4 (*slots)[CL], uint32_t& round, float4* all) {
+template <int N>
+__device__ __forceinline__ void exchange(const float4 (&mine)[N], float4 (*slots)[CL][R],
+                                         uint32_t& round, float4 (&all)[CL][N]) {
   const uint32_t rank = cluster_rank();
-  float4* buf = slots[round & 1];
-  if (threadIdx.x == 0) buf[rank] = mine;
+  float4 (*buf)[R] = slots[round & 1];
+  if (threadIdx.x == 0)
+#pragma unroll
+    for (int n = 0; n < N; ++n) buf[rank][n] = mine[n];
   cluster_sync();
 #pragma unroll
-  for (int c = 0; c < CL; ++c) all[c] = ld_remote(&buf[c], (uint32_t)c);  // CTA c's own slot
+  for (int c = 0; c < CL; ++c)
+#pragma unroll
+    for (int n = 0; n < N; ++n) all[c][n] = ld_remote(&buf[c][n], (uint32_t)c);  // CTA c's slot
   ++round;
 }
 
@@ -324,7 +407,7 @@ __device__ __forceinline__ void visit(const Weight<BF16>& wt, bool vec, int s0, 
 // *out and the function returns 0.
 template <bool BF16>
 __device__ __forceinline__ int cluster_draw(const Weight<BF16>& wt, bool vec, float u, int k0,
-                                            int k1, float4 (*slots)[CL], uint32_t& round,
+                                            int k1, float4 (*slots)[CL][R], uint32_t& round,
                                             float* shf, int* shi, int32_t* out) {
   constexpr int VN = Vec<BF16>::N;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -361,20 +444,21 @@ __device__ __forceinline__ int cluster_draw(const Weight<BF16>& wt, bool vec, fl
   }
   const float ex = before + incl - sum;
   __syncthreads();
-  float4 all[CL];
-  exchange(make_float4(ctot, __int_as_float(clast), 0.f, 0.f), slots, round, all);
+  float4 all[CL][1];
+  const float4 mine[1] = {make_float4(ctot, __int_as_float(clast), 0.f, 0.f)};
+  exchange<1>(mine, slots, round, all);
   float pre = 0.f, total = 0.f;
   int glast = -1;
   for (int c = 0; c < CL; ++c) {
-    total += all[c].x;
-    glast = max(glast, __float_as_int(all[c].y));
+    total += all[c][0].x;
+    glast = max(glast, __float_as_int(all[c][0].y));
   }
   if (!(total > 0.f)) return -1;  // the same on every CTA
   const float target = u * total;
   int cstar = -1;
   for (int c = 0; c < CL; ++c) {
-    if (cstar < 0 && all[c].x > 0.f && target < pre + all[c].x) cstar = c;
-    if (cstar < 0) pre += all[c].x;
+    if (cstar < 0 && all[c][0].x > 0.f && target < pre + all[c][0].x) cstar = c;
+    if (cstar < 0) pre += all[c][0].x;
   }
   const uint32_t rank = cluster_rank();
   if (cstar < 0) {  // rounding left the target at the end: the last token of positive weight
@@ -406,10 +490,15 @@ __device__ __forceinline__ int cluster_draw(const Weight<BF16>& wt, bool vec, fl
   return 0;
 }
 
-template <bool BF16>
-__global__ void __launch_bounds__(NT) accept_stochastic_kernel(StArgs a) {
-  __shared__ MS sh_ms[2 * NW];
-  __shared__ float4 slots[2][CL];
+// Two CTAs per SM (at most 128 registers a thread), so that the clusters of a batch of up to
+// 2 x SMs / CL sequences are resident at once.
+// PIPE: rows start on 16-byte boundaries and a CTA's slice of a row is one batch per thread
+// (the next position's loads are issued during this one's reductions).
+template <bool BF16, bool PIPE>
+__global__ void __launch_bounds__(NT, 2) accept_stochastic_kernel(StArgs a) {
+  __shared__ MS sh_ms[2 * R * NW];
+  __shared__ float4 slots[2][CL][R];
+  __shared__ float s_lx[256], s_dx[256], s_ua[256];  // per draft position (D <= 255)
   __shared__ float shf[NW];
   __shared__ int shi[NW + 1];
   __shared__ int64_t sh64[NW];
@@ -468,32 +557,67 @@ __global__ void __launch_bounds__(NT) accept_stochastic_kernel(StArgs a) {
     }
   };
   uint32_t round = 0;
-  float4 all[CL];
-  auto cluster_norms = [&](MS& P, MS& Q) {  // merge every CTA's parts in rank order
-    exchange(make_float4(P.m, P.s, Q.m, Q.s), slots, round, all);
-    P = MS{all[0].x, all[0].y};
-    Q = MS{all[0].z, all[0].w};
-    for (int c = 1; c < CL; ++c) {
-      P = ms_merge(P, MS{all[c].x, all[c].y});
-      Q = ms_merge(Q, MS{all[c].z, all[c].w});
-    }
+  // L2 prefetch of position j's rows (the target's bonus row for j = D); rows of positions
+  // after the first rejection may be fetched for nothing (at most the window's)
+  auto prefetch_pos = [&](int j) {
+    if (j <= D) prefetch_rows(q_off + j, d_off + j, j < D);
   };
+  for (int j = 0; j < PF; ++j) prefetch_pos(j);
 
+  // What each decision needs besides the normalisers (the drafted token's two logits and
+  // its uniform), loaded for every position at once.
+  for (int j = tid; j < D; j += NT) {
+    const int x = a.draft_tokens[d_off + j];
+    s_lx[j] = logit<BF16>(a.target, q_off + j, V, x);
+    s_dx[j] = logit<BF16>(a.draft, d_off + j, V, x);
+    s_ua[j] = a.u_accept[d_off + j];
+  }
+  // Positions in order, each: every CTA reduces its slice of the position's rows (the
+  // target's and the drafter's row of a draft position, the target's row alone for the
+  // bonus position D), the CTAs exchange and merge their parts in rank order, and the
+  // draft is decided. With 16-byte rows whose slice is one batch per thread, the next
+  // position's loads are issued as soon as this position's vectors are consumed, so they
+  // are in flight during its reductions and exchange.
+  const int nv = PIPE ? (k1 - k0) / Vec<BF16>::N : 0;
+  uint4 tv[PIPE ? UBR : 1], dv[PIPE ? UBR : 1];
+  if constexpr (PIPE) issue_rows<BF16>(a, q_off, d_off, D > 0, k0, nv, tv, dv);
   int n = D;  // drafts kept
-  MS P, Q;
-  prefetch_rows(q_off, d_off, D > 0);
-  for (int j = 0; j < D; ++j) {
-    const int64_t tr = q_off + j, dr = d_off + j;
-    // what the decision needs besides the normalisers, loaded before the rows stream
-    const int x = a.draft_tokens[dr];
-    const float lx = logit<BF16>(a.target, tr, V, x), dx = logit<BF16>(a.draft, dr, V, x);
-    const float ua = a.u_accept[dr];
-    slice_norms<BF16>(a, tr, dr, true, k0, k1, P, Q, sh_ms);
-    prefetch_rows(tr + 1, dr + 1, j + 1 < D);  // the next position's rows (the bonus row last)
-    cluster_norms(P, Q);
-    const float px = __fdiv_rn(ex2(__fmaf_rn(lx, a.c2, -P.m)), P.s);
-    const float qx = __fdiv_rn(ex2(__fmaf_rn(dx, a.c2, -Q.m)), Q.s);
-    if (!(__fmul_rn(ua, qx) < px)) {  // the same decision on every thread of the cluster
+  MS P, Q;    // normalisers of row n (the draw's row)
+  for (int j = 0; j <= D; ++j) {
+    prefetch_pos(j + PF);
+    MS acc[2];
+    if constexpr (PIPE) {
+      thread_parts<BF16>(tv, dv, j < D, nv, a.c2, acc);
+      if (j + 1 <= D) issue_rows<BF16>(a, q_off + j + 1, d_off + j + 1, j + 1 < D, k0, nv, tv, dv);
+      cta_merge<2>(acc, sh_ms);
+    } else {
+      const int64_t row[2] = {q_off + j, d_off + j};
+      const bool use[2] = {true, j < D};
+      round_norms<BF16>(a, row, use, k0, k1, acc, sh_ms);
+    }
+    float4 mine[1], all[CL][1];
+    mine[0] = make_float4(acc[0].m, acc[0].s, acc[1].m, acc[1].s);
+    exchange<1>(mine, slots, round, all);
+    // every CTA's part, merged as a tree over lanes 0 .. CL - 1 (the same in every warp of
+    // every CTA)
+    const int lane = tid & 31;
+    float4 mc = all[0][0];
+#pragma unroll
+    for (int c = 1; c < CL; ++c)
+      if (lane == c) mc = all[c][0];
+    P = lane < CL ? MS{mc.x, mc.y} : MS{-INFINITY, 0.f};
+    Q = lane < CL ? MS{mc.z, mc.w} : MS{-INFINITY, 0.f};
+#pragma unroll
+    for (int o = CL / 2; o > 0; o >>= 1) {
+      P = ms_merge(P, ms_shfl(P, o));
+      Q = ms_merge(Q, ms_shfl(Q, o));
+    }
+    P = MS{__shfl_sync(0xffffffffu, P.m, 0), __shfl_sync(0xffffffffu, P.s, 0)};
+    Q = MS{__shfl_sync(0xffffffffu, Q.m, 0), __shfl_sync(0xffffffffu, Q.s, 0)};
+    if (j == D) break;  // every draft kept: P is the bonus row's normaliser
+    const float px = __fdiv_rn(ex2(__fmaf_rn(s_lx[j], a.c2, -P.m)), P.s);
+    const float qx = __fdiv_rn(ex2(__fmaf_rn(s_dx[j], a.c2, -Q.m)), Q.s);
+    if (!(__fmul_rn(s_ua[j], qx) < px)) {  // the same decision on every thread of the cluster
       n = j;
       break;
     }
@@ -505,21 +629,15 @@ __global__ void __launch_bounds__(NT) accept_stochastic_kernel(StArgs a) {
                          P.m, __frcp_rn(P.s), Q.m, __frcp_rn(Q.s), true};
     status = cluster_draw<BF16>(w, a.vec, us, k0, k1, slots, round, shf, shi, a.next_token + b);
   }
-  if (status < 0) {  // every draft kept (row D), or an all-zero residual (row n)
-    const int64_t tr = q_off + n;
-    if (n == D) {
-      MS unused;
-      slice_norms<BF16>(a, tr, 0, false, k0, k1, P, unused, sh_ms);
-      cluster_norms(P, unused);
-    }
-    const Weight<BF16> w{a.target, a.draft, V, a.c2, tr, 0, P.m, 1.f, 0.f, 0.f, false};
+  if (status < 0) {  // every draft kept (row D: P already holds it), or an all-zero residual
+    const Weight<BF16> w{a.target, a.draft, V, a.c2, q_off + n, 0, P.m, 1.f, 0.f, 0.f, false};
     cluster_draw<BF16>(w, a.vec, us, k0, k1, slots, round, shf, shi, a.next_token + b);
   }
   if (rank == 0 && tid == 0) a.accept_len[b] = n + 1;
   cluster_sync();  // no CTA leaves while another may still read its shared memory
 }
 
-template <bool BF16>
+template <bool BF16, bool PIPE>
 cudaError_t launch_st(const StArgs& a, cudaStream_t s) {
   if (take_injected_launch_failure()) return cudaErrorLaunchFailure;  // nothing launched
   cudaLaunchConfig_t cfg = {};
@@ -536,7 +654,7 @@ cudaError_t launch_st(const StArgs& a, cudaStream_t s) {
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, accept_stochastic_kernel<BF16>, a);
+  return cudaLaunchKernelEx(&cfg, accept_stochastic_kernel<BF16, PIPE>, a);
 }
 
 }  // namespace
@@ -568,7 +686,9 @@ cudaError_t launch_accept_stochastic(int B, int max_draft, int vocab, int dtype,
           (draft == nullptr || ((uintptr_t)draft % al) == 0);
   // slices of whole vectors: every slice of an aligned row starts on a 16-byte boundary
   a.slice = ((vocab + CL - 1) / CL + vn - 1) / vn * vn;
-  return bf16 ? launch_st<true>(a, s) : launch_st<false>(a, s);
+  const bool pipe = a.vec && a.slice / vn <= NT * UBR;
+  if (bf16) return pipe ? launch_st<true, true>(a, s) : launch_st<true, false>(a, s);
+  return pipe ? launch_st<false, true>(a, s) : launch_st<false, false>(a, s);
 }
 
 }  // namespace sv

@@ -115,8 +115,12 @@ def check(x, temperature, min_decided=0.5):
     return al, nt
 
 
+# V = 7 and 32003: rows off 16-byte boundaries (scalar loads); 1000 and 128256: one batch of
+# 16-byte loads per thread and row slice (the next position's loads overlap this one's
+# reductions); 262144: several batches per slice
 CASES = [(7, "fp32", 1.0), (7, "bf16", 0.3), (1000, "bf16", 1.0), (1000, "fp32", 0.3),
-         (32003, "bf16", 0.3), (32003, "fp32", 1.0), (128256, "bf16", 0.3)]
+         (32003, "bf16", 0.3), (32003, "fp32", 1.0), (128256, "bf16", 0.3),
+         (262144, "bf16", 1.0)]
 
 
 @pytest.mark.parametrize("V,dtype,temperature", CASES)
