@@ -89,12 +89,15 @@ def parse():
                          "blocks of this many positions (0: skip)")
     ap.add_argument("--side-stochastic", type=int, default=1,
                     help="also time spec_accept_stochastic on the step's shapes (0: skip)")
-    ap.add_argument("--per-config", default="c3,c4:15,c4:16,c4:31,c5",
+    ap.add_argument("--per-config", default="c3,c4:15,c4:16,c4:31,c4:31:pairs,c5",
                     help="other workloads measured into the line's per_config object, as "
-                         "config[:D] items ('none': skip; only with the default --config)")
+                         "config[:D[:pairs]] items ('none': skip; only with the default "
+                         "--config; ':pairs' runs the row-pair kernel)")
     ap.add_argument("--per-config-steps", type=int, default=100)
     ap.add_argument("--only-step", action="store_true",
                     help="run W + K steps of the workload and exit (for profilers)")
+    ap.add_argument("--row-pairs", type=int, default=0, choices=[0, 1],
+                    help="1: the row-pair attention kernel wherever it applies")
     return ap.parse_args()
 
 
@@ -384,7 +387,14 @@ def run_reference(args):
 # workload (dram__bytes_read.sum + dram__bytes_write.sum), keyed by (config, D override,
 # kernel) with the kernel_source_hash() of the sources captured: an entry whose hash is not
 # the current one reads as None.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    ("c2", None, "tcgen05"): ("e8fb99e09f77f592", 549_249_024 + 3_062_528),
+    ("c3", None, "tcgen05"): ("e8fb99e09f77f592", 542_908_928 + 6_476_800),
+    ("c4", 15, "tcgen05"): ("e8fb99e09f77f592", 1_086_248_192 + 3_036_672),
+    ("c4", 16, "tcgen05"): ("e8fb99e09f77f592", 1_089_497_088 + 9_582_848),
+    ("c4", 31, "tcgen05"): ("e8fb99e09f77f592", 1_095_461_376 + 15_738_368),
+    ("c5", None, "tcgen05"): ("e8fb99e09f77f592", 9_004_260_352 + 6_507_264),
+}
 
 
 class Rig:
@@ -482,7 +492,8 @@ def timed_attention(sv, step, stream, K):
     return float(np.mean([a_.elapsed_time(b_) for a_, b_ in ev]))
 
 
-def measure_config(sv, synth, cfg, Dv, seed, dev, K, W, attn_kernel, src_hash):
+def measure_config(sv, synth, cfg, Dv, seed, dev, K, W, attn_kernel, src_hash,
+                   row_pairs=False):
     """The step of another workload: attention and step time, K/V GB/s, verified query
     tokens/s, accepted tokens/s and the attention kernel's roofline."""
     import torch
@@ -509,7 +520,11 @@ def measure_config(sv, synth, cfg, Dv, seed, dev, K, W, attn_kernel, src_hash):
            "mean_accept_len": round(accepted / w.B, 3),
            "attn_tflops": round(fl / (attn_ms / 1e3) / 1e12, 1),
            "roofline": roofline_record(kv, qo, fl, attn_ms / 1e3, hbm, tf, w.kv_dtype,
-                                       attn_kernel, ncu_traffic(cfg, Dv, attn_kernel, src_hash))}
+                                       attn_kernel,
+                                       None if row_pairs else
+                                       ncu_traffic(cfg, Dv, attn_kernel, src_hash))}
+    if row_pairs:
+        rec["kernel"] = "row pairs (one CTA per sequence and KV head, both 128-row tiles)"
     del rig
     torch.cuda.empty_cache()
     return rec
@@ -536,6 +551,7 @@ def run_ours(args):
     sv.load_library()
     if args.kernel != "auto":
         sv.set_attn_kernel(1 if args.kernel == "mma" else 2)
+    sv.api.set_row_pairs(args.row_pairs)
     attn_kernel = {1: "mma.sync", 2: "tcgen05"}[_active_kernel(sv)]
 
     w, T, D, p = workload(args)
@@ -902,12 +918,16 @@ def run_ours(args):
     if args.per_config != "none" and args.config == "c2" and args.D is None:
         per_config = {}
         for item in args.per_config.split(","):
-            cfg, _, dv = item.partition(":")
-            Dv = int(dv) if dv else None
-            key = cfg + ("_D%d" % Dv if Dv is not None else "")
+            parts = item.split(":")
+            cfg = parts[0]
+            Dv = int(parts[1]) if len(parts) > 1 and parts[1] else None
+            pairs = len(parts) > 2 and parts[2] == "pairs"
+            key = cfg + ("_D%d" % Dv if Dv is not None else "") + ("_row_pairs" if pairs else "")
+            prev_pairs = sv.api.set_row_pairs(1 if pairs else args.row_pairs)
             per_config[key] = measure_config(sv, synth, cfg, Dv, seed, dev,
                                              args.per_config_steps, max(3, args.warmup),
-                                             attn_kernel, src_hash)
+                                             attn_kernel, src_hash, row_pairs=pairs)
+            sv.api.set_row_pairs(prev_pairs)
 
     # max over ranks
     ms_step, attn_ms, e2e_ms, e2e_res_ms, ms_step_hl = max_over_ranks(

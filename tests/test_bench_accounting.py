@@ -126,4 +126,4 @@ def test_ncu_traffic_is_dropped_when_the_sources_change(monkeypatch):
     monkeypatch.setitem(bench.NCU_TRAFFIC, ("c3", None, "tcgen05"), ("0" * 16, 999))
     assert bench.ncu_traffic("c2", None, "tcgen05") == 12345
     assert bench.ncu_traffic("c3", None, "tcgen05") is None      # another kernel version
-    assert bench.ncu_traffic("c4", 15, "tcgen05") is None        # never captured
+    assert bench.ncu_traffic("c4", 7, "tcgen05") is None         # never captured
