@@ -4,15 +4,20 @@
 // rejected draft).
 //
 // One kernel of persistent CTAs, each scanning an equal contiguous range of the packed
-// logits with 16-byte streaming loads. Per thread and row, only each vector's maximum
-// (packed max instructions) is compared, without branches, and the best vector is kept;
-// the element index inside it is resolved once at the end of the row. Warp-shuffle
+// logits. When rows are whole 32-byte vectors (and the logits 32-byte aligned) the range is
+// one stream of 32-byte vectors that runs across row boundaries, so a CTA's loads do not
+// drain at every row end: a batch is taken in one pass per row it touches, and a row that
+// ends inside it is reduced before the next row's pass. Otherwise the range is scanned row
+// by row with 16-byte loads and scalar heads and tails. Either way only each vector's
+// maximum (packed max instructions) is compared, without branches, the best vector and its
+// words are kept, and the element index inside it is resolved once per row. Warp-shuffle
 // reductions with the comparator "larger value wins, equal values: smaller index wins"
 // give one candidate per warp and row, folded into the row's 64-bit key (order-preserving
 // value bits above the inverted index) with one atomicMax. Values are compared exactly in
-// fp32 (bf16 widens exactly). The last CTA to finish (a completion ticket in the
-// workspace) reads and clears every row's key, which is the target's token, and, per
-// sequence, finds the first position whose draft differs from it.
+// fp32 (bf16 widens exactly). Every CTA stages the drafts in shared memory while it scans;
+// the last CTA to finish (a completion ticket in the workspace) reads and clears every
+// row's key, which is the target's token, and, per sequence, finds the first position
+// whose draft differs from it.
 #include <cuda_bf16.h>
 
 #include "internal.cuh"
@@ -27,6 +32,13 @@ constexpr int ARGMAX_THREADS = 512;
 constexpr int ARGMAX_CTAS_PER_SM = 2;
 constexpr int UNROLL = 8;
 constexpr int NONE = 0x7fffffff;  // "no candidate yet"
+// Continuous scan: FLAT_U 32-byte vectors per thread per batch (ARGMAX_THREADS * FLAT_U
+// vectors, 64 KB per CTA); measured faster than 16-byte vectors eight at a time, and than
+// issuing the next batch before processing the current one.
+constexpr int FLAT_U = 4;
+constexpr int VW = 8;       // 32-bit words per vector
+constexpr int VB = VW * 4;  // bytes per vector
+constexpr int64_t FLAT_BATCH_VECS = (int64_t)ARGMAX_THREADS * FLAT_U;
 
 __device__ __forceinline__ bool better(float v1, int i1, float v2, int i2) {
   if (i1 == NONE) return false;
@@ -80,6 +92,7 @@ struct AcceptArgs {
                             // far; read and reset to 0 by the last CTA
   int32_t* amax;            // [B * (1 + max_draft)]: the target's token of every row
   int B, max_draft, vocab, nctas;
+  int64_t row_vecs;  // vectors per row (continuous scan only)
 };
 
 constexpr int FIN_B = 1024;   // sequences whose D_b stay in shared memory
@@ -189,6 +202,124 @@ __device__ void scan_range(const AcceptArgs& a, int64_t rows) {
   }
 }
 
+// One vector of logits in one load; read once, so not kept in L1.
+__device__ __forceinline__ void load_vec(const uint8_t* p, uint32_t (&w)[VW]) {
+  asm volatile(
+      "ld.global.nc.L1::no_allocate.L2::256B.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+      : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]),
+        "=r"(w[7])
+      : "l"(p));
+}
+
+template <bool BF16>
+__device__ __forceinline__ float elem_of(const uint32_t (&w)[VW], int t) {
+  if constexpr (BF16)
+    return bf16_at(w[t >> 1], t & 1);
+  else
+    return __uint_as_float(w[t]);
+}
+
+// Largest value of a vector (NaN ignored unless all are NaN).
+template <bool BF16>
+__device__ __forceinline__ float vmax_vec(const uint32_t (&w)[VW]) {
+  if constexpr (BF16) {
+    return fmaxf(vmax_bf16x8(make_uint4(w[0], w[1], w[2], w[3])),
+                 vmax_bf16x8(make_uint4(w[4], w[5], w[6], w[7])));
+  } else {
+    const float m0 = fmaxf(__uint_as_float(w[0]), __uint_as_float(w[1]));
+    const float m1 = fmaxf(__uint_as_float(w[2]), __uint_as_float(w[3]));
+    const float m2 = fmaxf(__uint_as_float(w[4]), __uint_as_float(w[5]));
+    const float m3 = fmaxf(__uint_as_float(w[6]), __uint_as_float(w[7]));
+    return fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+  }
+}
+
+// A thread's best vector of its current row: its maximum bv, its row-local index bvec
+// (-1: none yet) and its words, kept without branches; only a strictly larger maximum
+// replaces it (vectors reach a thread in increasing order, so the earliest of equal maxima
+// stays). The element index inside it is resolved once, when the row is flushed.
+struct Best {
+  float bv;
+  int bvec;
+  uint32_t bw[VW];
+};
+
+template <bool BF16>
+__device__ __forceinline__ void consider(const uint32_t (&w)[VW], int vrow, bool valid,
+                                         Best& b) {
+  const float vm = vmax_vec<BF16>(w);
+  const bool win = valid && (vm > b.bv || (b.bvec < 0 && vm == vm));
+  b.bv = win ? vm : b.bv;
+  b.bvec = win ? vrow : b.bvec;
+#pragma unroll
+  for (int t = 0; t < VW; ++t) b.bw[t] = win ? w[t] : b.bw[t];
+}
+
+// Row r's candidate: each thread's first element equal to its best vector's maximum, then
+// one key update per warp (the whole warp calls it); the thread's best is reset.
+template <bool BF16>
+__device__ __forceinline__ void flush_row(const AcceptArgs& a, int64_t r, Best& b) {
+  constexpr int VE = VB / (BF16 ? 2 : 4);  // elements per vector
+  float bv = b.bv;
+  int bi = NONE;
+  if (b.bvec >= 0) {
+    int q = VE - 1;
+#pragma unroll
+    for (int t = VE - 1; t >= 0; --t)
+      if (elem_of<BF16>(b.bw, t) == bv) q = t;
+    bi = b.bvec * VE + q;
+  }
+  warp_argmax(bv, bi);
+  if ((threadIdx.x & 31) == 0 && bi != NONE) atomicMax(a.key + r, row_key(bv, bi));
+  b.bv = -INFINITY;
+  b.bvec = -1;
+}
+
+// Continuous scan of CTA blockIdx.x's equal share of the rows * row_vecs vectors.
+// Thread t's batch at s holds vectors s + k * ARGMAX_THREADS + t (k < FLAT_U). A batch is
+// taken in one pass per row it touches: the vectors of the current row, then, while the
+// row ends inside the batch, the flush of the finished row (uniform over the CTA, so whole
+// warps reduce it) and a pass over the next row's vectors.
+template <bool BF16>
+__device__ void scan_flat(const AcceptArgs& a, int64_t rows) {
+  const int64_t rv = a.row_vecs, nv = rows * rv;
+  const int64_t v0 = nv * blockIdx.x / a.nctas, v1 = nv * (blockIdx.x + 1) / a.nctas;
+  const uint8_t* base = (const uint8_t*)a.logits;
+  int64_t r = v0 / rv, row0 = r * rv, rb = row0 + rv;  // current row [row0, rb)
+  Best b;
+  b.bv = -INFINITY;
+  b.bvec = -1;
+  auto issue = [&](uint32_t (&w)[FLAT_U][VW], int64_t s) {
+#pragma unroll
+    for (int k = 0; k < FLAT_U; ++k) {
+      const int64_t vi = s + (int64_t)k * ARGMAX_THREADS + threadIdx.x;
+      if (vi < v1) load_vec(base + vi * VB, w[k]);
+    }
+  };
+  auto process = [&](const uint32_t (&w)[FLAT_U][VW], int64_t s) {
+    const int64_t se = min(s + FLAT_BATCH_VECS, v1);  // end of the batch's valid vectors
+    while (true) {
+      const int64_t cut = min(rb, se);
+#pragma unroll
+      for (int k = 0; k < FLAT_U; ++k) {
+        const int64_t vi = s + (int64_t)k * ARGMAX_THREADS + threadIdx.x;
+        consider<BF16>(w[k], (int)(vi - row0), vi >= row0 && vi < cut, b);
+      }
+      if (rb >= se) break;
+      flush_row<BF16>(a, r, b);  // row r is finished
+      ++r;
+      row0 = rb;
+      rb += rv;
+    }
+  };
+  for (int64_t s = v0; s < v1; s += FLAT_BATCH_VECS) {
+    uint32_t w[FLAT_U][VW];
+    issue(w, s);
+    process(w, s);
+  }
+  flush_row<BF16>(a, r, b);  // the range's last row (no key update if it has no candidate)
+}
+
 // Exclusive scan over the CTA of (1 + D, D); returns the running totals through `carry`.
 __device__ __forceinline__ void block_scan2(long long& x, long long& y, long long* sh2,
                                             long long& cx, long long& cy) {
@@ -233,29 +364,25 @@ __device__ __forceinline__ void cp_async4(void* smem_dst, const void* gmem_src) 
 
 // Run by the last CTA: every row's target token, then per sequence (one warp each) the
 // accepted length. For up to FIN_CAP rows and drafts everything stays in shared memory,
-// so the only global round trip is the candidates' (the drafts are copied alongside).
-__device__ __noinline__ void finalize_all(const AcceptArgs& a, int64_t rows, const int* s_D) {
+// where every CTA staged the drafts during its scan, so the only global round trip left
+// is the read of the candidates.
+__device__ __forceinline__ void finalize_all(const AcceptArgs& a, int64_t rows, const int* s_D,
+                                             const int* s_draft, bool in_smem) {
   __shared__ long long sh2[2 * (ARGMAX_THREADS / 32)];
   __shared__ long long s_q[ARGMAX_THREADS], s_d[ARGMAX_THREADS];
   __shared__ int s_n[ARGMAX_THREADS];
-  __shared__ int s_amax[FIN_CAP], s_draft[FIN_CAP];
-  const int64_t ndraft = rows - a.B;  // sum of D_b
-  const bool in_smem = rows <= FIN_CAP && a.B <= FIN_B;
+  __shared__ int s_amax[FIN_CAP];
   int* amax = in_smem ? s_amax : a.amax;
   const int* draft = in_smem ? s_draft : a.draft_tokens;
-  if (in_smem) {
-    for (int j = threadIdx.x; j < ndraft; j += blockDim.x) cp_async4(s_draft + j, a.draft_tokens + j);
-    asm volatile("cp.async.commit_group;" ::: "memory");
-  }
   for (int64_t r = threadIdx.x; r < rows; r += blockDim.x) {
-    const unsigned long long k = atomicExch(a.key + r, 0ull);  // clean for the next call
+    const unsigned long long k = __ldcg(a.key + r);
+    a.key[r] = 0ull;  // clean for the next call
     // a row made only of NaN has no candidate: unspecified, report index 0
     const int bi = k == 0ull ? 0 : key_index(k);
     amax[r] = bi;
     if (a.target_tokens) a.target_tokens[r] = bi;
   }
-  if (in_smem) asm volatile("cp.async.wait_all;" ::: "memory");
-  __syncthreads();  // amax and the drafts are visible to the whole CTA
+  __syncthreads();  // amax is visible to the whole CTA
   long long cq = 0, cd = 0;
   for (int b0 = 0; b0 < a.B; b0 += blockDim.x) {
     const int b = b0 + threadIdx.x;
@@ -291,30 +418,48 @@ __device__ __noinline__ void finalize_all(const AcceptArgs& a, int64_t rows, con
     for (int64_t r = threadIdx.x; r < rows; r += blockDim.x) amax[r] = 0;
 }
 
-template <bool BF16>
+template <bool BF16, bool FLAT>
 __global__ void __launch_bounds__(ARGMAX_THREADS, ARGMAX_CTAS_PER_SM) accept_kernel(AcceptArgs a) {
   __shared__ int s_last;
   __shared__ int s_D[FIN_B];
+  __shared__ int s_draft[FIN_CAP];
   pdl_trigger();
   pdl_wait();
   int64_t rows;
   const bool ok = total_rows(a.draft_len, a.B, a.max_draft, &rows, s_D);
-  if (ok) scan_range<BF16>(a, rows);
-  // completion ticket: every CTA takes one after its candidates are written
+  const bool in_smem = ok && rows <= FIN_CAP && a.B <= FIN_B;
+  if (in_smem) {  // the drafts, for whichever CTA finishes last; they arrive during the scan
+    for (int j = threadIdx.x; j < rows - a.B; j += blockDim.x)
+      cp_async4(s_draft + j, a.draft_tokens + j);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
+  if (ok) {
+    if constexpr (FLAT)
+      scan_flat<BF16>(a, rows);
+    else
+      scan_range<BF16>(a, rows);
+  }
+  if (in_smem) asm volatile("cp.async.wait_all;" ::: "memory");
+  // completion ticket: every CTA takes one after its candidates are written; the fences
+  // order this CTA's key updates before its ticket and, in the last CTA, every other CTA's
+  // key updates before its reads
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
-    s_last = atomicAdd(a.ticket, 1u) == (uint32_t)a.nctas - 1;
+    const bool last = atomicAdd(a.ticket, 1u) == (uint32_t)a.nctas - 1;
+    if (last) {
+      __threadfence();
+      *a.ticket = 0u;  // no CTA of this call touches it again
+    }
+    s_last = last;
   }
   __syncthreads();
   if (!s_last) return;
-  __threadfence();  // the other CTAs' candidates are visible from here on
-  if (threadIdx.x == 0) atomicExch(a.ticket, 0u);
   if (!ok) {
     if (threadIdx.x == 0) atomicOr(a.flags, FLAG_ACCEPT_SHAPE);
     return;
   }
-  finalize_all(a, rows, s_D);
+  finalize_all(a, rows, s_D, s_draft, in_smem);
 }
 
 }  // namespace
@@ -355,9 +500,16 @@ cudaError_t launch_accept(int B, int max_draft, int vocab, int dtype, const void
   a.max_draft = max_draft;
   a.vocab = vocab;
   a.nctas = lay.nctas;
-  return dtype == SV_BF16
-             ? launch_pdl(accept_kernel<true>, dim3(lay.nctas), dim3(ARGMAX_THREADS), 0, s, a)
-             : launch_pdl(accept_kernel<false>, dim3(lay.nctas), dim3(ARGMAX_THREADS), 0, s, a);
+  // continuous scan: rows of whole, aligned vectors
+  const int64_t row_bytes = (int64_t)vocab * (dtype == SV_BF16 ? 2 : 4);
+  const bool flat = ((uintptr_t)logits % VB) == 0 && row_bytes % VB == 0;
+  a.row_vecs = row_bytes / VB;
+  const dim3 g(lay.nctas), b(ARGMAX_THREADS);
+  if (dtype == SV_BF16)
+    return flat ? launch_pdl(accept_kernel<true, true>, g, b, 0, s, a)
+                : launch_pdl(accept_kernel<true, false>, g, b, 0, s, a);
+  return flat ? launch_pdl(accept_kernel<false, true>, g, b, 0, s, a)
+              : launch_pdl(accept_kernel<false, false>, g, b, 0, s, a);
 }
 
 }  // namespace sv

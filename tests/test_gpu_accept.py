@@ -153,6 +153,40 @@ def test_many_rows_and_sequences(B, D, V):
     _check(synth.accept_inputs(w, 9))
 
 
+@pytest.mark.parametrize("V,dtype", [(1072, "bf16"), (536, "fp32"), (16, "bf16")])
+def test_row_boundaries_inside_a_batch(V, dtype):
+    """Rows of whole 32-byte vectors, 67 per row (coprime with the CTAs' batches) or one:
+    the continuous scan meets row ends at every offset of a batch and of a CTA's range.
+    Row kinds cycle so that a vector counted in the wrong row changes a result: 5 at the
+    last element; 6 at the first and the last (tie: the first); all -1 (tie: the first).
+    The argmax of each row is known in closed form; acceptance is checked by the oracle."""
+    B, D = 200, 4
+    R = B * (D + 1)
+    kind = np.arange(R) % 3
+    x = np.zeros((R, V), dtype=np.float32)
+    x[kind == 0, V - 1] = 5.0
+    x[kind == 1, 0] = 6.0
+    x[kind == 1, V - 1] = 6.0
+    x[kind == 2, :] = -1.0
+    expect = np.where(kind == 0, V - 1, 0).astype(np.int32)
+    logits = synth.bf16_bits(x) if dtype == "bf16" else x
+    draft_len = np.full(B, D, dtype=np.int32)
+    drafts = []
+    for b in range(B):
+        t = expect[b * (D + 1):b * (D + 1) + D].copy()
+        if b % 5 < D:
+            t[b % 5] = (t[b % 5] + 1) % V  # first mismatch at position b % 5
+        drafts.append(t)
+    a = {"logits": logits, "draft_tokens": np.concatenate(drafts).astype(np.int32),
+         "draft_len": draft_len}
+    al, nt, tgt = gpu_accept(a, D)
+    assert np.array_equal(tgt, expect)
+    ral, rnt, ramax = oracle.spec_accept(a["logits"], a["draft_tokens"], a["draft_len"])
+    assert np.array_equal(ramax, expect)
+    assert np.array_equal(al, ral) and np.array_equal(nt, rnt)
+    assert np.array_equal(al, np.minimum(np.arange(B) % 5, D) + 1)
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])
 def test_aligned_and_unaligned_logits(dtype):
     """The same logits on 16-byte row boundaries and shifted by one element (every row then
