@@ -564,25 +564,8 @@ __device__ __forceinline__ void attn_tc_body(const AttnParams& p, const CUtensor
           lh *= alpha;
           m_ref = mt;
         }
-        // O_w and the P buffer are reused once this warpgroup's previous P V is complete.
-        // Its barrier cannot be two phases behind: that tile's P was stored only after
-        // the P V before it had completed.
-        if (it >= 1) {
-          if (!(good = wwait(&bars->o_done[wg], (it - 1) & 1))) continue;
-          fence_after();
-        }
-        if (__any_sync(0xffffffffu, grow)) {  // (never on a unit's first tile)
-#pragma unroll 1
-          for (int c = 0; c < HD / 16; ++c) {  // 16 columns at a time: sv stays in registers
-            uint32_t ro[16];
-            tmem_ld16(tq + COL_O + wg * 128 + c * 16, ro);
-            tmem_wait_ld();
-            reg_fence16(ro);
-#pragma unroll
-            for (int e = 0; e < 16; ++e) ro[e] = __float_as_uint(__uint_as_float(ro[e]) * alpha);
-            tmem_st16(tq + COL_O + wg * 128 + c * 16, ro);
-          }
-        }
+        // P = 2^(s - m_ref) in registers, packed, while this warpgroup's previous P V may
+        // still be running
         const float nmu = m_ref == -INFINITY ? 0.f : -m_ref;
         float s8[8];
 #pragma unroll
@@ -593,13 +576,30 @@ __device__ __forceinline__ void attn_tc_body(const AttnParams& p, const CUtensor
           s8[c & 7] += sv[c];
         }
         lh += ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
-        {
-          uint32_t pk[HK / 2];
+        uint32_t pk[HK / 2];
 #pragma unroll
-          for (int e = 0; e < HK / 2; ++e) pk[e] = pack_p<F8>(sv[2 * e], sv[2 * e + 1]);
-          tmem_st32(tq + COL_P + wg * (HK / 2), pk);
-          tmem_wait_st();
+        for (int e = 0; e < HK / 2; ++e) pk[e] = pack_p<F8>(sv[2 * e], sv[2 * e + 1]);
+        // O_w and the P buffer are reused once this warpgroup's previous P V is complete.
+        // Its barrier cannot be two phases behind: that tile's P was stored only after
+        // the P V before it had completed.
+        if (it >= 1) {
+          if (!(good = wwait(&bars->o_done[wg], (it - 1) & 1))) continue;
+          fence_after();
         }
+        if (__any_sync(0xffffffffu, grow)) {  // (never on a unit's first tile)
+#pragma unroll 1
+          for (int c = 0; c < HD / 16; ++c) {  // 16 columns at a time: P stays in registers
+            uint32_t ro[16];
+            tmem_ld16(tq + COL_O + wg * 128 + c * 16, ro);
+            tmem_wait_ld();
+            reg_fence16(ro);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) ro[e] = __float_as_uint(__uint_as_float(ro[e]) * alpha);
+            tmem_st16(tq + COL_O + wg * 128 + c * 16, ro);
+          }
+        }
+        tmem_st32(tq + COL_P + wg * (HK / 2), pk);
+        tmem_wait_st();
         bool zeroed = false;
         // under a sliding window, keys before T - window + 1 left every row's window
         const int kvis = WIN ? T + 1 - window : -1;
