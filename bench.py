@@ -98,6 +98,9 @@ def parse():
                     help="run W + K steps of the workload and exit (for profilers)")
     ap.add_argument("--row-pairs", type=int, default=0, choices=[0, 1],
                     help="1: the row-pair attention kernel wherever it applies")
+    ap.add_argument("--kv-rings", type=int, default=-1, choices=[-1, 0, 1],
+                    help="bf16 K/V on the tcgen05 kernel: -1 by the call's shape (default), "
+                         "0 paired K + V stages, 1 separate K and V rings")
     return ap.parse_args()
 
 
@@ -552,6 +555,7 @@ def run_ours(args):
     if args.kernel != "auto":
         sv.set_attn_kernel(1 if args.kernel == "mma" else 2)
     sv.api.set_row_pairs(args.row_pairs)
+    sv.api.set_kv_rings(args.kv_rings)
     attn_kernel = {1: "mma.sync", 2: "tcgen05"}[_active_kernel(sv)]
 
     w, T, D, p = workload(args)

@@ -387,6 +387,18 @@ SV_API int sv_set_unit_ctas(int mode);
  * Returns the previous value, or -2 if mode is not 0 or 1. Process-wide. */
 SV_API int sv_set_row_pairs(int mode);
 
+/* K/V shared-memory rings of the tcgen05 kernel with bf16 K/V, for measurement and tests.
+ * 1 = separate rings of K tiles (four, each free once its score MMA is complete) and V
+ * tiles (three, each free once its P V is), filled by two producers, so K loads run
+ * further ahead of the score MMAs; 0 = three paired stages of one K and one V tile, free
+ * once the tile's P V is complete; -1 (default) = paired stages when a KV head's rows,
+ * num_q_heads / num_kv_heads * (1 + max_draft_len), fill more than one 128-row tile but
+ * not a whole number of them, or when the CTAs would each stream more than 1024 key tiles
+ * (by max_seq_len), split rings otherwise. Results are bit-identical across modes; FP8 K/V
+ * is unaffected. Returns the previous value, or -2 if mode is outside [-1, 1].
+ * Process-wide. */
+SV_API int sv_set_kv_rings(int mode);
+
 /* 1 if spec_verify_attn with this descriptor, cache layout (block_size 0: packed), SM count
  * and kernel (1 = mma.sync, 2 = tcgen05) runs the row-pair kernel under the current
  * setting, 0 if it runs the unit plan that sv_plan_preview describes, -1 if the arguments

@@ -36,7 +36,7 @@ EXPORTS = ("spec_verify_attn_workspace_size", "spec_verify_attn", "spec_verify_a
            "sv_workspace_status", "sv_status_string", "sv_set_attn_kernel", "sv_set_unit_ctas",
            "sv_set_profile_events", "sv_version", "sv_plan_preview",
            "sv_inject_launch_failure", "sv_inject_wait_timeout", "sv_set_row_pairs",
-           "sv_row_pair_mode",
+           "sv_row_pair_mode", "sv_set_kv_rings",
            "spec_accept_stochastic_workspace_size",
            "spec_accept_stochastic")
 
@@ -122,6 +122,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.sv_inject_wait_timeout.restype = ctypes.c_int
         lib.sv_set_row_pairs.argtypes = [ctypes.c_int]
         lib.sv_set_row_pairs.restype = ctypes.c_int
+        lib.sv_set_kv_rings.argtypes = [ctypes.c_int]
+        lib.sv_set_kv_rings.restype = ctypes.c_int
         lib.sv_row_pair_mode.argtypes = [ctypes.POINTER(AttnDesc), i32, i32, i32]
         lib.sv_row_pair_mode.restype = ctypes.c_int
         _lib = lib
@@ -436,6 +438,15 @@ def set_row_pairs(mode: int) -> int:
     prev = load_library().sv_set_row_pairs(int(mode))
     if prev < 0:
         raise ValueError("row-pair mode must be 0 or 1")
+    return prev
+
+
+def set_kv_rings(mode: int) -> int:
+    """bf16 K/V on the tcgen05 kernel: -1 by the call's shape (default), 0 paired K + V
+    stages, 1 separate K and V rings. Returns the previous mode."""
+    prev = load_library().sv_set_kv_rings(int(mode))
+    if prev < -1:
+        raise ValueError("ring mode must be -1, 0 or 1")
     return prev
 
 

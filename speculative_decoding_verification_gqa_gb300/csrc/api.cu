@@ -46,6 +46,16 @@ std::atomic<long long> g_stall_limit{0};
 int g_attn_kernel = 0;  // 0 automatic, 1 mma.sync, 2 tcgen05
 int g_unit_ctas = SV_UNIT_CTAS;  // -1 cost model, 0 split tile line, k > 0 k CTAs per unit
 int g_row_pairs = 0;  // 1: the row-pair kernel whenever it applies; 0: never (default)
+// bf16 K/V on the tcgen05 kernel: -1 by the call's shape (default), 0 paired K + V stages,
+// 1 separate K and V rings.
+int g_kv_rings = -1;
+// Split rings let the K loads run further ahead of the score MMAs. Measured attention time
+// (us, paired / split): c2 92.2 / 89.3; c4 (T = 16384, G = 8) with D = 0, 1, 3, 7, 15:
+// 166.5 / 162.0, 167.8 / 161.3, 168.0 / 162.7, 168.2 / 162.2, 169.3 / 164.0; D = 31
+// 257.0 / 247.8. Paired stages measured faster where a KV head's second row tile is partial
+// (D = 16: 247.1 / 259.3, D = 23: 250.7 / 255.8, although their whole steps ran faster
+// split) and on the ragged c5 batch, whose CTAs each stream about 900 tiles (1286 / 1315).
+constexpr int64_t KV_RINGS_MAX_TILES_PER_CTA = 1024;
 cudaEvent_t g_ev_start = nullptr;
 cudaEvent_t g_ev_stop = nullptr;
 
@@ -146,6 +156,13 @@ SV_API int sv_set_row_pairs(int mode) {
   return prev;
 }
 
+SV_API int sv_set_kv_rings(int mode) {
+  if (mode < -1 || mode > 1) return -2;
+  const int prev = g_kv_rings;
+  g_kv_rings = mode;
+  return prev;
+}
+
 SV_API void sv_set_profile_events(void* start_event, void* stop_event) {
   if (start_event && stop_event) {
     g_ev_start = (cudaEvent_t)start_event;
@@ -212,6 +229,9 @@ AttnParams shape_params(const sv_attn_desc* desc, const PagedArgs& pg, int which
   const bool small_blocks = pg.block_size > 0 && pg.block_size < kt;
   p.tile_floor = which == 2 && !small_blocks ? (fp8 ? SV_TILE_FLOOR_F8 : SV_TILE_FLOOR_BF16) : 0;
   p.unit_ctas_mode = g_unit_ctas;
+  const bool partial_row_tile = rows_per_kv > MT && rows_per_kv % MT != 0;
+  const bool long_stream = max_tiles > KV_RINGS_MAX_TILES_PER_CTA * p.n_ctas;
+  p.kv_rings = g_kv_rings >= 0 ? g_kv_rings : (partial_row_tile || long_stream ? 0 : 1);
   const float scale = desc->softmax_scale > 0.f ? desc->softmax_scale
                                                 : 1.f / sqrtf((float)desc->head_dim);
   p.scale_log2 = scale * 1.4426950408889634f;

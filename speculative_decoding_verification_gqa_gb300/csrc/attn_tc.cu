@@ -50,7 +50,9 @@ namespace {
 
 constexpr int KT = 128;           // keys per tile
 constexpr int HK = KT / 2;        // keys per warpgroup per tile
-constexpr int NS = 3;             // shared-memory ring depth, bf16 K/V
+constexpr int NS = 3;             // bf16, paired stages: ring depth (K and V tile each)
+constexpr int NSK = 4;            // bf16, split rings: K stages (free after their S MMA)
+constexpr int NSV = 3;            // bf16, split rings: V stages (free after their P V)
 constexpr int NS8 = 4;            // shared-memory ring depth, E4M3 K/V
 constexpr int NSMAX = 4;
 constexpr int NCV = 2;            // FP8: decoded V stages
@@ -65,7 +67,9 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_O = 0, COL_S = 256, COL_Q = 384, COL_P = 448;
 
 struct __align__(8) Bars {
-  uint64_t k_full[NSMAX], v_full[NSMAX], kv_empty[NSMAX];
+  uint64_t k_full[NSMAX], v_full[NSMAX];
+  uint64_t kv_empty[NSMAX];  // a K + V stage is free (split bf16 rings: a K stage)
+  uint64_t v_empty[NSMAX];   // split bf16 rings: a V stage is free
   uint64_t vc_full[NCV], vc_empty[NCV];  // FP8: decoded f16 V tiles
   uint64_t s_full, s_free;               // the score tile: written / read by both halves
   uint64_t p_full[2], o_done[2];         // per warpgroup: P published / its P V complete
@@ -145,22 +149,33 @@ __device__ __forceinline__ bool seg_next(const Plan& pl, int num_units, int64_t&
   return true;
 }
 
-// Shared memory. bf16 K/V: NS stages of (K tile, V tile), filled by TMA and read by the
-// MMAs. FP8 K/V: an NS8-stage ring of raw E4M3 K and V tiles filled by TMA (K read by the
-// S MMAs as it is), and an NCV-stage ring of V tiles decoded to f16 for the P V MMAs.
-template <int HD, bool F8>
+// Shared memory. bf16 K/V, paired stages (SPLIT = false): NS stages of (K tile, V tile),
+// filled by one TMA producer and freed by the tile's P V. bf16 K/V, split rings (SPLIT):
+// NSK K tiles and NSV V tiles, filled by two producers; a K tile is free once its S MMA is
+// complete, a V tile once its P V is, so K loads run further ahead of the score MMAs.
+// FP8 K/V: an NS8-stage ring of raw E4M3 K and V tiles filled by TMA (K read by the S MMAs
+// as it is), and an NCV-stage ring of V tiles decoded to f16 for the P V MMAs.
+template <int HD, bool F8, bool SPLIT>
 struct TcLayout {
   static_assert(!F8 || HD == 128, "E4M3 rows of one head are one 128-byte swizzle row");
-  static constexpr int NR = F8 ? NS8 : NS;        // TMA ring stages
+  static_assert(!(F8 && SPLIT), "split rings are a bf16 layout");
+  static constexpr int NR = NS8;                               // FP8: raw ring stages
+  static constexpr int NRK = F8 ? NS8 : (SPLIT ? NSK : NS);    // stages holding K tiles
+  static constexpr int NRV = F8 ? NS8 : (SPLIT ? NSV : NS);    // stages holding V tiles
   static constexpr int BLK = KT * 128;            // one 128-byte-wide column block of a tile
   static constexpr int NBLK = HD / 64;            // 16-bit column blocks per tile
   static constexpr int TILE = KT * HD * 2;        // one 16-bit K or V tile
-  static constexpr int STAGE = 2 * TILE;          // bf16: K then V
+  // bf16: stage st of the K tiles at KRING + st * KSTEP, of the V tiles at VRING + st * VSTEP
+  static constexpr int KRING = 0;
+  static constexpr int KSTEP = SPLIT ? TILE : 2 * TILE;
+  static constexpr int VRING = SPLIT ? NSK * TILE : TILE;
+  static constexpr int VSTEP = SPLIT ? TILE : 2 * TILE;
   static constexpr int RAW = KT * HD;             // one E4M3 tile
   static constexpr int CV = 0;                    // FP8 offsets
   static constexpr int RK = CV + NCV * TILE;
   static constexpr int RV = RK + NR * RAW;
-  static constexpr int BARS = F8 ? RV + NR * RAW : NR * STAGE;  // offset of the barrier block
+  static constexpr int BARS =
+      F8 ? RV + NR * RAW : (SPLIT ? NSK * TILE + NSV * TILE : NS * 2 * TILE);  // barriers
   static constexpr size_t SMEM = (size_t)BARS + sizeof(Bars);
   static_assert(SMEM <= 227 * 1024, "dynamic shared memory above the per-CTA limit");
   static constexpr int THREADS = F8 ? NTHREADS + 4 * 32 : NTHREADS;
@@ -168,10 +183,10 @@ struct TcLayout {
 
 // WIN: a sliding window is in force (p.window > 0); without it the window's lower mask
 // edge, the per-unit key base and the clearing of V rows before the window compile away.
-template <int HD, bool F8, bool WIN, class Plan>
+template <int HD, bool F8, bool WIN, bool SPLIT, class Plan>
 __device__ __forceinline__ void attn_tc_body(const AttnParams& p, const CUtensorMap& tmk,
                                              const CUtensorMap& tmv, const Plan& pl) {
-  using L = TcLayout<HD, F8>;
+  using L = TcLayout<HD, F8, SPLIT>;
   const int window = WIN ? p.window : 0;
   extern __shared__ __align__(1024) uint8_t smem[];  // 128-byte swizzled tiles: 1 KiB aligned
   Bars* bars = (Bars*)(smem + L::BARS);
@@ -191,11 +206,13 @@ __device__ __forceinline__ void attn_tc_body(const AttnParams& p, const CUtensor
   }
 
   if (tid == 0) {
-    for (int s = 0; s < L::NR; ++s) {
+    for (int s = 0; s < NSMAX; ++s) {
       mbar_init(&bars->k_full[s], 1);
       mbar_init(&bars->v_full[s], 1);
-      // bf16: freed by the P V commit; FP8: by the S commit and the V decoders
+      // FP8: freed by the S commit and the V decoders; bf16 paired stages: by the P V
+      // commit; split rings: by the S commit
       mbar_init(&bars->kv_empty[s], F8 ? NCONV + 1 : 1);
+      mbar_init(&bars->v_empty[s], 1);  // split rings: freed by the P V commit
     }
     for (int s = 0; s < NCV; ++s) {
       mbar_init(&bars->vc_full[s], NCONV);
@@ -226,8 +243,10 @@ __device__ __forceinline__ void attn_tc_body(const AttnParams& p, const CUtensor
   const uint32_t tmem = bars->tmem_base;
   const int u_first = rb.y;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+  if (warp == 0 || (SPLIT && warp == 2)) {
+    // ------------------------------------------------------------ TMA producers
+    // FP8 and paired bf16 stages: warp 0 loads K and V. Split bf16 rings: warp 0 fills the
+    // K ring and warp 2 the V ring, each waiting only for its own ring's stages.
     // Packed cache: lane 0 loads one box of KT rows per tile and tensor. Paged cache: a
     // tile is KT / box boxes of box = min(block_size, KT) rows, each from the physical
     // block the block table names, spread over the lanes (lane n looks up and loads box
@@ -239,6 +258,9 @@ __device__ __forceinline__ void attn_tc_body(const AttnParams& p, const CUtensor
       asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmk) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmv) : "memory");
     }
+    const bool do_k = !SPLIT || warp == 0, do_v = !SPLIT || warp == 2;
+    const uint32_t nr = do_k ? L::NRK : L::NRV;  // this producer's ring depth
+    uint64_t* empty = do_k ? bars->kv_empty : bars->v_empty;
     int64_t t = t_begin;
     int u = u_first;
     Seg s;
@@ -257,8 +279,8 @@ __device__ __forceinline__ void attn_tc_body(const AttnParams& p, const CUtensor
       } else {
 #pragma unroll
         for (int c = 0; c < L::NBLK; ++c)
-          tma_load_3d(saddr(smem + st * L::STAGE) + c * L::BLK + roff, &tmk, &bars->k_full[st],
-                      c * 64, g, grow);
+          tma_load_3d(saddr(smem + L::KRING + st * L::KSTEP) + c * L::BLK + roff, &tmk,
+                      &bars->k_full[st], c * 64, g, grow);
       }
     };
     auto load_v = [&](uint32_t st, int n, int g, int grow) {
@@ -269,7 +291,7 @@ __device__ __forceinline__ void attn_tc_body(const AttnParams& p, const CUtensor
       } else {
 #pragma unroll
         for (int c = 0; c < L::NBLK; ++c)
-          tma_load_3d(saddr(smem + st * L::STAGE) + L::TILE + c * L::BLK + roff, &tmv,
+          tma_load_3d(saddr(smem + L::VRING + st * L::VSTEP) + c * L::BLK + roff, &tmv,
                       &bars->v_full[st], c * 64, g, grow);
       }
     };
@@ -291,35 +313,39 @@ __device__ __forceinline__ void attn_tc_body(const AttnParams& p, const CUtensor
         return blk * p.block_size + (pos & (p.block_size - 1));
       };
       for (int j = s.j0; j < s.j1; ++j, ++it) {
-        const uint32_t st = it % L::NR;
+        const uint32_t st = it % nr;
         const bool mine = p.block_size == 0 ? lane == 0 : lane < nbox;
         const int grow = p.block_size == 0 ? row0 + j * KT : (mine ? paged_row(j, lane) : 0);
         bool w = true;
-        if (it >= L::NR && lane == 0)
-          w = mbar_wait(&bars->kv_empty[st], ((it / L::NR) - 1) & 1, wt);
+        if (it >= nr && lane == 0) w = mbar_wait(&empty[st], ((it / nr) - 1) & 1, wt);
         if (!__shfl_sync(0xffffffffu, w, 0)) {
           ok = false;
           break;
         }
         if (withhold && it == 0) continue;
         // the boxes of a tile add up to one full tile per tensor
-        if (lane == 0) mbar_expect_tx(&bars->k_full[st], F8 ? L::RAW : L::TILE);
-        __syncwarp();
-        if (mine) load_k(st, lane, s.g, grow);
-        if (lane == 0) mbar_expect_tx(&bars->v_full[st], F8 ? L::RAW : L::TILE);
-        __syncwarp();
-        if (mine) load_v(st, lane, s.g, grow);
+        if (do_k) {
+          if (lane == 0) mbar_expect_tx(&bars->k_full[st], F8 ? L::RAW : L::TILE);
+          __syncwarp();
+          if (mine) load_k(st, lane, s.g, grow);
+        }
+        if (do_v) {
+          if (lane == 0) mbar_expect_tx(&bars->v_full[st], F8 ? L::RAW : L::TILE);
+          __syncwarp();
+          if (mine) load_v(st, lane, s.g, grow);
+        }
       }
     }
     if (lane == 0) {
       // leave no copy in flight: wait (bounded) for the last fill of every stage. Normally
       // its readers have waited for it too; after another role gave up they may not have,
       // and the copy must land before the CTA's shared memory is released.
-      for (uint32_t st = withhold ? 1 : 0; st < L::NR && st < it; ++st) {
-        const uint32_t fills = (it - 1 - st) / L::NR + 1;
+      for (uint32_t st = withhold ? 1 : 0; st < nr && st < it; ++st) {
+        const uint32_t fills = (it - 1 - st) / nr + 1;
         const uint32_t par = (fills - 1) & 1;
         const long long t0 = clock64();
-        while (!(mbar_try(&bars->k_full[st], par) && mbar_try(&bars->v_full[st], par)) &&
+        while (!((!do_k || mbar_try(&bars->k_full[st], par)) &&
+                 (!do_v || mbar_try(&bars->v_full[st], par))) &&
                clock64() - t0 < TIMEOUT_CYCLES) {
         }
       }
@@ -330,7 +356,7 @@ __device__ __forceinline__ void attn_tc_body(const AttnParams& p, const CUtensor
       constexpr uint32_t ID_S = F8 ? idesc_e4m3(KT) : idesc_bf16(KT, 0);
       // K: K-major, 128-byte rows, 8-row groups 1024 B apart; 32 B per K step (16 bf16 or
       // 32 E4M3 elements)
-      const uint64_t kdesc0 = smem_desc(saddr(smem + (F8 ? L::RK : 0)), 16, 1024);
+      const uint64_t kdesc0 = smem_desc(saddr(smem + (F8 ? L::RK : L::KRING)), 16, 1024);
       int64_t t = t_begin;
       int u = u_first;
       Seg s;
@@ -340,14 +366,14 @@ __device__ __forceinline__ void attn_tc_body(const AttnParams& p, const CUtensor
         if (!mbar_wait(&bars->q_full, seg_i & 1, wt)) break;
         fence_after();
         for (int j = s.j0; j < s.j1; ++j, ++it) {
-          const uint32_t st = it % L::NR;
-          if (!mbar_wait(&bars->k_full[st], (it / L::NR) & 1, wt) ||
+          const uint32_t st = it % L::NRK;
+          if (!mbar_wait(&bars->k_full[st], (it / L::NRK) & 1, wt) ||
               (it >= 1 && !mbar_wait(&bars->s_free, (it - 1) & 1, wt))) {
             ok = false;
             break;
           }
           fence_after();
-          const uint64_t kd = kdesc0 + ((st * (F8 ? L::RAW : L::STAGE)) >> 4);
+          const uint64_t kd = kdesc0 + ((st * (F8 ? L::RAW : L::KSTEP)) >> 4);
           const uint32_t dcol = tmem + COL_S;
           if constexpr (F8) {
             // S = Q_hi K^T + Q_lo K^T: Q_hi in TMEM columns [COL_Q, +32), Q_lo in [+32, +64)
@@ -364,7 +390,8 @@ __device__ __forceinline__ void attn_tc_body(const AttnParams& p, const CUtensor
                      kd + ((((kk >> 2) * L::BLK) + (kk & 3) * 32) >> 4), ID_S, kk > 0 ? 1u : 0u);
           }
           mma_commit(&bars->s_full);
-          if constexpr (F8) mma_commit(&bars->kv_empty[st]);  // the raw K tile is read
+          // the K tile is read: an FP8 raw stage's K half, or a split ring's K stage
+          if constexpr (F8 || SPLIT) mma_commit(&bars->kv_empty[st]);
         }
         ++seg_i;
       }
@@ -378,7 +405,7 @@ __device__ __forceinline__ void attn_tc_body(const AttnParams& p, const CUtensor
     if (lane == 0) {
       constexpr uint32_t ID_PV = F8 ? idesc_f16(HD, 1) : idesc_bf16(HD, 1);
       // V: MN-major, 64-column blocks L::BLK apart (LBO), 8-key groups 1024 B apart (SBO)
-      const uint64_t vdesc0 = smem_desc(saddr(smem + (F8 ? L::CV : L::TILE)), L::BLK, 1024);
+      const uint64_t vdesc0 = smem_desc(saddr(smem + (F8 ? L::CV : L::VRING)), L::BLK, 1024);
       int64_t t = t_begin;
       int u = u_first;
       Seg s;
@@ -387,14 +414,14 @@ __device__ __forceinline__ void attn_tc_body(const AttnParams& p, const CUtensor
       while (ok && seg_next<WIN>(pl, num_units, t, t_end, u, s)) {
         bool first[2] = {true, true};  // each accumulator starts afresh in every unit
         for (int j = s.j0; j < s.j1; ++j, ++it) {
-          const uint32_t st = F8 ? it % NCV : it % L::NR;
+          const uint32_t st = F8 ? it % NCV : it % L::NRV;
           uint64_t* vready = F8 ? &bars->vc_full[st] : &bars->v_full[st];
-          const uint32_t vpar = F8 ? (it / NCV) & 1 : (it / L::NR) & 1;
+          const uint32_t vpar = F8 ? (it / NCV) & 1 : (it / L::NRV) & 1;
           if (!mbar_wait(vready, vpar, wt)) {
             ok = false;
             break;
           }
-          const uint64_t vd = vdesc0 + ((st * (F8 ? L::TILE : L::STAGE)) >> 4);
+          const uint64_t vd = vdesc0 + ((st * (F8 ? L::TILE : L::VSTEP)) >> 4);
           for (int w = 0; w < 2 && ok; ++w) {
             if (!mbar_wait(&bars->p_full[w], it & 1, wt)) {
               ok = false;
@@ -411,7 +438,7 @@ __device__ __forceinline__ void attn_tc_body(const AttnParams& p, const CUtensor
             mma_commit(&bars->o_done[w]);
           }
           if (!ok) break;
-          mma_commit(F8 ? &bars->vc_empty[st] : &bars->kv_empty[st]);
+          mma_commit(F8 ? &bars->vc_empty[st] : SPLIT ? &bars->v_empty[st] : &bars->kv_empty[st]);
         }
       }
       mma_commit(&bars->pv_final);
@@ -608,9 +635,9 @@ __device__ __forceinline__ void attn_tc_body(const AttnParams& p, const CUtensor
           // sequence or unwritten memory) and, under a sliding window, before the first
           // visible key (left the window: any bits), so that P = 0 never meets non-finite
           // data
-          const uint32_t st = it % L::NR;
-          if (!(good = wwait(&bars->v_full[st], (it / L::NR) & 1))) continue;
-          uint8_t* vt = smem + st * L::STAGE + L::TILE;
+          const uint32_t st = it % L::NRV;
+          if (!(good = wwait(&bars->v_full[st], (it / L::NRV) & 1))) continue;
+          uint8_t* vt = smem + L::VRING + st * L::VSTEP;
           auto clear_rows = [&](int first, int end) {  // tile rows [first, end)
             const int chunks = (end - first) * 8;  // 16-byte chunks per column block
             for (int q = r; q < chunks * L::NBLK; q += NSOFT / 2) {
@@ -770,16 +797,16 @@ __device__ __forceinline__ void attn_tc_body(const AttnParams& p, const CUtensor
 }
 
 // Device-planned launch: the plan in the workspace, written by the planning kernel.
-template <int HD, bool F8, bool WIN>
+template <int HD, bool F8, bool WIN, bool SPLIT>
 __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
     attn_tc_kernel(const AttnParams p, const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv) {
-  attn_tc_body<HD, F8, WIN>(p, tmk, tmv, WsPlan{p});
+  attn_tc_body<HD, F8, WIN, SPLIT>(p, tmk, tmv, WsPlan{p});
 }
 
 // Host-planned launch: the plan travels with the launch. CTA 0 also copies what the
 // combine kernel reads (unit list, unit starts, query offsets, counts) into the workspace.
-template <int HD, bool F8, bool WIN>
+template <int HD, bool F8, bool WIN, bool SPLIT>
 __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
     attn_tc_kernel_hp(const AttnParams p, const __grid_constant__ CUtensorMap tmk,
                       const __grid_constant__ CUtensorMap tmv,
@@ -797,7 +824,7 @@ __global__ void __launch_bounds__(F8 ? NTHREADS + 128 : NTHREADS, 1)
       p.hdr->unit_ctas = hp.unit_ctas;
     }
   }
-  attn_tc_body<HD, F8, WIN>(p, tmk, tmv, ParamPlan{hp});
+  attn_tc_body<HD, F8, WIN, SPLIT>(p, tmk, tmv, ParamPlan{hp});
 }
 
 // ---------------------------------------------------------------- host side
@@ -845,19 +872,27 @@ bool make_kv_map(CUtensorMap* map, const void* base, int64_t kv_rows, int hkv, i
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int HD, bool F8, bool WIN>
+template <int HD, bool F8, bool WIN, bool SPLIT>
 cudaError_t launch_hd(const AttnParams& p, cudaStream_t s) {
-  using L = TcLayout<HD, F8>;
+  using L = TcLayout<HD, F8, SPLIT>;
   CUtensorMap mk, mv;
   const int box = p.block_size > 0 ? min(p.block_size, KT) : KT;
   if (!make_kv_map(&mk, p.k, p.kv_rows, p.Hkv, HD, F8, box) ||
       !make_kv_map(&mv, p.v, p.kv_rows, p.Hkv, HD, F8, box))
     return cudaErrorInvalidValue;
-  auto kernel = attn_tc_kernel<HD, F8, WIN>;
+  auto kernel = attn_tc_kernel<HD, F8, WIN, SPLIT>;
   cudaError_t e =
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::SMEM);
   if (e != cudaSuccess) return e;
   return launch_pdl(kernel, dim3(p.n_ctas), dim3(L::THREADS), L::SMEM, s, p, mk, mv);
+}
+
+template <int HD, bool F8, bool WIN>
+cudaError_t launch_hd(const AttnParams& p, cudaStream_t s) {
+  if constexpr (F8)
+    return launch_hd<HD, F8, WIN, false>(p, s);
+  else
+    return p.kv_rings ? launch_hd<HD, F8, WIN, true>(p, s) : launch_hd<HD, F8, WIN, false>(p, s);
 }
 
 template <int HD, bool F8>
@@ -865,18 +900,27 @@ cudaError_t launch_hd(const AttnParams& p, cudaStream_t s) {
   return p.window > 0 ? launch_hd<HD, F8, true>(p, s) : launch_hd<HD, F8, false>(p, s);
 }
 
-template <int HD, bool F8, bool WIN>
+template <int HD, bool F8, bool WIN, bool SPLIT>
 cudaError_t launch_hd_hp(const AttnParams& p, const HostPlan& hp, cudaStream_t s) {
-  using L = TcLayout<HD, F8>;
+  using L = TcLayout<HD, F8, SPLIT>;
   CUtensorMap mk, mv;
   if (!make_kv_map(&mk, p.k, p.kv_rows, p.Hkv, HD, F8, KT) ||
       !make_kv_map(&mv, p.v, p.kv_rows, p.Hkv, HD, F8, KT))
     return cudaErrorInvalidValue;
-  auto kernel = attn_tc_kernel_hp<HD, F8, WIN>;
+  auto kernel = attn_tc_kernel_hp<HD, F8, WIN, SPLIT>;
   cudaError_t e =
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::SMEM);
   if (e != cudaSuccess) return e;
   return launch_pdl(kernel, dim3(p.n_ctas), dim3(L::THREADS), L::SMEM, s, p, mk, mv, hp);
+}
+
+template <int HD, bool F8, bool WIN>
+cudaError_t launch_hd_hp(const AttnParams& p, const HostPlan& hp, cudaStream_t s) {
+  if constexpr (F8)
+    return launch_hd_hp<HD, F8, WIN, false>(p, hp, s);
+  else
+    return p.kv_rings ? launch_hd_hp<HD, F8, WIN, true>(p, hp, s)
+                      : launch_hd_hp<HD, F8, WIN, false>(p, hp, s);
 }
 
 template <int HD, bool F8>

@@ -129,6 +129,8 @@ struct AttnParams {
   int window;                 // sliding window in positions (0: every earlier key); set to 0
                               // when it covers max_seq + max_draft + 1 positions
   float scale_log2;           // softmax_scale * log2(e)
+  int kv_rings;               // tcgen05 kernel, bf16 K/V: 1 separate K and V rings (K loads
+                              // run further ahead), 0 paired K + V stages
   long long wait_limit;       // tcgen05 kernel: clock cycles a barrier wait may take before
                               // it gives up (0: the default, about 2 s)
   int stall_first_tile;       // test hook: every CTA's producer withholds the K and V loads

@@ -274,3 +274,16 @@ def test_wait_timeout_hook_arms_and_disarms(lib):
     assert lib.sv_inject_wait_timeout(5000) == 1    # re-armed: the previous arming was pending
     assert lib.sv_inject_wait_timeout(-3) == 1      # disarmed
     assert lib.sv_inject_wait_timeout(0) == 0
+
+
+def test_kv_ring_mode_setter(lib):
+    """The ring-layout switch of the bf16 tcgen05 kernel: -1 (by the largest row tile), 0
+    (paired stages) or 1 (split rings); anything else is rejected and changes nothing."""
+    lib.sv_set_kv_rings.argtypes = [ctypes.c_int]
+    lib.sv_set_kv_rings.restype = ctypes.c_int
+    assert lib.sv_set_kv_rings(1) == -1   # the default is the automatic choice
+    assert lib.sv_set_kv_rings(0) == 1
+    assert lib.sv_set_kv_rings(2) == -2
+    assert lib.sv_set_kv_rings(-2) == -2
+    assert lib.sv_set_kv_rings(-1) == 0
+    assert lib.sv_set_kv_rings(-1) == -1

@@ -68,6 +68,32 @@ def test_small_shapes_full_oracle(kernel, name, kv):
     assert_close(got, ref)
 
 
+@pytest.mark.parametrize("window", [0, 300])
+@pytest.mark.parametrize("name", ["c1", "ragged", "tile_edges", "rows_136", "rows_256",
+                                  "llama3_8b_shape", "d64_ragged", "tiles_per_cta"])
+def test_kv_ring_modes_bit_identical(name, window):
+    """bf16 K/V on the tcgen05 kernel with paired K + V stages and with separate K and V
+    rings (by default chosen by the call's shape): the same output bits either way, and
+    the oracle's values; with and without a sliding window (whose V rows before the window
+    are cleared in the ring's stage)."""
+    if 2 not in _kernels():
+        pytest.skip("kernel not built")
+    prev_k = sv.set_attn_kernel(2)
+    try:
+        w, x = _small(kv="bf16", seed=zlib.crc32(name.encode()) % 1000 + 7, **SMALL[name])
+        outs = []
+        for mode in (0, 1):
+            prev = sv.api.set_kv_rings(mode)
+            try:
+                outs.append(gpu_attn(x, window=window))
+            finally:
+                sv.api.set_kv_rings(prev)
+        assert np.array_equal(outs[0], outs[1])
+        assert_close(outs[1], oracle_attn(w, x, window=window))
+    finally:
+        sv.set_attn_kernel(prev_k)
+
+
 def test_rows_beyond_packed_batch_untouched(kernel):
     w, x = _small(B=2, Hq=8, Hkv=2, d=128, T=(100, 50), D=(3, 2))
     q, k, v, sc, T, D = dev_attn(x)
