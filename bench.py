@@ -391,12 +391,12 @@ def run_reference(args):
 # kernel) with the kernel_source_hash() of the sources captured: an entry whose hash is not
 # the current one reads as None.
 NCU_TRAFFIC = {
-    ("c2", None, "tcgen05"): ("e8fb99e09f77f592", 549_249_024 + 3_062_528),
-    ("c3", None, "tcgen05"): ("e8fb99e09f77f592", 542_908_928 + 6_476_800),
-    ("c4", 15, "tcgen05"): ("e8fb99e09f77f592", 1_086_248_192 + 3_036_672),
-    ("c4", 16, "tcgen05"): ("e8fb99e09f77f592", 1_089_497_088 + 9_582_848),
-    ("c4", 31, "tcgen05"): ("e8fb99e09f77f592", 1_095_461_376 + 15_738_368),
-    ("c5", None, "tcgen05"): ("e8fb99e09f77f592", 9_004_260_352 + 6_507_264),
+    ("c2", None, "tcgen05"): ("7f9c3e0e594c0e9e", 549_245_696 + 2_929_664),
+    ("c3", None, "tcgen05"): ("7f9c3e0e594c0e9e", 542_897_152 + 6_938_624),
+    ("c4", 15, "tcgen05"): ("7f9c3e0e594c0e9e", 1_086_343_168 + 3_133_184),
+    ("c4", 16, "tcgen05"): ("7f9c3e0e594c0e9e", 1_089_641_472 + 9_625_600),
+    ("c4", 31, "tcgen05"): ("7f9c3e0e594c0e9e", 1_095_633_664 + 15_498_496),
+    ("c5", None, "tcgen05"): ("7f9c3e0e594c0e9e", 9_004_244_480 + 6_413_824),
 }
 
 
