@@ -170,8 +170,9 @@ __host__ __device__ inline bool cta_has_tiles(int c, int64_t TT, int C) {
 
 // Programmatic dependent launch: every kernel of the library is launched so that it may
 // start while the previous kernel on the stream drains; it lets its own dependents launch
-// at once (pdl_trigger) and waits for the previous grid's results (pdl_wait) before it
-// reads any input, so results are those of ordinary stream order.
+// (pdl_trigger: at once, except the tcgen05 attention kernel, whose CTAs release them when
+// their work is done) and waits for the previous grid's results (pdl_wait) before it reads
+// any input, so results are those of ordinary stream order.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
