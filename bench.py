@@ -647,6 +647,18 @@ def run_ours(args):
     verify_ms = float(np.median([e[0].elapsed_time(e[1]) for e in e3]))
     accept_ms = float(np.median([e[1].elapsed_time(e[2]) for e in e3]))
 
+    # Acceptance's share of the step: the step loop against the same loop with the verify
+    # call alone, both without events inside (the events around each call above expose
+    # every launch; in the step the launches overlap their predecessors)
+    def verify_only():
+        sv.spec_verify_attn(d["q"], d["k"], d["v"], d["T"], d["D"], max_draft_len=md,
+                            max_seq_len=ms, kv_scale=d.get("sc"), out=out, workspace=ws_attn,
+                            stream=stream)
+
+    for _ in range(3):
+        verify_only()
+    accept_in_step_ms = ms_step - timed_steps(verify_only, stream, K)
+
     # draft signals (confidence, entropy per row) over the step's logits matrix, as a
     # stand-in for the draft model's logits of the same shape (not part of the step)
     rows_l, V_l = d["logits"].shape
@@ -985,6 +997,7 @@ def run_ours(args):
             "attn_ms": round(attn_ms, 5),
             "verify_call_ms": round(verify_ms, 5),
             "accept_call_ms": round(accept_ms, 5),
+            "accept_in_step_ms": round(accept_in_step_ms, 5),
             "draft_signals": {"ms": round(signals_ms, 5),
                               "GB_per_s": round(logits_bytes / (signals_ms / 1e3) / 1e9, 1),
                               "rows": rows_l, "vocab": V_l,

@@ -15,8 +15,9 @@
 //     positions with 16-byte loads, all rows' loads in flight together (the slices of the
 //     positions ahead are prefetched into L2), and reduces a running max and sum of 2^t
 //     per row (t = logit / temperature in log2 units);
-//   * the CTAs exchange their (max, sum) pairs through distributed shared memory at one
-//     cluster barrier per round, and every CTA merges them in the same order, so every CTA
+//   * each CTA stores its (max, sum) pairs into every CTA's shared memory (distributed
+//     shared memory) before one cluster barrier per round, after which every CTA merges
+//     them from its own shared memory in the same order, so every CTA
 //     holds the same normalisers and takes the same keep / reject decisions from p(x) and
 //     q(x), in order, up to the first rejection;
 //   * rows of positions after the first rejection are read at most by the round that
@@ -86,10 +87,11 @@ __device__ __forceinline__ uint32_t cluster_size() {
   asm("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
   return r;
 }
-// Every thread of every CTA of the cluster; writes to shared memory before it are visible
-// to the other CTAs' distributed-shared-memory reads after it.
-// Only thread 0 of a CTA writes shared memory that other CTAs read (the exchange slots), so
-// only warp 0 arrives with release semantics.
+// Every thread of every CTA of the cluster; writes to the cluster's shared memory before it
+// (a CTA's own or, through distributed shared memory, another's) are visible to every
+// thread of the cluster after it.
+// Only thread 0 of a CTA writes what other CTAs read (the exchange slots), so only warp 0
+// arrives with release semantics.
 __device__ __forceinline__ void cluster_sync() {
   __syncwarp();  // the .aligned forms are executed by whole, converged warps
   if ((threadIdx.x >> 5) == 0)
@@ -98,15 +100,13 @@ __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-__device__ __forceinline__ float4 ld_remote(const float4* local, uint32_t rank) {
+// Stores v at the address of `local` in the shared memory of CTA `rank` of the cluster.
+__device__ __forceinline__ void st_remote(float4* local, uint32_t rank, const float4& v) {
   uint32_t ra;
   asm("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(saddr(local)), "r"(rank));
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(ra)
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(ra), "f"(v.x),
+               "f"(v.y), "f"(v.z), "f"(v.w)
                : "memory");
-  return v;
 }
 
 __device__ __forceinline__ uint4 ld_stream(const void* p) {
@@ -316,11 +316,13 @@ __device__ __forceinline__ void thread_parts(const uint4 (&tv)[UBR], const uint4
   }
 }
 
-// Exchange of N float4 per CTA through distributed shared memory: each CTA publishes
-// `mine`, and every CTA returns all CL x N values in rank order (the same in every CTA).
-// `slots` has two buffers, used alternately (`round` parity), so a fast CTA never
-// overwrites values a slower one has yet to read: it can only start round r + 2 after
-// every CTA has reached the barrier of round r + 1, i.e. finished reading round r.
+// Exchange of N float4 per CTA through distributed shared memory: each CTA stores `mine`
+// into its slot of every CTA's buffer (its own included) before the cluster barrier, and
+// after it every CTA reads all CL x N values from its own shared memory, in rank order
+// (the same in every CTA). `slots` has two buffers, used alternately (`round` parity), so
+// a fast CTA never overwrites values a slower one has yet to read: it can only start round
+// r + 2 after every CTA has reached the barrier of round r + 1, i.e. finished reading
+// round r.
 template <int N>
 __device__ __forceinline__ void exchange(const float4 (&mine)[N], float4 (*slots)[CL][R],
                                          uint32_t& round, float4 (&all)[CL][N]) {
@@ -328,12 +330,14 @@ __device__ __forceinline__ void exchange(const float4 (&mine)[N], float4 (*slots
   float4 (*buf)[R] = slots[round & 1];
   if (threadIdx.x == 0)
 #pragma unroll
-    for (int n = 0; n < N; ++n) buf[rank][n] = mine[n];
+    for (int c = 0; c < CL; ++c)
+#pragma unroll
+      for (int n = 0; n < N; ++n) st_remote(&buf[rank][n], (uint32_t)c, mine[n]);
   cluster_sync();
 #pragma unroll
   for (int c = 0; c < CL; ++c)
 #pragma unroll
-    for (int n = 0; n < N; ++n) all[c][n] = ld_remote(&buf[c][n], (uint32_t)c);  // CTA c's slot
+    for (int n = 0; n < N; ++n) all[c][n] = buf[c][n];  // CTA c's slot, stored here by CTA c
   ++round;
 }
 
@@ -581,6 +585,9 @@ __global__ void __launch_bounds__(NT, 2) accept_stochastic_kernel(StArgs a) {
   const int nv = PIPE ? (k1 - k0) / Vec<BF16>::N : 0;
   uint4 tv[PIPE ? UBR : 1], dv[PIPE ? UBR : 1];
   if constexpr (PIPE) issue_rows<BF16>(a, q_off, d_off, D > 0, k0, nv, tv, dv);
+  // every CTA of the cluster is running before the first exchange stores into its shared
+  // memory (all of them get here: the checks above return in all of them or in none)
+  cluster_sync();
   int n = D;  // drafts kept
   MS P, Q;    // normalisers of row n (the draw's row)
   for (int j = 0; j <= D; ++j) {
