@@ -391,12 +391,12 @@ def run_reference(args):
 # kernel) with the kernel_source_hash() of the sources captured: an entry whose hash is not
 # the current one reads as None.
 NCU_TRAFFIC = {
-    ("c2", None, "tcgen05"): ("7f9c3e0e594c0e9e", 549_245_696 + 2_929_664),
-    ("c3", None, "tcgen05"): ("7f9c3e0e594c0e9e", 542_897_152 + 6_938_624),
-    ("c4", 15, "tcgen05"): ("7f9c3e0e594c0e9e", 1_086_343_168 + 3_133_184),
-    ("c4", 16, "tcgen05"): ("7f9c3e0e594c0e9e", 1_089_641_472 + 9_625_600),
-    ("c4", 31, "tcgen05"): ("7f9c3e0e594c0e9e", 1_095_633_664 + 15_498_496),
-    ("c5", None, "tcgen05"): ("7f9c3e0e594c0e9e", 9_004_244_480 + 6_413_824),
+    ("c2", None, "tcgen05"): ("9307002905d7504d", 549_203_712 + 3_075_840),
+    ("c3", None, "tcgen05"): ("9307002905d7504d", 542_910_720 + 6_934_784),
+    ("c4", 15, "tcgen05"): ("9307002905d7504d", 1_086_248_704 + 3_004_416),
+    ("c4", 16, "tcgen05"): ("9307002905d7504d", 1_089_502_720 + 9_624_320),
+    ("c4", 31, "tcgen05"): ("9307002905d7504d", 1_095_737_856 + 15_554_048),
+    ("c5", None, "tcgen05"): ("9307002905d7504d", 9_004_302_848 + 6_224_640),
 }
 
 
