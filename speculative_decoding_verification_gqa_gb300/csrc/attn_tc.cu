@@ -9,9 +9,12 @@
 // online-softmax rule ("GPU and LLM, chapter 5", "Online softmax").
 //
 //   warp 0      TMA producer: K and V tiles of one KV head (128 keys x d, 128-byte swizzle)
-//               into a shared-memory ring (3 stages of bf16, 4 of E4M3); a stage is
-//               released once every reader of it has finished. A paged cache's tile is
-//               one box per block, each looked up and loaded by its own lane.
+//               into shared memory; a stage is released once every reader of it has
+//               finished. E4M3: 4 stages of a K and a V tile. bf16: 3 such stages, or
+//               (split rings, chosen per call) 4 stages of K tiles, each released by its
+//               S MMA, while warp 2 fills 3 stages of V tiles, released by their P V, so
+//               the K loads run further ahead. A paged cache's tile is one box per
+//               block, each looked up and loaded by its own lane.
 //   warp 1      S issuer (one thread): S = Q K^T (N = 128) into the score buffer, which is
 //               free again as soon as both warpgroups have read their halves. bf16:
 //               kind::f16 with Q (A) read from TMEM and K (B, K-major) from shared memory.
@@ -22,9 +25,9 @@
 //   warps 4..11 softmax, warpgroups 0 (warps 4-7) and 1 (8-11). Per unit they write Q into
 //               TMEM (half of d each). Per tile a thread reads its row's 64 scores of its
 //               half, releases the score buffer, applies the scale and the window-causal
-//               mask (and a sliding window's lower edge), updates m_w and l_w, and writes
-//               P_w = 2^(s - m_w) into its P buffer
-//               (after its previous P V has consumed the last one). At the end of a unit
+//               mask (and a sliding window's lower edge), updates m_w and l_w, computes
+//               P_w = 2^(s - m_w) into registers, and stores it into its P buffer once
+//               its previous P V has consumed the last one. At the end of a unit
 //               they merge (O_0, m_0, l_0) with (O_1, m_1, l_1) and store the output, or a
 //               split partial.
 //   warps 12-15 (FP8 K/V only) decode E4M3 V tiles to f16 tiles for P V (MMAs in f16, P
@@ -36,8 +39,9 @@
 // exact result is unchanged (numerator and denominator use the same reference).
 //
 // Every mbarrier wait is bounded: on timeout the kernel sets a flag in the workspace,
-// every role leaves its loop, the producer waits (bounded) for its copies in flight, and
-// TMEM is freed before the kernel returns.
+// every role leaves its loop, the producers wait (bounded) for their copies in flight, and
+// TMEM is freed before the kernel returns. The next kernel on the stream may launch once
+// every CTA has finished its work (not at the CTAs' start).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>

@@ -127,3 +127,14 @@ def test_ncu_traffic_is_dropped_when_the_sources_change(monkeypatch):
     assert bench.ncu_traffic("c2", None, "tcgen05") == 12345
     assert bench.ncu_traffic("c3", None, "tcgen05") is None      # another kernel version
     assert bench.ncu_traffic("c4", 7, "tcgen05") is None         # never captured
+
+
+def test_source_hash_ignores_comments_but_not_code():
+    """The capture key of the attention kernel's ncu traffic names the code, not its
+    comments: comment and layout edits keep it, any change to code or to a literal (inline
+    PTX lives in strings) does not."""
+    src = 'int a = 1; // note\n/* block */ asm("ld.global // x");\n'
+    assert bench.code_text(src) == bench.code_text('int a = 1;\n   asm("ld.global // x");')
+    assert bench.code_text(src) != bench.code_text('int a = 2; asm("ld.global // x");')
+    assert bench.code_text(src) != bench.code_text('int a = 1; asm("ld.global // y");')
+    assert bench.code_text("char c = '\"'; // q\nx;") == "char c = '\"'; x;"
