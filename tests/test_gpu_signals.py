@@ -54,8 +54,18 @@ def _rows(rows, V, seed, dtype):
 
 @pytest.mark.parametrize("rows,V,dtype", [(4, 1000, "fp32"), (7, 32000, "bf16"),
                                           (3, 128256, "bf16"), (5, 1001, "fp32"),
-                                          (9, 1001, "bf16"), (64, 7, "bf16"), (2, 65537, "fp32")])
+                                          (9, 1001, "bf16"), (64, 7, "bf16"), (2, 65537, "fp32"),
+                                          # rows of 67 and 97 32-byte vectors: row ends at every
+                                          # offset of a batch (the continuous path)
+                                          (200, 1072, "bf16"), (300, 776, "fp32"),
+                                          # about 14 rows per CTA range: near its limit
+                                          (1000, 640, "bf16"),
+                                          # more rows per range than it takes: row by row
+                                          (5000, 16, "bf16")])
 def test_random_rows(rows, V, dtype):
+    """Confidence and entropy of seeded rows against the oracle, across both scans: the
+    continuous one (rows of whole 32-byte vectors, at most 16 rows per CTA range) and the
+    row-by-row one (any other shape)."""
     _check(_rows(rows, V, rows * 1000 + V, dtype))
 
 
