@@ -14,7 +14,8 @@
 //               (split rings, chosen per call) 4 stages of K tiles, each released by its
 //               S MMA, while warp 2 fills 3 stages of V tiles, released by their P V, so
 //               the K loads run further ahead. A paged cache's tile is one box per
-//               block, each looked up and loaded by its own lane.
+//               block, each loaded by its own lane, the block-table entries read a
+//               group of tiles ahead.
 //   warp 1      S issuer (one thread): S = Q K^T (N = 128) into the score buffer, which is
 //               free again as soon as both warpgroups have read their halves. bf16:
 //               kind::f16 with Q (A) read from TMEM and K (B, K-major) from shared memory.
@@ -252,11 +253,12 @@ __device__ __forceinline__ void attn_tc_body(const AttnParams& p, const CUtensor
     // K ring and warp 2 the V ring, each waiting only for its own ring's stages.
     // Packed cache: lane 0 loads one box of KT rows per tile and tensor. Paged cache: a
     // tile is KT / box boxes of box = min(block_size, KT) rows, each from the physical
-    // block the block table names, spread over the lanes (lane n looks up and loads box
-    // n, so the lookups overlap each other and the wait for the stage); a box holding no
-    // position a row of the unit can see (past the sequence's end, or wholly before its
-    // sliding window) is not looked up and loads from a negative row, which fills it with
-    // zeros. Lane 0 waits for the stage and arms its barriers.
+    // block the block table names, spread over the lanes (lane n loads box n). The table
+    // entries are requested a group of tiles ahead (one entry per lane), so a lookup never
+    // waits at its tile behind the copies in flight; a box holding no position a row of
+    // the unit can see (past the sequence's end, or wholly before its sliding window) is
+    // not looked up and loads from a negative row, which fills it with zeros. Lane 0 waits
+    // for the stage and arms its barriers.
     if (lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmk) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmv) : "memory");
@@ -304,11 +306,24 @@ __device__ __forceinline__ void attn_tc_body(const AttnParams& p, const CUtensor
       const int nkeys = T + pl.D(s.b) + 1;
       const int kvis = first_visible_key(T, window);
       const int32_t* tab = p.block_table + (size_t)s.b * p.bt_stride;
-      // first cache row of box n of tile j (paged)
-      auto paged_row = [&](int j, int n) -> int {
-        const int pos = s.kbase + j * KT + n * box;
-        if (pos >= nkeys || pos + box <= kvis) return -box;
-        const int blk = __ldg(tab + (pos >> p.bs_log2));
+      // Paged: the block-table entries of a group of tg = 32 / nbox tiles are loaded one
+      // per lane (lane l: tile l / nbox of the group, box l % nbox) a whole group ahead of
+      // their use, so that no lookup waits behind this SM's copies in flight; at its tile
+      // each box's lane takes its entry from the group's lanes.
+      const int tg = 32 / nbox;
+      auto box_pos = [&](int j, int n) { return s.kbase + j * KT + n * box; };
+      auto visible = [&](int pos) { return pos < nkeys && pos + box > kvis; };
+      auto fetch = [&](int jg) -> int {  // this lane's entry of the group starting at tile jg
+        int e = 0;
+        const int j = jg + lane / nbox, pos = box_pos(j, lane % nbox);
+        if (p.block_size > 0 && j < s.j1 && visible(pos)) e = __ldg(tab + (pos >> p.bs_log2));
+        return e;
+      };
+      int ent_cur = fetch(s.j0), ent_nxt = fetch(s.j0 + tg);
+      // first cache row of box n of tile j (paged), from its table entry blk
+      auto paged_row = [&](int j, int n, int blk) -> int {
+        const int pos = box_pos(j, n);
+        if (!visible(pos)) return -box;
         if (blk < 0 || blk >= p.num_blocks) {  // a table entry outside the pool
           atomicOr(p.flags, FLAG_ATTN_SHAPE);
           return -box;
@@ -318,7 +333,16 @@ __device__ __forceinline__ void attn_tc_body(const AttnParams& p, const CUtensor
       for (int j = s.j0; j < s.j1; ++j, ++it) {
         const uint32_t st = it % nr;
         const bool mine = p.block_size == 0 ? lane == 0 : lane < nbox;
-        const int grow = p.block_size == 0 ? row0 + j * KT : (mine ? paged_row(j, lane) : 0);
+        int grow = row0 + j * KT;
+        if (p.block_size > 0) {
+          const int q = (j - s.j0) % tg;
+          if (q == 0 && j > s.j0) {  // the next group: its entries were requested tg tiles ago
+            ent_cur = ent_nxt;
+            ent_nxt = fetch(j + tg);
+          }
+          const int blk = __shfl_sync(0xffffffffu, ent_cur, q * nbox + lane % nbox);
+          grow = mine ? paged_row(j, lane, blk) : 0;
+        }
         bool w = true;
         if (it >= nr && lane == 0) w = mbar_wait(&empty[st], ((it / nr) - 1) & 1, wt);
         if (!__shfl_sync(0xffffffffu, w, 0)) {
