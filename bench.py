@@ -417,12 +417,12 @@ def run_reference(args):
 # kernel) with the kernel_source_hash() of the sources captured: an entry whose hash is not
 # the current one reads as None.
 NCU_TRAFFIC = {
-    ("c2", None, "tcgen05"): ("941eef68bfed3cb1", 549_203_712 + 3_075_840),
-    ("c3", None, "tcgen05"): ("941eef68bfed3cb1", 542_910_720 + 6_934_784),
-    ("c4", 15, "tcgen05"): ("941eef68bfed3cb1", 1_086_248_704 + 3_004_416),
-    ("c4", 16, "tcgen05"): ("941eef68bfed3cb1", 1_089_502_720 + 9_624_320),
-    ("c4", 31, "tcgen05"): ("941eef68bfed3cb1", 1_095_737_856 + 15_554_048),
-    ("c5", None, "tcgen05"): ("941eef68bfed3cb1", 9_004_302_848 + 6_224_640),
+    ("c2", None, "tcgen05"): ("44d6f69e72302ae9", 549_207_296 + 2_966_272),
+    ("c3", None, "tcgen05"): ("44d6f69e72302ae9", 542_928_128 + 6_818_304),
+    ("c4", 15, "tcgen05"): ("44d6f69e72302ae9", 1_086_343_936 + 2_665_216),
+    ("c4", 16, "tcgen05"): ("44d6f69e72302ae9", 1_089_371_904 + 9_577_984),
+    ("c4", 31, "tcgen05"): ("44d6f69e72302ae9", 1_097_123_840 + 15_088_128),
+    ("c5", None, "tcgen05"): ("44d6f69e72302ae9", 9_004_288_000 + 6_112_256),
 }
 
 
