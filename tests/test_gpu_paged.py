@@ -54,10 +54,10 @@ def gpu_paged(x, pg, *, window=0, workspace=None, table=None):
     return o.view(torch.int16).cpu().numpy().view(np.uint16)
 
 
-def same_policy_packed(x):
-    """The packed call under the split tile line, the policy the paged calls with blocks
-    shorter than a tile always use: the same tiles, hence the same bits."""
-    prev = sv.set_unit_ctas(0)
+def same_policy_packed(x, mode=-1):
+    """The packed call under the same unit-to-CTA policy as the paged one (by default the
+    cost model, which sees the same tile counts): the same tiles, hence the same bits."""
+    prev = sv.set_unit_ctas(mode)
     try:
         return gpu_attn(x)
     finally:
@@ -85,8 +85,10 @@ def test_ragged_batch_against_paged_oracle(kernel, kv, bs):
         sv.set_unit_ctas(prev)
     assert_close(got, paged_oracle(w, x, pg))
     # the same positions through the packed layout: the same tiles, the same bits
-    assert np.array_equal(got, same_policy_packed(x))
-    assert_close(gpu_paged(x, pg), paged_oracle(w, x, pg))  # the default policy
+    assert np.array_equal(got, same_policy_packed(x, 0))
+    dflt = gpu_paged(x, pg)  # the default policy
+    assert_close(dflt, paged_oracle(w, x, pg))
+    assert np.array_equal(dflt, same_policy_packed(x))
 
 
 @pytest.mark.parametrize("d", [64, 128])
@@ -147,7 +149,8 @@ def _full(cfg):
 @pytest.mark.parametrize("cfg", ["c2", "c3"])
 def test_full_size_16_position_blocks(kernel, cfg):
     """The workloads with 16-position blocks scattered over the pool: bit-identical to the
-    packed call on the same (split) tile line, and the oracle on sampled units."""
+    packed call under the same policy (c2: one CTA per unit, c3: the split tile line), and
+    the oracle on sampled units."""
     w, x, pg = _full(cfg)
     got = gpu_paged(x, pg)
     assert np.array_equal(got, same_policy_packed(x))
@@ -158,8 +161,8 @@ def test_full_size_16_position_blocks(kernel, cfg):
 
 @pytest.mark.parametrize("mode", [0, 1, 2])
 def test_paged_under_every_unit_cta_policy(kernel, mode):
-    """Forced unit-to-CTA policies apply to paged calls too (the model alone keeps them on
-    the split line for blocks shorter than a tile)."""
+    """Forced unit-to-CTA policies apply to paged calls too, and give the packed call's
+    bits under the same policy."""
     w, x = _small(kv="bf16", seed=19, **RAGGED)
     pg = synth.paged_layout(x, 16, seed=20, spare_blocks=2)
     prev = sv.set_unit_ctas(mode)
@@ -168,3 +171,4 @@ def test_paged_under_every_unit_cta_policy(kernel, mode):
     finally:
         sv.set_unit_ctas(prev)
     assert_close(got, paged_oracle(w, x, pg))
+    assert np.array_equal(got, same_policy_packed(x, mode))

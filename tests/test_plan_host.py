@@ -141,13 +141,15 @@ def test_policies_chosen_on_the_measured_workloads():
     assert w2["unit_ctas"] == 1 and w2["total_tiles"] == 128 * 33
     w3 = _plan(_desc(8, 64, 8, 128, 15, 32768, True, W=4096), [32768] * 8, [15] * 8)
     assert w3["unit_ctas"] == 2 and w3["total_tiles"] == 64 * 33
-    # the mma.sync kernel keeps the split line; a paged cache of small blocks does too
+    # the mma.sync kernel keeps the split line; a paged cache, of small blocks or large,
+    # takes the packed layout's choice (the same tile counts)
     assert _plan(_desc(16, 32, 8, 128, 31, 8192), [8192] * 16, [31] * 16,
                  kernel=1)["unit_ctas"] == 0
-    assert _plan(_desc(16, 32, 8, 128, 31, 8192), [8192] * 16, [31] * 16,
-                 block_size=16)["unit_ctas"] == 0
-    assert _plan(_desc(16, 32, 8, 128, 31, 8192), [8192] * 16, [31] * 16,
-                 block_size=128)["unit_ctas"] == 1
+    for bs in (16, 128):
+        assert _plan(_desc(16, 32, 8, 128, 31, 8192), [8192] * 16, [31] * 16,
+                     block_size=bs)["unit_ctas"] == 1
+        assert _plan(_desc(8, 64, 8, 128, 15, 32768, True), [32768] * 8, [15] * 8,
+                     block_size=bs)["unit_ctas"] == 0
 
 
 @pytest.mark.parametrize("seed", range(12))
