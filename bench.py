@@ -417,12 +417,12 @@ def run_reference(args):
 # kernel) with the kernel_source_hash() of the sources captured: an entry whose hash is not
 # the current one reads as None.
 NCU_TRAFFIC = {
-    ("c2", None, "tcgen05"): ("44d6f69e72302ae9", 549_207_296 + 2_966_272),
-    ("c3", None, "tcgen05"): ("44d6f69e72302ae9", 542_928_128 + 6_818_304),
-    ("c4", 15, "tcgen05"): ("44d6f69e72302ae9", 1_086_343_936 + 2_665_216),
-    ("c4", 16, "tcgen05"): ("44d6f69e72302ae9", 1_089_371_904 + 9_577_984),
-    ("c4", 31, "tcgen05"): ("44d6f69e72302ae9", 1_097_123_840 + 15_088_128),
-    ("c5", None, "tcgen05"): ("44d6f69e72302ae9", 9_004_288_000 + 6_112_256),
+    ("c2", None, "tcgen05"): ("0b9cf5ee686dba4c", 549_243_648 + 2_965_504),
+    ("c3", None, "tcgen05"): ("0b9cf5ee686dba4c", 542_913_536 + 6_734_336),
+    ("c4", 15, "tcgen05"): ("0b9cf5ee686dba4c", 1_086_251_008 + 2_953_472),
+    ("c4", 16, "tcgen05"): ("0b9cf5ee686dba4c", 1_089_538_816 + 9_582_592),
+    ("c4", 31, "tcgen05"): ("0b9cf5ee686dba4c", 1_095_598_080 + 15_463_168),
+    ("c5", None, "tcgen05"): ("0b9cf5ee686dba4c", 9_004_215_040 + 6_469_632),
 }
 
 
