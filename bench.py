@@ -417,12 +417,12 @@ def run_reference(args):
 # kernel) with the kernel_source_hash() of the sources captured: an entry whose hash is not
 # the current one reads as None.
 NCU_TRAFFIC = {
-    ("c2", None, "tcgen05"): ("0b9cf5ee686dba4c", 549_243_648 + 2_965_504),
-    ("c3", None, "tcgen05"): ("0b9cf5ee686dba4c", 542_913_536 + 6_734_336),
-    ("c4", 15, "tcgen05"): ("0b9cf5ee686dba4c", 1_086_251_008 + 2_953_472),
-    ("c4", 16, "tcgen05"): ("0b9cf5ee686dba4c", 1_089_538_816 + 9_582_592),
-    ("c4", 31, "tcgen05"): ("0b9cf5ee686dba4c", 1_095_598_080 + 15_463_168),
-    ("c5", None, "tcgen05"): ("0b9cf5ee686dba4c", 9_004_215_040 + 6_469_632),
+    ("c2", None, "tcgen05"): ("7be090ecd712d963", 549_204_480 + 2_689_280),
+    ("c3", None, "tcgen05"): ("7be090ecd712d963", 542_727_168 + 5_724_672),
+    ("c4", 15, "tcgen05"): ("7be090ecd712d963", 1_086_250_496 + 2_968_832),
+    ("c4", 16, "tcgen05"): ("7be090ecd712d963", 1_089_450_496 + 9_586_688),
+    ("c4", 31, "tcgen05"): ("7be090ecd712d963", 1_263_172_096 + 15_799_296),
+    ("c5", None, "tcgen05"): ("7be090ecd712d963", 9_004_360_448 + 6_521_600),
 }
 
 

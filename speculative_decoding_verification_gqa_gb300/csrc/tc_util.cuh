@@ -220,6 +220,27 @@ __device__ __forceinline__ bool softmax_pair_and(bool v) {
   return r != 0;
 }
 
+// max(a, b, c) in one instruction
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// (x0, x1) = (x0 * a + b, x1 * a + b), each rounded to nearest: one paired instruction
+__device__ __forceinline__ void fma2(float& x0, float& x1, float a, float b) {
+  asm("{\n .reg .b64 v, s, m;\n mov.b64 v, {%0, %1};\n mov.b64 s, {%2, %2};\n"
+      " mov.b64 m, {%3, %3};\n fma.rn.f32x2 v, v, s, m;\n mov.b64 {%0, %1}, v;\n}"
+      : "+f"(x0), "+f"(x1)
+      : "f"(a), "f"(b));
+}
+// (s0, s1) += (a0, a1), each rounded to nearest: one paired instruction
+__device__ __forceinline__ void add2(float& s0, float& s1, float a0, float a1) {
+  asm("{\n .reg .b64 v, w;\n mov.b64 v, {%0, %1};\n mov.b64 w, {%2, %3};\n"
+      " add.rn.f32x2 v, v, w;\n mov.b64 {%0, %1}, v;\n}"
+      : "+f"(s0), "+f"(s1)
+      : "f"(a0), "f"(a1));
+}
+
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
