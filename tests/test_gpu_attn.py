@@ -254,6 +254,32 @@ def test_running_max_grows_on_some_rows_only(kernel, kv):
     assert_close(gpu_attn(x), oracle_attn(w, x))
 
 
+@pytest.mark.parametrize("kv", ["bf16", "fp8_e4m3"])
+def test_row_maximum_at_every_position_of_a_half_tile(kernel, kv):
+    """Query row r (of 128: 16 window positions x 8 heads) meets one dominant key per
+    128-key tile, at key r of the tile, so across the rows the maximum of a warpgroup's
+    64-key half sits at each of its 64 positions: a score left out of the maximum would
+    leave 2^32 in P (an overflow in the 16-bit P) instead of 1."""
+    Hq, Hkv, d, T, D = 8, 1, 128, 256, 15
+    W = D + 1
+    rng = np.random.default_rng(17)
+    q = np.zeros((W, Hq, d), dtype=np.float32)
+    for i in range(W):
+        for h in range(Hq):
+            q[i, h, i * Hq + h] = 16.0                 # row r = i*G + h: channel r
+    k = np.zeros((T + W, Hkv, d), dtype=np.float32)
+    for key in range(T):
+        k[key, 0, key % 128] = 16.0                    # keys r and r + 128 match row r
+    v = rng.standard_normal((T + W, Hkv, d)).astype(np.float32)
+    w = synth.Workload("m", B=1, Hq=Hq, Hkv=Hkv, d=d, D=0, T=0, V=8, p=0.5, kv_dtype=kv)
+    x = dict(q=_bits(q))
+    x.update(dict(k=_bits(k), v=_bits(v), kv_scale=None) if kv == "bf16" else _fp8_kv(k, v))
+    x.update(seq_lens=np.array([T], dtype=np.int32), draft_len=np.array([D], dtype=np.int32))
+    got = gpu_attn(x)
+    assert np.isfinite(bf16_to_f64(got)).all()
+    assert_close(got, oracle_attn(w, x))
+
+
 def _fp8_kv(k, v):
     """Per-KV-head E4M3 quantisation of float K and V (scale = absmax / 448)."""
     sk = np.abs(k).max(axis=(0, 2)) / 448.0
