@@ -275,3 +275,28 @@ def test_row_pair_mode_query(lib):
         assert lib.sv_set_row_pairs(2) == -2 and lib.sv_set_row_pairs(-1) == -2
     finally:
         lib.sv_set_row_pairs(prev)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_paged_calls_take_the_packed_plan(seed):
+    """A paged cache (any block size) gets the packed layout's plan for the same lengths:
+    the same units, tile line, unit-to-CTA choice and CTA ranges (the paged and packed
+    calls then compute the same tiles, bit for bit)."""
+    rng = np.random.default_rng(seed)
+    B = int(rng.integers(1, 40))
+    Hkv = int(rng.choice([1, 2, 4, 8]))
+    G = int(rng.choice([1, 2, 4, 8, 16]))
+    Dm = int(rng.integers(0, 32))
+    Tm = int(rng.integers(1, 40000))
+    Tv = rng.integers(0, Tm + 1, B)
+    Dv = rng.integers(0, Dm + 1, B)
+    W = int(rng.choice([0, 0, 512, 4096]))
+    for fp8 in (False, True):
+        desc = _desc(B, Hkv * G, Hkv, 128, Dm, Tm, fp8, W)
+        packed = _plan(desc, Tv, Dv)
+        for bs in (8, 16, 64, 256):
+            paged = _plan(desc, Tv, Dv, block_size=bs)
+            for key in ("num_units", "total_tiles", "unit_ctas", "num_ctas"):
+                assert paged[key] == packed[key], (bs, key)
+            for key in ("units", "unit_begin", "cta_begin"):
+                assert np.array_equal(paged[key], packed[key]), (bs, key)
